@@ -1,0 +1,235 @@
+/*
+ * spec_verify.h -- C ABI of libspecverify.so, the GB300 (sm_103a) library for
+ * the verify-and-accept step of speculative decoding.
+ *
+ * The step runs after the target model's one forward over k drafted tokens
+ * (or over a flattened draft tree).  It reads the V-wide logit rows that
+ * forward produced, decides how much of the draft to keep, and supplies the
+ * one token the target adds at the break point ("accepted + 1").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is CALLER-OWNED DEVICE MEMORY unless stated.  The
+ *    library allocates nothing and frees nothing.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL is the legacy default stream).  Nothing is synchronised inside.
+ *  - The return value is a status.  SPEC_OK means the work was enqueued.  A
+ *    negative value means the arguments were rejected on the host and NOTHING
+ *    was launched (SPEC_ECUDA: a launch failed; spec_last_error() has the CUDA
+ *    message).  The library never traps, asserts or exits on the device.
+ *  - Problems found on the device in one request's data (a draft token
+ *    outside [0, V), a malformed tree, a bad length) are written to that
+ *    request's `status[b]` (SPEC_STATUS_*); such a request emits nothing
+ *    (n_emit = 0, outputs -1) and the other requests are unaffected.
+ *  - Logits: dtype SPEC_DTYPE_F32 or SPEC_DTYPE_BF16.  Each row holds V
+ *    contiguous values.  Row i of request b starts at element
+ *        b * req_stride + i * row_stride
+ *    of its buffer.  Strides are in elements and may be 0 (broadcast).  The
+ *    fast path wants every row start 16-byte aligned; other layouts are
+ *    served by a scalar path with the same results.  NaN logits are not
+ *    supported; -inf is (a masked token).
+ *  - Uniforms are fp32 in [0, 1), drawn by the caller.
+ *  - Argmax ties resolve to the lowest index.
+ *  - Workspace: `workspace` must hold spec_workspace_size(...) bytes and be
+ *    256-byte aligned.  Its contents need no initialisation and may be
+ *    reused by any later call of any shape.  Calls that may overlap on the
+ *    GPU (other streams) must not share a workspace.
+ *  - p = softmax(target_logits / T), q = softmax(draft_logits / T), the
+ *    target's and the draft's next-token distributions at a position
+ *    ("投机解码:为什么一个字都不改", section "一轮能出几个 token", the box
+ *    P = softmax(f([x1 ... xk]) / T)).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* return codes (host side) */
+#define SPEC_OK 0
+#define SPEC_EINVAL (-1)     /* bad pointer, size, stride or scalar argument */
+#define SPEC_EDTYPE (-2)     /* dtype is neither SPEC_DTYPE_F32 nor SPEC_DTYPE_BF16 */
+#define SPEC_EWORKSPACE (-3) /* workspace missing, misaligned or too small */
+#define SPEC_ECUDA (-4)      /* a CUDA call failed; see spec_last_error() */
+
+/* per-request status codes (device side, in status[b]) */
+#define SPEC_STATUS_OK 0
+#define SPEC_STATUS_TOKEN_RANGE 1 /* a draft/node token is outside [0, V) */
+#define SPEC_STATUS_BAD_TREE 2    /* parents[] is not a tree rooted at 0, or too deep */
+#define SPEC_STATUS_BAD_LENGTH 3  /* draft_len or hist_len outside its range */
+
+#define SPEC_DTYPE_F32 0
+#define SPEC_DTYPE_BF16 1
+
+/* `op` argument of spec_workspace_size */
+#define SPEC_OP_NGRAM 0
+#define SPEC_OP_GREEDY 1
+#define SPEC_OP_SAMPLE 2
+#define SPEC_OP_TREE 3
+
+/* Limits checked on the host. */
+#define SPEC_MAX_K 64        /* draft length of a chain */
+#define SPEC_MAX_WINDOW 64   /* n-gram window */
+#define SPEC_MAX_NODES 4096  /* nodes of a draft tree, root included */
+#define SPEC_MAX_DEPTH 64    /* depth of a draft tree */
+
+/*
+ * spec_ngram_draft -- the history-lookup drafter.
+ * ("第 13 篇：推理引擎一次猜几个字", 逐行要点, the 草稿器.猜 line: take the
+ * last few tokens of the context as a window, find the identical segment
+ * earlier in the history, and propose the tokens that followed it; no
+ * parameters, and a miss costs nothing.)
+ *
+ *   history    int32 [B, hist_stride]; request b holds hist_len[b] tokens.
+ *   hist_len   int32 [B], each in [0, hist_stride] (else SPEC_STATUS_BAD_LENGTH).
+ *   window     w in [1, SPEC_MAX_WINDOW]: the last w tokens h[n-w .. n).
+ *   k          draft length in [0, SPEC_MAX_K].
+ *   draft      out int32 [B, k]: h[i+w .. min(i+w+k, n)) for the RIGHTMOST
+ *              start i < n - w with h[i .. i+w) == h[n-w .. n); padded -1.
+ *   draft_len  out int32 [B]: number of proposed tokens (0 when no match).
+ *   status     out int32 [B].
+ */
+int spec_ngram_draft(const int32_t *history, const int32_t *hist_len, int B, int hist_stride,
+                     int window, int k, int32_t *draft, int32_t *draft_len, int32_t *status,
+                     void *stream);
+
+/*
+ * spec_verify_greedy -- greedy (argmax) prefix verification.
+ * ("第 13 篇", section ③ 伪代码 and 逐行要点: compare draft token i with the
+ * token the model would choose at that position, stop at the first
+ * difference, keep the accepted prefix and append the model's own token at
+ * the break point; "Speculative decoding explained", the four-case table.)
+ *
+ *   target        logits of positions 0..k: request b, position i at
+ *                 b*target_req_stride + i*row_stride (k+1 rows of V).
+ *   draft         int32 [B, k] drafted tokens.
+ *   draft_len     int32 [B] or NULL (= k): positions >= draft_len[b] are
+ *                 ignored and the final token comes from row draft_len[b].
+ *   max_emit      int32 [B] or NULL (= k+1): cap on emitted tokens, for a
+ *                 draft that reaches the end of the sequence (no extra token).
+ *   accepted      out int32 [B]: m = length of the accepted prefix.
+ *   out_tokens    out int32 [B, k+1]: draft[0..m) then argmax(row m), cut to
+ *                 n_emit tokens, padded -1.
+ *   n_emit        out int32 [B] = min(m + 1, max_emit[b]).
+ *   status        out int32 [B].
+ *   workspace     see the conventions; size from spec_workspace_size(
+ *                 SPEC_OP_GREEDY, B, k, V, dtype).
+ */
+int spec_verify_greedy(const void *target, int64_t target_req_stride, int64_t row_stride,
+                       int dtype, int B, int k, int V, const int32_t *draft,
+                       const int32_t *draft_len, const int32_t *max_emit, int32_t *accepted,
+                       int32_t *out_tokens, int32_t *n_emit, int32_t *status, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/*
+ * spec_verify_sample -- lossless sampling verification of a chain.
+ * ("投机解码:为什么一个字都不改", section 改进方案: accept the draft token x
+ * for sure when p(x) >= q(x), else with probability p(x)/q(x); on a
+ * rejection resample from norm(max(0, p - q)) and drop the rest of the
+ * draft; replay section: each round emits accepted + 1 tokens, the last one
+ * drawn from p when all k were accepted.)
+ *
+ *   target          [B, k+1, V] logits (strides as above).
+ *   draft_logits    [B, k, V] logits of the draft model, same dtype and
+ *                   row_stride, request stride draft_req_stride.
+ *   temperature     T > 0, applied to both: p = softmax(t/T), q = softmax(d/T).
+ *   draft           int32 [B, k]: x_i, drawn by the drafter from q_i.
+ *   draft_len, max_emit   as in spec_verify_greedy.
+ *   uniforms        fp32 [B, k+1]: u[b][i] tests position i (accept iff
+ *                   u_i * q_i(x_i) < p_i(x_i), i.e. u_i < min(1, p/q));
+ *                   u[b][k] drives the final draw: the smallest v whose
+ *                   prefix sum of the residual (or, after a full accept, of
+ *                   p_L) exceeds u times its total.
+ *   accepted, out_tokens, n_emit, status   as in spec_verify_greedy.
+ *   p_tok, q_tok    out fp32 [B, k] or NULL: p_i(x_i), q_i(x_i) for every
+ *                   i < draft_len (whether or not the test reached it); -1
+ *                   beyond draft_len.
+ *   resid_mass      out fp32 [B] or NULL: sum max(0, p_m - q_m) = 1 - alpha_m
+ *                   at the rejected position, 0 when everything was accepted.
+ *   workspace       size from spec_workspace_size(SPEC_OP_SAMPLE, B, k, V, dtype).
+ */
+int spec_verify_sample(const void *target, int64_t target_req_stride, const void *draft_logits,
+                       int64_t draft_req_stride, int64_t row_stride, int dtype, int B, int k,
+                       int V, float temperature, const int32_t *draft, const int32_t *draft_len,
+                       const int32_t *max_emit, const float *uniforms, int32_t *accepted,
+                       int32_t *out_tokens, int32_t *n_emit, float *p_tok, float *q_tok,
+                       float *resid_mass, int32_t *status, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/*
+ * spec_verify_tree -- verification of a draft tree, one target forward over
+ * all nodes with tree attention.
+ * ("Speculative Decoding II", EAGLE section: the sampling rule is applied
+ * recursively at each node of the draft tree, as in SpecInfer, so the output
+ * keeps the target's distribution.)
+ *
+ *   Node 0 is the root (the last committed token); parents int32 [B, N] with
+ *   parents[b][0] = -1 and 0 <= parents[b][i] < i; node_tok int32 [B, N] the
+ *   drafted token of each node (node_tok[b][0] is not read).  Depth of the
+ *   tree <= max_depth <= SPEC_MAX_DEPTH, N <= SPEC_MAX_NODES.
+ *   target, draft_logits   [B, N, V]: row u is the target's / the draft's
+ *                   next-token logits after node u.  Draft rows of leaves
+ *                   are never read; draft_logits may be NULL when T <= 0.
+ *   temperature     T > 0: sampling walk.  At node u, p = softmax(t_u/T),
+ *                   q = softmax(d_u/T); children are tested in increasing id
+ *                   order, child c accepted iff u[b][c] * q(x_c) < p(x_c);
+ *                   after a rejected child p <- norm(max(0, p - q)) (q kept);
+ *                   an accepted child is descended into; when no child is
+ *                   accepted, or u is a leaf, the final token is drawn from
+ *                   the current p with u[b][N].
+ *                   T <= 0: greedy walk, descend into the first child (id
+ *                   order) whose token is argmax(t_u); else emit argmax(t_u).
+ *   uniforms        fp32 [B, N+1].
+ *   accepted_len    out int32 [B]: number of tree nodes accepted.
+ *   path_nodes      out int32 [B, max_depth+1]: node ids from the root, pad -1.
+ *   out_tokens      out int32 [B, max_depth+1]: emitted tokens, pad -1.
+ *   n_emit          out int32 [B] = accepted_len + 1 (0 on a bad request).
+ *   status          out int32 [B].
+ *   workspace       size from spec_workspace_size(SPEC_OP_TREE, B, N, V, dtype)
+ *                   (may be 0; then workspace may be NULL).
+ */
+int spec_verify_tree(const void *target, int64_t target_req_stride, const void *draft_logits,
+                     int64_t draft_req_stride, int64_t row_stride, int dtype, int B, int N,
+                     int V, float temperature, const int32_t *parents, const int32_t *node_tok,
+                     const float *uniforms, int max_depth, int32_t *accepted_len,
+                     int32_t *path_nodes, int32_t *out_tokens, int32_t *n_emit,
+                     int32_t *status, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * spec_workspace_size -- bytes of workspace a call needs.
+ *   op = SPEC_OP_*; rows_per_req = k for chains, N for trees.
+ *   Returns 0 for invalid arguments and for ops that need none.
+ */
+size_t spec_workspace_size(int op, int B, int rows_per_req, int V, int dtype);
+
+/* Static text for a SPEC_* return code or a SPEC_STATUS_* value (pass
+ * status codes as 100 + status). */
+const char *spec_status_string(int code);
+
+/* Message of the last CUDA failure seen by this thread ("" if none). */
+const char *spec_last_error(void);
+
+/*
+ * Tracing.  With tracing on, every kernel the library launches is bracketed
+ * by a pair of CUDA events recorded on the launching stream.
+ * spec_trace_collect() waits for the recorded events, adds each launch's
+ * elapsed time to its kernel's total, writes up to `cap` entries (kernel
+ * name, total milliseconds, launch count) and clears the record.  It
+ * returns the number of distinct kernels, or a negative SPEC_* code.
+ * Tracing is process-wide and meant for eager (not graph-captured) runs.
+ */
+int spec_trace_enable(int on);
+int spec_trace_collect(const char **names, double *total_ms, int64_t *launches, int cap);
+
+/* Number of kernels this process has launched through the library. */
+int64_t spec_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

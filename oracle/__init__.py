@@ -80,7 +80,7 @@ def _logits(x):
         code = 1
     else:
         raise TypeError(f"logits must be float32 or bf16 bits (uint16), got {x.dtype}")
-    if x.strides[-1] != x.itemsize:
+    if x.strides[-1] != x.itemsize and x.size > 0 and x.shape[-1] > 1:
         raise ValueError("logit rows must be contiguous along V")
     return x, code
 

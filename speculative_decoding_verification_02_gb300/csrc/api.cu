@@ -1,0 +1,344 @@
+// C ABI of libspecverify.so: argument checks, workspace layout, launch
+// geometry, error mapping and tracing.  The arithmetic lives in chain.cu,
+// tree.cu and ngram.cu.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace sv {
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+int fail_cuda(cudaError_t e, const char *where) {
+  std::snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", where, cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return SPEC_ECUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_size(int dtype) { return dtype == SPEC_DTYPE_BF16 ? 2 : 4; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------ geometry
+
+// Logits per CTA of the streaming pass: 16 KB of one row.  The residual
+// pass uses the same chunks (16 KB of each row of the pair).
+int stream_chunk(int dtype) { return 16384 / elem_size(dtype); }
+
+// Workspace: per-(row, chunk) statistics, then for sampling the residual
+// mass per chunk and one arrival counter per request.  Nothing in it needs
+// initialising: the counters are zeroed by the first kernel of each call.
+struct ChainLayout {
+  int nc, chunk;
+  size_t part, part2, counter2, total;
+};
+
+ChainLayout chain_layout(bool sample, int B, int k, int V, int dtype) {
+  ChainLayout L{};
+  L.chunk = stream_chunk(dtype);
+  L.nc = (V + L.chunk - 1) / L.chunk;
+  const size_t rows = sample ? 2 * static_cast<size_t>(k) + 1 : static_cast<size_t>(k) + 1;
+  size_t off = 0;
+  L.part = off;
+  off = round_up(off + sizeof(Partial) * B * rows * L.nc, 256);
+  L.part2 = off;
+  off = round_up(off + (sample ? sizeof(float) * B * L.nc : 0), 256);
+  L.counter2 = off;
+  off = round_up(off + (sample ? sizeof(int) * B : 0), 256);
+  L.total = off;
+  return L;
+}
+
+// Tree walk: one thread-block cluster per request, each CTA owns a slice of
+// V.  Eight CTAs unless the slice would not stay small.
+void tree_geometry(int V, int &cluster, int &slice) {
+  cluster = V >= 8 * 2048 ? 8 : (V >= 4 * 2048 ? 4 : (V >= 2 * 2048 ? 2 : 1));
+  slice = ((V + cluster - 1) / cluster + 7) / 8 * 8;
+}
+
+cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// -------------------------------------------------------------- tracing
+
+struct TraceRec {
+  const char *name;
+  cudaEvent_t start, stop;
+};
+
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace;
+std::vector<cudaEvent_t> g_event_pool;
+long long g_launches = 0;
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+}  // namespace
+
+int trace_begin(const char *name, cudaStream_t st) {
+  std::lock_guard<std::mutex> g(g_trace_mu);
+  if (!g_trace_on) return -1;
+  TraceRec r{name, take_event(), take_event()};
+  if (!r.start || !r.stop) return -1;
+  cudaEventRecord(r.start, st);
+  g_trace.push_back(r);
+  return static_cast<int>(g_trace.size()) - 1;
+}
+
+void trace_end(int slot, cudaStream_t st) {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> g(g_trace_mu);
+  if (slot < static_cast<int>(g_trace.size())) cudaEventRecord(g_trace[slot].stop, st);
+}
+
+void count_launch() {
+  std::lock_guard<std::mutex> g(g_trace_mu);
+  ++g_launches;
+}
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" {
+
+size_t spec_workspace_size(int op, int B, int rows_per_req, int V, int dtype) {
+  if (B < 0 || rows_per_req < 0 || V <= 0 || (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16))
+    return 0;
+  switch (op) {
+    case SPEC_OP_GREEDY: return chain_layout(false, B, rows_per_req, V, dtype).total;
+    case SPEC_OP_SAMPLE: return chain_layout(true, B, rows_per_req, V, dtype).total;
+    default: return 0;  // n-gram and tree walks need no workspace
+  }
+}
+
+const char *spec_status_string(int code) {
+  switch (code) {
+    case SPEC_OK: return "ok";
+    case SPEC_EINVAL: return "invalid argument";
+    case SPEC_EDTYPE: return "unsupported dtype";
+    case SPEC_EWORKSPACE: return "workspace missing, misaligned or too small";
+    case SPEC_ECUDA: return "CUDA error (see spec_last_error)";
+    case 100 + SPEC_STATUS_OK: return "request ok";
+    case 100 + SPEC_STATUS_TOKEN_RANGE: return "request has a token outside [0, V)";
+    case 100 + SPEC_STATUS_BAD_TREE: return "request has a malformed or too deep tree";
+    case 100 + SPEC_STATUS_BAD_LENGTH: return "request has a length outside its range";
+    default: return "unknown code";
+  }
+}
+
+const char *spec_last_error(void) { return g_last_error; }
+
+int spec_trace_enable(int on) {
+  std::lock_guard<std::mutex> g(g_trace_mu);
+  g_trace_on = on != 0;
+  return SPEC_OK;
+}
+
+int spec_trace_collect(const char **names, double *total_ms, int64_t *launches, int cap) {
+  std::vector<TraceRec> recs;
+  {
+    std::lock_guard<std::mutex> g(g_trace_mu);
+    recs.swap(g_trace);
+  }
+  std::vector<const char *> nm;
+  std::vector<double> ms;
+  std::vector<int64_t> cnt;
+  int rc = SPEC_OK;
+  for (const TraceRec &r : recs) {
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    float t = 0.0f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, r.start, r.stop);
+    if (e != cudaSuccess) rc = fail_cuda(e, "spec_trace_collect");
+    size_t i = 0;
+    while (i < nm.size() && std::strcmp(nm[i], r.name) != 0) ++i;
+    if (i == nm.size()) {
+      nm.push_back(r.name);
+      ms.push_back(0.0);
+      cnt.push_back(0);
+    }
+    ms[i] += t;
+    cnt[i] += 1;
+  }
+  {
+    std::lock_guard<std::mutex> g(g_trace_mu);
+    for (const TraceRec &r : recs) {
+      g_event_pool.push_back(r.start);
+      g_event_pool.push_back(r.stop);
+    }
+  }
+  if (rc != SPEC_OK) return rc;
+  for (size_t i = 0; i < nm.size() && static_cast<int>(i) < cap; ++i) {
+    if (names) names[i] = nm[i];
+    if (total_ms) total_ms[i] = ms[i];
+    if (launches) launches[i] = cnt[i];
+  }
+  return static_cast<int>(nm.size());
+}
+
+int64_t spec_launch_count(void) {
+  std::lock_guard<std::mutex> g(g_trace_mu);
+  return g_launches;
+}
+
+int spec_ngram_draft(const int32_t *history, const int32_t *hist_len, int B, int hist_stride,
+                     int window, int k, int32_t *draft, int32_t *draft_len, int32_t *status,
+                     void *stream) {
+  if (B < 0 || hist_stride < 0 || window < 1 || window > SPEC_MAX_WINDOW || k < 0 ||
+      k > SPEC_MAX_K)
+    return SPEC_EINVAL;
+  if (B == 0) return SPEC_OK;
+  if (!hist_len || !draft_len || (k > 0 && !draft) || (hist_stride > 0 && !history))
+    return SPEC_EINVAL;
+  if (static_cast<int64_t>(B) > 2147483647LL) return SPEC_EINVAL;
+  NgramParams P{history, hist_len, B, hist_stride, window, k, draft, draft_len, status};
+  const cudaError_t e = launch_ngram(P, as_stream(stream));
+  return e == cudaSuccess ? SPEC_OK : fail_cuda(e, "spec_ngram_draft");
+}
+
+static int chain_common(bool sample, const void *target, int64_t t_req, const void *draftl,
+                        int64_t d_req, int64_t row, int dtype, int B, int k, int V, float T,
+                        const int32_t *draft, const int32_t *draft_len, const int32_t *max_emit,
+                        const float *uniforms, int32_t *accepted, int32_t *out_tokens,
+                        int32_t *n_emit, float *p_tok, float *q_tok, float *resid_mass,
+                        int32_t *status, void *workspace, size_t workspace_bytes, void *stream) {
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_EDTYPE;
+  if (B < 0 || k < 0 || k > SPEC_MAX_K || V <= 0 || t_req < 0 || d_req < 0 || row < 0)
+    return SPEC_EINVAL;
+  if (sample && !(T > 0.0f && std::isfinite(T))) return SPEC_EINVAL;
+  if (B == 0) return SPEC_OK;
+  if (!target || !accepted || !out_tokens || !n_emit || (k > 0 && !draft)) return SPEC_EINVAL;
+  if (sample && (!uniforms || (k > 0 && !draftl))) return SPEC_EINVAL;
+  const ChainLayout L = chain_layout(sample, B, k, V, dtype);
+  const long long rows = sample ? 2LL * k + 1 : k + 1LL;
+  if (static_cast<long long>(B) * rows * L.nc > 2147483647LL) return SPEC_EINVAL;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+      workspace_bytes < L.total)
+    return SPEC_EWORKSPACE;
+  const int es = elem_size(dtype);
+  const bool vec = aligned16(target) && (!sample || k == 0 || aligned16(draftl)) &&
+                   (t_req * es) % 16 == 0 && (d_req * es) % 16 == 0 && (row * es) % 16 == 0;
+  char *ws = static_cast<char *>(workspace);
+  ChainParams P{};
+  P.target = static_cast<const char *>(target);
+  P.draftl = static_cast<const char *>(draftl);
+  P.t_req = t_req;
+  P.d_req = d_req;
+  P.row = row;
+  P.dtype = dtype;
+  P.B = B;
+  P.k = k;
+  P.V = V;
+  P.nc = L.nc;
+  P.chunk = L.chunk;
+  P.c = sample ? static_cast<float>(1.4426950408889634 / static_cast<double>(T)) : 1.0f;
+  P.draft = draft;
+  P.draft_len = draft_len;
+  P.max_emit = max_emit;
+  P.uniforms = uniforms;
+  P.accepted = accepted;
+  P.out_tokens = out_tokens;
+  P.n_emit = n_emit;
+  P.status = status;
+  P.p_tok = p_tok;
+  P.q_tok = q_tok;
+  P.resid_mass = resid_mass;
+  P.counter2 = reinterpret_cast<int *>(ws + L.counter2);
+  P.part = reinterpret_cast<Partial *>(ws + L.part);
+  P.part2 = reinterpret_cast<float *>(ws + L.part2);
+  const cudaError_t e = launch_chain(P, sample, vec, as_stream(stream));
+  return e == cudaSuccess ? SPEC_OK : fail_cuda(e, sample ? "spec_verify_sample" : "spec_verify_greedy");
+}
+
+int spec_verify_greedy(const void *target, int64_t target_req_stride, int64_t row_stride,
+                       int dtype, int B, int k, int V, const int32_t *draft,
+                       const int32_t *draft_len, const int32_t *max_emit, int32_t *accepted,
+                       int32_t *out_tokens, int32_t *n_emit, int32_t *status, void *workspace,
+                       size_t workspace_bytes, void *stream) {
+  return chain_common(false, target, target_req_stride, nullptr, 0, row_stride, dtype, B, k, V,
+                      1.0f, draft, draft_len, max_emit, nullptr, accepted, out_tokens, n_emit,
+                      nullptr, nullptr, nullptr, status, workspace, workspace_bytes, stream);
+}
+
+int spec_verify_sample(const void *target, int64_t target_req_stride, const void *draft_logits,
+                       int64_t draft_req_stride, int64_t row_stride, int dtype, int B, int k,
+                       int V, float temperature, const int32_t *draft, const int32_t *draft_len,
+                       const int32_t *max_emit, const float *uniforms, int32_t *accepted,
+                       int32_t *out_tokens, int32_t *n_emit, float *p_tok, float *q_tok,
+                       float *resid_mass, int32_t *status, void *workspace,
+                       size_t workspace_bytes, void *stream) {
+  return chain_common(true, target, target_req_stride, draft_logits, draft_req_stride,
+                      row_stride, dtype, B, k, V, temperature, draft, draft_len, max_emit,
+                      uniforms, accepted, out_tokens, n_emit, p_tok, q_tok, resid_mass, status,
+                      workspace, workspace_bytes, stream);
+}
+
+int spec_verify_tree(const void *target, int64_t target_req_stride, const void *draft_logits,
+                     int64_t draft_req_stride, int64_t row_stride, int dtype, int B, int N,
+                     int V, float temperature, const int32_t *parents, const int32_t *node_tok,
+                     const float *uniforms, int max_depth, int32_t *accepted_len,
+                     int32_t *path_nodes, int32_t *out_tokens, int32_t *n_emit,
+                     int32_t *status, void *workspace, size_t workspace_bytes, void *stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_EDTYPE;
+  if (std::isnan(temperature)) return SPEC_EINVAL;
+  const bool greedy = !(temperature > 0.0f);
+  if (B < 0 || N < 1 || N > SPEC_MAX_NODES || V <= 0 || max_depth < 0 ||
+      max_depth > SPEC_MAX_DEPTH || target_req_stride < 0 || draft_req_stride < 0 ||
+      row_stride < 0 || (!greedy && !std::isfinite(temperature)))
+    return SPEC_EINVAL;
+  if (B == 0) return SPEC_OK;
+  if (!target || !parents || !node_tok || !uniforms || !accepted_len || !path_nodes ||
+      !out_tokens || !n_emit || (!greedy && !draft_logits))
+    return SPEC_EINVAL;
+  if (B > 2147483647 / 16) return SPEC_EINVAL;
+  const int es = elem_size(dtype);
+  const bool vec = aligned16(target) && (greedy || aligned16(draft_logits)) &&
+                   (target_req_stride * es) % 16 == 0 && (draft_req_stride * es) % 16 == 0 &&
+                   (row_stride * es) % 16 == 0;
+  TreeParams P{};
+  P.target = static_cast<const char *>(target);
+  P.draftl = static_cast<const char *>(draft_logits);
+  P.t_req = target_req_stride;
+  P.d_req = draft_req_stride;
+  P.row = row_stride;
+  P.dtype = dtype;
+  P.B = B;
+  P.N = N;
+  P.V = V;
+  P.max_depth = max_depth;
+  tree_geometry(V, P.cluster, P.slice);
+  P.c = greedy ? 1.0f : static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  P.greedy = greedy ? 1 : 0;
+  P.parents = parents;
+  P.node_tok = node_tok;
+  P.uniforms = uniforms;
+  P.accepted_len = accepted_len;
+  P.path_nodes = path_nodes;
+  P.out_tokens = out_tokens;
+  P.n_emit = n_emit;
+  P.status = status;
+  const cudaError_t e = launch_tree(P, vec, as_stream(stream));
+  return e == cudaSuccess ? SPEC_OK : fail_cuda(e, "spec_verify_tree");
+}
+
+}  // extern "C"

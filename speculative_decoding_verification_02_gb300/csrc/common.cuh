@@ -1,0 +1,392 @@
+// Device helpers shared by the verification kernels (sm_103a).
+//
+// Numerics: logits are widened exactly to fp32 (bf16 is the top half of an
+// fp32); every exponential is 2^((x - M) * c) with c = log2(e) / T, computed
+// by the hardware ex2.approx unit; sums accumulate in fp32.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "spec_verify.h"
+
+namespace sv {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kNoIndex = 0x7fffffff;
+
+// Per-(row, chunk) statistics written by the streaming pass:
+// m = max logit, s = sum 2^((x - m) * c) over the chunk, idx = first argmax.
+struct __align__(16) Partial {
+  float m;
+  float s;
+  int idx;
+  int pad;
+};
+
+// ---------------------------------------------------------------- loads
+
+// 16-byte streaming load that does not allocate in L1 (rows are read once).
+__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Element v of a row, widened to fp32.
+template <int DT>
+__device__ __forceinline__ float load_one(const char *row, int64_t v) {
+  if (DT == SPEC_DTYPE_F32) return __ldg(reinterpret_cast<const float *>(row) + v);
+  const unsigned short h = __ldg(reinterpret_cast<const unsigned short *>(row) + v);
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// Unpack one 16-byte group: 8 bf16 or 4 fp32 values.
+template <int DT>
+__device__ __forceinline__ void unpack16(const uint4 &g, float *x) {
+  if (DT == SPEC_DTYPE_F32) {
+    x[0] = __uint_as_float(g.x);
+    x[1] = __uint_as_float(g.y);
+    x[2] = __uint_as_float(g.z);
+    x[3] = __uint_as_float(g.w);
+  } else {
+    x[0] = bf16_lo(g.x); x[1] = bf16_hi(g.x);
+    x[2] = bf16_lo(g.y); x[3] = bf16_hi(g.y);
+    x[4] = bf16_lo(g.z); x[5] = bf16_hi(g.z);
+    x[6] = bf16_lo(g.w); x[7] = bf16_hi(g.w);
+  }
+}
+
+template <int DT>
+struct Elems {
+  static constexpr int kSize = DT == SPEC_DTYPE_F32 ? 4 : 2;  // bytes per logit
+  static constexpr int kPerGroup = 16 / kSize;                // logits per 16-byte group
+};
+
+// ------------------------------------------------------------- arithmetic
+
+// 2^x on the special-function unit (x = -inf gives +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Merge (m2, s2, i2) into (m, s, i): the running max, the sum rescaled to the
+// new max, and the first index of the max (ties keep the lower index).
+__device__ __forceinline__ void merge_stats(float &m, float &s, int &i, float m2, float s2, int i2,
+                                            float c) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) {
+    s = 0.0f;
+  } else {
+    s = s * ex2((m - M) * c) + s2 * ex2((m2 - M) * c);
+  }
+  i = (m > m2) ? i : (m2 > m) ? i2 : min(i, i2);
+  m = M;
+}
+
+__device__ __forceinline__ void merge_argmax(float &m, int &i, float m2, int i2) {
+  i = (m > m2) ? i : (m2 > m) ? i2 : min(i, i2);
+  m = fmaxf(m, m2);
+}
+
+__device__ __forceinline__ void warp_merge_stats(float &m, float &s, int &i, float c) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+    merge_stats(m, s, i, m2, s2, i2, c);
+  }
+}
+
+__device__ __forceinline__ void warp_merge_argmax(float &m, int &i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+    merge_argmax(m, i, m2, i2);
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_inclusive_scan(float v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+// --------------------------------------------------- weighted row selection
+
+// Weight of element v in an inverse-CDF draw over one row (a) or a row pair
+// (a, b):  w_v = max(0, alpha * 2^((a_v - Ma) c) - beta * 2^((b_v - Mb) c)).
+// beta = 0 (and b = nullptr) draws from the row's own softmax.
+struct Weights {
+  const char *a;
+  const char *b;
+  float Ma, Mb, alpha, beta, c;
+};
+
+template <int DT>
+__device__ __forceinline__ float weight_at(const Weights &W, float a, float b) {
+  float w = W.alpha * ex2((a - W.Ma) * W.c);
+  if (W.b != nullptr) w -= W.beta * ex2((b - W.Mb) * W.c);
+  return fmaxf(w, 0.0f);
+}
+
+// The eight weights of elements [v0, v0 + 8) (those >= hi are 0).
+template <int DT, bool VEC>
+__device__ __forceinline__ void weights8(const Weights &W, int v0, int hi, float *w) {
+  float a[8], b[8];
+  if (VEC && v0 + 8 <= hi) {
+    if (DT == SPEC_DTYPE_F32) {
+      unpack16<DT>(*reinterpret_cast<const uint4 *>(W.a + static_cast<int64_t>(v0) * 4), a);
+      unpack16<DT>(*reinterpret_cast<const uint4 *>(W.a + static_cast<int64_t>(v0) * 4 + 16), a + 4);
+      if (W.b != nullptr) {
+        unpack16<DT>(*reinterpret_cast<const uint4 *>(W.b + static_cast<int64_t>(v0) * 4), b);
+        unpack16<DT>(*reinterpret_cast<const uint4 *>(W.b + static_cast<int64_t>(v0) * 4 + 16), b + 4);
+      }
+    } else {
+      unpack16<DT>(*reinterpret_cast<const uint4 *>(W.a + static_cast<int64_t>(v0) * 2), a);
+      if (W.b != nullptr)
+        unpack16<DT>(*reinterpret_cast<const uint4 *>(W.b + static_cast<int64_t>(v0) * 2), b);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const bool in = v0 + e < hi;
+      a[e] = in ? load_one<DT>(W.a, v0 + e) : -INFINITY;
+      b[e] = (in && W.b != nullptr) ? load_one<DT>(W.b, v0 + e) : -INFINITY;
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) w[e] = (v0 + e < hi) ? weight_at<DT>(W, a[e], b[e]) : 0.0f;
+}
+
+// Block-wide inverse-CDF selection inside [lo, hi): the smallest v with
+// (sum of w over [lo, v]) > thr.  If rounding leaves no such v, the last v in
+// the range with w > 0 (or -1 when every weight is 0).  lo must be a
+// multiple of 8.  Called by all kThreads threads; returns the same value in
+// every thread.
+template <int DT, bool VEC>
+__device__ int block_select(const Weights &W, int lo, int hi, float thr) {
+  __shared__ float s_wsum[kWarps];
+  __shared__ int s_pick, s_last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ntiles = (hi - lo + 255) / 256;  // 32 lanes x 8 elements per tile
+  const int tpw = (ntiles + kWarps - 1) / kWarps;
+  const int t0 = warp * tpw, t1 = min(ntiles, t0 + tpw);
+  if (threadIdx.x == 0) {
+    s_pick = kNoIndex;
+    s_last = -1;
+  }
+  // pass 1: each warp's total
+  float acc = 0.0f;
+  for (int t = t0; t < t1; ++t) {
+    float w[8];
+    weights8<DT, VEC>(W, lo + t * 256 + lane * 8, hi, w);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc += w[e];
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) s_wsum[warp] = acc;
+  __syncthreads();
+  float carry = 0.0f;
+  for (int i = 0; i < warp; ++i) carry += s_wsum[i];
+  // pass 2: walk tiles with a running prefix; first crossing wins
+  int last_pos = -1;
+  for (int t = t0; t < t1; ++t) {
+    const int v0 = lo + t * 256 + lane * 8;
+    float w[8];
+    weights8<DT, VEC>(W, v0, hi, w);
+    float ls = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      ls += w[e];
+      if (w[e] > 0.0f) last_pos = v0 + e;
+    }
+    const float incl = warp_inclusive_scan(ls, lane);
+    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = 0.0f;
+    const unsigned cross = __ballot_sync(0xffffffffu, carry + incl > thr);
+    if (cross) {
+      const int first = __ffs(cross) - 1;
+      if (lane == first) {
+        float run = carry + excl;
+        int pick = -1, lastp = -1;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          run += w[e];
+          if (w[e] > 0.0f) lastp = v0 + e;
+          if (pick < 0 && run > thr) pick = v0 + e;
+        }
+        if (pick < 0) pick = lastp >= 0 ? lastp : v0;
+        atomicMin(&s_pick, pick);
+      }
+      break;
+    }
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  // fallback: the last element with positive weight
+  for (int o = 16; o > 0; o >>= 1) last_pos = max(last_pos, __shfl_xor_sync(0xffffffffu, last_pos, o));
+  if (lane == 0) atomicMax(&s_last, last_pos);
+  __syncthreads();
+  const int r = s_pick != kNoIndex ? s_pick : s_last;
+  __syncthreads();
+  return r;
+}
+
+// ------------------------------------------------------------ streaming
+
+constexpr int kBatch = 4;  // 16-byte groups each thread keeps in flight
+
+// Load flavours: a row streamed once (no L1 allocation), a row re-read from
+// L2 by another CTA, a row re-read by the same CTA (L1 allocation).
+enum : int { kLoadStream = 0, kLoadL2 = 1, kLoadCached = 2 };
+
+template <int LD>
+__device__ __forceinline__ uint4 load16(const uint4 *p) {
+  if (LD == kLoadStream) return ld_stream16(p);
+  if (LD == kLoadL2) return __ldcg(p);
+  return __ldg(p);
+}
+
+// Statistics of row[v0, v1) for the calling thread (strided over the block).
+template <int DT, bool SOFTMAX, bool VEC, int LD>
+__device__ __forceinline__ void thread_chunk_stats(const char *row, int v0, int v1, float c,
+                                                   float &m, float &s, int &idx) {
+  constexpr int EPG = Elems<DT>::kPerGroup;
+  constexpr int ES = Elems<DT>::kSize;
+  int vtail = v0;
+  if (VEC) {
+    const int ng = (v1 - v0) / EPG;
+    const uint4 *base = reinterpret_cast<const uint4 *>(row + static_cast<int64_t>(v0) * ES);
+    for (int g0 = threadIdx.x; g0 < ng; g0 += kThreads * kBatch) {
+      uint4 g[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int gi = g0 + u * kThreads;
+        if (gi < ng) g[u] = load16<LD>(base + gi);
+      }
+      float x[kBatch][EPG];
+      float bm = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int gi = g0 + u * kThreads;
+        if (gi < ng) {
+          unpack16<DT>(g[u], x[u]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < EPG; ++e) x[u][e] = -INFINITY;
+        }
+#pragma unroll
+        for (int e = 0; e < EPG; ++e) bm = fmaxf(bm, x[u][e]);
+      }
+      if (bm > m) {  // a new running max: rescale the sum, find its first index
+        if (SOFTMAX) s *= ex2((m - bm) * c);
+        m = bm;
+        int first = kNoIndex;
+#pragma unroll
+        for (int u = kBatch - 1; u >= 0; --u)
+#pragma unroll
+          for (int e = EPG - 1; e >= 0; --e)
+            if (x[u][e] == bm) first = v0 + (g0 + u * kThreads) * EPG + e;
+        idx = first;
+      }
+      if (SOFTMAX && m != -INFINITY) {
+        const float mc = m * c;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+#pragma unroll
+          for (int e = 0; e < EPG; ++e) s += ex2(fmaf(x[u][e], c, -mc));
+      }
+    }
+    vtail = v0 + ng * EPG;
+  }
+  for (int v = vtail + threadIdx.x; v < v1; v += kThreads) {
+    const float x = load_one<DT>(row, v);
+    if (x > m) {
+      if (SOFTMAX) s *= ex2((m - x) * c);
+      m = x;
+      idx = v;
+    }
+    if (SOFTMAX && m != -INFINITY) s += ex2((x - m) * c);
+  }
+}
+
+// Block-wide merge; the result is valid in thread 0.
+template <bool SOFTMAX>
+__device__ __forceinline__ void block_merge(float &m, float &s, int &idx, float c) {
+  __shared__ float sm[kWarps], ss[kWarps];
+  __shared__ int si[kWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (SOFTMAX) warp_merge_stats(m, s, idx, c); else warp_merge_argmax(m, idx);
+  if (lane == 0) {
+    sm[warp] = m;
+    ss[warp] = s;
+    si[warp] = idx;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    m = lane < kWarps ? sm[lane] : -INFINITY;
+    s = lane < kWarps ? ss[lane] : 0.0f;
+    idx = lane < kWarps ? si[lane] : kNoIndex;
+    if (SOFTMAX) warp_merge_stats(m, s, idx, c); else warp_merge_argmax(m, idx);
+  }
+}
+
+template <int DT, bool VEC, int LD>
+__device__ __forceinline__ float thread_chunk_weight_sum(const Weights &W, int v0, int v1) {
+  constexpr int EPG = Elems<DT>::kPerGroup;
+  constexpr int ES = Elems<DT>::kSize;
+  float acc = 0.0f;
+  int vtail = v0;
+  if (VEC) {
+    const int ng = (v1 - v0) / EPG;
+    const uint4 *ga = reinterpret_cast<const uint4 *>(W.a + static_cast<int64_t>(v0) * ES);
+    const uint4 *gb = reinterpret_cast<const uint4 *>(W.b + static_cast<int64_t>(v0) * ES);
+    for (int g0 = threadIdx.x; g0 < ng; g0 += kThreads * kBatch) {
+      uint4 A[kBatch], Bv[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int gi = g0 + u * kThreads;
+        if (gi < ng) {
+          A[u] = load16<LD>(ga + gi);
+          Bv[u] = load16<LD>(gb + gi);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        if (g0 + u * kThreads < ng) {
+          float a[EPG], bb[EPG];
+          unpack16<DT>(A[u], a);
+          unpack16<DT>(Bv[u], bb);
+#pragma unroll
+          for (int e = 0; e < EPG; ++e) acc += weight_at<DT>(W, a[e], bb[e]);
+        }
+      }
+    }
+    vtail = v0 + ng * EPG;
+  }
+  for (int v = vtail + threadIdx.x; v < v1; v += kThreads)
+    acc += weight_at<DT>(W, load_one<DT>(W.a, v), load_one<DT>(W.b, v));
+  return acc;
+}
+
+
+}  // namespace sv

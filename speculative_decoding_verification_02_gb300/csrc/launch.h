@@ -1,0 +1,81 @@
+// Host-side parameter blocks and launchers shared by the .cu files of the
+// library.  Not part of the public ABI (that is include/spec_verify.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "spec_verify.h"
+
+namespace sv {
+
+struct Partial;
+
+struct ChainParams {
+  const char *target;
+  const char *draftl;
+  int64_t t_req, d_req, row;  // element strides
+  int dtype, B, k, V;
+  int nc, chunk;    // chunks per row, logits per chunk (both passes)
+  float c;          // log2(e) / T
+  const int32_t *draft, *draft_len, *max_emit;
+  const float *uniforms;
+  int32_t *accepted, *out_tokens, *n_emit, *status;
+  float *p_tok, *q_tok, *resid_mass;
+  Partial *part;     // [B][rows][nc] streaming-pass statistics
+  float *part2;      // [B][nc] residual mass per chunk
+  int *counter2;     // [B] arrival counter of the residual pass
+};
+
+struct TreeParams {
+  const char *target;
+  const char *draftl;
+  int64_t t_req, d_req, row;
+  int dtype, B, N, V, max_depth;
+  int cluster;     // CTAs per request
+  int slice;       // logits per CTA (multiple of 8)
+  float c;         // log2(e) / T; unused when greedy
+  int greedy;
+  const int32_t *parents, *node_tok;
+  const float *uniforms;
+  int32_t *accepted_len, *path_nodes, *out_tokens, *n_emit, *status;
+};
+
+struct NgramParams {
+  const int32_t *history, *hist_len;
+  int B, hist_stride, window, k;
+  int32_t *draft, *draft_len, *status;
+};
+
+cudaError_t launch_chain(const ChainParams &P, bool sample, bool vec, cudaStream_t st);
+cudaError_t launch_tree(const TreeParams &P, bool vec, cudaStream_t st);
+cudaError_t launch_ngram(const NgramParams &P, cudaStream_t st);
+
+// Tracing hooks (api.cu).  trace_begin returns a slot (or -1 when tracing is
+// off); trace_end records the closing event of that slot.
+int trace_begin(const char *name, cudaStream_t st);
+void trace_end(int slot, cudaStream_t st);
+void count_launch();
+
+template <class F>
+cudaError_t trace_launch(const char *name, cudaStream_t st, F &&launch) {
+  const int slot = trace_begin(name, st);
+  launch();
+  const cudaError_t e = cudaGetLastError();
+  trace_end(slot, st);
+  count_launch();
+  return e;
+}
+
+template <class F>
+cudaError_t trace_launch_ex(const char *name, cudaStream_t st, F &&launch) {
+  const int slot = trace_begin(name, st);
+  cudaError_t e = launch();
+  if (e == cudaSuccess) e = cudaGetLastError();
+  trace_end(slot, st);
+  count_launch();
+  return e;
+}
+
+}  // namespace sv

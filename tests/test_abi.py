@@ -1,0 +1,131 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, and rejects bad arguments on the host before launching."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from speculative_decoding_verification_02_gb300 import api, build
+    build.build()
+    return api.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_four_entry_points():
+    names = _declared()
+    for n in ("spec_ngram_draft", "spec_verify_greedy", "spec_verify_sample", "spec_verify_tree"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+
+
+def test_header_constants_match_binding():
+    from speculative_decoding_verification_02_gb300 import api
+    text = open(HEADER).read()
+    consts = dict(re.findall(r"#define (SPEC_\w+) \(?(-?\d+)\)?", text))
+    assert int(consts["SPEC_OK"]) == api.SPEC_OK and int(consts["SPEC_EINVAL"]) == api.SPEC_EINVAL
+    assert int(consts["SPEC_EDTYPE"]) == api.SPEC_EDTYPE
+    assert int(consts["SPEC_EWORKSPACE"]) == api.SPEC_EWORKSPACE
+    assert int(consts["SPEC_ECUDA"]) == api.SPEC_ECUDA
+    assert int(consts["SPEC_DTYPE_BF16"]) == api.DTYPE_BF16
+    assert int(consts["SPEC_STATUS_BAD_TREE"]) == api.STATUS_BAD_TREE
+
+
+FAKE = ctypes.c_void_p(0x10000)   # never dereferenced: every call below fails validation
+
+
+def _sample(L, **kw):
+    a = dict(target=FAKE, t_req=5 * 1024, draft=FAKE, d_req=4 * 1024, row=1024, dtype=1, B=2, k=4,
+             V=1024, T=1.0, x=FAKE, dlen=None, maxe=None, u=FAKE, acc=FAKE, out=FAKE, ne=FAKE,
+             pt=None, qt=None, rm=None, st=FAKE, ws=ctypes.c_void_p(0x100000), wsb=1 << 30, stream=None)
+    a.update(kw)
+    return L.spec_verify_sample(*a.values())
+
+
+def test_sample_argument_checks(L):
+    from speculative_decoding_verification_02_gb300 import api
+    n0 = L.spec_launch_count()
+    assert _sample(L, dtype=7) == api.SPEC_EDTYPE
+    assert _sample(L, B=-1) == api.SPEC_EINVAL
+    assert _sample(L, k=65) == api.SPEC_EINVAL
+    assert _sample(L, V=0) == api.SPEC_EINVAL
+    assert _sample(L, T=0.0) == api.SPEC_EINVAL
+    assert _sample(L, T=float("inf")) == api.SPEC_EINVAL
+    assert _sample(L, T=float("nan")) == api.SPEC_EINVAL
+    assert _sample(L, target=None) == api.SPEC_EINVAL
+    assert _sample(L, u=None) == api.SPEC_EINVAL
+    assert _sample(L, row=-1) == api.SPEC_EINVAL
+    assert _sample(L, ws=None) == api.SPEC_EWORKSPACE
+    assert _sample(L, ws=ctypes.c_void_p(0x100010)) == api.SPEC_EWORKSPACE       # misaligned
+    assert _sample(L, wsb=16) == api.SPEC_EWORKSPACE                             # too small
+    assert _sample(L, B=0) == api.SPEC_OK                                        # nothing to do
+    assert L.spec_launch_count() == n0                                           # nothing launched
+
+
+def test_greedy_tree_ngram_argument_checks(L):
+    from speculative_decoding_verification_02_gb300 import api
+    n0 = L.spec_launch_count()
+    ws = ctypes.c_void_p(0x100000)
+    assert L.spec_verify_greedy(FAKE, 0, 0, 0, 1, 2, 0, FAKE, None, None, FAKE, FAKE, FAKE, None, ws,
+                                1 << 20, None) == api.SPEC_EINVAL
+    assert L.spec_verify_greedy(FAKE, 0, 0, 3, 1, 2, 10, FAKE, None, None, FAKE, FAKE, FAKE, None, ws,
+                                1 << 20, None) == api.SPEC_EDTYPE
+    assert L.spec_verify_greedy(None, 0, 0, 0, 1, 2, 10, FAKE, None, None, FAKE, FAKE, FAKE, None, ws,
+                                1 << 20, None) == api.SPEC_EINVAL
+    tree = lambda **kw: L.spec_verify_tree(*dict(dict(t=FAKE, tr=0, d=FAKE, dr=0, r=64, dt=0, B=1, N=4, V=64,
+                                                      T=1.0, par=FAKE, tok=FAKE, u=FAKE, md=3, al=FAKE,
+                                                      pn=FAKE, ot=FAKE, ne=FAKE, st=FAKE, ws=None, wb=0,
+                                                      s=None), **kw).values())
+    assert tree(N=0) == api.SPEC_EINVAL
+    assert tree(N=4097) == api.SPEC_EINVAL
+    assert tree(md=65) == api.SPEC_EINVAL
+    assert tree(md=-1) == api.SPEC_EINVAL
+    assert tree(T=float("nan")) == api.SPEC_EINVAL
+    assert tree(d=None) == api.SPEC_EINVAL            # sampling needs draft logits
+    assert tree(par=None) == api.SPEC_EINVAL
+    assert tree(dt=9) == api.SPEC_EDTYPE
+    assert tree(B=0) == api.SPEC_OK
+    ng = lambda **kw: L.spec_ngram_draft(*dict(dict(h=FAKE, hl=FAKE, B=2, hs=16, w=3, k=4, d=FAKE, dl=FAKE,
+                                                    st=None, s=None), **kw).values())
+    assert ng(w=0) == api.SPEC_EINVAL
+    assert ng(w=65) == api.SPEC_EINVAL
+    assert ng(k=65) == api.SPEC_EINVAL
+    assert ng(hl=None) == api.SPEC_EINVAL
+    assert ng(B=0) == api.SPEC_OK
+    assert L.spec_launch_count() == n0
+
+
+def test_workspace_sizes(L):
+    from speculative_decoding_verification_02_gb300 import api
+    s1 = L.spec_workspace_size(api.OP_SAMPLE, 1, 4, 248320, 1)
+    s64 = L.spec_workspace_size(api.OP_SAMPLE, 64, 8, 128256, 1)
+    assert 0 < s1 < s64 and s1 % 256 == 0 and s64 % 256 == 0
+    assert L.spec_workspace_size(api.OP_GREEDY, 64, 4, 32000, 0) > 0
+    assert L.spec_workspace_size(api.OP_TREE, 16, 60, 128256, 1) == 0
+    assert L.spec_workspace_size(api.OP_SAMPLE, -1, 4, 10, 1) == 0
+    assert L.spec_workspace_size(api.OP_SAMPLE, 1, 4, 10, 5) == 0
+    # the streaming pass keeps 16 bytes per (row, 16 KB chunk): small next to the logits
+    assert s64 < 0.01 * 64 * 17 * 128256 * 2
+
+
+def test_status_strings(L):
+    assert L.spec_status_string(0) == b"ok"
+    assert b"workspace" in L.spec_status_string(-3)
+    assert b"tree" in L.spec_status_string(102)
+    assert L.spec_last_error() is not None
