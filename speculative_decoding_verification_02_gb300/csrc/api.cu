@@ -30,9 +30,21 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // ------------------------------------------------------------ geometry
 
-// Logits per CTA of the streaming pass: 16 KB of one row.  The residual
-// pass uses the same chunks (16 KB of each row of the pair).
-int stream_chunk(int dtype) { return 16384 / elem_size(dtype); }
+// Logits per CTA of the streaming pass (the residual pass uses the same
+// chunks).  Sized from the call's total bytes so that the grid is about four
+// waves of four CTAs on each of the GB300's 152 SMs, between 8 KB and 64 KB
+// of one row: small calls spread over every SM, large ones keep each CTA
+// streaming long enough to amortise its start-up and reduction.
+constexpr long long kSmCount = 152;
+
+int stream_chunk(int dtype, long long rows_total, int V) {
+  const long long es = elem_size(dtype);
+  const long long target_ctas = kSmCount * 4 * 4;
+  const long long per = rows_total * V * es / target_ctas;
+  long long bytes = 8192;
+  while (bytes < per && bytes < 65536) bytes *= 2;
+  return static_cast<int>(bytes / es);
+}
 
 // Workspace: per-(row, chunk) statistics, then for sampling the residual
 // mass per chunk and one arrival counter per request.  Nothing in it needs
@@ -44,7 +56,7 @@ struct ChainLayout {
 
 ChainLayout chain_layout(bool sample, int B, int k, int V, int dtype) {
   ChainLayout L{};
-  L.chunk = stream_chunk(dtype);
+  L.chunk = stream_chunk(dtype, static_cast<long long>(B) * (sample ? 2LL * k + 1 : k + 1LL), V);
   L.nc = (V + L.chunk - 1) / L.chunk;
   const size_t rows = sample ? 2 * static_cast<size_t>(k) + 1 : static_cast<size_t>(k) + 1;
   size_t off = 0;

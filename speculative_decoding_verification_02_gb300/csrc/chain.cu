@@ -1,10 +1,12 @@
 // Chain verification kernels: greedy prefix acceptance and lossless sampling
-// acceptance with residual resampling.  Two launches per call:
+// acceptance with residual resampling.  Two launches per call, the second
+// one a programmatic dependent launch of the first:
 //
 // chain_stats_kernel  one CTA per (request, row, V-chunk).  Streams the chunk
 //     once with 16-byte loads, keeps a running max / sum 2^((x - max) c) /
 //     first argmax per thread, reduces through warp shuffles and shared
-//     memory, and writes one Partial to the workspace.
+//     memory, and writes one Partial to the workspace, together with the
+//     logit of the row's drafted token when that token falls in the chunk.
 //
 // chain_greedy_accept_kernel  one CTA per request: merges the partials of
 //     target rows 0..L into argmaxes and accepts x_i while x_i == argmax(row
@@ -16,14 +18,15 @@
 //     them reach the same decision: p_i(x_i), q_i(x_i), accept while
 //     u_i q_i(x_i) < p_i(x_i), i.e. u_i < min(1, p/q)
 //     ("投机解码:为什么一个字都不改", 改进方案).  Then
-//       all accepted  the bonus token is drawn from p_L: the chunk holding
-//                     u * sum is found from the streaming pass's chunk
-//                     totals and only that CTA scans its chunk;
+//       all accepted  the bonus token is drawn from p_L: one warp finds the
+//                     chunk holding u * sum from the chunk totals, and only
+//                     the CTA of that chunk scans it;
 //       rejected at m every CTA adds up max(0, p_m - q_m) over its chunk;
-//                     the last to finish (an arrival counter that the
-//                     stats kernel zeroed, so the workspace needs no
+//                     the last to finish (an arrival counter that the stats
+//                     kernel zeroed, so the workspace needs no
 //                     initialisation) picks the chunk where u * R falls and
 //                     scans it: a draw from norm(max(0, p - q)).
+// Both accept kernels read their inputs before waiting on the stats grid.
 // No kernel waits on another CTA.
 #include "common.cuh"
 #include "launch.h"
@@ -31,10 +34,11 @@
 namespace sv {
 
 constexpr int kMaxRows = 2 * SPEC_MAX_K + 1;
+constexpr int kPickCache = 512;  // chunk weights kept in shared memory by warp_pick
 
 __device__ __forceinline__ Partial ld_partial(const Partial *p) {
   const float4 v = __ldcg(reinterpret_cast<const float4 *>(p));
-  return Partial{v.x, v.y, __float_as_int(v.z), 0};
+  return Partial{v.x, v.y, __float_as_int(v.z), v.w};
 }
 
 template <int DT>
@@ -48,6 +52,7 @@ __device__ __forceinline__ const char *row_ptr(const char *base, int64_t req_str
 
 template <int DT, bool SOFTMAX, bool VEC>
 __global__ void __launch_bounds__(kThreads) chain_stats_kernel(const ChainParams P) {
+  pdl_launch_dependents();
   const int rows = SOFTMAX ? 2 * P.k + 1 : P.k + 1;
   const int per_req = rows * P.nc;
   const int b = blockIdx.x / per_req;
@@ -57,205 +62,275 @@ __global__ void __launch_bounds__(kThreads) chain_stats_kernel(const ChainParams
   const int L = P.draft_len ? P.draft_len[b] : P.k;
   if (L < 0 || L > P.k) return;  // reported by the accept kernel
   const char *row;
+  int pos;
   if (r <= P.k) {
     if (r > L) return;
+    pos = r;
     row = row_ptr<DT>(P.target, P.t_req, P.row, b, r);
   } else {
-    if (r - P.k - 1 >= L) return;
-    row = row_ptr<DT>(P.draftl, P.d_req, P.row, b, r - P.k - 1);
+    pos = r - P.k - 1;
+    if (pos >= L) return;
+    row = row_ptr<DT>(P.draftl, P.d_req, P.row, b, pos);
+  }
+  const int v0 = j * P.chunk, v1 = min(P.V, v0 + P.chunk);
+  // the logit of this row's drafted token, if it lies in this chunk
+  float xt = -INFINITY;
+  if (SOFTMAX && threadIdx.x == 0 && pos < L) {
+    const int t = P.draft[static_cast<int64_t>(b) * P.k + pos];
+    if (t >= v0 && t < v1) xt = load_one<DT>(row, t);
   }
   float m = -INFINITY, s = 0.0f;
   int idx = kNoIndex;
-  const int v0 = j * P.chunk, v1 = min(P.V, v0 + P.chunk);
   thread_chunk_stats<DT, SOFTMAX, VEC, kLoadStream>(row, v0, v1, P.c, m, s, idx);
   block_merge<SOFTMAX>(m, s, idx, P.c);
   if (threadIdx.x == 0)
     *reinterpret_cast<float4 *>(P.part + (static_cast<int64_t>(b) * rows + r) * P.nc + j) =
-        make_float4(m, s, __int_as_float(idx), 0.0f);
+        make_float4(m, s, __int_as_float(idx), xt);
 }
 
 // --------------------------------------------------------------- accept scan
 
-// What every CTA of a request knows after the merge.
-struct Verdict {
-  int bad;      // SPEC_STATUS_* (0 = fine)
-  int L, m, ne;
-  int final_tok;  // greedy: argmax(row m)
+// Inputs of one request, read before the dependency wait.
+struct Prologue {
+  int L, bad, cap;
 };
 
-// Merges the request's partials (target rows 0..L, then for sampling draft
-// rows 0..L-1) and runs the accept scan.  Called by all threads of a CTA;
-// the row statistics are left in sM / sS / sA, and for sampling sXT / sXD
-// hold p_i(x_i) / q_i(x_i).
-template <int DT, bool SAMPLE>
-__device__ Verdict accept_scan(const ChainParams &P, int b, float *sM, float *sS, int *sA,
-                               float *sXT, float *sXD, int *sTok) {
-  __shared__ Verdict sv;
-  __shared__ int s_bad;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int k = P.k;
-  const int rows = SAMPLE ? 2 * k + 1 : k + 1;
-  const int L = P.draft_len ? P.draft_len[b] : k;
-  const bool len_ok = L >= 0 && L <= k;
-  if (tid == 0) s_bad = len_ok ? SPEC_STATUS_OK : SPEC_STATUS_BAD_LENGTH;
-  __syncthreads();
-  if (len_ok && tid < L) {
-    const int t = P.draft[static_cast<int64_t>(b) * k + tid];
-    sTok[tid] = t;
-    if (t < 0 || t >= P.V) atomicMax(&s_bad, SPEC_STATUS_TOKEN_RANGE);
-  }
-  __syncthreads();
-  if (s_bad != SPEC_STATUS_OK) {
-    Verdict v{s_bad, L, 0, 0, -1};
-    __syncthreads();
-    return v;
-  }
-  const int nrows = SAMPLE ? 2 * L + 1 : L + 1;
-  for (int rr = warp; rr < nrows; rr += kWarps) {
-    const int r = rr <= L ? rr : (k + 1) + (rr - L - 1);
-    const Partial *pp = P.part + (static_cast<int64_t>(b) * rows + r) * P.nc;
-    float m = -INFINITY, s = 0.0f;
-    int idx = kNoIndex;
-    for (int j = lane; j < P.nc; j += 32) {
-      const Partial q = ld_partial(pp + j);
-      if (SAMPLE) merge_stats(m, s, idx, q.m, q.s, q.idx, P.c); else merge_argmax(m, idx, q.m, q.idx);
-    }
-    if (SAMPLE) warp_merge_stats(m, s, idx, P.c); else warp_merge_argmax(m, idx);
-    if (lane == 0) {
-      sM[rr] = m;
-      sS[rr] = s;
-      sA[rr] = idx == kNoIndex ? 0 : idx;  // an all -inf row: every index ties, take 0
-    }
-  }
-  if (SAMPLE) {
-    for (int i = tid; i < 2 * L; i += kThreads) {
-      if (i < L)
-        sXT[i] = load_one<DT>(row_ptr<DT>(P.target, P.t_req, P.row, b, i), sTok[i]);
-      else
-        sXD[i - L] = load_one<DT>(row_ptr<DT>(P.draftl, P.d_req, P.row, b, i - L), sTok[i - L]);
-    }
-  }
-  __syncthreads();
+__device__ Prologue read_request(const ChainParams &P, int b, int *sTok, float *sU, bool sample) {
+  __shared__ int s_bad, s_L;
+  const int tid = threadIdx.x, k = P.k;
+  __shared__ int s_cap;
   if (tid == 0) {
-    int m = 0;
-    if (SAMPLE) {
-      const float *u = P.uniforms + static_cast<int64_t>(b) * (k + 1);
-      for (int i = 0; i < L; ++i) {
-        const float p = ex2((sXT[i] - sM[i]) * P.c) / sS[i];
-        const float q = ex2((sXD[i] - sM[L + 1 + i]) * P.c) / sS[L + 1 + i];
-        sXT[i] = p;  // now p_i(x_i)
-        sXD[i] = q;  // and q_i(x_i)
-        if (m == i && u[i] * q < p) m = i + 1;
-      }
-    } else {
-      while (m < L && sA[m] == sTok[m]) ++m;
-    }
-    const int cap = P.max_emit ? P.max_emit[b] : k + 1;
-    sv = Verdict{SPEC_STATUS_OK, L, m, max(0, min(m + 1, cap)), sA[m]};
+    const int L = P.draft_len ? P.draft_len[b] : k;
+    s_L = L;
+    s_bad = (L >= 0 && L <= k) ? SPEC_STATUS_OK : SPEC_STATUS_BAD_LENGTH;
   }
+  if (tid == 32) s_cap = P.max_emit ? P.max_emit[b] : k + 1;
+  if (tid < k) sTok[tid] = P.draft[static_cast<int64_t>(b) * k + tid];
+  if (sample && tid >= 64 && tid <= 64 + k) sU[tid - 64] = P.uniforms[static_cast<int64_t>(b) * (k + 1) + tid - 64];
   __syncthreads();
-  const Verdict v = sv;
+  const int L = s_L;
+  if (s_bad == SPEC_STATUS_OK && tid < L && (sTok[tid] < 0 || sTok[tid] >= P.V))
+    atomicMax(&s_bad, SPEC_STATUS_TOKEN_RANGE);
   __syncthreads();
-  return v;
+  Prologue pr{L, s_bad, s_cap};
+  __syncthreads();
+  return pr;
+}
+
+// Merges the partials of row r with one warp: max, sum 2^((x - max) c),
+// first argmax, and the drafted token's logit (tokchunk = its chunk, or -1).
+template <bool SOFTMAX>
+__device__ __forceinline__ void warp_merge_row(const Partial *pp, int nc, float c, int tokchunk,
+                                               float &M, float &S, int &A, float &X) {
+  const int lane = threadIdx.x & 31;
+  float m = -INFINITY, s = 0.0f, x = -INFINITY;
+  int idx = kNoIndex;
+  for (int j = lane; j < nc; j += 32) {
+    const Partial q = ld_partial(pp + j);
+    if (SOFTMAX) merge_stats(m, s, idx, q.m, q.s, q.idx, c); else merge_argmax(m, idx, q.m, q.idx);
+    if (j == tokchunk) x = q.x;
+  }
+  if (SOFTMAX) warp_merge_stats(m, s, idx, c); else warp_merge_argmax(m, idx);
+  M = m;
+  S = s;
+  A = idx == kNoIndex ? 0 : idx;  // an all -inf row: every index ties, take 0
+  X = tokchunk >= 0 ? __shfl_sync(0xffffffffu, x, tokchunk & 31) : -INFINITY;
+}
+
+// One warp: the index j* in [0, n) where u * (w_0 + ... + w_{n-1}) falls,
+// i.e. the smallest j with w_0 + ... + w_j > u * total, and the threshold
+// relative to the start of chunk j*.  If rounding leaves no such j, the last
+// j with w_j > 0 and an infinite threshold (its last positive element).
+// Lane l owns the contiguous range [l*cpl, (l+1)*cpl); each weight is read
+// once (kept in `cache` when n <= cap).  All lanes return the same values;
+// `total` is the sum of the weights.
+template <class W>
+__device__ __forceinline__ void warp_pick(W weight, int n, float u, float *cache, int cap, int &jsel,
+                                          float &thr_local, float &total) {
+  const int lane = threadIdx.x & 31;
+  const int cpl = (n + 31) / 32;
+  const int j0 = min(n, lane * cpl), j1 = min(n, j0 + cpl);
+  const bool cached = n <= cap;
+  float ls = 0.0f;
+  int lastpos = -1;
+  for (int j = j0; j < j1; ++j) {
+    const float w = weight(j);
+    if (cached) cache[j] = w;
+    ls += w;
+    if (w > 0.0f) lastpos = j;
+  }
+  __syncwarp();
+  const float incl = warp_inclusive_scan(ls, lane);
+  total = __shfl_sync(0xffffffffu, incl, 31);
+  const float thr = u * total;
+  float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) excl = 0.0f;
+  const unsigned cross = __ballot_sync(0xffffffffu, incl > thr);
+  if (cross) {
+    const int first = __ffs(cross) - 1;
+    int pick = -1;
+    float base = 0.0f;
+    if (lane == first) {
+      float run = excl;
+      for (int j = j0; j < j1; ++j) {
+        const float w = cached ? cache[j] : weight(j);
+        if (run + w > thr) {
+          pick = j;
+          base = run;
+          break;
+        }
+        run += w;
+      }
+      if (pick < 0) {  // rounding inside the lane: take its last chunk with mass
+        pick = lastpos >= 0 ? lastpos : j0;
+        base = thr;
+      }
+    }
+    jsel = __shfl_sync(0xffffffffu, pick, first);
+    base = __shfl_sync(0xffffffffu, base, first);
+    thr_local = fmaxf(thr - base, 0.0f);
+  } else {
+    for (int o = 16; o > 0; o >>= 1) lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, o));
+    jsel = max(lastpos, 0);
+    thr_local = INFINITY;
+  }
 }
 
 // The outputs that do not depend on the final draw (written once per request).
 template <bool SAMPLE>
-__device__ void write_common(const ChainParams &P, int b, const Verdict &v, const int *sTok,
-                             const float *sXT, const float *sXD, bool final_known, int final_tok) {
+__device__ void write_common(const ChainParams &P, int b, int bad, int L, int m, int ne,
+                             const int *sTok, const float *sP, const float *sQ, bool final_known,
+                             int final_tok) {
   const int k = P.k;
   int32_t *out = P.out_tokens + static_cast<int64_t>(b) * (k + 1);
   const int tid = threadIdx.x;
-  if (v.bad) {
-    for (int j = tid; j <= k; j += kThreads) out[j] = -1;
-  } else {
-    for (int j = tid; j <= k; j += kThreads) {
-      if (j == v.m && j < v.ne && !final_known) continue;  // the drawing CTA writes it
-      out[j] = j < v.ne ? (j < v.m ? sTok[j] : final_tok) : -1;
+  for (int j = tid; j <= k; j += kThreads) {
+    if (bad) {
+      out[j] = -1;
+    } else {
+      if (j == m && j < ne && !final_known) continue;  // the drawing CTA writes it
+      out[j] = j < ne ? (j < m ? sTok[j] : final_tok) : -1;
     }
   }
   if (SAMPLE) {
     for (int j = tid; j < k; j += kThreads) {
-      const bool ok = !v.bad && j < v.L;
-      if (P.p_tok) P.p_tok[static_cast<int64_t>(b) * k + j] = ok ? sXT[j] : -1.0f;
-      if (P.q_tok) P.q_tok[static_cast<int64_t>(b) * k + j] = ok ? sXD[j] : -1.0f;
+      const bool ok = !bad && j < L;
+      if (P.p_tok) P.p_tok[static_cast<int64_t>(b) * k + j] = ok ? sP[j] : -1.0f;
+      if (P.q_tok) P.q_tok[static_cast<int64_t>(b) * k + j] = ok ? sQ[j] : -1.0f;
     }
   }
   if (tid == 0) {
-    P.accepted[b] = v.bad ? 0 : v.m;
-    P.n_emit[b] = v.bad ? 0 : v.ne;
-    if (P.status) P.status[b] = v.bad;
-    if (SAMPLE && v.bad && P.resid_mass) P.resid_mass[b] = 0.0f;
+    P.accepted[b] = bad ? 0 : m;
+    P.n_emit[b] = bad ? 0 : ne;
+    if (P.status) P.status[b] = bad;
+    if (SAMPLE && bad && P.resid_mass) P.resid_mass[b] = 0.0f;
   }
 }
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads) chain_greedy_accept_kernel(const ChainParams P) {
-  __shared__ float sM[SPEC_MAX_K + 1], sS[SPEC_MAX_K + 1];
   __shared__ int sA[SPEC_MAX_K + 1], sTok[SPEC_MAX_K];
+  __shared__ int s_m;
   const int b = blockIdx.x;
-  const Verdict v = accept_scan<DT, false>(P, b, sM, sS, sA, nullptr, nullptr, sTok);
-  write_common<false>(P, b, v, sTok, nullptr, nullptr, true, v.final_tok);
-}
-
-// Chunk j* of a row's streaming-pass totals where u * total falls; returns
-// the threshold relative to the chunk start (INFINITY when rounding left u *
-// total past the end: the last chunk with mass is taken).
-__device__ __forceinline__ void pick_chunk(const Partial *pp, int nc, float M, float c, float u,
-                                           int &jsel_out, float &thr_out) {
-  float tot = 0.0f;
-  for (int j = 0; j < nc; ++j) {
-    const Partial q = ld_partial(pp + j);
-    tot += q.s * ex2((q.m - M) * c);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const Prologue pr = read_request(P, b, sTok, nullptr, false);
+  pdl_wait();
+  if (pr.bad) {
+    write_common<false>(P, b, pr.bad, pr.L, 0, 0, sTok, nullptr, nullptr, true, -1);
+    return;
   }
-  const float thr = u * tot;
-  float cum = 0.0f, base = 0.0f;
-  int jsel = -1, jlast = 0;
-  for (int j = 0; j < nc; ++j) {
-    const Partial q = ld_partial(pp + j);
-    const float w = q.s * ex2((q.m - M) * c);
-    if (w > 0.0f) jlast = j;
-    if (jsel < 0 && cum + w > thr) {
-      jsel = j;
-      base = cum;
-    }
-    cum += w;
+  const int rows = P.k + 1;
+  for (int r = warp; r <= pr.L; r += kWarps) {
+    float M, S, X;
+    int A;
+    warp_merge_row<false>(P.part + (static_cast<int64_t>(b) * rows + r) * P.nc, P.nc, 1.0f, -1, M, S, A, X);
+    if (lane == 0) sA[r] = A;
   }
-  jsel_out = jsel >= 0 ? jsel : jlast;
-  thr_out = jsel >= 0 ? thr - base : INFINITY;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int m = 0;
+    while (m < pr.L && sA[m] == sTok[m]) ++m;
+    s_m = m;
+  }
+  __syncthreads();
+  const int m = s_m;
+  write_common<false>(P, b, 0, pr.L, m, max(0, min(m + 1, pr.cap)), sTok, nullptr, nullptr, true, sA[m]);
 }
 
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const ChainParams P) {
-  __shared__ float sM[kMaxRows], sS[kMaxRows];
-  __shared__ int sA[kMaxRows], sTok[SPEC_MAX_K];
-  __shared__ float sXT[SPEC_MAX_K], sXD[SPEC_MAX_K];
+  __shared__ float sM[kMaxRows], sS[kMaxRows], sX[kMaxRows];
+  __shared__ int sTok[SPEC_MAX_K];
+  __shared__ float sU[SPEC_MAX_K + 1], sP[SPEC_MAX_K], sQ[SPEC_MAX_K];
   __shared__ float s_red[kWarps];
-  __shared__ int s_last, s_j;
+  __shared__ float s_wcache[kPickCache];
+  __shared__ int s_last, s_j, s_m;
   __shared__ float s_thr, s_tot;
   __shared__ bool s_fallback;
   const int nc = P.nc;
   const int b = blockIdx.x / nc, j = blockIdx.x - b * nc;
   const int k = P.k, rows = 2 * k + 1;
-  const int tid = threadIdx.x;
-  const Verdict v = accept_scan<DT, true>(P, b, sM, sS, sA, sXT, sXD, sTok);
-  if (j == 0) write_common<true>(P, b, v, sTok, sXT, sXD, false, -1);
-  if (v.bad) return;
-  const int m = v.m, L = v.L;
-  const float u_final = P.uniforms[static_cast<int64_t>(b) * (k + 1) + k];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const Prologue pr = read_request(P, b, sTok, sU, true);
+  pdl_wait();
+  if (pr.bad) {
+    if (j == 0) write_common<true>(P, b, pr.bad, pr.L, 0, 0, sTok, sP, sQ, true, -1);
+    return;
+  }
+  const int L = pr.L;
+  // merge: target rows 0..L are rr = 0..L, draft rows 0..L-1 are rr = L+1..2L
+  for (int rr = warp; rr < 2 * L + 1; rr += kWarps) {
+    const int r = rr <= L ? rr : (k + 1) + (rr - L - 1);
+    const int pos = rr <= L ? rr : rr - L - 1;
+    const int tokchunk = pos < L ? sTok[pos] / P.chunk : -1;
+    float M, S, X;
+    int A;
+    warp_merge_row<true>(P.part + (static_cast<int64_t>(b) * rows + r) * nc, nc, P.c, tokchunk, M, S, A, X);
+    if (lane == 0) {
+      sM[rr] = M;
+      sS[rr] = S;
+      sX[rr] = X;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int m = 0;
+    for (int i = 0; i < L; ++i) {
+      const float p = ex2((sX[i] - sM[i]) * P.c) / sS[i];
+      const float q = ex2((sX[L + 1 + i] - sM[L + 1 + i]) * P.c) / sS[L + 1 + i];
+      sP[i] = p;
+      sQ[i] = q;
+      if (m == i && sU[i] * q < p) m = i + 1;
+    }
+    s_m = m;
+  }
+  __syncthreads();
+  const int m = s_m;
+  const int ne = max(0, min(m + 1, pr.cap));
+  if (j == 0) write_common<true>(P, b, 0, L, m, ne, sTok, sP, sQ, false, -1);
+  const float u_final = sU[k];
 
   if (m == L) {
-    // every draft token accepted: bonus draw from p_L
-    if (tid == 0)
-      pick_chunk(P.part + (static_cast<int64_t>(b) * rows + L) * nc, nc, sM[L], P.c, u_final, s_j,
-                 s_thr);
+    // every draft token accepted: bonus draw from p_L, chunk picked by one warp
+    if (warp == 0) {
+      const Partial *pp = P.part + (static_cast<int64_t>(b) * rows + L) * nc;
+      const float M = sM[L], c = P.c;
+      int js;
+      float th, tot;
+      warp_pick([&](int jj) { const Partial q = ld_partial(pp + jj); return q.s * ex2((q.m - M) * c); }, nc,
+                u_final, s_wcache, kPickCache, js, th, tot);
+      if (lane == 0) {
+        s_j = js;
+        s_thr = th;
+      }
+    }
     __syncthreads();
     if (j != s_j) return;
     Weights W{row_ptr<DT>(P.target, P.t_req, P.row, b, L), nullptr, sM[L], 0.0f, 1.0f, 0.0f, P.c};
     const int lo = j * P.chunk, hi = min(P.V, lo + P.chunk);
     const int tok = block_select<DT, VEC>(W, lo, hi, s_thr);
     if (tid == 0) {
-      if (m < v.ne) P.out_tokens[static_cast<int64_t>(b) * (k + 1) + m] = tok;
+      if (m < ne) P.out_tokens[static_cast<int64_t>(b) * (k + 1) + m] = tok;
       if (P.resid_mass) P.resid_mass[b] = 0.0f;
     }
     return;
@@ -266,7 +341,7 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
             sM[m], sM[L + 1 + m], 1.0f / sS[m], 1.0f / sS[L + 1 + m], P.c};
   const int v0 = j * P.chunk, v1 = min(P.V, v0 + P.chunk);
   const float acc = warp_sum(thread_chunk_weight_sum<DT, VEC, kLoadL2>(W, v0, v1));
-  if ((tid & 31) == 0) s_red[tid >> 5] = acc;
+  if (lane == 0) s_red[warp] = acc;
   __syncthreads();
   if (tid == 0) {
     float t = 0.0f;
@@ -278,31 +353,25 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  if (tid == 0) {
+  if (warp == 0) {
     const float *pp = P.part2 + static_cast<int64_t>(b) * nc;
-    float tot = 0.0f;
-    for (int i = 0; i < nc; ++i) tot += __ldcg(pp + i);
-    s_tot = tot;
-    s_fallback = !(tot > 0.0f);
-    if (!s_fallback) {
-      const float thr = u_final * tot;
-      float cum = 0.0f, base = 0.0f;
-      int jsel = -1, jlast = 0;
-      for (int i = 0; i < nc; ++i) {
-        const float w = __ldcg(pp + i);
-        if (w > 0.0f) jlast = i;
-        if (jsel < 0 && cum + w > thr) {
-          jsel = i;
-          base = cum;
-        }
-        cum += w;
-      }
-      s_j = jsel >= 0 ? jsel : jlast;
-      s_thr = jsel >= 0 ? thr - base : INFINITY;
-    } else {
+    int js;
+    float th, tot;
+    warp_pick([&](int jj) { return __ldcg(pp + jj); }, nc, u_final, s_wcache, kPickCache, js, th, tot);
+    const bool fallback = !(tot > 0.0f);
+    if (fallback) {
       // zero residual mass (only through rounding): draw from p_m instead
-      pick_chunk(P.part + (static_cast<int64_t>(b) * rows + m) * nc, nc, sM[m], P.c, u_final, s_j,
-                 s_thr);
+      const Partial *p1 = P.part + (static_cast<int64_t>(b) * rows + m) * nc;
+      const float M = sM[m], c = P.c;
+      float tp;
+      warp_pick([&](int jj) { const Partial q = ld_partial(p1 + jj); return q.s * ex2((q.m - M) * c); }, nc,
+                u_final, s_wcache, kPickCache, js, th, tp);
+    }
+    if (lane == 0) {
+      s_j = js;
+      s_thr = th;
+      s_tot = tot;
+      s_fallback = fallback;
     }
   }
   __syncthreads();
@@ -314,12 +383,30 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
   const int lo = s_j * P.chunk, hi = min(P.V, lo + P.chunk);
   const int tok = block_select<DT, VEC>(W, lo, hi, s_thr);
   if (tid == 0) {
-    if (m < v.ne) P.out_tokens[static_cast<int64_t>(b) * (k + 1) + m] = tok;
+    if (m < ne) P.out_tokens[static_cast<int64_t>(b) * (k + 1) + m] = tok;
     if (P.resid_mass) P.resid_mass[b] = s_fallback ? 0.0f : s_tot;
   }
 }
 
 // ------------------------------------------------------------------- host
+
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous kernel in the stream is still running, and waits for it with
+// griddepcontrol.wait before touching its results.
+template <class K>
+static cudaError_t launch_dependent(K kern, unsigned grid, cudaStream_t st, const ChainParams &P) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, P);
+}
 
 template <int DT, bool VEC>
 static cudaError_t launch_chain_t(const ChainParams &P, bool sample, cudaStream_t st) {
@@ -331,16 +418,16 @@ static cudaError_t launch_chain_t(const ChainParams &P, bool sample, cudaStream_
     });
     if (e != cudaSuccess) return e;
     const unsigned grid2 = static_cast<unsigned>(static_cast<long long>(P.B) * P.nc);
-    return trace_launch("chain_sample_accept", st, [&] {
-      chain_sample_accept_kernel<DT, VEC><<<grid2, kThreads, 0, st>>>(P);
+    return trace_launch_ex("chain_sample_accept", st, [&] {
+      return launch_dependent(chain_sample_accept_kernel<DT, VEC>, grid2, st, P);
     });
   }
   cudaError_t e = trace_launch("chain_stats_greedy", st, [&] {
     chain_stats_kernel<DT, false, VEC><<<grid1, kThreads, 0, st>>>(P);
   });
   if (e != cudaSuccess) return e;
-  return trace_launch("chain_greedy_accept", st, [&] {
-    chain_greedy_accept_kernel<DT><<<P.B, kThreads, 0, st>>>(P);
+  return trace_launch_ex("chain_greedy_accept", st, [&] {
+    return launch_dependent(chain_greedy_accept_kernel<DT>, static_cast<unsigned>(P.B), st, P);
   });
 }
 

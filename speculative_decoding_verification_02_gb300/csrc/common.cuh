@@ -17,13 +17,22 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kNoIndex = 0x7fffffff;
 
 // Per-(row, chunk) statistics written by the streaming pass:
-// m = max logit, s = sum 2^((x - m) * c) over the chunk, idx = first argmax.
+// m = max logit, s = sum 2^((x - m) * c) over the chunk, idx = first argmax,
+// x = the logit of the row's drafted token when it falls in this chunk.
 struct __align__(16) Partial {
   float m;
   float s;
   int idx;
-  int pad;
+  float x;
 };
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue, and (in that kernel) wait until this grid has finished and its
+// writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------- loads
 
@@ -181,68 +190,62 @@ __device__ __forceinline__ void weights8(const Weights &W, int v0, int hi, float
 // Block-wide inverse-CDF selection inside [lo, hi): the smallest v with
 // (sum of w over [lo, v]) > thr.  If rounding leaves no such v, the last v in
 // the range with w > 0 (or -1 when every weight is 0).  lo must be a
-// multiple of 8.  Called by all kThreads threads; returns the same value in
-// every thread.
+// multiple of 8.  Each thread takes a contiguous segment of kSelPerThread
+// elements (all its loads in flight at once), the block scans the segment
+// sums, and every thread whose prefix passes thr walks its own segment; the
+// smallest proposal wins.  Called by all kThreads threads; returns the same
+// value in every thread.
+constexpr int kSelPerThread = 32;
+
 template <int DT, bool VEC>
 __device__ int block_select(const Weights &W, int lo, int hi, float thr) {
   __shared__ float s_wsum[kWarps];
   __shared__ int s_pick, s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int ntiles = (hi - lo + 255) / 256;  // 32 lanes x 8 elements per tile
-  const int tpw = (ntiles + kWarps - 1) / kWarps;
-  const int t0 = warp * tpw, t1 = min(ntiles, t0 + tpw);
   if (threadIdx.x == 0) {
     s_pick = kNoIndex;
     s_last = -1;
   }
-  // pass 1: each warp's total
-  float acc = 0.0f;
-  for (int t = t0; t < t1; ++t) {
-    float w[8];
-    weights8<DT, VEC>(W, lo + t * 256 + lane * 8, hi, w);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc += w[e];
-  }
-  acc = warp_sum(acc);
-  if (lane == 0) s_wsum[warp] = acc;
-  __syncthreads();
   float carry = 0.0f;
-  for (int i = 0; i < warp; ++i) carry += s_wsum[i];
-  // pass 2: walk tiles with a running prefix; first crossing wins
   int last_pos = -1;
-  for (int t = t0; t < t1; ++t) {
-    const int v0 = lo + t * 256 + lane * 8;
-    float w[8];
-    weights8<DT, VEC>(W, v0, hi, w);
+  for (int base = lo; base < hi; base += kThreads * kSelPerThread) {
+    const int v0 = base + threadIdx.x * kSelPerThread;
+    float w[kSelPerThread];
+#pragma unroll
+    for (int q = 0; q < kSelPerThread / 8; ++q) weights8<DT, VEC>(W, v0 + 8 * q, hi, w + 8 * q);
     float ls = 0.0f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
+    for (int e = 0; e < kSelPerThread; ++e) {
       ls += w[e];
       if (w[e] > 0.0f) last_pos = v0 + e;
     }
     const float incl = warp_inclusive_scan(ls, lane);
-    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 0) excl = 0.0f;
-    const unsigned cross = __ballot_sync(0xffffffffu, carry + incl > thr);
-    if (cross) {
-      const int first = __ffs(cross) - 1;
-      if (lane == first) {
-        float run = carry + excl;
-        int pick = -1, lastp = -1;
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    float wbase = carry, total = carry;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          run += w[e];
-          if (w[e] > 0.0f) lastp = v0 + e;
-          if (pick < 0 && run > thr) pick = v0 + e;
-        }
-        if (pick < 0) pick = lastp >= 0 ? lastp : v0;
-        atomicMin(&s_pick, pick);
-      }
-      break;
+    for (int i = 0; i < kWarps; ++i) {
+      if (i < warp) wbase += s_wsum[i];
+      total += s_wsum[i];
     }
-    carry += __shfl_sync(0xffffffffu, incl, 31);
+    if (wbase + incl > thr) {
+      float run = wbase + incl - ls;
+      int pick = -1, lastp = -1;
+#pragma unroll
+      for (int e = 0; e < kSelPerThread; ++e) {
+        run += w[e];
+        if (w[e] > 0.0f) lastp = v0 + e;
+        if (pick < 0 && run > thr) pick = v0 + e;
+      }
+      if (pick < 0) pick = lastp;
+      if (pick >= 0) atomicMin(&s_pick, pick);
+    }
+    __syncthreads();
+    const bool done = s_pick != kNoIndex;
+    carry = total;
+    __syncthreads();
+    if (done) break;
   }
-  // fallback: the last element with positive weight
   for (int o = 16; o > 0; o >>= 1) last_pos = max(last_pos, __shfl_xor_sync(0xffffffffu, last_pos, o));
   if (lane == 0) atomicMax(&s_last, last_pos);
   __syncthreads();
@@ -267,54 +270,80 @@ __device__ __forceinline__ uint4 load16(const uint4 *p) {
 }
 
 // Statistics of row[v0, v1) for the calling thread (strided over the block).
+// Folds one batch of kBatch 16-byte groups (the raw words, unpacked again in
+// each pass to keep few registers live) into the running (m, s, idx).
+template <int DT, bool SOFTMAX>
+__device__ __forceinline__ void fold_batch(const uint4 *g, int first_elem, float c, float &m, float &s,
+                                           int &idx) {
+  constexpr int EPG = Elems<DT>::kPerGroup;
+  float bm = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) {
+    float x[EPG];
+    unpack16<DT>(g[u], x);
+#pragma unroll
+    for (int e = 0; e < EPG; ++e) bm = fmaxf(bm, x[e]);
+  }
+  if (bm > m) {  // a new running max: rescale the sum, find its first index
+    if (SOFTMAX) s *= ex2((m - bm) * c);
+    m = bm;
+    int first = kNoIndex;
+#pragma unroll
+    for (int u = kBatch - 1; u >= 0; --u) {
+      float x[EPG];
+      unpack16<DT>(g[u], x);
+#pragma unroll
+      for (int e = EPG - 1; e >= 0; --e)
+        if (x[e] == bm) first = first_elem + u * kThreads * EPG + e;
+    }
+    idx = first;
+  }
+  if (SOFTMAX && m != -INFINITY) {
+    const float mc = m * c;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      float x[EPG];
+      unpack16<DT>(g[u], x);
+#pragma unroll
+      for (int e = 0; e < EPG; ++e) s += ex2(fmaf(x[e], c, -mc));
+    }
+  }
+}
+
+// Statistics of row[v0, v1) for the calling thread (strided over the block):
+// running max m, sum of 2^((x - m) c), first index of the max.  The next
+// batch of loads is issued before the current one is folded, so each thread
+// keeps two batches of 16-byte loads in flight.
 template <int DT, bool SOFTMAX, bool VEC, int LD>
 __device__ __forceinline__ void thread_chunk_stats(const char *row, int v0, int v1, float c,
                                                    float &m, float &s, int &idx) {
   constexpr int EPG = Elems<DT>::kPerGroup;
   constexpr int ES = Elems<DT>::kSize;
+  constexpr uint32_t kNegInf = DT == SPEC_DTYPE_F32 ? 0xff800000u : 0xff80ff80u;  // -inf words
+  constexpr int kStride = kThreads * kBatch;
   int vtail = v0;
   if (VEC) {
     const int ng = (v1 - v0) / EPG;
     const uint4 *base = reinterpret_cast<const uint4 *>(row + static_cast<int64_t>(v0) * ES);
-    for (int g0 = threadIdx.x; g0 < ng; g0 += kThreads * kBatch) {
-      uint4 g[kBatch];
+    uint4 cur[kBatch], nxt[kBatch];
+    int g0 = threadIdx.x;
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int gi = g0 + u * kThreads;
-        if (gi < ng) g[u] = load16<LD>(base + gi);
-      }
-      float x[kBatch][EPG];
-      float bm = -INFINITY;
+    for (int u = 0; u < kBatch; ++u) {
+      const int gi = g0 + u * kThreads;
+      cur[u] = gi < ng ? load16<LD>(base + gi) : make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
+    }
+    for (; g0 < ng; g0 += kStride) {
+      const int g1 = g0 + kStride;
+      if (g1 < ng) {
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int gi = g0 + u * kThreads;
-        if (gi < ng) {
-          unpack16<DT>(g[u], x[u]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < EPG; ++e) x[u][e] = -INFINITY;
+        for (int u = 0; u < kBatch; ++u) {
+          const int gi = g1 + u * kThreads;
+          nxt[u] = gi < ng ? load16<LD>(base + gi) : make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
         }
-#pragma unroll
-        for (int e = 0; e < EPG; ++e) bm = fmaxf(bm, x[u][e]);
       }
-      if (bm > m) {  // a new running max: rescale the sum, find its first index
-        if (SOFTMAX) s *= ex2((m - bm) * c);
-        m = bm;
-        int first = kNoIndex;
+      fold_batch<DT, SOFTMAX>(cur, v0 + g0 * EPG, c, m, s, idx);
 #pragma unroll
-        for (int u = kBatch - 1; u >= 0; --u)
-#pragma unroll
-          for (int e = EPG - 1; e >= 0; --e)
-            if (x[u][e] == bm) first = v0 + (g0 + u * kThreads) * EPG + e;
-        idx = first;
-      }
-      if (SOFTMAX && m != -INFINITY) {
-        const float mc = m * c;
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u)
-#pragma unroll
-          for (int e = 0; e < EPG; ++e) s += ex2(fmaf(x[u][e], c, -mc));
-      }
+      for (int u = 0; u < kBatch; ++u) cur[u] = nxt[u];
     }
     vtail = v0 + ng * EPG;
   }

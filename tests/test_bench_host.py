@@ -1,0 +1,64 @@
+"""bench.py host logic without a GPU: the reference arm's JSON line, and the
+max-over-ranks / sum-over-ranks reductions of the multi-GPU path on two
+gloo ranks."""
+import json
+import os
+import socket
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_reference_arm_json_line(capsys, monkeypatch):
+    monkeypatch.setenv("SPEC_REF_SECONDS", "5")
+    assert bench.main(["--impl", "reference", "--workload", "small", "--steps", "3", "--warmup", "1"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "rows/s"
+    assert line["e2e"]["value"] == line["value"] and line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+
+
+def test_reference_arm_other_ranks_exit_quietly(capsys, monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert bench.main(["--impl", "reference", "--workload", "small", "--steps", "2"]) == 0
+    assert capsys.readouterr().out.strip() == ""
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE="2",
+                      LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=2)
+    ws, r, local = bench.dist_env()
+    mx = bench.reduce_max(10.0 * (rank + 1), "cpu")
+    sm = bench.reduce_sum(9.0, "cpu")
+    bench.barrier()
+    q.put((r, ws, mx, sm))
+    dist.destroy_process_group()
+
+
+def test_two_rank_reductions_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    # timing is the max over ranks, rows add up: value = sum(rows) / max(time)
+    assert res == [(0, 2, 20.0, 18.0), (1, 2, 20.0, 18.0)]
