@@ -199,6 +199,44 @@ int spec_verify_tree(const void *target, int64_t target_req_stride, const void *
                      int32_t *path_nodes, int32_t *out_tokens, int32_t *n_emit,
                      int32_t *status, void *workspace, size_t workspace_bytes, void *stream);
 
+/* Size of the scratch array behind spec_verify_sample_noalloc (4 MiB). */
+#define SPEC_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+
+/*
+ * spec_verify_sample_noalloc -- spec_verify_sample for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this entry
+ * point; it exists for the library's users.
+ *
+ * Some callers cannot supply a workspace: a serving loop that divides its
+ * whole device-memory budget up at start-up and forbids allocations while it
+ * serves, or code that must not stall on a cudaMalloc (which can synchronise
+ * the device).  This entry point takes the same arguments as
+ * spec_verify_sample minus the workspace, and uses instead a fixed scratch
+ * array of SPEC_NOALLOC_SCRATCH_BYTES compiled into the library.  It calls no
+ * allocator.
+ *
+ *  - Every GPU on which the library is loaded holds that array in device
+ *    memory until the process exits.
+ *  - The first call on a device looks up the array's device address on the
+ *    current device (cudaGetSymbolAddress) and caches it; make that first
+ *    call before any stream capture.  `stream` must belong to the current
+ *    device.
+ *  - A problem whose scratch (spec_workspace_size(SPEC_OP_SAMPLE, B, k, V,
+ *    dtype)) exceeds the array is refused with SPEC_EWORKSPACE and a message
+ *    in spec_last_error(); use spec_verify_sample then.
+ *  - All calls share the one array and it keeps the last call's contents.
+ *    Nothing in it has to start at zero (each call's first kernel clears
+ *    what it counts with), but calls that may overlap on the GPU (different
+ *    streams, or different host threads without ordering) race on it.
+ */
+int spec_verify_sample_noalloc(const void *target, int64_t target_req_stride,
+                               const void *draft_logits, int64_t draft_req_stride,
+                               int64_t row_stride, int dtype, int B, int k, int V,
+                               float temperature, const int32_t *draft, const int32_t *draft_len,
+                               const int32_t *max_emit, const float *uniforms, int32_t *accepted,
+                               int32_t *out_tokens, int32_t *n_emit, float *p_tok, float *q_tok,
+                               float *resid_mass, int32_t *status, void *stream);
+
 /*
  * spec_workspace_size -- bytes of workspace a call needs.
  *   op = SPEC_OP_*; rows_per_req = k for chains, N for trees.

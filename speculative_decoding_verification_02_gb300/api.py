@@ -279,3 +279,42 @@ def spec_verify_tree(target: torch.Tensor, draft_logits, parents: torch.Tensor, 
                                 _p(o["status"]), None, 0, _stream(stream, dev))
     _check(rc, "spec_verify_tree")
     return o
+
+
+def spec_verify_sample_noalloc(target: torch.Tensor, draft_logits: torch.Tensor, draft: torch.Tensor,
+                               uniforms: torch.Tensor, temperature: float = 1.0, draft_len=None,
+                               max_emit=None, *, out=None, stream=None) -> dict:
+    """spec_verify_sample without a workspace, for callers that cannot allocate
+    device memory while they run: the library's fixed scratch array is used
+    instead (SPEC_NOALLOC_SCRATCH_BYTES; larger problems raise SpecError).
+    Outputs are allocated here unless `out` is given."""
+    L = lib()
+    fn = L.spec_verify_sample_noalloc
+    P, I, I64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    fn.argtypes = [P, I64, P, I64, I64, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P, P, P]
+    target = _logits3(target, "target")
+    draft_logits = _logits3(draft_logits, "draft_logits")
+    dev = target.device
+    B, R, V = target.shape
+    k = R - 1
+    if tuple(draft_logits.shape) != (B, k, V) or draft_logits.dtype != target.dtype:
+        raise ValueError("draft_logits must be [B, k, V] with the target's dtype")
+    if k > 1 and draft_logits.stride(1) != target.stride(1):
+        raise ValueError("target and draft rows must share a row stride")
+    draft = _i32(draft, (B, k), "draft", dev)
+    uniforms = _f32(uniforms, (B, k + 1), "uniforms", dev)
+    draft_len = _i32(draft_len, (B,), "draft_len", dev)
+    max_emit = _i32(max_emit, (B,), "max_emit", dev)
+    o = out or dict(accepted=torch.empty(B, dtype=torch.int32, device=dev),
+                    out_tokens=torch.empty((B, k + 1), dtype=torch.int32, device=dev),
+                    n_emit=torch.empty(B, dtype=torch.int32, device=dev),
+                    status=torch.empty(B, dtype=torch.int32, device=dev),
+                    p_tok=torch.empty((B, k), dtype=torch.float32, device=dev),
+                    q_tok=torch.empty((B, k), dtype=torch.float32, device=dev),
+                    resid_mass=torch.empty(B, dtype=torch.float32, device=dev))
+    rc = fn(_p(target), target.stride(0), _p(draft_logits), draft_logits.stride(0), target.stride(1),
+            _dtype_code(target), B, k, V, float(temperature), _p(draft), _p(draft_len), _p(max_emit),
+            _p(uniforms), _p(o["accepted"]), _p(o["out_tokens"]), _p(o["n_emit"]), _p(o.get("p_tok")),
+            _p(o.get("q_tok")), _p(o.get("resid_mass")), _p(o["status"]), _stream(stream, dev))
+    _check(rc, "spec_verify_sample_noalloc")
+    return o

@@ -126,6 +126,8 @@ void count_launch() {
   ++g_launches;
 }
 
+void set_last_error(const char *msg) { std::snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
 }  // namespace sv
 
 using namespace sv;

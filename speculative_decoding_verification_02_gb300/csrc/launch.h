@@ -57,6 +57,8 @@ cudaError_t launch_ngram(const NgramParams &P, cudaStream_t st);
 int trace_begin(const char *name, cudaStream_t st);
 void trace_end(int slot, cudaStream_t st);
 void count_launch();
+// Sets the message spec_last_error() returns on this thread.
+void set_last_error(const char *msg);
 
 template <class F>
 cudaError_t trace_launch(const char *name, cudaStream_t st, F &&launch) {
