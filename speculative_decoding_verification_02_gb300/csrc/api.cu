@@ -30,27 +30,29 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // ------------------------------------------------------------ geometry
 
-// Logits per CTA of the streaming pass (the residual pass uses the same
-// chunks).  Sized from the call's total bytes so that the grid is about four
-// waves of four CTAs on each of the GB300's 152 SMs, between 8 KB and 64 KB
-// of one row: small calls spread over every SM, large ones keep each CTA
-// streaming long enough to amortise its start-up and reduction.
+// Logits per CTA of the streaming pass, sized from the call's total bytes so
+// that the grid is about four waves of four CTAs on each of the GB300's 152
+// SMs, between 16 KB and 128 KB of one row: small calls spread over every
+// SM, large ones keep each CTA streaming long enough to amortise its
+// start-up and reduction.  The chunked accept kernel uses 16 KB chunks.
 constexpr long long kSmCount = 152;
 
 int stream_chunk(int dtype, long long rows_total, int V) {
   const long long es = elem_size(dtype);
   const long long target_ctas = kSmCount * 4 * 4;
   const long long per = rows_total * V * es / target_ctas;
-  long long bytes = 8192;
-  while (bytes < per && bytes < 65536) bytes *= 2;
+  long long bytes = 16384;
+  while (bytes < per && bytes < 131072) bytes *= 2;
   return static_cast<int>(bytes / es);
 }
+
+int accept_chunk(int dtype) { return 16384 / elem_size(dtype); }
 
 // Workspace: per-(row, chunk) statistics, then for sampling the residual
 // mass per chunk and one arrival counter per request.  Nothing in it needs
 // initialising: the counters are zeroed by the first kernel of each call.
 struct ChainLayout {
-  int nc, chunk;
+  int nc, chunk, nc2, chunk2;
   size_t part, part2, counter2, total;
 };
 
@@ -58,12 +60,14 @@ ChainLayout chain_layout(bool sample, int B, int k, int V, int dtype) {
   ChainLayout L{};
   L.chunk = stream_chunk(dtype, static_cast<long long>(B) * (sample ? 2LL * k + 1 : k + 1LL), V);
   L.nc = (V + L.chunk - 1) / L.chunk;
+  L.chunk2 = accept_chunk(dtype);
+  L.nc2 = (V + L.chunk2 - 1) / L.chunk2;
   const size_t rows = sample ? 2 * static_cast<size_t>(k) + 1 : static_cast<size_t>(k) + 1;
   size_t off = 0;
   L.part = off;
   off = round_up(off + sizeof(Partial) * B * rows * L.nc, 256);
   L.part2 = off;
-  off = round_up(off + (sample ? sizeof(float) * B * L.nc : 0), 256);
+  off = round_up(off + (sample ? sizeof(float) * B * L.nc2 : 0), 256);
   L.counter2 = off;
   off = round_up(off + (sample ? sizeof(int) * B : 0), 256);
   L.total = off;
@@ -75,6 +79,22 @@ ChainLayout chain_layout(bool sample, int B, int k, int V, int dtype) {
 void tree_geometry(int V, int &cluster, int &slice) {
   cluster = V >= 8 * 2048 ? 8 : (V >= 4 * 2048 ? 4 : (V >= 2 * 2048 ? 2 : 1));
   slice = ((V + cluster - 1) / cluster + 7) / 8 * 8;
+}
+
+// Sampling accept kernel: one cluster of up to 16 CTAs (1024 threads, 16
+// logits each) per request when V fits and all the clusters fit in one wave
+// of the 152 SMs (one such CTA fills an SM); otherwise the chunked accept
+// kernel, whose small CTAs share SMs.
+void cluster_geometry(int B, int V, int &cluster, int &slice) {
+  const int per_cta = 1024 * 16;
+  const int n = (V + per_cta - 1) / per_cta;
+  if (n > 16 || static_cast<long long>(B) * n > kSmCount) {
+    cluster = 0;
+    slice = 0;
+    return;
+  }
+  cluster = n;
+  slice = ((V + n - 1) / n + 15) / 16 * 16;
 }
 
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
@@ -243,7 +263,9 @@ static int chain_common(bool sample, const void *target, int64_t t_req, const vo
   if (sample && (!uniforms || (k > 0 && !draftl))) return SPEC_EINVAL;
   const ChainLayout L = chain_layout(sample, B, k, V, dtype);
   const long long rows = sample ? 2LL * k + 1 : k + 1LL;
-  if (static_cast<long long>(B) * rows * L.nc > 2147483647LL) return SPEC_EINVAL;
+  if (static_cast<long long>(B) * rows * L.nc > 2147483647LL ||
+      static_cast<long long>(B) * L.nc2 > 2147483647LL)
+    return SPEC_EINVAL;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
       workspace_bytes < L.total)
     return SPEC_EWORKSPACE;
@@ -263,6 +285,8 @@ static int chain_common(bool sample, const void *target, int64_t t_req, const vo
   P.V = V;
   P.nc = L.nc;
   P.chunk = L.chunk;
+  P.nc2 = L.nc2;
+  P.chunk2 = L.chunk2;
   P.c = sample ? static_cast<float>(1.4426950408889634 / static_cast<double>(T)) : 1.0f;
   P.draft = draft;
   P.draft_len = draft_len;
@@ -277,6 +301,8 @@ static int chain_common(bool sample, const void *target, int64_t t_req, const vo
   P.resid_mass = resid_mass;
   P.counter2 = reinterpret_cast<int *>(ws + L.counter2);
   P.part = reinterpret_cast<Partial *>(ws + L.part);
+  cluster_geometry(B, V, P.cluster, P.slice);
+  if (!sample) P.cluster = 0;
   P.part2 = reinterpret_cast<float *>(ws + L.part2);
   const cudaError_t e = launch_chain(P, sample, vec, as_stream(stream));
   return e == cudaSuccess ? SPEC_OK : fail_cuda(e, sample ? "spec_verify_sample" : "spec_verify_greedy");

@@ -28,13 +28,25 @@
 //                     scans it: a draw from norm(max(0, p - q)).
 // Both accept kernels read their inputs before waiting on the stats grid.
 // No kernel waits on another CTA.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "launch.h"
+
+namespace cg = cooperative_groups;
 
 namespace sv {
 
 constexpr int kMaxRows = 2 * SPEC_MAX_K + 1;
 constexpr int kPickCache = 512;  // chunk weights kept in shared memory by warp_pick
+
+// Arrival counter with release (this thread's earlier writes become visible
+// first) and acquire (the caller sees what earlier arrivals published).
+__device__ __forceinline__ int atomic_add_acq_rel(int *p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 
 __device__ __forceinline__ Partial ld_partial(const Partial *p) {
   const float4 v = __ldcg(reinterpret_cast<const float4 *>(p));
@@ -73,16 +85,12 @@ __global__ void __launch_bounds__(kThreads) chain_stats_kernel(const ChainParams
     row = row_ptr<DT>(P.draftl, P.d_req, P.row, b, pos);
   }
   const int v0 = j * P.chunk, v1 = min(P.V, v0 + P.chunk);
-  // the logit of this row's drafted token, if it lies in this chunk
-  float xt = -INFINITY;
-  if (SOFTMAX && threadIdx.x == 0 && pos < L) {
-    const int t = P.draft[static_cast<int64_t>(b) * P.k + pos];
-    if (t >= v0 && t < v1) xt = load_one<DT>(row, t);
-  }
-  float m = -INFINITY, s = 0.0f;
+  // the row's drafted token: its logit is picked up while streaming
+  const int tok = (SOFTMAX && pos < L) ? P.draft[static_cast<int64_t>(b) * P.k + pos] : -1;
+  float m = -INFINITY, s = 0.0f, xt = -INFINITY;
   int idx = kNoIndex;
-  thread_chunk_stats<DT, SOFTMAX, VEC, kLoadStream>(row, v0, v1, P.c, m, s, idx);
-  block_merge<SOFTMAX>(m, s, idx, P.c);
+  thread_chunk_stats<DT, SOFTMAX, VEC, kLoadStream>(row, v0, v1, P.c, m, s, idx, tok, xt);
+  block_merge<SOFTMAX>(m, s, idx, P.c, xt);
   if (threadIdx.x == 0)
     *reinterpret_cast<float4 *>(P.part + (static_cast<int64_t>(b) * rows + r) * P.nc + j) =
         make_float4(m, s, __int_as_float(idx), xt);
@@ -117,24 +125,60 @@ __device__ Prologue read_request(const ChainParams &P, int b, int *sTok, float *
   return pr;
 }
 
-// Merges the partials of row r with one warp: max, sum 2^((x - max) c),
-// first argmax, and the drafted token's logit (tokchunk = its chunk, or -1).
+constexpr int kMergeUnroll = 4;  // partials per lane whose loads are issued together
+
+// Merges with one warp the partials of row A and, if ppB is non-null, row B:
+// max, sum 2^((x - max) c), first argmax, and the drafted token's logit
+// (tokchunk = the chunk holding the token, or -1).  The loads of the first
+// 32 * kMergeUnroll chunks of both rows are all issued before any is used.
+struct RowStats {
+  float M, S, X;
+  int A;
+};
+
 template <bool SOFTMAX>
-__device__ __forceinline__ void warp_merge_row(const Partial *pp, int nc, float c, int tokchunk,
-                                               float &M, float &S, int &A, float &X) {
+__device__ __forceinline__ RowStats merge_prefetched(const float4 *q, const Partial *pp, int nc, float c,
+                                                     int tokchunk) {
   const int lane = threadIdx.x & 31;
   float m = -INFINITY, s = 0.0f, x = -INFINITY;
   int idx = kNoIndex;
-  for (int j = lane; j < nc; j += 32) {
-    const Partial q = ld_partial(pp + j);
-    if (SOFTMAX) merge_stats(m, s, idx, q.m, q.s, q.idx, c); else merge_argmax(m, idx, q.m, q.idx);
-    if (j == tokchunk) x = q.x;
+#pragma unroll
+  for (int u = 0; u < kMergeUnroll; ++u) {
+    const int j = lane + 32 * u;
+    if (j < nc) {
+      if (SOFTMAX) merge_stats(m, s, idx, q[u].x, q[u].y, __float_as_int(q[u].z), c);
+      else merge_argmax(m, idx, q[u].x, __float_as_int(q[u].z));
+      if (j == tokchunk) x = q[u].w;
+    }
+  }
+  for (int j = lane + 32 * kMergeUnroll; j < nc; j += 32) {  // very long rows only
+    const Partial r = ld_partial(pp + j);
+    if (SOFTMAX) merge_stats(m, s, idx, r.m, r.s, r.idx, c); else merge_argmax(m, idx, r.m, r.idx);
+    if (j == tokchunk) x = r.x;
   }
   if (SOFTMAX) warp_merge_stats(m, s, idx, c); else warp_merge_argmax(m, idx);
-  M = m;
-  S = s;
-  A = idx == kNoIndex ? 0 : idx;  // an all -inf row: every index ties, take 0
-  X = tokchunk >= 0 ? __shfl_sync(0xffffffffu, x, tokchunk & 31) : -INFINITY;
+  RowStats out;
+  out.M = m;
+  out.S = s;
+  out.A = idx == kNoIndex ? 0 : idx;  // an all -inf row: every index ties, take 0
+  out.X = tokchunk >= 0 ? __shfl_sync(0xffffffffu, x, tokchunk & 31) : -INFINITY;
+  return out;
+}
+
+template <bool SOFTMAX>
+__device__ __forceinline__ void warp_merge_two_rows(const Partial *ppA, const Partial *ppB, int nc, float c,
+                                                    int tokA, int tokB, RowStats &a, RowStats &b) {
+  const int lane = threadIdx.x & 31;
+  const float4 neutral = make_float4(-INFINITY, 0.0f, __int_as_float(kNoIndex), -INFINITY);
+  float4 qa[kMergeUnroll], qb[kMergeUnroll];
+#pragma unroll
+  for (int u = 0; u < kMergeUnroll; ++u) {
+    const int j = lane + 32 * u;
+    qa[u] = j < nc ? __ldcg(reinterpret_cast<const float4 *>(ppA + j)) : neutral;
+    qb[u] = (ppB != nullptr && j < nc) ? __ldcg(reinterpret_cast<const float4 *>(ppB + j)) : neutral;
+  }
+  a = merge_prefetched<SOFTMAX>(qa, ppA, nc, c, tokA);
+  if (ppB != nullptr) b = merge_prefetched<SOFTMAX>(qb, ppB, nc, c, tokB);
 }
 
 // One warp: the index j* in [0, n) where u * (w_0 + ... + w_{n-1}) falls,
@@ -153,7 +197,20 @@ __device__ __forceinline__ void warp_pick(W weight, int n, float u, float *cache
   const bool cached = n <= cap;
   float ls = 0.0f;
   int lastpos = -1;
-  for (int j = j0; j < j1; ++j) {
+  constexpr int kUnroll = 4;  // the first kUnroll weights' loads are issued together
+  float wq[kUnroll];
+#pragma unroll
+  for (int q = 0; q < kUnroll; ++q) wq[q] = (j0 + q < j1) ? weight(j0 + q) : 0.0f;
+#pragma unroll
+  for (int q = 0; q < kUnroll; ++q) {
+    const int j = j0 + q;
+    if (j < j1) {
+      if (cached) cache[j] = wq[q];
+      ls += wq[q];
+      if (wq[q] > 0.0f) lastpos = j;
+    }
+  }
+  for (int j = j0 + kUnroll; j < j1; ++j) {
     const float w = weight(j);
     if (cached) cache[j] = w;
     ls += w;
@@ -240,11 +297,17 @@ __global__ void __launch_bounds__(kThreads) chain_greedy_accept_kernel(const Cha
     return;
   }
   const int rows = P.k + 1;
-  for (int r = warp; r <= pr.L; r += kWarps) {
-    float M, S, X;
-    int A;
-    warp_merge_row<false>(P.part + (static_cast<int64_t>(b) * rows + r) * P.nc, P.nc, 1.0f, -1, M, S, A, X);
-    if (lane == 0) sA[r] = A;
+  const Partial *base = P.part + static_cast<int64_t>(b) * rows * P.nc;
+  for (int r = warp; r <= pr.L; r += 2 * kWarps) {
+    const int r2 = r + kWarps;
+    RowStats a, bb;
+    warp_merge_two_rows<false>(base + static_cast<int64_t>(r) * P.nc,
+                               r2 <= pr.L ? base + static_cast<int64_t>(r2) * P.nc : nullptr, P.nc, 1.0f, -1, -1,
+                               a, bb);
+    if (lane == 0) {
+      sA[r] = a.A;
+      if (r2 <= pr.L) sA[r2] = bb.A;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -268,7 +331,7 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
   __shared__ float s_thr, s_tot;
   __shared__ bool s_fallback;
   const int nc = P.nc;
-  const int b = blockIdx.x / nc, j = blockIdx.x - b * nc;
+  const int b = blockIdx.x / P.nc2, j = blockIdx.x - b * P.nc2;
   const int k = P.k, rows = 2 * k + 1;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const Prologue pr = read_request(P, b, sTok, sU, true);
@@ -278,18 +341,30 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
     return;
   }
   const int L = pr.L;
-  // merge: target rows 0..L are rr = 0..L, draft rows 0..L-1 are rr = L+1..2L
-  for (int rr = warp; rr < 2 * L + 1; rr += kWarps) {
-    const int r = rr <= L ? rr : (k + 1) + (rr - L - 1);
+  // merge: target rows 0..L are rr = 0..L, draft rows 0..L-1 are rr = L+1..2L;
+  // each warp takes two rows at a time with all their loads in flight
+  const int nrr = 2 * L + 1;
+  const Partial *base = P.part + static_cast<int64_t>(b) * rows * nc;
+  auto row_of = [&](int rr) { return rr <= L ? rr : (k + 1) + (rr - L - 1); };
+  auto tok_chunk = [&](int rr) {
     const int pos = rr <= L ? rr : rr - L - 1;
-    const int tokchunk = pos < L ? sTok[pos] / P.chunk : -1;
-    float M, S, X;
-    int A;
-    warp_merge_row<true>(P.part + (static_cast<int64_t>(b) * rows + r) * nc, nc, P.c, tokchunk, M, S, A, X);
+    return pos < L ? sTok[pos] / P.chunk : -1;
+  };
+  for (int rr = warp; rr < nrr; rr += 2 * kWarps) {
+    const int rr2 = rr + kWarps;
+    RowStats a, bb;
+    warp_merge_two_rows<true>(base + static_cast<int64_t>(row_of(rr)) * nc,
+                              rr2 < nrr ? base + static_cast<int64_t>(row_of(rr2)) * nc : nullptr, nc, P.c,
+                              tok_chunk(rr), rr2 < nrr ? tok_chunk(rr2) : -1, a, bb);
     if (lane == 0) {
-      sM[rr] = M;
-      sS[rr] = S;
-      sX[rr] = X;
+      sM[rr] = a.M;
+      sS[rr] = a.S;
+      sX[rr] = a.X;
+      if (rr2 < nrr) {
+        sM[rr2] = bb.M;
+        sS[rr2] = bb.S;
+        sX[rr2] = bb.X;
+      }
     }
   }
   __syncthreads();
@@ -310,57 +385,36 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
   if (j == 0) write_common<true>(P, b, 0, L, m, ne, sTok, sP, sQ, false, -1);
   const float u_final = sU[k];
 
-  if (m == L) {
-    // every draft token accepted: bonus draw from p_L, chunk picked by one warp
-    if (warp == 0) {
-      const Partial *pp = P.part + (static_cast<int64_t>(b) * rows + L) * nc;
-      const float M = sM[L], c = P.c;
-      int js;
-      float th, tot;
-      warp_pick([&](int jj) { const Partial q = ld_partial(pp + jj); return q.s * ex2((q.m - M) * c); }, nc,
-                u_final, s_wcache, kPickCache, js, th, tot);
-      if (lane == 0) {
-        s_j = js;
-        s_thr = th;
-      }
-    }
-    __syncthreads();
-    if (j != s_j) return;
-    Weights W{row_ptr<DT>(P.target, P.t_req, P.row, b, L), nullptr, sM[L], 0.0f, 1.0f, 0.0f, P.c};
-    const int lo = j * P.chunk, hi = min(P.V, lo + P.chunk);
-    const int tok = block_select<DT, VEC>(W, lo, hi, s_thr);
-    if (tid == 0) {
-      if (m < ne) P.out_tokens[static_cast<int64_t>(b) * (k + 1) + m] = tok;
-      if (P.resid_mass) P.resid_mass[b] = 0.0f;
-    }
-    return;
-  }
-
-  // rejected at m: residual mass of this chunk
-  Weights W{row_ptr<DT>(P.target, P.t_req, P.row, b, m), row_ptr<DT>(P.draftl, P.d_req, P.row, b, m),
-            sM[m], sM[L + 1 + m], 1.0f / sS[m], 1.0f / sS[L + 1 + m], P.c};
-  const int v0 = j * P.chunk, v1 = min(P.V, v0 + P.chunk);
+  // the final draw: the residual max(0, p_m - q_m) after a rejection, p_L
+  // after a full accept; the mass of this CTA's chunk, then the last CTA to
+  // arrive picks the chunk where u * total falls and scans it
+  Weights W = m < L
+                  ? Weights{row_ptr<DT>(P.target, P.t_req, P.row, b, m), row_ptr<DT>(P.draftl, P.d_req, P.row, b, m),
+                            sM[m], sM[L + 1 + m], 1.0f / sS[m], 1.0f / sS[L + 1 + m], P.c}
+                  : Weights{row_ptr<DT>(P.target, P.t_req, P.row, b, L), nullptr, sM[L], 0.0f, 1.0f / sS[L], 0.0f,
+                            P.c};
+  const int nc2 = P.nc2;
+  const int v0 = j * P.chunk2, v1 = min(P.V, v0 + P.chunk2);
   const float acc = warp_sum(thread_chunk_weight_sum<DT, VEC, kLoadL2>(W, v0, v1));
   if (lane == 0) s_red[warp] = acc;
   __syncthreads();
   if (tid == 0) {
     float t = 0.0f;
     for (int w = 0; w < kWarps; ++w) t += s_red[w];
-    P.part2[static_cast<int64_t>(b) * nc + j] = t;
-    __threadfence();
-    s_last = atomicAdd(P.counter2 + b, 1) == nc - 1;
+    P.part2[static_cast<int64_t>(b) * nc2 + j] = t;
+    s_last = atomic_add_acq_rel(P.counter2 + b, 1) == nc2 - 1;  // publishes part2, sees the others'
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   if (warp == 0) {
-    const float *pp = P.part2 + static_cast<int64_t>(b) * nc;
+    const float *pp = P.part2 + static_cast<int64_t>(b) * nc2;
     int js;
     float th, tot;
-    warp_pick([&](int jj) { return __ldcg(pp + jj); }, nc, u_final, s_wcache, kPickCache, js, th, tot);
-    const bool fallback = !(tot > 0.0f);
+    warp_pick([&](int jj) { return __ldcg(pp + jj); }, nc2, u_final, s_wcache, kPickCache, js, th, tot);
+    const bool fallback = !(tot > 0.0f) && m < L;
     if (fallback) {
-      // zero residual mass (only through rounding): draw from p_m instead
+      // zero residual mass (only through rounding): draw from p_m instead,
+      // its chunks picked from the streaming pass's statistics
       const Partial *p1 = P.part + (static_cast<int64_t>(b) * rows + m) * nc;
       const float M = sM[m], c = P.c;
       float tp;
@@ -375,17 +429,223 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
     }
   }
   __syncthreads();
+  int lo, hi;
   if (s_fallback) {
     W.b = nullptr;
     W.alpha = 1.0f;
     W.beta = 0.0f;
+    lo = s_j * P.chunk;
+    hi = min(P.V, lo + P.chunk);
+  } else {
+    lo = s_j * P.chunk2;
+    hi = min(P.V, lo + P.chunk2);
   }
-  const int lo = s_j * P.chunk, hi = min(P.V, lo + P.chunk);
   const int tok = block_select<DT, VEC>(W, lo, hi, s_thr);
   if (tid == 0) {
     if (m < ne) P.out_tokens[static_cast<int64_t>(b) * (k + 1) + m] = tok;
-    if (P.resid_mass) P.resid_mass[b] = s_fallback ? 0.0f : s_tot;
+    if (P.resid_mass) P.resid_mass[b] = (m < L && !s_fallback) ? s_tot : 0.0f;
   }
+}
+
+// ------------------------------------------------------- cluster accept
+
+// Sampling accept with one thread-block cluster per request (used when V fits
+// the cluster: V <= 16 CTAs x 1024 threads x 16 logits).  Every CTA merges
+// the request's partials and reaches the same decision.  The final draw
+// then needs one pass over V of the weights w_v -- max(0, p_m - q_m) after a
+// rejection, p_L after a full accept -- and nothing else: each thread
+// computes the weights of its 16 contiguous logits and keeps them in
+// registers, the CTA scans the thread sums, the CTAs swap their slice totals
+// through distributed shared memory, and the CTA whose slice holds u * total
+// finds the token from its threads' registers.  No atomics, no second pass.
+constexpr int kClusterThreads = 1024;
+constexpr int kClusterWarps = kClusterThreads / 32;
+constexpr int kSegment = 16;  // contiguous logits per thread
+constexpr int kMaxCluster = 16;
+
+// Inclusive scan of one value per thread over a 1024-thread block.  Returns
+// the thread's exclusive prefix; `total` receives the block sum.
+__device__ __forceinline__ float block_exclusive_scan_1024(float v, float &total) {
+  __shared__ float s_w[kClusterWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float incl = warp_inclusive_scan(v, lane);
+  if (lane == 31) s_w[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const float t = s_w[lane];
+    const float ti = warp_inclusive_scan(t, lane);
+    s_w[lane] = ti - t;  // exclusive prefix of each warp
+  }
+  __syncthreads();
+  float tot = 0.0f;
+  // the block total is the last warp's exclusive prefix plus its own total
+  const float last_incl = __shfl_sync(0xffffffffu, incl, 31);
+  const float warp_base = s_w[warp];
+  if (warp == kClusterWarps - 1) tot = warp_base + last_incl;
+  __shared__ float s_total;
+  if (threadIdx.x == kClusterThreads - 1) s_total = tot;
+  __syncthreads();
+  total = s_total;
+  const float ex = warp_base + incl - v;
+  __syncthreads();
+  return ex;
+}
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kClusterThreads) chain_sample_accept_cluster_kernel(const ChainParams P) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int CS = P.cluster;
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int b = blockIdx.x / CS;
+  const int k = P.k, rows = 2 * k + 1, nc = P.nc;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ float sM[kMaxRows], sS[kMaxRows], sX[kMaxRows];
+  __shared__ int sTok[SPEC_MAX_K];
+  __shared__ float sU[SPEC_MAX_K + 1], sP[SPEC_MAX_K], sQ[SPEC_MAX_K];
+  __shared__ float s_slot[2], s_tots[kMaxCluster];
+  __shared__ int s_m, s_wpick[kClusterWarps], s_wlast[kClusterWarps];
+
+  const Prologue pr = read_request(P, b, sTok, sU, true);
+  pdl_wait();
+  if (pr.bad) {  // every CTA of the cluster leaves here; no shared memory was exchanged
+    if (rank == 0) write_common<true>(P, b, pr.bad, pr.L, 0, 0, sTok, sP, sQ, true, -1);
+    return;
+  }
+  const int L = pr.L;
+  const int nrr = 2 * L + 1;
+  const Partial *base = P.part + static_cast<int64_t>(b) * rows * nc;
+  auto row_of = [&](int rr) { return rr <= L ? rr : (k + 1) + (rr - L - 1); };
+  auto tok_chunk = [&](int rr) {
+    const int pos = rr <= L ? rr : rr - L - 1;
+    return pos < L ? sTok[pos] / P.chunk : -1;
+  };
+  for (int rr = warp; rr < nrr; rr += 2 * kClusterWarps) {
+    const int rr2 = rr + kClusterWarps;
+    RowStats a, bb;
+    warp_merge_two_rows<true>(base + static_cast<int64_t>(row_of(rr)) * nc,
+                              rr2 < nrr ? base + static_cast<int64_t>(row_of(rr2)) * nc : nullptr, nc, P.c,
+                              tok_chunk(rr), rr2 < nrr ? tok_chunk(rr2) : -1, a, bb);
+    if (lane == 0) {
+      sM[rr] = a.M;
+      sS[rr] = a.S;
+      sX[rr] = a.X;
+      if (rr2 < nrr) {
+        sM[rr2] = bb.M;
+        sS[rr2] = bb.S;
+        sX[rr2] = bb.X;
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int m = 0;
+    for (int i = 0; i < L; ++i) {
+      const float p = ex2((sX[i] - sM[i]) * P.c) / sS[i];
+      const float q = ex2((sX[L + 1 + i] - sM[L + 1 + i]) * P.c) / sS[L + 1 + i];
+      sP[i] = p;
+      sQ[i] = q;
+      if (m == i && sU[i] * q < p) m = i + 1;
+    }
+    s_m = m;
+  }
+  __syncthreads();
+  const int m = s_m;
+  const int ne = max(0, min(m + 1, pr.cap));
+  if (rank == 0) write_common<true>(P, b, 0, L, m, ne, sTok, sP, sQ, false, -1);
+
+  // weights of this thread's 16 logits: the residual after a rejection,
+  // p_L after a full accept
+  Weights W = m < L
+                  ? Weights{row_ptr<DT>(P.target, P.t_req, P.row, b, m), row_ptr<DT>(P.draftl, P.d_req, P.row, b, m),
+                            sM[m], sM[L + 1 + m], 1.0f / sS[m], 1.0f / sS[L + 1 + m], P.c}
+                  : Weights{row_ptr<DT>(P.target, P.t_req, P.row, b, L), nullptr, sM[L], 0.0f, 1.0f / sS[L], 0.0f,
+                            P.c};
+  const int lo = min(P.V, rank * P.slice), hi = min(P.V, lo + P.slice);
+  const int v0 = lo + tid * kSegment;
+  const float u_final = sU[k];
+  int phase = 0;
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    float w[kSegment];
+    weights8<DT, VEC>(W, v0, hi, w);
+    weights8<DT, VEC>(W, v0 + 8, hi, w + 8);
+    float seg = 0.0f;
+#pragma unroll
+    for (int e = 0; e < kSegment; ++e) seg += w[e];
+    float cta_total;
+    const float ex = block_exclusive_scan_1024(seg, cta_total);
+    // swap slice totals through distributed shared memory: thread r fetches
+    // rank r's total, so the remote loads are in flight together
+    if (tid == 0) s_slot[phase & 1] = cta_total;
+    cluster.sync();
+    if (tid < CS) s_tots[tid] = *cluster.map_shared_rank(&s_slot[phase & 1], tid);
+    __syncthreads();
+    float total = 0.0f, rbase = 0.0f, thr = 0.0f;
+    int rsel = -1, rlast = 0;
+    for (int r = 0; r < CS; ++r) total += s_tots[r];
+    thr = u_final * total;
+    {
+      float cum = 0.0f;
+      for (int r = 0; r < CS; ++r) {
+        const float t = s_tots[r];
+        if (t > 0.0f) rlast = r;
+        if (rsel < 0 && cum + t > thr) {
+          rsel = r;
+          rbase = cum;
+        }
+        cum += t;
+      }
+    }
+    __syncthreads();
+    ++phase;
+    if (!(total > 0.0f) && m < L && attempt == 0) {
+      // zero residual mass (only through rounding): draw from p_m instead
+      W.b = nullptr;
+      W.beta = 0.0f;
+      continue;
+    }
+    cluster_arrive();  // this CTA reads no other CTA's shared memory from here on
+    const int owner = rsel >= 0 ? rsel : rlast;
+    if (rank == owner) {
+      // the first thread whose running prefix passes the threshold holds the
+      // token; each warp proposes its first such lane, thread 0 takes the
+      // first proposing warp
+      const float tl = rsel >= 0 ? thr - rbase : INFINITY;
+      int lastp = -1;
+#pragma unroll
+      for (int e = 0; e < kSegment; ++e)
+        if (w[e] > 0.0f) lastp = v0 + e;
+      const unsigned cross = __ballot_sync(0xffffffffu, ex + seg > tl);
+      int pick = -1;
+      if (cross && lane == __ffs(cross) - 1) {
+        float run = ex;
+#pragma unroll
+        for (int e = 0; e < kSegment; ++e) {
+          run += w[e];
+          if (pick < 0 && run > tl) pick = v0 + e;
+        }
+        if (pick < 0) pick = lastp;
+      }
+      if (cross) pick = __shfl_sync(0xffffffffu, pick, __ffs(cross) - 1);
+      for (int o = 16; o > 0; o >>= 1) lastp = max(lastp, __shfl_xor_sync(0xffffffffu, lastp, o));
+      if (lane == 0) {
+        s_wpick[warp] = cross ? pick : -1;
+        s_wlast[warp] = lastp;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        int tok = -1, last = -1;
+        for (int i = 0; i < kClusterWarps; ++i) {
+          if (tok < 0 && s_wpick[i] >= 0) tok = s_wpick[i];
+          last = max(last, s_wlast[i]);
+        }
+        if (tok < 0) tok = last;
+        if (m < ne) P.out_tokens[static_cast<int64_t>(b) * (k + 1) + m] = tok;
+        if (P.resid_mass) P.resid_mass[b] = (m < L && W.b != nullptr) ? total : 0.0f;
+      }
+    }
+    break;
+  }
+  cluster_wait();  // no CTA leaves while another may still read its slots
 }
 
 // ------------------------------------------------------------------- host
@@ -417,7 +677,28 @@ static cudaError_t launch_chain_t(const ChainParams &P, bool sample, cudaStream_
       chain_stats_kernel<DT, true, VEC><<<grid1, kThreads, 0, st>>>(P);
     });
     if (e != cudaSuccess) return e;
-    const unsigned grid2 = static_cast<unsigned>(static_cast<long long>(P.B) * P.nc);
+    if (P.cluster > 0) {
+      auto kern = chain_sample_accept_cluster_kernel<DT, VEC>;
+      if (P.cluster > 8) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+      }
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(P.B) * P.cluster));
+      cfg.blockDim = dim3(kClusterThreads);
+      cfg.stream = st;
+      cudaLaunchAttribute attr[2];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = P.cluster;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[1].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 2;
+      return trace_launch_ex("chain_sample_accept_cluster", st, [&] { return cudaLaunchKernelEx(&cfg, kern, P); });
+    }
+    const unsigned grid2 = static_cast<unsigned>(static_cast<long long>(P.B) * P.nc2);
     return trace_launch_ex("chain_sample_accept", st, [&] {
       return launch_dependent(chain_sample_accept_kernel<DT, VEC>, grid2, st, P);
     });

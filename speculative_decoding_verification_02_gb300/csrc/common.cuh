@@ -6,6 +6,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "spec_verify.h"
@@ -33,6 +34,14 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Split cluster barrier: arrive once this CTA has finished reading other
+// CTAs' shared memory, wait just before exiting, so that no CTA leaves while
+// another may still read from it -- without stalling at the end.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------- loads
 
@@ -270,22 +279,84 @@ __device__ __forceinline__ uint4 load16(const uint4 *p) {
 }
 
 // Statistics of row[v0, v1) for the calling thread (strided over the block).
-// Folds one batch of kBatch 16-byte groups (the raw words, unpacked again in
-// each pass to keep few registers live) into the running (m, s, idx).
-template <int DT, bool SOFTMAX>
-__device__ __forceinline__ void fold_batch(const uint4 *g, int first_elem, float c, float &m, float &s,
-                                           int &idx) {
-  constexpr int EPG = Elems<DT>::kPerGroup;
+// Maximum of the logits of one batch of kBatch 16-byte groups: bf16 pairs
+// are compared two at a time.
+template <int DT>
+__device__ __forceinline__ float batch_max(const uint4 *g) {
+  if (DT == SPEC_DTYPE_BF16) {
+    auto h2 = [](uint32_t w) { return *reinterpret_cast<const __nv_bfloat162 *>(&w); };
+    __nv_bfloat162 mx = h2(g[0].x);
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (u) mx = __hmax2(mx, h2(g[u].x));
+      mx = __hmax2(mx, h2(g[u].y));
+      mx = __hmax2(mx, h2(g[u].z));
+      mx = __hmax2(mx, h2(g[u].w));
+    }
+    return fmaxf(__low2float(mx), __high2float(mx));
+  }
   float bm = -INFINITY;
 #pragma unroll
   for (int u = 0; u < kBatch; ++u) {
-    float x[EPG];
-    unpack16<DT>(g[u], x);
-#pragma unroll
-    for (int e = 0; e < EPG; ++e) bm = fmaxf(bm, x[e]);
+    bm = fmaxf(bm, fmaxf(fmaxf(__uint_as_float(g[u].x), __uint_as_float(g[u].y)),
+                         fmaxf(__uint_as_float(g[u].z), __uint_as_float(g[u].w))));
   }
+  return bm;
+}
+
+// Adds 2^(x c - mc) over the batch into the two-lane accumulator: one packed
+// FMA per two logits, one ex2 per logit, one packed add per two.
+template <int DT>
+__device__ __forceinline__ void batch_sumexp(const uint4 *g, float c, float mc, float2 &acc) {
+  const float2 cc = make_float2(c, c), nm = make_float2(-mc, -mc);
+  auto fold = [&](float a, float b) {
+    const float2 z = __ffma2_rn(make_float2(a, b), cc, nm);
+    acc = __fadd2_rn(acc, make_float2(ex2(z.x), ex2(z.y)));
+  };
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) {
+    if (DT == SPEC_DTYPE_BF16) {
+      fold(bf16_lo(g[u].x), bf16_hi(g[u].x));
+      fold(bf16_lo(g[u].y), bf16_hi(g[u].y));
+      fold(bf16_lo(g[u].z), bf16_hi(g[u].z));
+      fold(bf16_lo(g[u].w), bf16_hi(g[u].w));
+    } else {
+      fold(__uint_as_float(g[u].x), __uint_as_float(g[u].y));
+      fold(__uint_as_float(g[u].z), __uint_as_float(g[u].w));
+    }
+  }
+}
+
+// The logit at index `tok` if it lies in group g (whose first logit has index
+// gstart), else -inf.
+template <int DT>
+__device__ __forceinline__ float group_logit(const uint4 &g, int gstart, int tok) {
+  constexpr int EPG = Elems<DT>::kPerGroup;
+  const unsigned off = static_cast<unsigned>(tok - gstart);
+  if (off >= static_cast<unsigned>(EPG)) return -INFINITY;
+  const unsigned wi = DT == SPEC_DTYPE_BF16 ? off >> 1 : off;
+  const uint32_t w = wi == 0 ? g.x : wi == 1 ? g.y : wi == 2 ? g.z : g.w;
+  if (DT == SPEC_DTYPE_F32) return __uint_as_float(w);
+  return (off & 1) ? bf16_hi(w) : bf16_lo(w);
+}
+
+// Folds one batch into the running (m, two-lane sum, idx), and picks up the
+// logit at index `tok` (-1: none) into xt.
+template <int DT, bool SOFTMAX>
+__device__ __forceinline__ void fold_batch(const uint4 *g, int first_elem, float c, float &m, float2 &s2,
+                                           int &idx, int tok, float &xt) {
+  constexpr int EPG = Elems<DT>::kPerGroup;
+  if (tok >= 0) {
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) xt = fmaxf(xt, group_logit<DT>(g[u], first_elem + u * kThreads * EPG, tok));
+  }
+  const float bm = batch_max<DT>(g);
   if (bm > m) {  // a new running max: rescale the sum, find its first index
-    if (SOFTMAX) s *= ex2((m - bm) * c);
+    if (SOFTMAX) {
+      const float f = ex2((m - bm) * c);
+      s2.x *= f;
+      s2.y *= f;
+    }
     m = bm;
     int first = kNoIndex;
 #pragma unroll
@@ -298,30 +369,23 @@ __device__ __forceinline__ void fold_batch(const uint4 *g, int first_elem, float
     }
     idx = first;
   }
-  if (SOFTMAX && m != -INFINITY) {
-    const float mc = m * c;
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      float x[EPG];
-      unpack16<DT>(g[u], x);
-#pragma unroll
-      for (int e = 0; e < EPG; ++e) s += ex2(fmaf(x[e], c, -mc));
-    }
-  }
+  if (SOFTMAX && m != -INFINITY) batch_sumexp<DT>(g, c, m * c, s2);
 }
 
 // Statistics of row[v0, v1) for the calling thread (strided over the block):
-// running max m, sum of 2^((x - m) c), first index of the max.  The next
-// batch of loads is issued before the current one is folded, so each thread
-// keeps two batches of 16-byte loads in flight.
+// running max m, sum of 2^((x - m) c), first index of the max, and the logit
+// at index `tok` if this thread reads it (xt, else left as is; tok = -1 for
+// none).  The next batch of loads is issued before the current one is
+// folded, so each thread keeps two batches of 16-byte loads in flight.
 template <int DT, bool SOFTMAX, bool VEC, int LD>
 __device__ __forceinline__ void thread_chunk_stats(const char *row, int v0, int v1, float c,
-                                                   float &m, float &s, int &idx) {
+                                                   float &m, float &s, int &idx, int tok, float &xt) {
   constexpr int EPG = Elems<DT>::kPerGroup;
   constexpr int ES = Elems<DT>::kSize;
   constexpr uint32_t kNegInf = DT == SPEC_DTYPE_F32 ? 0xff800000u : 0xff80ff80u;  // -inf words
   constexpr int kStride = kThreads * kBatch;
   int vtail = v0;
+  float2 s2 = make_float2(s, 0.0f);
   if (VEC) {
     const int ng = (v1 - v0) / EPG;
     const uint4 *base = reinterpret_cast<const uint4 *>(row + static_cast<int64_t>(v0) * ES);
@@ -341,14 +405,16 @@ __device__ __forceinline__ void thread_chunk_stats(const char *row, int v0, int 
           nxt[u] = gi < ng ? load16<LD>(base + gi) : make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
         }
       }
-      fold_batch<DT, SOFTMAX>(cur, v0 + g0 * EPG, c, m, s, idx);
+      fold_batch<DT, SOFTMAX>(cur, v0 + g0 * EPG, c, m, s2, idx, tok, xt);
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) cur[u] = nxt[u];
     }
     vtail = v0 + ng * EPG;
   }
+  s = s2.x + s2.y;
   for (int v = vtail + threadIdx.x; v < v1; v += kThreads) {
     const float x = load_one<DT>(row, v);
+    if (v == tok) xt = x;
     if (x > m) {
       if (SOFTMAX) s *= ex2((m - x) * c);
       m = x;
@@ -360,22 +426,28 @@ __device__ __forceinline__ void thread_chunk_stats(const char *row, int v0, int 
 
 // Block-wide merge; the result is valid in thread 0.
 template <bool SOFTMAX>
-__device__ __forceinline__ void block_merge(float &m, float &s, int &idx, float c) {
-  __shared__ float sm[kWarps], ss[kWarps];
+__device__ __forceinline__ void block_merge(float &m, float &s, int &idx, float c, float &xt) {
+  __shared__ float sm[kWarps], ss[kWarps], sx[kWarps];
   __shared__ int si[kWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (SOFTMAX) warp_merge_stats(m, s, idx, c); else warp_merge_argmax(m, idx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) xt = fmaxf(xt, __shfl_xor_sync(0xffffffffu, xt, o));
   if (lane == 0) {
     sm[warp] = m;
     ss[warp] = s;
     si[warp] = idx;
+    sx[warp] = xt;
   }
   __syncthreads();
   if (warp == 0) {
     m = lane < kWarps ? sm[lane] : -INFINITY;
     s = lane < kWarps ? ss[lane] : 0.0f;
     idx = lane < kWarps ? si[lane] : kNoIndex;
+    xt = lane < kWarps ? sx[lane] : -INFINITY;
     if (SOFTMAX) warp_merge_stats(m, s, idx, c); else warp_merge_argmax(m, idx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) xt = fmaxf(xt, __shfl_xor_sync(0xffffffffu, xt, o));
   }
 }
 
@@ -388,7 +460,7 @@ __device__ __forceinline__ float thread_chunk_weight_sum(const Weights &W, int v
   if (VEC) {
     const int ng = (v1 - v0) / EPG;
     const uint4 *ga = reinterpret_cast<const uint4 *>(W.a + static_cast<int64_t>(v0) * ES);
-    const uint4 *gb = reinterpret_cast<const uint4 *>(W.b + static_cast<int64_t>(v0) * ES);
+    const uint4 *gb = W.b != nullptr ? reinterpret_cast<const uint4 *>(W.b + static_cast<int64_t>(v0) * ES) : nullptr;
     for (int g0 = threadIdx.x; g0 < ng; g0 += kThreads * kBatch) {
       uint4 A[kBatch], Bv[kBatch];
 #pragma unroll
@@ -396,7 +468,7 @@ __device__ __forceinline__ float thread_chunk_weight_sum(const Weights &W, int v
         const int gi = g0 + u * kThreads;
         if (gi < ng) {
           A[u] = load16<LD>(ga + gi);
-          Bv[u] = load16<LD>(gb + gi);
+          if (W.b != nullptr) Bv[u] = load16<LD>(gb + gi);
         }
       }
 #pragma unroll
@@ -404,7 +476,7 @@ __device__ __forceinline__ float thread_chunk_weight_sum(const Weights &W, int v
         if (g0 + u * kThreads < ng) {
           float a[EPG], bb[EPG];
           unpack16<DT>(A[u], a);
-          unpack16<DT>(Bv[u], bb);
+          if (W.b != nullptr) unpack16<DT>(Bv[u], bb);
 #pragma unroll
           for (int e = 0; e < EPG; ++e) acc += weight_at<DT>(W, a[e], bb[e]);
         }
@@ -413,7 +485,7 @@ __device__ __forceinline__ float thread_chunk_weight_sum(const Weights &W, int v
     vtail = v0 + ng * EPG;
   }
   for (int v = vtail + threadIdx.x; v < v1; v += kThreads)
-    acc += weight_at<DT>(W, load_one<DT>(W.a, v), load_one<DT>(W.b, v));
+    acc += weight_at<DT>(W, load_one<DT>(W.a, v), W.b != nullptr ? load_one<DT>(W.b, v) : -INFINITY);
   return acc;
 }
 

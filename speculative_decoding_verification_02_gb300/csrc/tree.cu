@@ -163,10 +163,10 @@ __global__ void __launch_bounds__(kThreads) tree_walk_kernel(const TreeParams P)
     const char *trow = node_row<DT>(P.target, P.t_req, P.row, b, node);
 
     if (P.greedy) {
-      float m = -INFINITY, s = 0.0f;
+      float m = -INFINITY, s = 0.0f, xt = -INFINITY;
       int idx = kNoIndex;
-      thread_chunk_stats<DT, false, VEC, kLoadCached>(trow, lo, hi, 1.0f, m, s, idx);
-      block_merge<false>(m, s, idx, 1.0f);
+      thread_chunk_stats<DT, false, VEC, kLoadCached>(trow, lo, hi, 1.0f, m, s, idx, -1, xt);
+      block_merge<false>(m, s, idx, 1.0f, xt);
       Slot mine{m, 0.0f, 0.0f, 0.0f, idx, 0.0f, 0, 0};
       exchange(mine);
       float M = -INFINITY;
@@ -197,10 +197,10 @@ __global__ void __launch_bounds__(kThreads) tree_walk_kernel(const TreeParams P)
     const char *drow = nkids > 0 ? node_row<DT>(P.draftl, P.d_req, P.row, b, node) : nullptr;
     Slot mine{-INFINITY, 0.0f, -INFINITY, 0.0f, kNoIndex, 0.0f, 0, 0};
     {
-      float m = -INFINITY, s = 0.0f;
+      float m = -INFINITY, s = 0.0f, xt = -INFINITY;
       int idx = kNoIndex;
-      thread_chunk_stats<DT, true, VEC, kLoadCached>(trow, lo, hi, c, m, s, idx);
-      block_merge<true>(m, s, idx, c);
+      thread_chunk_stats<DT, true, VEC, kLoadCached>(trow, lo, hi, c, m, s, idx, -1, xt);
+      block_merge<true>(m, s, idx, c, xt);
       if (tid == 0) {
         mine.mt = m;
         mine.st = s;
@@ -211,8 +211,8 @@ __global__ void __launch_bounds__(kThreads) tree_walk_kernel(const TreeParams P)
         m = -INFINITY;
         s = 0.0f;
         idx = kNoIndex;
-        thread_chunk_stats<DT, true, VEC, kLoadCached>(drow, lo, hi, c, m, s, idx);
-        block_merge<true>(m, s, idx, c);
+        thread_chunk_stats<DT, true, VEC, kLoadCached>(drow, lo, hi, c, m, s, idx, -1, xt);
+        block_merge<true>(m, s, idx, c, xt);
         if (tid == 0) {
           mine.md = m;
           mine.sd = s;
