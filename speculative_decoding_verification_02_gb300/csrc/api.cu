@@ -1,6 +1,7 @@
 // C ABI of libspecverify.so: argument checks, workspace layout, launch
 // geometry, error mapping and tracing.  The arithmetic lives in chain.cu,
 // tree.cu and ngram.cu.
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -46,13 +47,24 @@ int stream_chunk(int dtype, long long rows_total, int V) {
   return static_cast<int>(bytes / es);
 }
 
-int accept_chunk(int dtype) { return 16384 / elem_size(dtype); }
+// Chunks of the chunked accept kernel: about one wave of its CTAs (two per
+// SM) over the whole batch, at least 4,096 logits, a multiple of 2,048, at
+// most 64 sub-chunks of 256 x 16 bytes.
+int accept_chunk(int B, int V, int dtype) {
+  const long long per_req = std::max<long long>(1, 2 * kSmCount / std::max(B, 1));
+  long long chunk = (V + per_req - 1) / per_req;
+  chunk = (chunk + 2047) / 2048 * 2048;
+  const long long cap = 64LL * 256 * (16 / elem_size(dtype));
+  return static_cast<int>(std::min(std::max<long long>(chunk, 4096), cap));
+}
+
+int sub_chunk(int dtype) { return 256 * (16 / elem_size(dtype)); }
 
 // Workspace: per-(row, chunk) statistics, then for sampling the residual
 // mass per chunk and one arrival counter per request.  Nothing in it needs
 // initialising: the counters are zeroed by the first kernel of each call.
 struct ChainLayout {
-  int nc, chunk, nc2, chunk2;
+  int nc, chunk, nc2, chunk2, nsub;
   size_t part, part2, counter2, total;
 };
 
@@ -60,14 +72,15 @@ ChainLayout chain_layout(bool sample, int B, int k, int V, int dtype) {
   ChainLayout L{};
   L.chunk = stream_chunk(dtype, static_cast<long long>(B) * (sample ? 2LL * k + 1 : k + 1LL), V);
   L.nc = (V + L.chunk - 1) / L.chunk;
-  L.chunk2 = accept_chunk(dtype);
+  L.chunk2 = accept_chunk(B, V, dtype);
   L.nc2 = (V + L.chunk2 - 1) / L.chunk2;
+  L.nsub = (V + sub_chunk(dtype) - 1) / sub_chunk(dtype);
   const size_t rows = sample ? 2 * static_cast<size_t>(k) + 1 : static_cast<size_t>(k) + 1;
   size_t off = 0;
   L.part = off;
   off = round_up(off + sizeof(Partial) * B * rows * L.nc, 256);
   L.part2 = off;
-  off = round_up(off + (sample ? sizeof(float) * B * L.nc2 : 0), 256);
+  off = round_up(off + (sample ? sizeof(float) * B * L.nsub : 0), 256);
   L.counter2 = off;
   off = round_up(off + (sample ? sizeof(int) * B : 0), 256);
   L.total = off;
@@ -287,6 +300,7 @@ static int chain_common(bool sample, const void *target, int64_t t_req, const vo
   P.chunk = L.chunk;
   P.nc2 = L.nc2;
   P.chunk2 = L.chunk2;
+  P.nsub = L.nsub;
   P.c = sample ? static_cast<float>(1.4426950408889634 / static_cast<double>(T)) : 1.0f;
   P.draft = draft;
   P.draft_len = draft_len;

@@ -39,6 +39,8 @@ namespace sv {
 
 constexpr int kMaxRows = 2 * SPEC_MAX_K + 1;
 constexpr int kPickCache = 512;  // chunk weights kept in shared memory by warp_pick
+constexpr int kMaxSubs = 64;     // sub-chunks per CTA of the chunked accept kernel
+constexpr int kSubBatch = 8;     // sub-chunk groups whose loads are in flight together
 
 // Arrival counter with release (this thread's earlier writes become visible
 // first) and acquire (the caller sees what earlier arrivals published).
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
   __shared__ float sM[kMaxRows], sS[kMaxRows], sX[kMaxRows];
   __shared__ int sTok[SPEC_MAX_K];
   __shared__ float sU[SPEC_MAX_K + 1], sP[SPEC_MAX_K], sQ[SPEC_MAX_K];
-  __shared__ float s_red[kWarps];
+  __shared__ float s_sub[kWarps][kMaxSubs];
   __shared__ float s_wcache[kPickCache];
   __shared__ int s_last, s_j, s_m;
   __shared__ float s_thr, s_tot;
@@ -393,24 +395,63 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
                             sM[m], sM[L + 1 + m], 1.0f / sS[m], 1.0f / sS[L + 1 + m], P.c}
                   : Weights{row_ptr<DT>(P.target, P.t_req, P.row, b, L), nullptr, sM[L], 0.0f, 1.0f / sS[L], 0.0f,
                             P.c};
-  const int nc2 = P.nc2;
+  // Per sub-chunk of kThreads 16-byte groups (each thread adds up its one
+  // group of it), so the last CTA only has to scan one sub-chunk.
+  constexpr int EPG = Elems<DT>::kPerGroup;
+  constexpr int ES = Elems<DT>::kSize;
+  const int sub = kThreads * EPG;
   const int v0 = j * P.chunk2, v1 = min(P.V, v0 + P.chunk2);
-  const float acc = warp_sum(thread_chunk_weight_sum<DT, VEC, kLoadL2>(W, v0, v1));
-  if (lane == 0) s_red[warp] = acc;
-  __syncthreads();
-  if (tid == 0) {
-    float t = 0.0f;
-    for (int w = 0; w < kWarps; ++w) t += s_red[w];
-    P.part2[static_cast<int64_t>(b) * nc2 + j] = t;
-    s_last = atomic_add_acq_rel(P.counter2 + b, 1) == nc2 - 1;  // publishes part2, sees the others'
+  const int nsub = (v1 - v0 + sub - 1) / sub;  // <= kMaxSubs by the choice of chunk2
+  for (int i0 = 0; i0 < nsub; i0 += kSubBatch) {
+    uint4 A[kSubBatch], Bv[kSubBatch];
+    bool full[kSubBatch];
+#pragma unroll
+    for (int q = 0; q < kSubBatch; ++q) {
+      const int gv = v0 + ((i0 + q) * kThreads + tid) * EPG;  // first logit of this thread's group
+      full[q] = VEC && i0 + q < nsub && gv + EPG <= v1;
+      if (full[q]) {
+        A[q] = __ldcg(reinterpret_cast<const uint4 *>(W.a + static_cast<int64_t>(gv) * ES));
+        if (W.b != nullptr) Bv[q] = __ldcg(reinterpret_cast<const uint4 *>(W.b + static_cast<int64_t>(gv) * ES));
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kSubBatch; ++q) {
+      if (i0 + q >= nsub) break;
+      const int gv = v0 + ((i0 + q) * kThreads + tid) * EPG;
+      float ws = 0.0f;
+      if (full[q]) {
+        float a[EPG], bb[EPG];
+        unpack16<DT>(A[q], a);
+        if (W.b != nullptr) unpack16<DT>(Bv[q], bb);
+#pragma unroll
+        for (int e = 0; e < EPG; ++e) ws += weight_at<DT>(W, a[e], bb[e]);
+      } else {
+        for (int e = 0; e < EPG; ++e) {
+          const int v = gv + e;
+          if (v < v1)
+            ws += weight_at<DT>(W, load_one<DT>(W.a, v), W.b != nullptr ? load_one<DT>(W.b, v) : -INFINITY);
+        }
+      }
+      ws = warp_sum(ws);
+      if (lane == 0) s_sub[warp][i0 + q] = ws;
+    }
   }
+  __syncthreads();
+  const int nsub_all = P.nsub;
+  float *part2 = P.part2 + static_cast<int64_t>(b) * nsub_all;
+  if (tid < nsub) {
+    float t = 0.0f;
+    for (int w = 0; w < kWarps; ++w) t += s_sub[w][tid];
+    part2[v0 / sub + tid] = t;
+  }
+  __syncthreads();
+  if (tid == 0) s_last = atomic_add_acq_rel(P.counter2 + b, 1) == P.nc2 - 1;  // publishes part2 (cumulative)
   __syncthreads();
   if (!s_last) return;
   if (warp == 0) {
-    const float *pp = P.part2 + static_cast<int64_t>(b) * nc2;
     int js;
     float th, tot;
-    warp_pick([&](int jj) { return __ldcg(pp + jj); }, nc2, u_final, s_wcache, kPickCache, js, th, tot);
+    warp_pick([&](int jj) { return __ldcg(part2 + jj); }, nsub_all, u_final, s_wcache, kPickCache, js, th, tot);
     const bool fallback = !(tot > 0.0f) && m < L;
     if (fallback) {
       // zero residual mass (only through rounding): draw from p_m instead,
@@ -437,8 +478,8 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
     lo = s_j * P.chunk;
     hi = min(P.V, lo + P.chunk);
   } else {
-    lo = s_j * P.chunk2;
-    hi = min(P.V, lo + P.chunk2);
+    lo = s_j * sub;
+    hi = min(P.V, lo + sub);
   }
   const int tok = block_select<DT, VEC>(W, lo, hi, s_thr);
   if (tid == 0) {

@@ -327,13 +327,9 @@ __device__ __forceinline__ void batch_sumexp(const uint4 *g, float c, float mc, 
   }
 }
 
-// The logit at index `tok` if it lies in group g (whose first logit has index
-// gstart), else -inf.
+// The logit at offset `off` (< 16 bytes' worth of logits) within group g.
 template <int DT>
-__device__ __forceinline__ float group_logit(const uint4 &g, int gstart, int tok) {
-  constexpr int EPG = Elems<DT>::kPerGroup;
-  const unsigned off = static_cast<unsigned>(tok - gstart);
-  if (off >= static_cast<unsigned>(EPG)) return -INFINITY;
+__device__ __forceinline__ float group_logit(const uint4 &g, unsigned off) {
   const unsigned wi = DT == SPEC_DTYPE_BF16 ? off >> 1 : off;
   const uint32_t w = wi == 0 ? g.x : wi == 1 ? g.y : wi == 2 ? g.z : g.w;
   if (DT == SPEC_DTYPE_F32) return __uint_as_float(w);
@@ -341,14 +337,21 @@ __device__ __forceinline__ float group_logit(const uint4 &g, int gstart, int tok
 }
 
 // Folds one batch into the running (m, two-lane sum, idx), and picks up the
-// logit at index `tok` (-1: none) into xt.
+// logit at index `tok` (-1: none) into xt.  The batch's groups start at
+// logits first_elem + u * kThreads * EPG, u < kBatch.
 template <int DT, bool SOFTMAX>
 __device__ __forceinline__ void fold_batch(const uint4 *g, int first_elem, float c, float &m, float2 &s2,
                                            int &idx, int tok, float &xt) {
   constexpr int EPG = Elems<DT>::kPerGroup;
-  if (tok >= 0) {
+  constexpr int kSpan = kThreads * EPG;  // logits between a thread's consecutive groups
+  static_assert((kSpan & (kSpan - 1)) == 0, "group spacing must be a power of two");
+  // does the drafted token fall in one of this batch's groups?  (rare)
+  const unsigned d = static_cast<unsigned>(tok - first_elem);
+  if (d < static_cast<unsigned>(kBatch * kSpan) && (d & (kSpan - 1)) < static_cast<unsigned>(EPG)) {
+    const unsigned u = d / kSpan, off = d & (kSpan - 1);
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) xt = fmaxf(xt, group_logit<DT>(g[u], first_elem + u * kThreads * EPG, tok));
+    for (int q = 0; q < kBatch; ++q)
+      if (q == static_cast<int>(u)) xt = group_logit<DT>(g[q], off);
   }
   const float bm = batch_max<DT>(g);
   if (bm > m) {  // a new running max: rescale the sum, find its first index
@@ -365,7 +368,7 @@ __device__ __forceinline__ void fold_batch(const uint4 *g, int first_elem, float
       unpack16<DT>(g[u], x);
 #pragma unroll
       for (int e = EPG - 1; e >= 0; --e)
-        if (x[e] == bm) first = first_elem + u * kThreads * EPG + e;
+        if (x[e] == bm) first = first_elem + u * kSpan + e;
     }
     idx = first;
   }
@@ -375,8 +378,9 @@ __device__ __forceinline__ void fold_batch(const uint4 *g, int first_elem, float
 // Statistics of row[v0, v1) for the calling thread (strided over the block):
 // running max m, sum of 2^((x - m) c), first index of the max, and the logit
 // at index `tok` if this thread reads it (xt, else left as is; tok = -1 for
-// none).  The next batch of loads is issued before the current one is
-// folded, so each thread keeps two batches of 16-byte loads in flight.
+// none).  Full batches are loaded without predicates at fixed offsets from a
+// pointer that advances by one batch stride; two batches are in flight
+// (ping-pong), the last, partial batch is loaded with bounds checks.
 template <int DT, bool SOFTMAX, bool VEC, int LD>
 __device__ __forceinline__ void thread_chunk_stats(const char *row, int v0, int v1, float c,
                                                    float &m, float &s, int &idx, int tok, float &xt) {
@@ -388,26 +392,39 @@ __device__ __forceinline__ void thread_chunk_stats(const char *row, int v0, int 
   float2 s2 = make_float2(s, 0.0f);
   if (VEC) {
     const int ng = (v1 - v0) / EPG;
-    const uint4 *base = reinterpret_cast<const uint4 *>(row + static_cast<int64_t>(v0) * ES);
-    uint4 cur[kBatch], nxt[kBatch];
-    int g0 = threadIdx.x;
+    const uint4 *p = reinterpret_cast<const uint4 *>(row + static_cast<int64_t>(v0) * ES) + threadIdx.x;
+    // this thread's groups: threadIdx.x + i * kThreads, i < mine
+    const int mine = ng > static_cast<int>(threadIdx.x) ? (ng - 1 - static_cast<int>(threadIdx.x)) / kThreads + 1 : 0;
+    const int nfull = mine / kBatch;  // batches whose kBatch groups all exist
+    int e0 = v0 + static_cast<int>(threadIdx.x) * EPG;  // first logit of the current batch
+    auto load_batch = [&](uint4 *g, const uint4 *q) {
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int gi = g0 + u * kThreads;
-      cur[u] = gi < ng ? load16<LD>(base + gi) : make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
+      for (int u = 0; u < kBatch; ++u) g[u] = load16<LD>(q + u * kThreads);
+    };
+    uint4 ga[kBatch], gb[kBatch];
+    int i = 0;
+    if (nfull > 0) load_batch(ga, p);
+    for (; i + 2 <= nfull; i += 2) {
+      load_batch(gb, p + kStride);
+      fold_batch<DT, SOFTMAX>(ga, e0, c, m, s2, idx, tok, xt);
+      e0 += kStride * EPG;
+      if (i + 2 < nfull) load_batch(ga, p + 2 * kStride);
+      fold_batch<DT, SOFTMAX>(gb, e0, c, m, s2, idx, tok, xt);
+      e0 += kStride * EPG;
+      p += 2 * kStride;
     }
-    for (; g0 < ng; g0 += kStride) {
-      const int g1 = g0 + kStride;
-      if (g1 < ng) {
+    if (i < nfull) {  // an odd full batch is already in ga
+      fold_batch<DT, SOFTMAX>(ga, e0, c, m, s2, idx, tok, xt);
+      e0 += kStride * EPG;
+      p += kStride;
+      ++i;
+    }
+    const int rest = mine - nfull * kBatch;  // groups of a last, partial batch
+    if (rest > 0) {
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int gi = g1 + u * kThreads;
-          nxt[u] = gi < ng ? load16<LD>(base + gi) : make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
-        }
-      }
-      fold_batch<DT, SOFTMAX>(cur, v0 + g0 * EPG, c, m, s2, idx, tok, xt);
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) cur[u] = nxt[u];
+      for (int u = 0; u < kBatch; ++u)
+        ga[u] = u < rest ? load16<LD>(p + u * kThreads) : make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
+      fold_batch<DT, SOFTMAX>(ga, e0, c, m, s2, idx, tok, xt);
     }
     vtail = v0 + ng * EPG;
   }

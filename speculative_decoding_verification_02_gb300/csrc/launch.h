@@ -19,13 +19,14 @@ struct ChainParams {
   int dtype, B, k, V;
   int nc, chunk;    // streaming pass: chunks per row, logits per chunk
   int nc2, chunk2;  // chunked accept kernel: chunks per row, logits per chunk
+  int nsub;         // sub-chunks (256 groups of 16 bytes) per row in part2
   float c;          // log2(e) / T
   const int32_t *draft, *draft_len, *max_emit;
   const float *uniforms;
   int32_t *accepted, *out_tokens, *n_emit, *status;
   float *p_tok, *q_tok, *resid_mass;
   Partial *part;     // [B][rows][nc] streaming-pass statistics
-  float *part2;      // [B][nc2] mass of the final draw's weights per chunk
+  float *part2;      // [B][nsub] mass of the final draw's weights per sub-chunk
   int *counter2;     // [B] arrival counter of the residual pass
   int cluster;       // sampling accept: CTAs per request (0 = chunked accept kernel)
   int slice;         // logits per CTA of the cluster accept kernel

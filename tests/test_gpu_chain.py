@@ -263,3 +263,20 @@ def test_workspace_reuse_and_graph_replay():
         g.replay()
         torch.cuda.synchronize()
         check_chain_sample(prob, host(o), r)
+
+
+@pytest.mark.parametrize("seed,B,k,V,dtype,T", [(21, 160, 4, 3001, "bf16", 0.9), (22, 170, 3, 2500, "fp32", 1.0),
+                                               (23, 2, 4, 300_000, "bf16", 1.0), (24, 200, 6, 40_003, "bf16", 1.1)])
+def test_sample_parity_chunked_accept_path(seed, B, k, V, dtype, T):
+    """Shapes that take the chunked accept kernel (too many requests for one
+    wave of clusters, or V beyond a cluster's reach)."""
+    prob = workloads.chain_problem(seed, B, k, V, dtype, T, target_std=1.5,
+                                   noise_std=np.linspace(0.3, 2.0, B).astype(np.float32))
+    rng = np.random.default_rng(seed)
+    draft_len = rng.integers(0, k + 1, B).astype(np.int32)
+    max_emit = rng.integers(1, k + 2, B).astype(np.int32)
+    g = _run_sample(prob, draft_len, max_emit)
+    r = _oracle_sample(prob, draft_len, max_emit)
+    stats = check_chain_sample(prob, g, r, draft_len=draft_len)
+    print("near-threshold", stats)
+    assert (r["accepted"] < draft_len).any() and (r["accepted"] == draft_len).any()
