@@ -1,19 +1,27 @@
 """Benchmark of the verify-and-accept step on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload vocab248k|batch64|tree60|small]
+                    [--workload vocab248k|batch64|small|tree60|ngram]
 
-One step is one spec_verify_sample call (the whole chain path: row
-statistics, accept scan, residual or bonus draw) on one batch.  The default
-workload is the one the headline metric is quoted on: B=1 request, k=4
-drafted tokens, V=248,320 bf16 logits (9 verified rows per step).  Inputs
-rotate over 64 resident input sets (286 MB, more than twice the 126 MB L2) so
-no step reads logits from L2; the calls are replayed from a CUDA graph.
+One step is one pass of the path over one batch:
+  vocab248k  spec_verify_sample, B=1, k=4, V=248,320 bf16 (the default: the
+             workload the headline metric is quoted on; 9 rows per step)
+  batch64    spec_verify_sample, B=64, k=8, V=128,256 bf16 (1,088 rows)
+  small      spec_verify_sample, B=4, k=4, V=2,048 fp32 (36 rows)
+  tree60     spec_verify_tree, 16 trees of 60 nodes, V=128,256 bf16
+             (960 node rows per step)
+  ngram      spec_ngram_draft on 64 histories of 4,096 tokens, then
+             spec_verify_greedy of the drafts, V=32,000 fp32 (320 rows)
+Inputs rotate over enough resident copies that one cycle reads more than
+twice the 126 MB L2, so no step finds its logits in L2; the calls are
+replayed from a CUDA graph.
 
-Printed JSON line (rank 0): value = verified rows/s over all ranks, roofline
-of the dominant kernel against the measured HBM copy bandwidth, the oracle's
-CPU rate on the machine's host cores, the end-to-end rate through the C ABI with
-host buffers, SM clocks sampled during the run.
+Printed JSON line (rank 0): value = verified rows/s over all ranks; a
+roofline entry for the kernel with the largest share of device time (its
+algorithmic bytes per launch over its CUDA-event time, against the measured
+HBM copy bandwidth); the oracle's rate on the host cores; the end-to-end
+rate through the C ABI with host buffers (H2D of the inputs and D2H of the
+results inside the timed region); SM clocks sampled during the run.
 
 Multi-GPU: under torchrun every rank runs the same workload on its own GPU
 (independent replicas, no collective on the data path); the timing is the
@@ -40,34 +48,91 @@ METRIC = "verified logit rows/sec at V=248,320; achieved HBM GB/s vs GB300 peak"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 126 * 1024 * 1024
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-KERNEL_SOURCES = ["speculative_decoding_verification_02_gb300/csrc/chain.cu",
-                  "speculative_decoding_verification_02_gb300/csrc/common.cuh"]
+CSRC = "speculative_decoding_verification_02_gb300/csrc"
+KERNEL_SOURCES = {"chain": [f"{CSRC}/chain.cu", f"{CSRC}/common.cuh"],
+                  "tree": [f"{CSRC}/tree.cu", f"{CSRC}/common.cuh"],
+                  "ngram": [f"{CSRC}/ngram.cu", f"{CSRC}/chain.cu", f"{CSRC}/common.cuh"]}
 
 
-# --------------------------------------------------------------- workloads
+# ----------------------------------------------------------------- helpers
 
-def make_workload(name: str):
-    from speculative_decoding_verification_02_gb300 import workloads as W
-    if name == "vocab248k":
-        return W.chain_vocab248k(W.SEED_BASE + 3, B=1), "chain sampling verify, B=1, k=4, V=248,320 bf16 " \
-            "(t~N(0,3) with 5 ids +8, d=0.8t+N(0,1), T=1)"
-    if name == "batch64":
-        return W.chain_batch64(), "chain sampling verify, B=64, k=8, V=128,256 bf16 " \
-            "(t~N(0,2.5), d=t+N(0,s) s in {0.3,1,2}, T=0.7)"
-    if name == "small":
-        return W.chain_small(), "chain sampling verify, B=4, k=4, V=2048 fp32 (t~N(0,2), d=t+N(0,0.5), T=1)"
-    raise ValueError(name)
+def to_dev(x, dev):
+    import torch
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:
+        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(x).to(dev)
 
 
-def row_bytes(prob) -> int:
-    """Algorithmic bytes of one call's streaming pass: every target and draft
-    row read once."""
-    B, R, V = prob["target"].shape
-    es = 2 if prob["target"].dtype == np.uint16 else 4
-    return B * (2 * R - 1) * V * es
+def elem_bytes(a) -> int:
+    return 2 if a.dtype == np.uint16 else 4
 
 
-# ------------------------------------------------------------------ clocks
+def peak_hbm():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_sha(kind: str) -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str, kind: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, if the kernel sources are unchanged since the capture."""
+    path = os.path.join(PROFILE_DIR, f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha") != source_sha(kind):
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def dist_env():
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def reduce_max(value: float, device) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, device) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
 
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons every 200 ms while running."""
@@ -87,7 +152,7 @@ class ClockSampler:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                                           "-lms", "200", "-i", str(self.gpu)], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
-        except (OSError, FileNotFoundError):
+        except OSError:
             self.proc = None
         return self
 
@@ -123,139 +188,237 @@ class ClockSampler:
                 "samples": len(sms)}
 
 
-# ----------------------------------------------------------------- helpers
+# --------------------------------------------------------------- workloads
 
-def peak_hbm():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    try:
-        with open(path) as f:
-            return float(json.load(f)["hbm_gbs"]), "measured"
-    except (OSError, KeyError, ValueError):
-        return FALLBACK_HBM_GBS, "fallback"
+class ChainWorkload:
+    """spec_verify_sample on one chain problem."""
+    kind = "chain"
 
+    def __init__(self, name):
+        from speculative_decoding_verification_02_gb300 import workloads as W
+        if name == "vocab248k":
+            self.prob = W.chain_vocab248k(W.SEED_BASE + 3, B=1)
+            self.desc = ("chain sampling verify, B=1, k=4, V=248,320 bf16 "
+                         "(t~N(0,3) with 5 ids +8, d=0.8t+N(0,1), T=1)")
+        elif name == "batch64":
+            self.prob = W.chain_batch64()
+            self.desc = ("chain sampling verify, B=64, k=8, V=128,256 bf16 "
+                         "(t~N(0,2.5), d=t+N(0,s), s in {0.3,1,2}, T=0.7)")
+        else:
+            self.prob = W.chain_small()
+            self.desc = "chain sampling verify, B=4, k=4, V=2048 fp32 (t~N(0,2), d=t+N(0,0.5), T=1)"
+        p = self.prob
+        self.B, R, self.V = p["target"].shape
+        self.k = R - 1
+        self.es = elem_bytes(p["target"])
+        self.rows_per_step = self.B * (2 * self.k + 1)
+        self.set_bytes = self.rows_per_step * self.V * self.es
+        self.logits = "bf16" if self.es == 2 else "fp32"
 
-def source_sha() -> str:
-    h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
-    return h.hexdigest()[:16]
+    def device_set(self, dev, i):
+        import torch
+        p = self.prob
+        g = torch.Generator().manual_seed(1000 + i)
+        u = torch.rand((self.B, self.k + 1), generator=g).clamp_(max=1 - 2 ** -24) if i else \
+            torch.from_numpy(p["uniforms"])
+        return dict(T=to_dev(p["target"], dev), D=to_dev(p["draft_logits"], dev), X=to_dev(p["draft"], dev),
+                    U=u.to(dev))
 
+    def call(self, s, out, stream):
+        from speculative_decoding_verification_02_gb300 import api
+        return api.spec_verify_sample(s["T"], s["D"], s["X"], s["U"], self.prob["T"], out=out, stream=stream)
 
-def profiled_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary of this kernel and
-    workload, if the kernel sources are unchanged since the capture."""
-    path = os.path.join(PROFILE_DIR, f"{kernel}_{workload}.md")
-    if not os.path.exists(path):
+    result_keys = ("accepted", "out_tokens", "n_emit", "status")
+
+    def kernel_bytes(self, name, outs):
+        """Algorithmic bytes of one launch of kernel `name`, averaged over the
+        rotating sets (the draw's bytes depend on where each call stopped)."""
+        row = self.V * self.es
+        if name.startswith("chain_stats"):
+            return self.set_bytes
+        if name.startswith("chain_sample_accept"):
+            tot = 0.0
+            for o in outs:
+                acc = o["accepted"].cpu().numpy()
+                # a rejection reads the target and draft rows of the rejected
+                # position, a full accept the bonus row
+                tot += sum(2 * row if a < self.k else row for a in acc)
+            return tot / len(outs)
         return None
-    vals = {}
-    for line in open(path):
-        if ":" in line and line.strip().startswith("- "):
-            k, v = line.strip()[2:].split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
-    if vals.get("source_sha") != source_sha():
+
+    def oracle_call(self, n, threads):
+        """At least n requests through the oracle: a single-request workload is
+        broadcast to n requests (no copy), a batch is verified whole, repeatedly."""
+        import oracle
+        p = self.prob
+        if self.B == 1:
+            tgt = np.broadcast_to(p["target"][:1], (n,) + p["target"].shape[1:])
+            dl = np.broadcast_to(p["draft_logits"][:1], (n,) + p["draft_logits"].shape[1:])
+            idx = np.zeros(n, dtype=np.int64)
+            oracle.verify_sample(tgt, dl, p["draft"][idx], p["uniforms"][idx], p["T"], threads=threads)
+            return n * (2 * self.k + 1)
+        reps = max(1, -(-n // self.B))
+        for _ in range(reps):
+            oracle.verify_sample(p["target"], p["draft_logits"], p["draft"], p["uniforms"], p["T"], threads=threads)
+        return reps * self.B * (2 * self.k + 1)
+
+
+class TreeWorkload:
+    """spec_verify_tree on 16 draft trees of 60 nodes."""
+    kind = "tree"
+
+    def __init__(self, name):
+        from speculative_decoding_verification_02_gb300 import workloads as W
+        self.prob = W.tree60()
+        self.desc = ("EAGLE-style tree verify, B=16, 60-node trees of depth 6 with <=10 children, "
+                     "V=128,256 bf16 (t~N(0,3) with 5 ids +8, d=0.8t+N(0,1)), T=1")
+        p = self.prob
+        self.B, self.N, self.V = p["target"].shape
+        self.es = 2
+        self.rows_per_step = self.B * self.N
+        self.set_bytes = 2 * self.B * self.N * self.V * self.es
+        self.logits = "bf16"
+        self.kids = [set(int(x) for x in p["parents"][b] if x >= 0) for b in range(self.B)]
+
+    def device_set(self, dev, i):
+        p = self.prob
+        return dict(T=to_dev(p["target"], dev), D=to_dev(p["draft_logits"], dev), P=to_dev(p["parents"], dev),
+                    X=to_dev(p["node_tok"], dev), U=to_dev(p["uniforms"], dev))
+
+    def call(self, s, out, stream):
+        from speculative_decoding_verification_02_gb300 import api
+        return api.spec_verify_tree(s["T"], s["D"], s["P"], s["X"], s["U"], self.prob["T"], self.prob["depth"],
+                                    out=out, stream=stream)
+
+    result_keys = ("accepted_len", "path_nodes", "out_tokens", "n_emit", "status")
+
+    def kernel_bytes(self, name, outs):
+        """Rows the walk must read: each visited node's target row, and its
+        draft row when it has children (sibling passes re-read cached data)."""
+        row = self.V * self.es
+        tot = 0.0
+        for o in outs:
+            path = o["path_nodes"].cpu().numpy()
+            for b in range(self.B):
+                for u in path[b]:
+                    if u >= 0:
+                        tot += row * (2 if int(u) in self.kids[b] else 1)
+        return tot / len(outs)
+
+    def oracle_call(self, n, threads):
+        """At least n requests: the batch of trees is verified whole, repeatedly."""
+        import oracle
+        p = self.prob
+        reps = max(1, -(-n // self.B))
+        for _ in range(reps):
+            oracle.verify_tree(p["target"], p["draft_logits"], p["parents"], p["node_tok"], p["uniforms"], p["T"],
+                               p["depth"], threads=threads)
+        return reps * self.B * self.N
+
+
+class NgramWorkload:
+    """spec_ngram_draft, then spec_verify_greedy of its drafts."""
+    kind = "ngram"
+
+    def __init__(self, name):
+        from speculative_decoding_verification_02_gb300 import workloads as W
+        self.prob = W.ngram_problem(W.SEED_BASE + 2, boost=10.0)
+        self.desc = ("n-gram history-lookup draft + greedy verify, B=64, int32 history 4096 over V=32,000 "
+                     "with planted repeated spans 8-32, window 3, k=4; target N(0,1) fp32")
+        p = self.prob
+        self.B, self.H = p["history"].shape
+        self.k, self.V, self.w = p["k"], p["V"], p["window"]
+        self.es = 4
+        self.rows_per_step = self.B * (self.k + 1)
+        self.set_bytes = self.rows_per_step * self.V * 4 + self.B * self.H * 4
+        self.logits = "fp32"
+
+    def device_set(self, dev, i):
+        p = self.prob
+        return dict(H=to_dev(p["history"], dev), L=to_dev(p["hist_len"], dev), T=to_dev(p["target"], dev))
+
+    def call(self, s, out, stream):
+        from speculative_decoding_verification_02_gb300 import api
+        o1 = out[0] if out else None
+        o2 = out[1] if out else None
+        d = api.spec_ngram_draft(s["H"], s["L"], self.w, self.k, out=o1, stream=stream)
+        g = api.spec_verify_greedy(s["T"], d["draft"], d["draft_len"], out=o2, stream=stream)
+        return (d, g)
+
+    result_keys = None
+
+    def kernel_bytes(self, name, outs):
+        if name == "ngram_draft":
+            return self.B * self.H * 4
+        if name.startswith("chain_stats"):
+            tot = 0.0
+            for d, _ in outs:
+                lens = d["draft_len"].cpu().numpy()
+                tot += float(np.sum(lens + 1)) * self.V * self.es
+            return tot / len(outs)
         return None
-    try:
-        return float(vals["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+
+    def oracle_call(self, n, threads):
+        import oracle
+        p = self.prob
+        reps = max(1, n // self.B)
+        for _ in range(reps):
+            d, dl, _ = oracle.ngram_draft(p["history"], p["hist_len"], self.w, self.k)
+            oracle.verify_greedy(p["target"], d, dl)
+        return reps * self.rows_per_step
 
 
-def dist_env():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+WORKLOADS = {"vocab248k": ChainWorkload, "batch64": ChainWorkload, "small": ChainWorkload,
+             "tree60": TreeWorkload, "ngram": NgramWorkload}
 
 
-def reduce_max(value: float, device) -> float:
-    import torch
-    import torch.distributed as dist
-    if not (dist.is_available() and dist.is_initialized()):
-        return value
-    t = torch.tensor([value], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def reduce_sum(value: float, device) -> float:
-    import torch
-    import torch.distributed as dist
-    if not (dist.is_available() and dist.is_initialized()):
-        return value
-    t = torch.tensor([value], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
-
-
-def barrier():
-    import torch.distributed as dist
-    if dist.is_available() and dist.is_initialized():
-        dist.barrier()
-
-
-# --------------------------------------------------------------- CPU oracle
-
-def oracle_rate(prob, target_seconds: float, max_requests: int | None = None):
+def oracle_rate(wl, target_seconds: float):
     """Rows/s of the fp64 oracle on this host's cores over a bounded sample of
-    the workload (requests replicated from the problem, one call)."""
+    the workload (whole requests, sized to about target_seconds)."""
     import oracle
-    B, R, V = prob["target"].shape
     threads = oracle.max_threads()
-    # calibrate with one request, then size the sample to ~target_seconds
     t0 = time.perf_counter()
-    oracle.verify_sample(prob["target"][:1], prob["draft_logits"][:1], prob["draft"][:1], prob["uniforms"][:1],
-                         prob["T"], threads=1)
-    one = max(time.perf_counter() - t0, 1e-6)
-    n = max(1, int(target_seconds * threads / one))
-    if max_requests:
-        n = min(n, max_requests)
-    idx = np.arange(n) % B
-    tgt = np.broadcast_to(prob["target"][:1], (n,) + prob["target"].shape[1:]) if B == 1 else prob["target"][idx]
-    dl = np.broadcast_to(prob["draft_logits"][:1], (n,) + prob["draft_logits"].shape[1:]) if B == 1 \
-        else prob["draft_logits"][idx]
+    calib = wl.oracle_call(1, threads)   # one batch (or one request)
+    per_row = max(time.perf_counter() - t0, 1e-6) / calib
+    rows_per_req = calib if wl.B == 1 else calib / wl.B
+    n = max(1, int(target_seconds / per_row / rows_per_req))
     t0 = time.perf_counter()
-    oracle.verify_sample(tgt, dl, prob["draft"][idx], prob["uniforms"][idx], prob["T"], threads=threads)
+    rows = wl.oracle_call(n, threads)
     dt = time.perf_counter() - t0
-    rows = n * (2 * R - 1)
     return rows / dt, threads, n, dt
 
 
 # ------------------------------------------------------------ reference arm
 
-def run_reference(args, workload_name):
+def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    prob, desc = make_workload(workload_name)
     import oracle
-    B, R, V = prob["target"].shape
-    rows_per_step = B * (2 * R - 1)
-    threads = min(oracle.max_threads(), B)   # the oracle parallelises over requests
+    wl = WORKLOADS[args.workload](args.workload)
+    threads = min(oracle.max_threads(), wl.B)  # the oracle parallelises over requests
     budget = float(os.environ.get("SPEC_REF_SECONDS", "60"))
     t_start = time.perf_counter()
-    steps_done = 0
     for _ in range(args.warmup):
-        oracle.verify_sample(prob["target"], prob["draft_logits"], prob["draft"], prob["uniforms"], prob["T"],
-                             threads=threads)
+        wl.oracle_call(wl.B, threads)
         if time.perf_counter() - t_start > budget / 4:
             break
+    steps_done = rows = 0
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.verify_sample(prob["target"], prob["draft_logits"], prob["draft"], prob["uniforms"], prob["T"],
-                             threads=threads)
+        rows += wl.oracle_call(wl.B, threads)
         steps_done += 1
         if time.perf_counter() - t0 > budget:
             break
     dt = time.perf_counter() - t0
-    value = steps_done * rows_per_step / dt
+    value = rows / dt
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / steps_done,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": desc, "rows_per_step": rows_per_step},
+            "data": "synthetic", "config": {"workload": wl.desc, "rows_per_step": wl.rows_per_step},
             "cpu_baseline": {"kind": "oracle", "value": value, "unit": "rows/s", "cores": threads,
                              "sample": f"{steps_done} of {args.steps} steps timed (cap {budget:.0f} s), "
-                                       f"one call of the workload each"},
+                                       f"one batch of the workload each"},
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -263,7 +426,7 @@ def run_reference(args, workload_name):
 
 # -------------------------------------------------------------- our arm
 
-def run_ours(args, workload_name):
+def run_ours(args):
     import torch
     import torch.distributed as dist
 
@@ -277,43 +440,19 @@ def run_ours(args, workload_name):
     __graft_entry__.build()
     from speculative_decoding_verification_02_gb300 import api
 
-    prob, desc = make_workload(workload_name)
-    B, R, V = prob["target"].shape
-    k = R - 1
-    rows_per_step = B * (2 * k + 1)
-    step_bytes = row_bytes(prob)
-
-    def to_dev(x):
-        x = np.ascontiguousarray(x)
-        if x.dtype == np.uint16:
-            return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
-        return torch.from_numpy(x).to(dev)
-
-    # rotating input sets: enough copies that one cycle is > 2x L2
-    nsets = max(4, min(256, int(np.ceil(2 * L2_BYTES / step_bytes))))
-    nsets = int(2 ** np.ceil(np.log2(nsets)))
-    T0, D0 = to_dev(prob["target"]), to_dev(prob["draft_logits"])
-    X0, U0 = to_dev(prob["draft"]), to_dev(prob["uniforms"])
-    sets = []
-    rng = torch.Generator(device="cpu").manual_seed(1234)
-    for s in range(nsets):
-        # each set: the same logits at a different address, its own uniforms
-        u = torch.rand((B, k + 1), generator=rng).clamp_(max=1 - 2 ** -24).to(dev)
-        sets.append(dict(T=T0.clone(), D=D0.clone(), X=X0.clone(), U=u if s else U0.clone()))
-    outs = [None] * nsets
+    wl = WORKLOADS[args.workload](args.workload)
+    # rotating input sets: one cycle reads more than twice the L2
+    nsets = max(2, int(np.ceil(2 * L2_BYTES / wl.set_bytes)))
+    nsets = min(256, int(2 ** np.ceil(np.log2(nsets))))
+    if wl.kind == "tree":
+        nsets = 6   # a walk reads ~1/8 of a set; six sets put ~2.4x L2 between reuses
+    sets = [wl.device_set(dev, i) for i in range(nsets)]
     stream = torch.cuda.Stream(device=dev)
-
-    def call(i, out=None):
-        st = sets[i % nsets]
-        return api.spec_verify_sample(st["T"], st["D"], st["X"], st["U"], prob["T"], out=out, stream=stream)
-
     with torch.cuda.stream(stream):
-        for i in range(nsets):
-            outs[i] = call(i)
-    launches_per_call = None
+        outs = [wl.call(sets[i], None, stream) for i in range(nsets)]
     n0 = api.launch_count()
     with torch.cuda.stream(stream):
-        call(0, outs[0])
+        wl.call(sets[0], outs[0], stream)
     launches_per_call = api.launch_count() - n0
     torch.cuda.synchronize(dev)
 
@@ -322,7 +461,7 @@ def run_ours(args, workload_name):
     with torch.cuda.stream(stream):
         with torch.cuda.graph(graph, stream=stream):
             for i in range(nsets):
-                call(i, outs[i])
+                wl.call(sets[i], outs[i], stream)
     rem = args.steps % nsets
     graph_rem = None
     if rem:
@@ -330,17 +469,16 @@ def run_ours(args, workload_name):
         with torch.cuda.stream(stream):
             with torch.cuda.graph(graph_rem, stream=stream):
                 for i in range(rem):
-                    call(i, outs[i])
+                    wl.call(sets[i], outs[i], stream)
     torch.cuda.synchronize(dev)
 
     sampler = ClockSampler(local)
     with sampler:
-        # warm-up: W steps
         with torch.cuda.stream(stream):
             for _ in range(args.warmup // nsets):
                 graph.replay()
             for i in range(args.warmup % nsets):
-                call(i, outs[i])
+                wl.call(sets[i], outs[i], stream)
         torch.cuda.synchronize(dev)
         barrier()
         torch.cuda.synchronize(dev)
@@ -357,47 +495,60 @@ def run_ours(args, workload_name):
         ms = ev0.elapsed_time(ev1)
     clocks = sampler.summary()
     ms_max = reduce_max(ms, dev)
-    total_rows = reduce_sum(args.steps * rows_per_step, dev)
+    total_rows = reduce_sum(args.steps * wl.rows_per_step, dev)
     value = total_rows / (ms_max / 1e3)
 
-    # kernel timing pass: the same calls, each kernel bracketed by events
+    # kernel timing pass: the same calls eagerly, each kernel bracketed by
+    # CUDA events on the launching stream (dependent launches serialised)
     api.trace_enable(True)
     api.trace_collect()
+    reps = max(1, min(4, 256 // nsets))
     with torch.cuda.stream(stream):
-        for i in range(4 * nsets):
-            call(i, outs[i % nsets])
+        for r in range(reps):
+            for i in range(nsets):
+                wl.call(sets[i], outs[i], stream)
     torch.cuda.synchronize(dev)
     trace = api.trace_collect()
     api.trace_enable(False)
-    dom = max(trace.items(), key=lambda kv: kv[1][0])
-    dom_name, (dom_ms, dom_n) = dom
-    dom_avg_s = dom_ms / dom_n / 1e3
-    achieved = step_bytes / dom_avg_s / 1e9 if dom_name.startswith("chain_stats") else None
     peak, peak_kind = peak_hbm()
+    kernels = {}
+    for kname, (t_ms, cnt) in trace.items():
+        avg_s = t_ms / cnt / 1e3
+        nbytes = wl.kernel_bytes(kname, outs)
+        kernels[kname] = {"avg_us": avg_s * 1e6, "launches": cnt, "share": t_ms / sum(v[0] for v in trace.values()),
+                          "algorithmic_bytes_per_launch": nbytes,
+                          "achieved_gbs": (nbytes / avg_s / 1e9) if nbytes else None}
+    dom = max(kernels, key=lambda n: kernels[n]["avg_us"] * kernels[n]["launches"])
+    achieved = kernels[dom]["achieved_gbs"]
 
     # end to end through the C ABI with host buffers: H2D inputs, call, D2H results
-    steps_e2e = max(3, min(args.steps, 2000))
-    h_sets = []
-    for s in range(nsets):
-        h_sets.append({k2: v.cpu().pin_memory() for k2, v in sets[s].items()})
+    steps_e2e = max(3, min(args.steps, int(2e9 // max(wl.set_bytes, 1)), 2000))
+    n_host = max(1, min(4, nsets, int(1e9 // max(wl.set_bytes, 1))))
+    h_sets = [{k2: v.cpu().pin_memory() for k2, v in sets[i].items()} for i in range(n_host)]
     d_in = {k2: torch.empty_like(v) for k2, v in sets[0].items()}
-    d_out = call(0)
-    h_out = {k2: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k2, v in d_out.items()
-             if k2 in ("accepted", "out_tokens", "n_emit", "status")}
+    with torch.cuda.stream(stream):
+        d_out = wl.call(d_in, None, stream)
+    res = d_out if isinstance(d_out, tuple) else (d_out,)
+    keys = wl.result_keys
+    h_out = []
+    for o in res:
+        h_out.append({k2: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k2, v in o.items()
+                      if keys is None or k2 in keys})
     h2d = sum(v.numel() * v.element_size() for v in h_sets[0].values())
-    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
+    d2h = sum(v.numel() * v.element_size() for ho in h_out for v in ho.values())
     torch.cuda.synchronize(dev)
 
     def e2e_step(i):
-        hs = h_sets[i % nsets]
+        hs = h_sets[i % len(h_sets)]
         for k2 in d_in:
             d_in[k2].copy_(hs[k2], non_blocking=True)
-        o = api.spec_verify_sample(d_in["T"], d_in["D"], d_in["X"], d_in["U"], prob["T"], out=d_out, stream=stream)
-        for k2 in h_out:
-            h_out[k2].copy_(o[k2], non_blocking=True)
+        o = wl.call(d_in, d_out, stream)
+        for ho, oo in zip(h_out, o if isinstance(o, tuple) else (o,)):
+            for k2 in ho:
+                ho[k2].copy_(oo[k2], non_blocking=True)
 
     with torch.cuda.stream(stream):
-        for i in range(min(args.warmup, 50)):
+        for i in range(min(args.warmup, 3)):
             e2e_step(i)
     torch.cuda.synchronize(dev)
     barrier()
@@ -410,34 +561,31 @@ def run_ours(args, workload_name):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - t_wall
-    e2e_ms = max(e0.elapsed_time(e1), 1e3 * wall)
-    e2e_ms = reduce_max(e2e_ms, dev)
-    e2e_value = reduce_sum(steps_e2e * rows_per_step, dev) / (e2e_ms / 1e3)
+    e2e_ms = reduce_max(max(e0.elapsed_time(e1), 1e3 * wall), dev)
+    e2e_value = reduce_sum(steps_e2e * wl.rows_per_step, dev) / (e2e_ms / 1e3)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        rate, threads, n, dt = oracle_rate(prob, target_seconds=float(os.environ.get("SPEC_CPU_SECONDS", "10")))
+        rate, threads, n, dt = oracle_rate(wl, float(os.environ.get("SPEC_CPU_SECONDS", "10")))
         cpu = {"value": rate, "unit": "rows/s", "cores": threads, "kind": "oracle",
-               "sample": f"{n} requests of the workload in one oracle call ({dt:.1f} s, fp64, OpenMP)"}
+               "sample": f"{n} requests of the workload through the oracle ({dt:.1f} s, fp64, OpenMP over requests)"}
 
     if rank == 0:
-        traffic = profiled_traffic(dom_name, workload_name)
         line = {
             "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": desc, "rows_per_step": rows_per_step, "logits": "bf16" if
-                       prob["target"].dtype == np.uint16 else "fp32",
-                       "bytes_per_step": step_bytes, "parallelism": f"replicas x{ws}",
-                       "l2": f"inputs rotate over {nsets} resident sets ({nsets * step_bytes / 2**20:.0f} MiB > L2)",
-                       "launch": f"CUDA graph of {nsets} calls", "hbm_gbs_whole_step":
-                           step_bytes * args.steps / (ms_max / 1e3) / 1e9},
-            "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak,
-                         "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": (achieved / peak) if achieved else None,
-                         "traffic": traffic, "avg_launch_us": dom_avg_s * 1e6,
-                         "algorithmic_bytes_per_launch": step_bytes,
-                         "kernels": {n: {"avg_us": 1e3 * t / c, "launches": c} for n, (t, c) in trace.items()}},
+            "config": {"workload": wl.desc, "rows_per_step": wl.rows_per_step, "logits": wl.logits,
+                       "parallelism": f"replicas x{ws}",
+                       "l2": f"inputs rotate over {nsets} resident sets ({nsets * wl.set_bytes / 2**20:.0f} MiB, "
+                             f"more than twice the L2 between reuses)",
+                       "launch": f"CUDA graph of {nsets} calls"},
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+                         "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
+                         "traffic": profiled_traffic(dom, args.workload, wl.kind),
+                         "avg_launch_us": kernels[dom]["avg_us"],
+                         "algorithmic_bytes_per_launch": kernels[dom]["algorithmic_bytes_per_launch"],
+                         "kernels": kernels},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": steps_e2e},
@@ -456,14 +604,13 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200_000)
     ap.add_argument("--warmup", type=int, default=2_000)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="vocab248k", choices=["vocab248k", "batch64", "small"])
+    ap.add_argument("--workload", default="vocab248k", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
-    if args.warmup < 3:
-        args.warmup = 3
+    args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
-        return run_reference(args, args.workload)
-    return run_ours(args, args.workload)
+        return run_reference(args)
+    return run_ours(args)
 
 
 if __name__ == "__main__":

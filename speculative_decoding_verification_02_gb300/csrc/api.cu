@@ -88,9 +88,11 @@ ChainLayout chain_layout(bool sample, int B, int k, int V, int dtype) {
 }
 
 // Tree walk: one thread-block cluster per request, each CTA owns a slice of
-// V.  Eight CTAs unless the slice would not stay small.
-void tree_geometry(int V, int &cluster, int &slice) {
-  cluster = V >= 8 * 2048 ? 8 : (V >= 4 * 2048 ? 4 : (V >= 2 * 2048 ? 2 : 1));
+// V.  Up to sixteen CTAs (at least 2,048 logits each), but no more than keep
+// every cluster resident at once (one walk CTA per SM).
+void tree_geometry(int B, int V, int &cluster, int &slice) {
+  cluster = V >= 16 * 2048 ? 16 : V >= 8 * 2048 ? 8 : (V >= 4 * 2048 ? 4 : (V >= 2 * 2048 ? 2 : 1));
+  while (cluster > 1 && static_cast<long long>(B) * cluster > kSmCount) cluster /= 2;
   slice = ((V + cluster - 1) / cluster + 7) / 8 * 8;
 }
 
@@ -160,6 +162,11 @@ void count_launch() {
 }
 
 void set_last_error(const char *msg) { std::snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
+bool trace_enabled() {
+  std::lock_guard<std::mutex> g(g_trace_mu);
+  return g_trace_on;
+}
 
 }  // namespace sv
 
@@ -380,7 +387,9 @@ int spec_verify_tree(const void *target, int64_t target_req_stride, const void *
   P.N = N;
   P.V = V;
   P.max_depth = max_depth;
-  tree_geometry(V, P.cluster, P.slice);
+  tree_geometry(B, V, P.cluster, P.slice);
+  P.stage = 1;
+  if (tree_dynamic_smem(P) > 200 * 1024) P.stage = 0;  // very large V: re-read the slice instead
   P.c = greedy ? 1.0f : static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   P.greedy = greedy ? 1 : 0;
   P.parents = parents;

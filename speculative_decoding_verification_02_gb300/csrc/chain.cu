@@ -705,7 +705,7 @@ static cudaError_t launch_dependent(K kern, unsigned grid, cudaStream_t st, cons
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = trace_enabled() ? 0 : 1;
   return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
@@ -736,7 +736,7 @@ static cudaError_t launch_chain_t(const ChainParams &P, bool sample, cudaStream_
       attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
       attr[1].val.programmaticStreamSerializationAllowed = 1;
       cfg.attrs = attr;
-      cfg.numAttrs = 2;
+      cfg.numAttrs = trace_enabled() ? 1 : 2;
       return trace_launch_ex("chain_sample_accept_cluster", st, [&] { return cudaLaunchKernelEx(&cfg, kern, P); });
     }
     const unsigned grid2 = static_cast<unsigned>(static_cast<long long>(P.B) * P.nc2);

@@ -202,13 +202,16 @@ __device__ __forceinline__ void weights8(const Weights &W, int v0, int hi, float
 // multiple of 8.  Each thread takes a contiguous segment of kSelPerThread
 // elements (all its loads in flight at once), the block scans the segment
 // sums, and every thread whose prefix passes thr walks its own segment; the
-// smallest proposal wins.  Called by all kThreads threads; returns the same
+// smallest proposal wins.  Called by all NT threads; returns the same
 // value in every thread.
 constexpr int kSelPerThread = 32;
 
-template <int DT, bool VEC>
-__device__ int block_select(const Weights &W, int lo, int hi, float thr) {
-  __shared__ float s_wsum[kWarps];
+// fill8(v0, hi, w) writes the weights of elements [v0, v0 + 8) into w (0 for
+// elements >= hi).
+template <int NT = kThreads, class Fill8>
+__device__ int block_select_with(Fill8 &&fill8, int lo, int hi, float thr) {
+  constexpr int NW = NT / 32;
+  __shared__ float s_wsum[NW];
   __shared__ int s_pick, s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
@@ -217,11 +220,11 @@ __device__ int block_select(const Weights &W, int lo, int hi, float thr) {
   }
   float carry = 0.0f;
   int last_pos = -1;
-  for (int base = lo; base < hi; base += kThreads * kSelPerThread) {
+  for (int base = lo; base < hi; base += NT * kSelPerThread) {
     const int v0 = base + threadIdx.x * kSelPerThread;
     float w[kSelPerThread];
 #pragma unroll
-    for (int q = 0; q < kSelPerThread / 8; ++q) weights8<DT, VEC>(W, v0 + 8 * q, hi, w + 8 * q);
+    for (int q = 0; q < kSelPerThread / 8; ++q) fill8(v0 + 8 * q, hi, w + 8 * q);
     float ls = 0.0f;
 #pragma unroll
     for (int e = 0; e < kSelPerThread; ++e) {
@@ -233,7 +236,7 @@ __device__ int block_select(const Weights &W, int lo, int hi, float thr) {
     __syncthreads();
     float wbase = carry, total = carry;
 #pragma unroll
-    for (int i = 0; i < kWarps; ++i) {
+    for (int i = 0; i < NW; ++i) {
       if (i < warp) wbase += s_wsum[i];
       total += s_wsum[i];
     }
@@ -261,6 +264,11 @@ __device__ int block_select(const Weights &W, int lo, int hi, float thr) {
   const int r = s_pick != kNoIndex ? s_pick : s_last;
   __syncthreads();
   return r;
+}
+
+template <int DT, bool VEC, int NT = kThreads>
+__device__ int block_select(const Weights &W, int lo, int hi, float thr) {
+  return block_select_with<NT>([&](int v0, int h, float *w) { weights8<DT, VEC>(W, v0, h, w); }, lo, hi, thr);
 }
 
 // ------------------------------------------------------------ streaming
@@ -338,12 +346,12 @@ __device__ __forceinline__ float group_logit(const uint4 &g, unsigned off) {
 
 // Folds one batch into the running (m, two-lane sum, idx), and picks up the
 // logit at index `tok` (-1: none) into xt.  The batch's groups start at
-// logits first_elem + u * kThreads * EPG, u < kBatch.
-template <int DT, bool SOFTMAX>
+// logits first_elem + u * NT * EPG, u < kBatch.
+template <int DT, bool SOFTMAX, int NT = kThreads>
 __device__ __forceinline__ void fold_batch(const uint4 *g, int first_elem, float c, float &m, float2 &s2,
                                            int &idx, int tok, float &xt) {
   constexpr int EPG = Elems<DT>::kPerGroup;
-  constexpr int kSpan = kThreads * EPG;  // logits between a thread's consecutive groups
+  constexpr int kSpan = NT * EPG;  // logits between a thread's consecutive groups
   static_assert((kSpan & (kSpan - 1)) == 0, "group spacing must be a power of two");
   // does the drafted token fall in one of this batch's groups?  (rare)
   const unsigned d = static_cast<unsigned>(tok - first_elem);
@@ -381,40 +389,40 @@ __device__ __forceinline__ void fold_batch(const uint4 *g, int first_elem, float
 // none).  Full batches are loaded without predicates at fixed offsets from a
 // pointer that advances by one batch stride; two batches are in flight
 // (ping-pong), the last, partial batch is loaded with bounds checks.
-template <int DT, bool SOFTMAX, bool VEC, int LD>
+template <int DT, bool SOFTMAX, bool VEC, int LD, int NT = kThreads>
 __device__ __forceinline__ void thread_chunk_stats(const char *row, int v0, int v1, float c,
                                                    float &m, float &s, int &idx, int tok, float &xt) {
   constexpr int EPG = Elems<DT>::kPerGroup;
   constexpr int ES = Elems<DT>::kSize;
   constexpr uint32_t kNegInf = DT == SPEC_DTYPE_F32 ? 0xff800000u : 0xff80ff80u;  // -inf words
-  constexpr int kStride = kThreads * kBatch;
+  constexpr int kStride = NT * kBatch;
   int vtail = v0;
   float2 s2 = make_float2(s, 0.0f);
   if (VEC) {
     const int ng = (v1 - v0) / EPG;
     const uint4 *p = reinterpret_cast<const uint4 *>(row + static_cast<int64_t>(v0) * ES) + threadIdx.x;
-    // this thread's groups: threadIdx.x + i * kThreads, i < mine
-    const int mine = ng > static_cast<int>(threadIdx.x) ? (ng - 1 - static_cast<int>(threadIdx.x)) / kThreads + 1 : 0;
+    // this thread's groups: threadIdx.x + i * NT, i < mine
+    const int mine = ng > static_cast<int>(threadIdx.x) ? (ng - 1 - static_cast<int>(threadIdx.x)) / NT + 1 : 0;
     const int nfull = mine / kBatch;  // batches whose kBatch groups all exist
     int e0 = v0 + static_cast<int>(threadIdx.x) * EPG;  // first logit of the current batch
     auto load_batch = [&](uint4 *g, const uint4 *q) {
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) g[u] = load16<LD>(q + u * kThreads);
+      for (int u = 0; u < kBatch; ++u) g[u] = load16<LD>(q + u * NT);
     };
     uint4 ga[kBatch], gb[kBatch];
     int i = 0;
     if (nfull > 0) load_batch(ga, p);
     for (; i + 2 <= nfull; i += 2) {
       load_batch(gb, p + kStride);
-      fold_batch<DT, SOFTMAX>(ga, e0, c, m, s2, idx, tok, xt);
+      fold_batch<DT, SOFTMAX, NT>(ga, e0, c, m, s2, idx, tok, xt);
       e0 += kStride * EPG;
       if (i + 2 < nfull) load_batch(ga, p + 2 * kStride);
-      fold_batch<DT, SOFTMAX>(gb, e0, c, m, s2, idx, tok, xt);
+      fold_batch<DT, SOFTMAX, NT>(gb, e0, c, m, s2, idx, tok, xt);
       e0 += kStride * EPG;
       p += 2 * kStride;
     }
     if (i < nfull) {  // an odd full batch is already in ga
-      fold_batch<DT, SOFTMAX>(ga, e0, c, m, s2, idx, tok, xt);
+      fold_batch<DT, SOFTMAX, NT>(ga, e0, c, m, s2, idx, tok, xt);
       e0 += kStride * EPG;
       p += kStride;
       ++i;
@@ -423,13 +431,13 @@ __device__ __forceinline__ void thread_chunk_stats(const char *row, int v0, int 
     if (rest > 0) {
 #pragma unroll
       for (int u = 0; u < kBatch; ++u)
-        ga[u] = u < rest ? load16<LD>(p + u * kThreads) : make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
-      fold_batch<DT, SOFTMAX>(ga, e0, c, m, s2, idx, tok, xt);
+        ga[u] = u < rest ? load16<LD>(p + u * NT) : make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
+      fold_batch<DT, SOFTMAX, NT>(ga, e0, c, m, s2, idx, tok, xt);
     }
     vtail = v0 + ng * EPG;
   }
   s = s2.x + s2.y;
-  for (int v = vtail + threadIdx.x; v < v1; v += kThreads) {
+  for (int v = vtail + threadIdx.x; v < v1; v += NT) {
     const float x = load_one<DT>(row, v);
     if (v == tok) xt = x;
     if (x > m) {
@@ -442,10 +450,11 @@ __device__ __forceinline__ void thread_chunk_stats(const char *row, int v0, int 
 }
 
 // Block-wide merge; the result is valid in thread 0.
-template <bool SOFTMAX>
+template <bool SOFTMAX, int NT = kThreads>
 __device__ __forceinline__ void block_merge(float &m, float &s, int &idx, float c, float &xt) {
-  __shared__ float sm[kWarps], ss[kWarps], sx[kWarps];
-  __shared__ int si[kWarps];
+  constexpr int NW = NT / 32;
+  __shared__ float sm[NW], ss[NW], sx[NW];
+  __shared__ int si[NW];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (SOFTMAX) warp_merge_stats(m, s, idx, c); else warp_merge_argmax(m, idx);
 #pragma unroll
@@ -458,17 +467,17 @@ __device__ __forceinline__ void block_merge(float &m, float &s, int &idx, float 
   }
   __syncthreads();
   if (warp == 0) {
-    m = lane < kWarps ? sm[lane] : -INFINITY;
-    s = lane < kWarps ? ss[lane] : 0.0f;
-    idx = lane < kWarps ? si[lane] : kNoIndex;
-    xt = lane < kWarps ? sx[lane] : -INFINITY;
+    m = lane < NW ? sm[lane] : -INFINITY;
+    s = lane < NW ? ss[lane] : 0.0f;
+    idx = lane < NW ? si[lane] : kNoIndex;
+    xt = lane < NW ? sx[lane] : -INFINITY;
     if (SOFTMAX) warp_merge_stats(m, s, idx, c); else warp_merge_argmax(m, idx);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) xt = fmaxf(xt, __shfl_xor_sync(0xffffffffu, xt, o));
   }
 }
 
-template <int DT, bool VEC, int LD>
+template <int DT, bool VEC, int LD, int NT = kThreads>
 __device__ __forceinline__ float thread_chunk_weight_sum(const Weights &W, int v0, int v1) {
   constexpr int EPG = Elems<DT>::kPerGroup;
   constexpr int ES = Elems<DT>::kSize;
@@ -478,11 +487,11 @@ __device__ __forceinline__ float thread_chunk_weight_sum(const Weights &W, int v
     const int ng = (v1 - v0) / EPG;
     const uint4 *ga = reinterpret_cast<const uint4 *>(W.a + static_cast<int64_t>(v0) * ES);
     const uint4 *gb = W.b != nullptr ? reinterpret_cast<const uint4 *>(W.b + static_cast<int64_t>(v0) * ES) : nullptr;
-    for (int g0 = threadIdx.x; g0 < ng; g0 += kThreads * kBatch) {
+    for (int g0 = threadIdx.x; g0 < ng; g0 += NT * kBatch) {
       uint4 A[kBatch], Bv[kBatch];
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
-        const int gi = g0 + u * kThreads;
+        const int gi = g0 + u * NT;
         if (gi < ng) {
           A[u] = load16<LD>(ga + gi);
           if (W.b != nullptr) Bv[u] = load16<LD>(gb + gi);
@@ -490,7 +499,7 @@ __device__ __forceinline__ float thread_chunk_weight_sum(const Weights &W, int v
       }
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
-        if (g0 + u * kThreads < ng) {
+        if (g0 + u * NT < ng) {
           float a[EPG], bb[EPG];
           unpack16<DT>(A[u], a);
           if (W.b != nullptr) unpack16<DT>(Bv[u], bb);
@@ -501,7 +510,7 @@ __device__ __forceinline__ float thread_chunk_weight_sum(const Weights &W, int v
     }
     vtail = v0 + ng * EPG;
   }
-  for (int v = vtail + threadIdx.x; v < v1; v += kThreads)
+  for (int v = vtail + threadIdx.x; v < v1; v += NT)
     acc += weight_at<DT>(W, load_one<DT>(W.a, v), W.b != nullptr ? load_one<DT>(W.b, v) : -INFINITY);
   return acc;
 }

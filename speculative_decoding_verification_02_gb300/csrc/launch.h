@@ -39,6 +39,7 @@ struct TreeParams {
   int dtype, B, N, V, max_depth;
   int cluster;     // CTAs per request
   int slice;       // logits per CTA (multiple of 8)
+  int stage;       // 1: the first rejection at a node stages p and q of the slice in shared memory
   float c;         // log2(e) / T; unused when greedy
   int greedy;
   const int32_t *parents, *node_tok;
@@ -54,6 +55,7 @@ struct NgramParams {
 
 cudaError_t launch_chain(const ChainParams &P, bool sample, bool vec, cudaStream_t st);
 cudaError_t launch_tree(const TreeParams &P, bool vec, cudaStream_t st);
+size_t tree_dynamic_smem(const TreeParams &P);
 cudaError_t launch_ngram(const NgramParams &P, cudaStream_t st);
 
 // Tracing hooks (api.cu).  trace_begin returns a slot (or -1 when tracing is
@@ -63,6 +65,10 @@ void trace_end(int slot, cudaStream_t st);
 void count_launch();
 // Sets the message spec_last_error() returns on this thread.
 void set_last_error(const char *msg);
+// True while spec_trace_enable(1) is in force.  Traced calls launch their
+// dependent kernels without programmatic dependent launch, so that each
+// kernel's event pair brackets only its own execution.
+bool trace_enabled();
 
 template <class F>
 cudaError_t trace_launch(const char *name, cudaStream_t st, F &&launch) {

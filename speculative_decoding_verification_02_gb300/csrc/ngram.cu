@@ -13,7 +13,7 @@
 
 namespace sv {
 
-constexpr int kTile = 2048;  // start positions per tile
+constexpr int kTile = 8192;  // start positions per tile (32 KB of history)
 
 __global__ void __launch_bounds__(kThreads) ngram_kernel(const NgramParams P) {
   __shared__ int s_hist[kTile + SPEC_MAX_WINDOW];
@@ -38,7 +38,8 @@ __global__ void __launch_bounds__(kThreads) ngram_kernel(const NgramParams P) {
   for (int t1 = nstart; t1 > 0; t1 -= kTile) {
     const int t0 = max(0, t1 - kTile);
     // stage h[t0, t1 + w - 1): every start in [t0, t1) with its window
-    for (int i = tid; i < t1 - t0 + w - 1; i += kThreads) s_hist[i] = h[t0 + i];
+#pragma unroll 8
+    for (int i = tid; i < t1 - t0 + w - 1; i += kThreads) s_hist[i] = __ldg(h + t0 + i);
     __syncthreads();
     for (int i = t1 - 1 - tid; i >= t0; i -= kThreads) {
       bool same = true;
