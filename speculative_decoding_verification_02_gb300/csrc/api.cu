@@ -388,6 +388,7 @@ int spec_verify_tree(const void *target, int64_t target_req_stride, const void *
   P.V = V;
   P.max_depth = max_depth;
   tree_geometry(B, V, P.cluster, P.slice);
+  P.seg = ((P.slice + kTreeThreads - 1) / kTreeThreads + 7) / 8 * 8;
   P.stage = 1;
   if (tree_dynamic_smem(P) > 200 * 1024) P.stage = 0;  // very large V: re-read the slice instead
   P.c = greedy ? 1.0f : static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));

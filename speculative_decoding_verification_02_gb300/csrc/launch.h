@@ -32,6 +32,8 @@ struct ChainParams {
   int slice;         // logits per CTA of the cluster accept kernel
 };
 
+constexpr int kTreeThreads = 512;  // threads per tree-walk CTA
+
 struct TreeParams {
   const char *target;
   const char *draftl;
@@ -39,6 +41,7 @@ struct TreeParams {
   int dtype, B, N, V, max_depth;
   int cluster;     // CTAs per request
   int slice;       // logits per CTA (multiple of 8)
+  int seg;         // logits per thread: contiguous segments of the slice (multiple of 8)
   int stage;       // 1: the first rejection at a node stages p and q of the slice in shared memory
   float c;         // log2(e) / T; unused when greedy
   int greedy;
