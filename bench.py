@@ -234,8 +234,8 @@ class ChainWorkload:
         """Algorithmic bytes of one launch of kernel `name`, averaged over the
         rotating sets (the draw's bytes depend on where each call stopped)."""
         row = self.V * self.es
-        if name.startswith("chain_stats"):
-            return self.set_bytes
+        if name.startswith("chain_stats") or name.startswith("chain_fused"):
+            return self.set_bytes  # every row once (the fused kernel's draw re-reads two from L2)
         if name.startswith("chain_sample_accept"):
             tot = 0.0
             for o in outs:
@@ -350,7 +350,7 @@ class NgramWorkload:
     def kernel_bytes(self, name, outs):
         if name == "ngram_draft":
             return self.B * self.H * 4
-        if name.startswith("chain_stats"):
+        if name.startswith("chain_stats") or name.startswith("chain_fused"):
             tot = 0.0
             for d, _ in outs:
                 lens = d["draft_len"].cpu().numpy()

@@ -266,6 +266,28 @@ int spec_trace_collect(const char **names, double *total_ms, int64_t *launches, 
 /* Number of kernels this process has launched through the library. */
 int64_t spec_launch_count(void);
 
+/*
+ * Chain verification paths.  spec_verify_greedy and spec_verify_sample give
+ * the same results on either path; the paths differ in speed:
+ *   SPEC_CHAIN_TWO_PASS  a streaming pass over every row on all SMs, then an
+ *                        accept kernel (suits large batches: bandwidth-bound);
+ *   SPEC_CHAIN_FUSED     one thread-block cluster per request does the whole
+ *                        call in one launch and uses no workspace (suits
+ *                        small problems: latency-bound); when the requests'
+ *                        clusters cannot all be resident at once the call
+ *                        runs on the two-pass path instead;
+ *   SPEC_CHAIN_AUTO      the library picks per call (the default).
+ * spec_set_chain_path sets the path for calls made after it, process-wide;
+ * it returns SPEC_OK, or SPEC_EINVAL for an unknown value.  The workspace
+ * requirements of the entry points do not change with the path.  This
+ * switch has no counterpart in the method; it exists for tuning and so that
+ * both paths can be tested on any shape.
+ */
+#define SPEC_CHAIN_AUTO 0
+#define SPEC_CHAIN_TWO_PASS 1
+#define SPEC_CHAIN_FUSED 2
+int spec_set_chain_path(int path);
+
 #ifdef __cplusplus
 }
 #endif

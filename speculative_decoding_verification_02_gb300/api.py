@@ -22,6 +22,7 @@ SPEC_OK, SPEC_EINVAL, SPEC_EDTYPE, SPEC_EWORKSPACE, SPEC_ECUDA = 0, -1, -2, -3, 
 STATUS_OK, STATUS_TOKEN_RANGE, STATUS_BAD_TREE, STATUS_BAD_LENGTH = 0, 1, 2, 3
 DTYPE_F32, DTYPE_BF16 = 0, 1
 OP_NGRAM, OP_GREEDY, OP_SAMPLE, OP_TREE = 0, 1, 2, 3
+CHAIN_AUTO, CHAIN_TWO_PASS, CHAIN_FUSED = 0, 1, 2
 
 _lock = threading.Lock()
 _lib = None
@@ -60,6 +61,7 @@ def lib():
         L.spec_trace_collect.argtypes = [P, P, P, I]
         L.spec_launch_count.argtypes = []
         L.spec_launch_count.restype = ctypes.c_int64
+        L.spec_set_chain_path.argtypes = [I]
         _lib = L
         return L
 
@@ -139,6 +141,12 @@ def workspace(nbytes: int, device, stream=None) -> torch.Tensor:
             raise RuntimeError("workspace allocation is not 256-byte aligned")
         _workspaces[key] = ws
     return ws
+
+
+def set_chain_path(path: int):
+    """Chain verification path for later calls, process-wide: CHAIN_AUTO,
+    CHAIN_TWO_PASS or CHAIN_FUSED (same results, different speed)."""
+    _check(lib().spec_set_chain_path(int(path)), "spec_set_chain_path")
 
 
 def trace_enable(on: bool = True):

@@ -2,6 +2,7 @@
 // geometry, error mapping and tracing.  The arithmetic lives in chain.cu,
 // tree.cu and ngram.cu.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -37,6 +38,11 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // SM, large ones keep each CTA streaming long enough to amortise its
 // start-up and reduction.  The chunked accept kernel uses 16 KB chunks.
 constexpr long long kSmCount = 152;
+
+// Chain path (spec_set_chain_path).  In AUTO the fused kernel takes
+// vocabularies up to kFusedAutoMaxV, where it is as fast as the two-pass path.
+std::atomic<int> g_chain_path{SPEC_CHAIN_AUTO};
+constexpr int kFusedAutoMaxV = 8192;
 
 int stream_chunk(int dtype, long long rows_total, int V) {
   const long long es = elem_size(dtype);
@@ -248,6 +254,12 @@ int spec_trace_collect(const char **names, double *total_ms, int64_t *launches, 
   return static_cast<int>(nm.size());
 }
 
+int spec_set_chain_path(int path) {
+  if (path != SPEC_CHAIN_AUTO && path != SPEC_CHAIN_TWO_PASS && path != SPEC_CHAIN_FUSED) return SPEC_EINVAL;
+  g_chain_path.store(path, std::memory_order_relaxed);
+  return SPEC_OK;
+}
+
 int64_t spec_launch_count(void) {
   std::lock_guard<std::mutex> g(g_trace_mu);
   return g_launches;
@@ -322,10 +334,18 @@ static int chain_common(bool sample, const void *target, int64_t t_req, const vo
   P.resid_mass = resid_mass;
   P.counter2 = reinterpret_cast<int *>(ws + L.counter2);
   P.part = reinterpret_cast<Partial *>(ws + L.part);
-  cluster_geometry(B, V, P.cluster, P.slice);
-  if (!sample) P.cluster = 0;
   P.part2 = reinterpret_cast<float *>(ws + L.part2);
-  const cudaError_t e = launch_chain(P, sample, vec, as_stream(stream));
+  cudaError_t e;
+  const bool fvec = vec && V % (16 / es) == 0;  // the fused kernel's 16-byte path also wants V a multiple of a group
+  const int path = g_chain_path.load(std::memory_order_relaxed);
+  const bool want_fused = path == SPEC_CHAIN_FUSED || (path == SPEC_CHAIN_AUTO && V <= kFusedAutoMaxV);
+  if (want_fused && chain_fused_plan(P, sample, fvec)) {
+    e = launch_chain_fused(P, sample, fvec, as_stream(stream));
+  } else {
+    cluster_geometry(B, V, P.cluster, P.slice);
+    if (!sample) P.cluster = 0;
+    e = launch_chain(P, sample, vec, as_stream(stream));
+  }
   return e == cudaSuccess ? SPEC_OK : fail_cuda(e, sample ? "spec_verify_sample" : "spec_verify_greedy");
 }
 
@@ -388,7 +408,8 @@ int spec_verify_tree(const void *target, int64_t target_req_stride, const void *
   P.V = V;
   P.max_depth = max_depth;
   tree_geometry(B, V, P.cluster, P.slice);
-  P.seg = ((P.slice + kTreeThreads - 1) / kTreeThreads + 7) / 8 * 8;
+  const int epg = 16 / elem_size(dtype);
+  P.groups = ((P.slice + epg - 1) / epg + kTreeThreads - 1) / kTreeThreads;
   P.stage = 1;
   if (tree_dynamic_smem(P) > 200 * 1024) P.stage = 0;  // very large V: re-read the slice instead
   P.c = greedy ? 1.0f : static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
@@ -401,7 +422,8 @@ int spec_verify_tree(const void *target, int64_t target_req_stride, const void *
   P.out_tokens = out_tokens;
   P.n_emit = n_emit;
   P.status = status;
-  const cudaError_t e = launch_tree(P, vec, as_stream(stream));
+  // the cluster kernels' 16-byte path also wants V a multiple of a group
+  const cudaError_t e = launch_tree(P, vec && V % (16 / es) == 0, as_stream(stream));
   return e == cudaSuccess ? SPEC_OK : fail_cuda(e, "spec_verify_tree");
 }
 

@@ -30,6 +30,7 @@
 // No kernel waits on another CTA.
 #include <cooperative_groups.h>
 
+#include "chain_common.cuh"
 #include "common.cuh"
 #include "launch.h"
 
@@ -53,13 +54,6 @@ __device__ __forceinline__ int atomic_add_acq_rel(int *p, int v) {
 __device__ __forceinline__ Partial ld_partial(const Partial *p) {
   const float4 v = __ldcg(reinterpret_cast<const float4 *>(p));
   return Partial{v.x, v.y, __float_as_int(v.z), v.w};
-}
-
-template <int DT>
-__device__ __forceinline__ const char *row_ptr(const char *base, int64_t req_stride,
-                                               int64_t row_stride, int b, int i) {
-  return base + (static_cast<int64_t>(b) * req_stride + static_cast<int64_t>(i) * row_stride) *
-                    Elems<DT>::kSize;
 }
 
 // ------------------------------------------------------------ streaming pass
@@ -99,33 +93,6 @@ __global__ void __launch_bounds__(kThreads) chain_stats_kernel(const ChainParams
 }
 
 // --------------------------------------------------------------- accept scan
-
-// Inputs of one request, read before the dependency wait.
-struct Prologue {
-  int L, bad, cap;
-};
-
-__device__ Prologue read_request(const ChainParams &P, int b, int *sTok, float *sU, bool sample) {
-  __shared__ int s_bad, s_L;
-  const int tid = threadIdx.x, k = P.k;
-  __shared__ int s_cap;
-  if (tid == 0) {
-    const int L = P.draft_len ? P.draft_len[b] : k;
-    s_L = L;
-    s_bad = (L >= 0 && L <= k) ? SPEC_STATUS_OK : SPEC_STATUS_BAD_LENGTH;
-  }
-  if (tid == 32) s_cap = P.max_emit ? P.max_emit[b] : k + 1;
-  if (tid < k) sTok[tid] = P.draft[static_cast<int64_t>(b) * k + tid];
-  if (sample && tid >= 64 && tid <= 64 + k) sU[tid - 64] = P.uniforms[static_cast<int64_t>(b) * (k + 1) + tid - 64];
-  __syncthreads();
-  const int L = s_L;
-  if (s_bad == SPEC_STATUS_OK && tid < L && (sTok[tid] < 0 || sTok[tid] >= P.V))
-    atomicMax(&s_bad, SPEC_STATUS_TOKEN_RANGE);
-  __syncthreads();
-  Prologue pr{L, s_bad, s_cap};
-  __syncthreads();
-  return pr;
-}
 
 constexpr int kMergeUnroll = 4;  // partials per lane whose loads are issued together
 
@@ -252,37 +219,6 @@ __device__ __forceinline__ void warp_pick(W weight, int n, float u, float *cache
     for (int o = 16; o > 0; o >>= 1) lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, o));
     jsel = max(lastpos, 0);
     thr_local = INFINITY;
-  }
-}
-
-// The outputs that do not depend on the final draw (written once per request).
-template <bool SAMPLE>
-__device__ void write_common(const ChainParams &P, int b, int bad, int L, int m, int ne,
-                             const int *sTok, const float *sP, const float *sQ, bool final_known,
-                             int final_tok) {
-  const int k = P.k;
-  int32_t *out = P.out_tokens + static_cast<int64_t>(b) * (k + 1);
-  const int tid = threadIdx.x;
-  for (int j = tid; j <= k; j += kThreads) {
-    if (bad) {
-      out[j] = -1;
-    } else {
-      if (j == m && j < ne && !final_known) continue;  // the drawing CTA writes it
-      out[j] = j < ne ? (j < m ? sTok[j] : final_tok) : -1;
-    }
-  }
-  if (SAMPLE) {
-    for (int j = tid; j < k; j += kThreads) {
-      const bool ok = !bad && j < L;
-      if (P.p_tok) P.p_tok[static_cast<int64_t>(b) * k + j] = ok ? sP[j] : -1.0f;
-      if (P.q_tok) P.q_tok[static_cast<int64_t>(b) * k + j] = ok ? sQ[j] : -1.0f;
-    }
-  }
-  if (tid == 0) {
-    P.accepted[b] = bad ? 0 : m;
-    P.n_emit[b] = bad ? 0 : ne;
-    if (P.status) P.status[b] = bad;
-    if (SAMPLE && bad && P.resid_mass) P.resid_mass[b] = 0.0f;
   }
 }
 

@@ -1,0 +1,363 @@
+// Fused chain verification: one thread-block cluster per request performs
+// the whole call -- every row's statistics, the acceptance decision and the
+// final draw -- in one launch.  Sampling mode follows the acceptance rule of
+// "投机解码:为什么一个字都不改" (改进方案): accept x_i while
+// u_i q_i(x_i) < p_i(x_i), then draw from norm(max(0, p_m - q_m)) after a
+// rejection at m, or from p_L after a full accept; greedy mode accepts x_i
+// while x_i == argmax(row i) and emits argmax(row m)
+// ("第 13 篇：推理引擎一次猜几个字", ③ 伪代码).
+//
+// Each CTA of a request's cluster owns one slice of the vocabulary and each
+// of its warps one contiguous range of that slice (lanes interleaved, so
+// loads stay coalesced):
+//   1. rows are streamed kRowBatch at a time with all their loads in flight;
+//      each lane folds its groups of each row into (max, sum
+//      2^((x - max) c), first argmax) and warps merge those with redux and
+//      shuffle reductions;
+//   2. warp w merges rows w, w + 16, ... over the CTA's warps and pushes the
+//      CTA's statistics of the row into every CTA of the cluster
+//      (distributed shared memory); after one cluster barrier every CTA
+//      merges the slices in rank order and takes the same decision, the
+//      accepted prefix m;
+//   3. (sampling) each warp adds up the final draw's weights over its range;
+//      the slice masses are exchanged like the statistics, the rank whose
+//      slice holds u * total is found, and in that CTA a scan of the warp
+//      masses and a walk of the chosen warp's range give the token.
+// Used when the clusters of all requests are resident at once: one launch
+// then replaces the streaming pass and the accept kernel, and the workspace
+// is not touched.  The kernel waits for the previous grid in the stream
+// (programmatic dependent launch) before it reads anything.
+#include <cooperative_groups.h>
+
+#include <mutex>
+#include <vector>
+
+#include "chain_common.cuh"
+#include "common.cuh"
+#include "launch.h"
+#include "segments.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace sv {
+
+constexpr int kFusedWarps = kFusedThreads / 32;
+constexpr int kRowBatch = 4;  // rows whose loads are in flight together
+constexpr int kFusedMaxCluster = 16;
+constexpr int kFusedMaxRows = 2 * SPEC_MAX_K + 1;
+constexpr int kFusedMinSlice = 4096;  // fewest logits per CTA when choosing the cluster size
+
+struct __align__(16) RowPart {
+  float m, s;  // max, sum of 2^((x - m) c)
+  int i;       // first argmax
+  float pad;
+};
+
+// This lane's sum of the draw weights W over its groups (lane_group split of
+// [lo, hi), G rounds; logits >= hi weigh 0).
+template <int DT, bool VEC>
+__device__ __forceinline__ float lane_weight_sum(const Weights &W, int lo, int hi, int G) {
+  constexpr int EPG = Elems<DT>::kPerGroup;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float acc = 0.0f;
+  for (int j0 = 0; j0 < G; j0 += kBatch) {
+    const int g0 = lane_group(warp, j0, G, lane);  // round j0 + u: group g0 + 32 u
+    uint4 xa[kBatch], xb[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (j0 + u < G) {
+        xa[u] = load_group<DT, VEC>(W.a, lo + (g0 + 32 * u) * EPG, hi);
+        if (W.b) xb[u] = load_group<DT, VEC>(W.b, lo + (g0 + 32 * u) * EPG, hi);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (j0 + u < G) {
+        float x[EPG], y[EPG];
+        unpack16<DT>(xa[u], x);
+        if (W.b) unpack16<DT>(xb[u], y);
+#pragma unroll
+        for (int e = 0; e < EPG; ++e) acc += weight_at<DT>(W, x[e], W.b ? y[e] : 0.0f);
+      }
+    }
+  }
+  return acc;
+}
+
+template <int DT, bool VEC, bool SAMPLE>
+__global__ void __launch_bounds__(kFusedThreads) chain_fused_kernel(const ChainParams P) {
+  cg::cluster_group cluster = cg::this_cluster();
+  constexpr int EPG = Elems<DT>::kPerGroup;
+  const int CS = P.cluster;
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int b = blockIdx.x / CS;
+  const int k = P.k;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rows_max = SAMPLE ? 2 * k + 1 : k + 1;
+  extern __shared__ RowPart dyn_parts[];
+  RowPart *s_wpart = dyn_parts;                           // [warp][row] warp statistics
+  RowPart *s_cpart = dyn_parts + kFusedWarps * rows_max;  // [rank][row] slice statistics
+  __shared__ int sTok[SPEC_MAX_K], sOk[SPEC_MAX_K], sA[kFusedMaxRows];
+  __shared__ float sU[SPEC_MAX_K + 1], sP[SPEC_MAX_K], sQ[SPEC_MAX_K];
+  __shared__ float sM[kFusedMaxRows], sS[kFusedMaxRows], sX[kFusedMaxRows];
+  __shared__ float s_red[kFusedWarps], s_z[2][kFusedMaxCluster];
+  const RowPart kEmpty{-INFINITY, 0.0f, kNoIndex, 0.0f};
+
+  pdl_wait();  // the inputs may be the previous kernel's outputs
+  pdl_launch_dependents();
+  const Prologue pr = read_request(P, b, sTok, sU, SAMPLE);
+  if (pr.bad) {  // every CTA of the cluster leaves here; no shared memory was exchanged
+    if (rank == 0) write_common<SAMPLE>(P, b, pr.bad, pr.L, 0, 0, sTok, sP, sQ, true, -1);
+    return;
+  }
+  const int L = pr.L;
+  const int nrows = SAMPLE ? 2 * L + 1 : L + 1;  // target rows 0..L, then draft rows 0..L-1
+  auto row_of = [&](int rr) {
+    return rr <= L ? row_ptr<DT>(P.target, P.t_req, P.row, b, rr)
+                   : row_ptr<DT>(P.draftl, P.d_req, P.row, b, rr - L - 1);
+  };
+  const float c = P.c;
+  // the drafted tokens' logits (thread rr reads row rr's), in flight with the stream
+  float xtok = -INFINITY;
+  if (SAMPLE && tid < nrows) {
+    const int pos = tid <= L ? tid : tid - L - 1;
+    if (pos < L) xtok = load_one<DT>(row_of(tid), sTok[pos]);
+  }
+  const int lo = min(P.V, rank * P.slice), hi = min(P.V, lo + P.slice);
+  const int G = P.groups;  // rounds of 16-byte groups per lane
+
+  // ---- 1. row statistics over the slice, kRowBatch rows at a time
+  for (int rr0 = 0; rr0 < nrows; rr0 += kRowBatch) {
+    RowStats R[kRowBatch];
+    const char *rp[kRowBatch];
+#pragma unroll
+    for (int r = 0; r < kRowBatch; ++r) {
+      R[r] = row_stats_empty();
+      rp[r] = rr0 + r < nrows ? row_of(rr0 + r) : nullptr;
+    }
+    lane_rows_stats<DT, SAMPLE, VEC, kRowBatch>(rp, lo, hi, G, c, R);
+#pragma unroll
+    for (int r = 0; r < kRowBatch; ++r) {
+      if (rr0 + r < nrows) {
+        float m = R[r].m, s = R[r].s.x + R[r].s.y;
+        int i = R[r].i;
+        if (SAMPLE) warp_allmerge<true>(m, s, i, c);
+        else warp_allargmax(m, i);
+        if (lane == 0) s_wpart[warp * rows_max + rr0 + r] = RowPart{m, s, i, 0.0f};
+      }
+    }
+  }
+  if (SAMPLE && tid < nrows) sX[tid] = xtok;
+  __syncthreads();
+
+  // ---- 2. the CTA's statistics of each row, pushed into every CTA
+  for (int rr = warp; rr < nrows; rr += kFusedWarps) {
+    RowPart x = lane < kFusedWarps ? s_wpart[lane * rows_max + rr] : kEmpty;
+    if (SAMPLE) warp_allmerge<true>(x.m, x.s, x.i, c);
+    else warp_allargmax(x.m, x.i);
+    if (lane < CS) *cluster.map_shared_rank(&s_cpart[rank * rows_max + rr], lane) = x;
+  }
+  cluster.sync();
+  // every CTA merges the slices (lane r holds rank r) and decides alike
+  for (int rr = warp; rr < nrows; rr += kFusedWarps) {
+    RowPart x = lane < CS ? s_cpart[lane * rows_max + rr] : kEmpty;
+    if (SAMPLE) warp_allmerge<true>(x.m, x.s, x.i, c);
+    else warp_allargmax(x.m, x.i);
+    if (lane == 0) {
+      sM[rr] = x.m;
+      sS[rr] = x.s;
+      sA[rr] = x.i == kNoIndex ? 0 : x.i;
+    }
+  }
+  __syncthreads();
+  if (tid < L) {
+    if (SAMPLE) {
+      const float p = ex2((sX[tid] - sM[tid]) * c) / sS[tid];
+      const float q = ex2((sX[L + 1 + tid] - sM[L + 1 + tid]) * c) / sS[L + 1 + tid];
+      sP[tid] = p;
+      sQ[tid] = q;
+      sOk[tid] = sU[tid] * q < p;
+    } else {
+      sOk[tid] = sA[tid] == sTok[tid];
+    }
+  }
+  __syncthreads();
+  int m = L;  // the first rejected position
+  for (int i0 = 0; i0 < L; i0 += 32) {
+    const unsigned rej = __ballot_sync(0xffffffffu, i0 + lane < L && !sOk[i0 + lane]);
+    if (rej) {
+      m = i0 + __ffs(rej) - 1;
+      break;
+    }
+  }
+  const int ne = max(0, min(m + 1, pr.cap));
+  if (rank == 0) write_common<SAMPLE>(P, b, 0, L, m, ne, sTok, sP, sQ, !SAMPLE, sA[m]);
+  if (!SAMPLE) return;
+
+  // ---- 3. the final draw: residual after a rejection, p_L after a full accept
+  Weights W = m < L ? Weights{row_of(m), row_of(L + 1 + m), sM[m], sM[L + 1 + m], 1.0f / sS[m],
+                              1.0f / sS[L + 1 + m], c}
+                    : Weights{row_of(L), nullptr, sM[L], 0.0f, 1.0f / sS[L], 0.0f, c};
+  float wmass = 0.0f, rmass = 0.0f, total = 0.0f;
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    wmass = warp_sum(lane_weight_sum<DT, VEC>(W, lo, hi, G));  // this warp's range
+    const float ws = wmass;
+    if (lane == 0) s_red[warp] = ws;
+    __syncthreads();
+    if (warp == 0) {
+      const float z = warp_sum(lane < kFusedWarps ? s_red[lane] : 0.0f);
+      if (lane < CS) *cluster.map_shared_rank(&s_z[attempt][rank], lane) = z;
+    }
+    cluster.sync();
+    rmass = lane < CS ? s_z[attempt][lane] : 0.0f;  // lane r: rank r's mass
+    total = warp_sum(rmass);
+    if (!(total > 0.0f) && m < L && attempt == 0) {
+      // zero residual mass (only through rounding): draw from p_m instead
+      W.b = nullptr;
+      W.beta = 0.0f;
+      continue;
+    }
+    break;
+  }
+  // the rank whose slice holds u * total
+  const float incl_r = warp_inclusive_scan(rmass, lane);
+  const float thr = sU[k] * __shfl_sync(0xffffffffu, incl_r, 31);
+  const unsigned hit_r = __ballot_sync(0xffffffffu, lane < CS && rmass > 0.0f && incl_r > thr);
+  const unsigned pos_r = __ballot_sync(0xffffffffu, lane < CS && rmass > 0.0f);
+  int draw_rank;
+  float tl = INFINITY;  // threshold within the drawing rank's slice
+  if (hit_r) {
+    draw_rank = __ffs(hit_r) - 1;
+    const float before = __shfl_sync(0xffffffffu, incl_r, max(draw_rank - 1, 0));
+    tl = thr - (draw_rank > 0 ? before : 0.0f);
+  } else {
+    draw_rank = pos_r ? 31 - __clz(pos_r) : 0;  // rounding: the last rank with mass
+  }
+  if (rank != draw_rank) return;  // no CTA touches another's shared memory from here on
+  const int tok = range_draw<kFusedThreads, EPG>(wmass, tl, lo, G, sA[m], [&](int g, float *w) {
+    float x[EPG], y[EPG];
+    unpack16<DT>(load_group<DT, VEC>(W.a, lo + g * EPG, hi), x);
+    if (W.b) unpack16<DT>(load_group<DT, VEC>(W.b, lo + g * EPG, hi), y);
+#pragma unroll
+    for (int e = 0; e < EPG; ++e) w[e] = weight_at<DT>(W, x[e], W.b ? y[e] : 0.0f);
+  });
+  if (tid == 0) {
+    if (m < ne) P.out_tokens[static_cast<int64_t>(b) * (k + 1) + m] = tok;
+    if (P.resid_mass) P.resid_mass[b] = (m < L && W.b != nullptr) ? total : 0.0f;
+  }
+}
+
+// ------------------------------------------------------------------- host
+
+size_t chain_fused_smem(int k, bool sample, int cluster) {
+  const int rows = sample ? 2 * k + 1 : k + 1;
+  return sizeof(RowPart) * static_cast<size_t>(kFusedWarps + cluster) * rows;
+}
+
+template <int DT, bool VEC, bool SAMPLE>
+static cudaError_t prepare(int cluster, size_t smem) {
+  auto kern = chain_fused_kernel<DT, VEC, SAMPLE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e == cudaSuccess && cluster > 8) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+static void cluster_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, int cluster, unsigned grid,
+                           size_t smem, cudaStream_t st, bool pdl) {
+  cfg = cudaLaunchConfig_t{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kFusedThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+}
+
+// How many clusters of `cluster` CTAs of the fused kernel fit on the device
+// at once (cached per device and shape).
+static int resident_clusters(int dtype, bool vec, bool sample, int k, int cluster) {
+  struct Key {
+    int dev, dtype, vec, sample, k, cluster, n;
+  };
+  static std::mutex mu;
+  static std::vector<Key> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    for (const Key &q : cache)
+      if (q.dev == dev && q.dtype == dtype && q.vec == vec && q.sample == sample && q.k == k && q.cluster == cluster)
+        return q.n;
+  }
+  const size_t smem = chain_fused_smem(k, sample, cluster);
+  int n = 0;
+  auto query = [&](auto kern, cudaError_t prep) {
+    if (prep != cudaSuccess) return;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    cluster_config(cfg, attr, cluster, static_cast<unsigned>(cluster), smem, nullptr, false);
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  };
+#define SV_QUERY(DT, V, S) query(chain_fused_kernel<DT, V, S>, prepare<DT, V, S>(cluster, smem))
+  if (dtype == SPEC_DTYPE_BF16) {
+    if (vec) { if (sample) SV_QUERY(SPEC_DTYPE_BF16, true, true); else SV_QUERY(SPEC_DTYPE_BF16, true, false); }
+    else { if (sample) SV_QUERY(SPEC_DTYPE_BF16, false, true); else SV_QUERY(SPEC_DTYPE_BF16, false, false); }
+  } else {
+    if (vec) { if (sample) SV_QUERY(SPEC_DTYPE_F32, true, true); else SV_QUERY(SPEC_DTYPE_F32, true, false); }
+    else { if (sample) SV_QUERY(SPEC_DTYPE_F32, false, true); else SV_QUERY(SPEC_DTYPE_F32, false, false); }
+  }
+#undef SV_QUERY
+  cudaGetLastError();  // a refused query leaves no error behind
+  std::lock_guard<std::mutex> g(mu);
+  cache.push_back(Key{dev, dtype, vec, sample, k, cluster, n});
+  return n;
+}
+
+bool chain_fused_plan(ChainParams &P, bool sample, bool vec) {
+  // at least kFusedMinSlice logits per CTA, at most 16 CTAs per request, and
+  // every request's cluster resident at once
+  int cs = (P.V + kFusedMinSlice - 1) / kFusedMinSlice;
+  cs = cs < 1 ? 1 : (cs > kFusedMaxCluster ? kFusedMaxCluster : cs);
+  for (; cs >= 1; --cs) {
+    if (resident_clusters(P.dtype, vec, sample, P.k, cs) >= P.B) break;
+  }
+  if (cs < 1) return false;
+  P.cluster = cs;
+  P.slice = ((P.V + cs - 1) / cs + 7) / 8 * 8;
+  const int epg = P.dtype == SPEC_DTYPE_F32 ? 4 : 8;
+  P.groups = ((P.slice + epg - 1) / epg + kFusedThreads - 1) / kFusedThreads;
+  return true;
+}
+
+template <int DT, bool VEC, bool SAMPLE>
+static cudaError_t launch_fused_t(const ChainParams &P, cudaStream_t st) {
+  const size_t smem = chain_fused_smem(P.k, SAMPLE, P.cluster);
+  cudaError_t e = prepare<DT, VEC, SAMPLE>(P.cluster, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  cluster_config(cfg, attr, P.cluster, static_cast<unsigned>(P.B * P.cluster), smem, st, !trace_enabled());
+  return trace_launch_ex(SAMPLE ? "chain_fused_sample" : "chain_fused_greedy", st,
+                         [&] { return cudaLaunchKernelEx(&cfg, chain_fused_kernel<DT, VEC, SAMPLE>, P); });
+}
+
+template <int DT, bool VEC>
+static cudaError_t launch_fused_mode(const ChainParams &P, bool sample, cudaStream_t st) {
+  return sample ? launch_fused_t<DT, VEC, true>(P, st) : launch_fused_t<DT, VEC, false>(P, st);
+}
+
+cudaError_t launch_chain_fused(const ChainParams &P, bool sample, bool vec, cudaStream_t st) {
+  if (P.dtype == SPEC_DTYPE_BF16)
+    return vec ? launch_fused_mode<SPEC_DTYPE_BF16, true>(P, sample, st)
+               : launch_fused_mode<SPEC_DTYPE_BF16, false>(P, sample, st);
+  return vec ? launch_fused_mode<SPEC_DTYPE_F32, true>(P, sample, st)
+             : launch_fused_mode<SPEC_DTYPE_F32, false>(P, sample, st);
+}
+
+}  // namespace sv

@@ -28,11 +28,13 @@ struct ChainParams {
   Partial *part;     // [B][rows][nc] streaming-pass statistics
   float *part2;      // [B][nsub] mass of the final draw's weights per sub-chunk
   int *counter2;     // [B] arrival counter of the residual pass
-  int cluster;       // sampling accept: CTAs per request (0 = chunked accept kernel)
-  int slice;         // logits per CTA of the cluster accept kernel
+  int cluster;       // cluster kernels: CTAs per request (sampling accept: 0 = chunked accept kernel)
+  int slice;         // logits per CTA of a cluster kernel
+  int groups;        // fused kernel: rounds of 16-byte groups per lane (warp ranges of the slice)
 };
 
-constexpr int kTreeThreads = 512;  // threads per tree-walk CTA
+constexpr int kTreeThreads = 512;   // threads per tree-walk CTA
+constexpr int kFusedThreads = 512;  // threads per CTA of the fused chain kernel
 
 struct TreeParams {
   const char *target;
@@ -41,7 +43,7 @@ struct TreeParams {
   int dtype, B, N, V, max_depth;
   int cluster;     // CTAs per request
   int slice;       // logits per CTA (multiple of 8)
-  int seg;         // logits per thread: contiguous segments of the slice (multiple of 8)
+  int groups;      // rounds of 16-byte groups per lane (each warp: a contiguous range of the slice)
   int stage;       // 1: the first rejection at a node stages p and q of the slice in shared memory
   float c;         // log2(e) / T; unused when greedy
   int greedy;
@@ -57,6 +59,11 @@ struct NgramParams {
 };
 
 cudaError_t launch_chain(const ChainParams &P, bool sample, bool vec, cudaStream_t st);
+// Fused chain kernel: chain_fused_plan picks the cluster geometry (cluster,
+// slice, groups) and returns false when the requests' clusters cannot all be
+// resident at once (then the two-kernel path runs).
+bool chain_fused_plan(ChainParams &P, bool sample, bool vec);
+cudaError_t launch_chain_fused(const ChainParams &P, bool sample, bool vec, cudaStream_t st);
 cudaError_t launch_tree(const TreeParams &P, bool vec, cudaStream_t st);
 size_t tree_dynamic_smem(const TreeParams &P);
 cudaError_t launch_ngram(const NgramParams &P, cudaStream_t st);

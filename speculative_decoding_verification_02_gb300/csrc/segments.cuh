@@ -1,0 +1,216 @@
+// Pieces shared by the cluster kernels (tree walk, fused chain verify), in
+// which each warp of a CTA owns one contiguous range of the CTA's
+// vocabulary slice: warp reductions whose result lands in every lane,
+// per-lane row statistics, and the inverse-CDF draw inside a slice from
+// per-warp masses.
+#pragma once
+
+#include "common.cuh"
+
+namespace sv {
+
+// ------------------------------------------------ warp-wide reductions
+
+// Order-preserving map of fp32 (NaN excluded) onto int32, so that one
+// integer redux finds the largest float.
+__device__ __forceinline__ int float_key(float x) {
+  const int b = __float_as_int(x);
+  return b >= 0 ? b : b ^ 0x7fffffff;
+}
+__device__ __forceinline__ float key_float(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff); }
+
+__device__ __forceinline__ float warp_allmax(float x) {
+  return key_float(__reduce_max_sync(0xffffffffu, float_key(x)));
+}
+
+// Lowest index among the lanes whose m equals the warp's max M.
+__device__ __forceinline__ int warp_first_index(float m, float M, int i) {
+  return static_cast<int>(__reduce_min_sync(0xffffffffu, static_cast<unsigned>(m == M ? i : kNoIndex)));
+}
+
+// (m, s, i) of all lanes merged: the max, the sums rescaled to it and added,
+// the first index of the max (IDX) -- one max, one exponential per lane.
+template <bool IDX>
+__device__ __forceinline__ void warp_allmerge(float &m, float &s, int &i, float c) {
+  const float M = warp_allmax(m);
+  const float r = M == -INFINITY ? 0.0f : s * ex2((m - M) * c);
+  if (IDX) i = warp_first_index(m, M, i);
+  s = warp_sum(r);
+  m = M;
+}
+
+__device__ __forceinline__ void warp_allargmax(float &m, int &i) {
+  const float M = warp_allmax(m);
+  i = warp_first_index(m, M, i);
+  m = M;
+}
+
+// ------------------------------------------------------ per-lane work
+
+// Running statistics of one row over a lane's groups.
+struct RowStats {
+  float m;   // max logit
+  float2 s;  // sum of 2^((x - m) c), two lanes
+  int i;     // first index of the max
+};
+
+__device__ __forceinline__ RowStats row_stats_empty() {
+  return RowStats{-INFINITY, make_float2(0.0f, 0.0f), kNoIndex};
+}
+
+template <bool SOFTMAX>
+__device__ __forceinline__ void fold_one(RowStats &R, float x, int v, float c) {
+  if (x > R.m) {
+    if (SOFTMAX) {
+      const float f = ex2((R.m - x) * c);
+      R.s.x *= f;
+      R.s.y *= f;
+    }
+    R.m = x;
+    R.i = v;
+  }
+  if (SOFTMAX && R.m != -INFINITY) R.s.x += ex2((x - R.m) * c);
+}
+
+// Work split of a CTA's slice [lo, hi): 16-byte groups of EPG logits, group
+// g holding logits lo + g EPG ...; lane l of warp w takes the groups
+//     g = (w G + j) 32 + l,   j < G,
+// so that each warp load instruction reads 32 consecutive groups (512
+// bytes) and each warp covers one contiguous range of 32 G groups.
+__device__ __forceinline__ int lane_group(int warp, int j, int G, int lane) { return ((warp * G + j) << 5) + lane; }
+
+// The 16-byte group of `row` starting at logit e; logits >= hi read as
+// -inf.  VEC: the row is 16-byte aligned and hi a multiple of the group
+// size, so a group is wholly inside [.., hi) or wholly outside, and a group
+// inside is one 16-byte load.
+template <int DT, bool VEC>
+__device__ __forceinline__ uint4 load_group(const char *row, int e, int hi) {
+  constexpr uint32_t kNegInf = DT == SPEC_DTYPE_F32 ? 0xff800000u : 0xff80ff80u;  // -inf words
+  if constexpr (VEC) {
+    return e < hi ? __ldg(reinterpret_cast<const uint4 *>(row + static_cast<int64_t>(e) * Elems<DT>::kSize))
+                  : make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
+  } else {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (DT == SPEC_DTYPE_F32) {
+        w[q] = e + q < hi ? __float_as_uint(load_one<DT>(row, e + q)) : kNegInf;
+      } else {
+        const uint32_t l = e + 2 * q < hi ? __float_as_uint(load_one<DT>(row, e + 2 * q)) >> 16 : 0xff80u;
+        const uint32_t h = e + 2 * q + 1 < hi ? __float_as_uint(load_one<DT>(row, e + 2 * q + 1)) >> 16 : 0xff80u;
+        w[q] = l | (h << 16);
+      }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Folds this lane's groups (the lane_group split, G rounds) of NR rows into
+// R[r]; a null rows[r] is skipped.  kBatch rounds of every row are loaded
+// before any of them is folded.
+template <int DT, bool SOFTMAX, bool VEC, int NR>
+__device__ __forceinline__ void lane_rows_stats(const char *const *rows, int lo, int hi, int G, float c,
+                                                RowStats *R) {
+  constexpr int EPG = Elems<DT>::kPerGroup;
+  constexpr uint32_t kNegInf = DT == SPEC_DTYPE_F32 ? 0xff800000u : 0xff80ff80u;  // -inf words
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float unused = 0.0f;
+  for (int j0 = 0; j0 < G; j0 += kBatch) {
+    const int e0 = lo + lane_group(warp, j0, G, lane) * EPG;  // round j0 + u starts at e0 + u 32 EPG
+    uint4 x[NR][kBatch];
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        x[r][u] = (rows[r] && j0 + u < G) ? load_group<DT, VEC>(rows[r], e0 + u * 32 * EPG, hi)
+                                          : make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+      if (rows[r]) fold_batch<DT, SOFTMAX, 32>(x[r], e0, c, R[r].m, R[r].s, R[r].i, -1, unused);
+  }
+}
+
+// Inverse-CDF draw inside one CTA's slice [lo, hi) from per-warp masses
+// (the lane_group split).  `wmass` is the calling warp's sum of weights
+// (the same in all its lanes); the drawn logit is the first whose running
+// sum over the slice passes tl (tl = INFINITY: the last positive weight).
+// A scan of the warp masses finds the warp whose range holds the crossing;
+// that warp walks its range 32 groups at a time (a lane scan, then one lane
+// scans its group).  group_weights(g, w) writes the EPG weights of group g
+// (0 for logits >= hi).  Rounding between the scans falls back to the last
+// positive weight of the last warp with mass; `fallback` is returned when
+// no warp has any.  Called by all NT threads; returns the token in every
+// thread.
+template <int NT, int EPG, class GroupWeights>
+__device__ int range_draw(float wmass, float tl, int lo, int G, int fallback, GroupWeights &&group_weights) {
+  constexpr int NW = NT / 32;
+  __shared__ float s_wsum[NW];
+  __shared__ int s_tok;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) s_wsum[warp] = wmass;
+  __syncthreads();
+  const float wv = lane < NW ? s_wsum[lane] : 0.0f;
+  const float winc = warp_inclusive_scan(wv, lane);
+  const unsigned hit_w = __ballot_sync(0xffffffffu, wv > 0.0f && winc > tl);
+  const unsigned pos_w = __ballot_sync(0xffffffffu, wv > 0.0f);
+  int wsel = -1;
+  float thr_local = INFINITY;
+  if (hit_w) {
+    wsel = __ffs(hit_w) - 1;
+    const float before = __shfl_sync(0xffffffffu, winc, max(wsel - 1, 0));
+    thr_local = tl - (wsel > 0 ? before : 0.0f);
+  } else if (pos_w) {  // rounding: the last warp with mass, its last positive weight
+    wsel = 31 - __clz(pos_w);
+  }
+  if (warp == wsel) {
+    float run = 0.0f;
+    int pick = -1, lastp = -1;
+    for (int j = 0; j < G; ++j) {
+      const int g = lane_group(wsel, j, G, lane);
+      float w[EPG];
+      group_weights(g, w);
+      float lm = 0.0f;
+      int le = -1;  // this lane's last positive weight
+#pragma unroll
+      for (int e = 0; e < EPG; ++e) {
+        lm += w[e];
+        if (w[e] > 0.0f) le = e;
+      }
+      const float incl = warp_inclusive_scan(lm, lane);
+      float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+      if (lane == 0) excl = 0.0f;
+      const unsigned hit = __ballot_sync(0xffffffffu, lm > 0.0f && run + incl > thr_local);
+      const unsigned pos = __ballot_sync(0xffffffffu, lm > 0.0f);
+      if (pos) {
+        const int hl = 31 - __clz(pos);
+        lastp = (g - lane + hl) * EPG + __shfl_sync(0xffffffffu, le, hl);
+      }
+      if (hit) {
+        const int lh = __ffs(hit) - 1;
+        int pe = le;  // rounding inside the lane: its last positive weight
+        float r = run + excl;
+#pragma unroll
+        for (int e = 0; e < EPG; ++e) {
+          r += w[e];
+          if (w[e] > 0.0f && r > thr_local) {
+            pe = e;
+            break;
+          }
+        }
+        pick = (g - lane + lh) * EPG + __shfl_sync(0xffffffffu, pe, lh);
+        break;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (pick < 0) pick = lastp;
+    if (lane == 0) s_tok = pick >= 0 ? lo + pick : fallback;
+  } else if (wsel < 0 && threadIdx.x == 0) {
+    s_tok = fallback;  // no positive weight in the slice (underflow only)
+  }
+  __syncthreads();
+  const int r = s_tok;
+  __syncthreads();  // the shared words are free again
+  return r;
+}
+
+}  // namespace sv

@@ -3,15 +3,15 @@
 // rule is applied recursively at every node, as in SpecInfer).
 //
 // Each CTA of the cluster owns one slice of the vocabulary and each of its
-// threads one contiguous segment of that slice.  Only the rows of the nodes
-// the walk visits are read.  Per visited node u:
-//   1. one pass over the segment reduces t_u, and d_u when u has children,
-//      to (max, sum 2^((x - max) c), first argmax), both rows' loads in
-//      flight together; warps merge with redux and shuffle reductions, warp
-//      0 merges the warps and pushes the CTA's statistics into every CTA of
-//      the cluster (distributed shared memory), and after one cluster
-//      barrier every CTA holds all slices' statistics and takes the same
-//      decisions;
+// warps one contiguous range of that slice (lanes interleaved, so loads stay
+// coalesced).  Only the rows of the nodes the walk visits are read.  Per
+// visited node u:
+//   1. one pass reduces t_u, and d_u when u has children, to (max, sum
+//      2^((x - max) c), first argmax), both rows' loads in flight together;
+//      warps merge with redux and shuffle reductions, warp 0 merges the
+//      warps and pushes the CTA's statistics into every CTA of the cluster
+//      (distributed shared memory), and after one cluster barrier every CTA
+//      holds all slices' statistics and takes the same decisions;
 //   2. children are tested in increasing id order.  The residual after j
 //      rejected children is kept in closed form,
 //          p^(j) = max(0, p - c_j q) / Z_j,   c_0 = 0, Z_0 = 1,
@@ -19,21 +19,23 @@
 //      which is what repeating p <- norm(max(0, p - q)) with q fixed gives
 //      (induction on j; a term with p_v <= c_j q_v stays at zero).  Child x
 //      is accepted iff u * q(x) * Z_j < max(0, p(x) - c_j q(x)), i.e.
-//      u < min(1, p^(j)(x) / q(x)).  A rejection costs one segment pass and
-//      one cluster exchange for Z_{j+1}; the first rejection at a node also
-//      stores the normalised p and q of the slice in shared memory, so later
-//      rejections and the final draw need no more exponentials or loads;
+//      u < min(1, p^(j)(x) / q(x)).  A rejection costs one pass over the
+//      slice and one cluster exchange for Z_{j+1}; the first rejection at a
+//      node also stores the normalised p and q of the slice in shared
+//      memory, so later rejections and the final draw need no more
+//      exponentials or loads;
 //   3. an accepted child is descended into; otherwise the final token is
 //      drawn from p^(j) with the last uniform: the rank whose slice holds the
 //      crossing is found from the per-rank masses already exchanged; in that
-//      CTA a block scan of the per-thread segment masses finds the thread
-//      whose segment holds it, and one warp scans that segment.
+//      CTA a scan of the per-warp masses finds the warp whose range holds
+//      it, and that warp walks its range.
 // Greedy mode (T <= 0): per node one argmax exchange, then the first child
 // whose token equals the argmax.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "launch.h"
+#include "segments.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -63,147 +65,50 @@ __device__ __forceinline__ void prefetch_l2(const char *p, int bytes) {
   if (bytes > 0) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// ------------------------------------------------ warp-wide reductions
-// The results land in every lane.
+// Where p_v, q_v of element e of group g are staged: the slice's groups in
+// lane_group order, element-major within each warp round, so that
+// consecutive lanes touch consecutive words.
+__device__ __forceinline__ int stage_index(int g, int e, int epg) { return (((g >> 5) * epg + e) << 5) + (g & 31); }
 
-// Order-preserving map of fp32 (NaN excluded) onto int32, so that one
-// integer redux finds the largest float.
-__device__ __forceinline__ int float_key(float x) {
-  const int b = __float_as_int(x);
-  return b >= 0 ? b : b ^ 0x7fffffff;
-}
-__device__ __forceinline__ float key_float(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff); }
-
-__device__ __forceinline__ float warp_allmax(float x) {
-  return key_float(__reduce_max_sync(0xffffffffu, float_key(x)));
-}
-
-// Lowest index among the lanes whose m equals the warp's max M.
-__device__ __forceinline__ int warp_first_index(float m, float M, int i) {
-  return static_cast<int>(__reduce_min_sync(0xffffffffu, static_cast<unsigned>(m == M ? i : kNoIndex)));
-}
-
-// (m, s, i) of all lanes merged: the max, the sums rescaled to it and added,
-// the first index of the max (IDX) -- one max, one exponential per lane.
-template <bool IDX>
-__device__ __forceinline__ void warp_allmerge(float &m, float &s, int &i, float c) {
-  const float M = warp_allmax(m);
-  const float r = M == -INFINITY ? 0.0f : s * ex2((m - M) * c);
-  if (IDX) i = warp_first_index(m, M, i);
-  s = warp_sum(r);
-  m = M;
-}
-
-__device__ __forceinline__ void warp_allargmax(float &m, int &i) {
-  const float M = warp_allmax(m);
-  i = warp_first_index(m, M, i);
-  m = M;
-}
-
-// ------------------------------------------------- per-thread segments
-
-// Running statistics of one row over a thread's segment.
-struct RowStats {
-  float m;   // max logit
-  float2 s;  // sum of 2^((x - m) c), two lanes
-  int i;     // first index of the max
-};
-
-template <bool SOFTMAX>
-__device__ __forceinline__ void fold_one(RowStats &R, float x, int v, float c) {
-  if (x > R.m) {
-    if (SOFTMAX) {
-      const float f = ex2((R.m - x) * c);
-      R.s.x *= f;
-      R.s.y *= f;
-    }
-    R.m = x;
-    R.i = v;
-  }
-  if (SOFTMAX && R.m != -INFINITY) R.s.x += ex2((x - R.m) * c);
-}
-
-// Folds logits [a, b) of trow into T and, unless drow is null, of drow into
-// D.  a is a multiple of 8; a batch of both rows is loaded before either is
-// folded.
-template <int DT, bool SOFTMAX, bool VEC>
-__device__ __forceinline__ void segment_stats(const char *trow, const char *drow, int a, int b, float c,
-                                              RowStats &T, RowStats &D) {
-  constexpr int EPG = Elems<DT>::kPerGroup;
-  constexpr int ES = Elems<DT>::kSize;
-  constexpr uint32_t kNegInf = DT == SPEC_DTYPE_F32 ? 0xff800000u : 0xff80ff80u;  // -inf words
-  const uint4 neg = make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
-  float unused = 0.0f;
-  int vt = a;
-  if (VEC) {
-    const int ng = b > a ? (b - a) / EPG : 0;
-    const uint4 *gt = reinterpret_cast<const uint4 *>(trow + static_cast<int64_t>(a) * ES);
-    const uint4 *gd = drow ? reinterpret_cast<const uint4 *>(drow + static_cast<int64_t>(a) * ES) : nullptr;
-    for (int g0 = 0; g0 < ng; g0 += kBatch) {
-      uint4 xt[kBatch], xd[kBatch];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) xt[u] = g0 + u < ng ? __ldg(gt + g0 + u) : neg;
-      if (gd) {
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) xd[u] = g0 + u < ng ? __ldg(gd + g0 + u) : neg;
-      }
-      fold_batch<DT, SOFTMAX, 1>(xt, a + g0 * EPG, c, T.m, T.s, T.i, -1, unused);
-      if (gd) fold_batch<DT, SOFTMAX, 1>(xd, a + g0 * EPG, c, D.m, D.s, D.i, -1, unused);
-    }
-    vt = a + ng * EPG;
-  }
-  for (int v = vt; v < b; ++v) {
-    fold_one<SOFTMAX>(T, load_one<DT>(trow, v), v, c);
-    if (drow) fold_one<SOFTMAX>(D, load_one<DT>(drow, v), v, c);
-  }
-}
-
-// p_v = 2^(t_v c - Mtc) iSt and q_v = 2^(d_v c - Mdc) iSd over logits
-// [a, b); returns this thread's sum of max(0, p_v - cres q_v).  STORE also
-// writes p_v, q_v to sp, sq at (v - a) * kTreeThreads + threadIdx.x
-// (consecutive threads, consecutive words).
+// p_v = 2^(t_v c - Mtc) iSt and q_v = 2^(d_v c - Mdc) iSd over this lane's
+// groups (logits >= hi read as -inf, so give 0); returns the lane's sum of
+// max(0, p_v - cres q_v).  STORE also writes p_v, q_v to sp, sq.
 template <int DT, bool VEC, bool STORE>
-__device__ __forceinline__ float segment_residual(const char *trow, const char *drow, int a, int b, float Mtc,
-                                                  float Mdc, float c, float iSt, float iSd, float cres,
-                                                  float *sp, float *sq) {
+__device__ __forceinline__ float lane_residual(const char *trow, const char *drow, int lo, int hi, int G,
+                                               float Mtc, float Mdc, float c, float iSt, float iSd, float cres,
+                                               float *sp, float *sq) {
   constexpr int EPG = Elems<DT>::kPerGroup;
-  constexpr int ES = Elems<DT>::kSize;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float part = 0.0f;
-  auto one = [&](float t, float d, int o) {
-    const float pv = ex2(fmaf(t, c, -Mtc)) * iSt;
-    const float qv = ex2(fmaf(d, c, -Mdc)) * iSd;
-    if (STORE) {
-      sp[o * kTreeThreads + threadIdx.x] = pv;
-      sq[o * kTreeThreads + threadIdx.x] = qv;
-    }
-    part += fmaxf(0.0f, pv - cres * qv);
-  };
-  int vt = a;
-  if (VEC) {
-    const int ng = b > a ? (b - a) / EPG : 0;
-    const uint4 *gt = reinterpret_cast<const uint4 *>(trow + static_cast<int64_t>(a) * ES);
-    const uint4 *gd = reinterpret_cast<const uint4 *>(drow + static_cast<int64_t>(a) * ES);
-    for (int g0 = 0; g0 < ng; g0 += kBatch) {
-      uint4 xt[kBatch], xd[kBatch];
+  for (int j0 = 0; j0 < G; j0 += kBatch) {
+    const int g0 = lane_group(warp, j0, G, lane);  // round j0 + u: group g0 + 32 u
+    uint4 xt[kBatch], xd[kBatch];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        xt[u] = g0 + u < ng ? __ldg(gt + g0 + u) : make_uint4(0u, 0u, 0u, 0u);
-        xd[u] = g0 + u < ng ? __ldg(gd + g0 + u) : make_uint4(0u, 0u, 0u, 0u);
+    for (int u = 0; u < kBatch; ++u) {
+      if (j0 + u < G) {
+        xt[u] = load_group<DT, VEC>(trow, lo + (g0 + 32 * u) * EPG, hi);
+        xd[u] = load_group<DT, VEC>(drow, lo + (g0 + 32 * u) * EPG, hi);
       }
+    }
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        if (g0 + u < ng) {
-          float t[EPG], d[EPG];
-          unpack16<DT>(xt[u], t);
-          unpack16<DT>(xd[u], d);
+    for (int u = 0; u < kBatch; ++u) {
+      if (j0 + u < G) {
+        float t[EPG], d[EPG];
+        unpack16<DT>(xt[u], t);
+        unpack16<DT>(xd[u], d);
 #pragma unroll
-          for (int e = 0; e < EPG; ++e) one(t[e], d[e], (g0 + u) * EPG + e);
+        for (int e = 0; e < EPG; ++e) {
+          const float pv = ex2(fmaf(t[e], c, -Mtc)) * iSt;
+          const float qv = ex2(fmaf(d[e], c, -Mdc)) * iSd;
+          if (STORE) {
+            sp[stage_index(g0 + 32 * u, e, EPG)] = pv;
+            sq[stage_index(g0 + 32 * u, e, EPG)] = qv;
+          }
+          part += fmaxf(0.0f, pv - cres * qv);
         }
       }
     }
-    vt = a + ng * EPG;
   }
-  for (int v = vt; v < b; ++v) one(load_one<DT>(trow, v), load_one<DT>(drow, v), v - a);
   return part;
 }
 
@@ -223,14 +128,15 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
   float *s_kt = reinterpret_cast<float *>(dyn + 3 * N);   // [N] target logit of each child's token
   float *s_kd = reinterpret_cast<float *>(dyn + 4 * N);   // [N] draft logit of each child's token
   float *s_uni = reinterpret_cast<float *>(dyn + 5 * N);  // [N + 1] the request's uniforms
-  float *s_p = s_uni + N + 1;                             // [seg][threads] staged p of the segments
-  float *s_q = s_p + static_cast<size_t>(P.seg) * kTreeThreads;  // [seg][threads] staged q
+  constexpr int EPG = Elems<DT>::kPerGroup;
+  const int G = P.groups;                                 // rounds of 16-byte groups per lane
+  float *s_p = s_uni + N + 1;                             // [G * EPG * threads] staged p (stage_index)
+  float *s_q = s_p + static_cast<size_t>(G) * EPG * kTreeThreads;  // staged q
   __shared__ Slot s_all[2][kMaxCluster];  // [exchange parity][source rank]
   __shared__ Slot s_part[kTreeWarps];
   __shared__ float s_red[kTreeWarps];
-  __shared__ unsigned s_pos[kTreeWarps];
   __shared__ int s_path[SPEC_MAX_DEPTH + 1], s_out[SPEC_MAX_DEPTH + 1];
-  __shared__ int s_bad, s_cnt[kTreeWarps], s_final;
+  __shared__ int s_bad, s_cnt[kTreeWarps];
   const Slot kEmpty{-INFINITY, 0.0f, -INFINITY, 0.0f, kNoIndex, 0.0f, 0, 0};
 
   // ---- load and validate the tree (every CTA does the same)
@@ -275,7 +181,6 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
   }
 
   const int lo = min(P.V, rank * P.slice), hi = min(P.V, lo + P.slice);
-  const int sa = min(hi, lo + tid * P.seg), sb = min(hi, sa + P.seg);  // this thread's segment
   const float c = P.c;
   int phase = 0;
 
@@ -291,9 +196,9 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
     return ph;
   };
   // Sum of x over the cluster, in every thread; lane r of every warp also
-  // gets rank r's part.
-  auto cluster_sum = [&](float x, float &part_of_lane) {
-    const float ws = warp_sum(x);
+  // gets rank r's part, and ws the calling warp's.
+  auto cluster_sum = [&](float x, float &part_of_lane, float &ws) {
+    ws = warp_sum(x);
     if (lane == 0) s_red[warp] = ws;
     __syncthreads();
     Slot z = kEmpty;
@@ -336,7 +241,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
       prefetch_l2(node_row<DT>(P.target, P.t_req, P.row, b, ch) + off, bytes);
       if (!GREEDY) prefetch_l2(node_row<DT>(P.draftl, P.d_req, P.row, b, ch) + off, bytes);
     }
-    // the children's token logits: loaded now, stored after the segment pass
+    // the children's token logits: loaded now, stored after the statistics pass
     float kt0 = 0.0f, kd0 = 0.0f;
     if (drow) {
       if (tid < nkids) {
@@ -351,21 +256,22 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
       }
     }
 
-    // ---- row statistics: segment pass, warp merge, block merge, exchange
-    RowStats T{-INFINITY, make_float2(0.0f, 0.0f), kNoIndex}, D = T;
-    segment_stats<DT, !GREEDY, VEC>(trow, drow, sa, sb, c, T, D);
+    // ---- row statistics: lane pass, warp merge, block merge, exchange
+    RowStats R[2] = {row_stats_empty(), row_stats_empty()};
+    const char *rows[2] = {trow, drow};
+    lane_rows_stats<DT, !GREEDY, VEC, 2>(rows, lo, hi, G, c, R);
     if (drow && tid < nkids) {
       s_kt[tid] = kt0;
       s_kd[tid] = kd0;
     }
-    const float th_m = T.m, th_s = T.s.x + T.s.y;  // this thread's own statistics of t
+    float w_m = R[0].m, w_s = R[0].s.x + R[0].s.y;  // this warp's statistics of t (after the merge)
     {
-      float m = T.m, s = th_s, dm = D.m, ds = D.s.x + D.s.y;
-      int i = T.i, di = kNoIndex;
-      if (GREEDY) warp_allargmax(m, i);
-      else warp_allmerge<true>(m, s, i, c);
+      float dm = R[1].m, ds = R[1].s.x + R[1].s.y;
+      int i = R[0].i, di = kNoIndex;
+      if (GREEDY) warp_allargmax(w_m, i);
+      else warp_allmerge<true>(w_m, w_s, i, c);
       if (drow) warp_allmerge<false>(dm, ds, di, c);
-      if (lane == 0) s_part[warp] = Slot{m, s, dm, ds, i, 0.0f, 0, 0};
+      if (lane == 0) s_part[warp] = Slot{w_m, w_s, dm, ds, i, 0.0f, 0, 0};
     }
     __syncthreads();
     Slot mine = kEmpty;
@@ -415,10 +321,10 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
     const int cta_it = __shfl_sync(0xffffffffu, r.it, rank);  // this slice's argmax
     // lane r: rank r's share of the current draw distribution (p so far)
     float rmass = lane < ncl ? r.st * ex2((r.mt - Mt) * c) * iSt : 0.0f;
-    float my_mass = -1.0f;  // this thread's share of it; < 0: p, from the segment statistics
+    float w_mass = -1.0f;  // this warp's share of it; < 0: p, from the warp's statistics
 
     float cres = 0.0f, Z = 1.0f;
-    bool staged = false;  // s_p / s_q hold this node's segments
+    bool staged = false;  // s_p / s_q hold this node's slice
     int next = -1;
     for (int ki = 0; ki < nkids; ++ki) {
       const int ch = s_kids[ki];
@@ -432,21 +338,25 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
       const float cnew = cres + Z;
       float part = 0.0f;
       if (staged) {
-        for (int o = 0; o < sb - sa; ++o)
-          part += fmaxf(0.0f, s_p[o * kTreeThreads + tid] - cnew * s_q[o * kTreeThreads + tid]);
+        for (int j = 0; j < G; ++j) {
+          const int g = lane_group(warp, j, G, lane);
+#pragma unroll
+          for (int e = 0; e < EPG; ++e)
+            part += fmaxf(0.0f, s_p[stage_index(g, e, EPG)] - cnew * s_q[stage_index(g, e, EPG)]);
+        }
       } else if (P.stage) {
-        part = segment_residual<DT, VEC, true>(trow, drow, sa, sb, Mt * c, Md * c, c, iSt, iSd, cnew, s_p, s_q);
+        part = lane_residual<DT, VEC, true>(trow, drow, lo, hi, G, Mt * c, Md * c, c, iSt, iSd, cnew, s_p, s_q);
         staged = true;
       } else {
-        part = segment_residual<DT, VEC, false>(trow, drow, sa, sb, Mt * c, Md * c, c, iSt, iSd, cnew, s_p, s_q);
+        part = lane_residual<DT, VEC, false>(trow, drow, lo, hi, G, Mt * c, Md * c, c, iSt, iSd, cnew, s_p, s_q);
       }
-      float zr;
-      const float Znew = cluster_sum(part, zr);
+      float zr, wz;
+      const float Znew = cluster_sum(part, zr, wz);
       if (Znew > 0.0f) {  // a zero-mass residual (rounding only) keeps the previous p
         cres = cnew;
         Z = Znew;
         rmass = zr;
-        my_mass = part;
+        w_mass = wz;
       }
     }
     if (next >= 0) {
@@ -473,70 +383,27 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
       draw_rank = pos_r ? 31 - __clz(pos_r) : 0;  // rounding: the last rank with mass
     }
     if (rank == draw_rank) {
-      // the thread whose segment holds the crossing: block scan of the masses
-      const float mass =
-          my_mass >= 0.0f ? my_mass : (th_m == -INFINITY ? 0.0f : th_s * ex2((th_m - Mt) * c) * iSt);
-      const float incl = warp_inclusive_scan(mass, lane);
-      const unsigned posw = __ballot_sync(0xffffffffu, mass > 0.0f);
-      if (lane == 31) s_red[warp] = incl;
-      if (lane == 0) s_pos[warp] = posw;
-      __syncthreads();
-      const float winc = warp_inclusive_scan(lane < kTreeWarps ? s_red[lane] : 0.0f, lane);
-      const unsigned hit_w = __ballot_sync(0xffffffffu, lane < kTreeWarps && winc > tl);
-      const unsigned nz_w = __ballot_sync(0xffffffffu, lane < kTreeWarps && s_pos[lane] != 0u);
-      int wsel = -1, lsel = 0;
-      float thr_local = INFINITY;
-      if (hit_w) {
-        wsel = __ffs(hit_w) - 1;
-        if (warp == wsel) {
-          const float wb = __shfl_sync(0xffffffffu, winc, max(wsel - 1, 0));
-          const float base = wsel > 0 ? wb : 0.0f;
-          const float G = base + incl;
-          const unsigned hit = __ballot_sync(0xffffffffu, mass > 0.0f && G > tl);
-          // (no hit: rounding between the two scans; the warp's last thread with mass)
-          lsel = hit ? __ffs(hit) - 1 : (posw ? 31 - __clz(posw) : 31);
-          const float gprev = __shfl_sync(0xffffffffu, G, max(lsel - 1, 0));
-          thr_local = hit ? tl - (lsel > 0 ? gprev : base) : INFINITY;
+      // the warp whose range holds the crossing, then that range
+      const float mass = w_mass >= 0.0f ? w_mass : (w_m == -INFINITY ? 0.0f : w_s * ex2((w_m - Mt) * c) * iSt);
+      const float Mtc = Mt * c, Mdc = Md * c;
+      final_tok = range_draw<kTreeThreads, EPG>(mass, tl, lo, G, cta_it, [&](int g, float *w) {
+        if (staged) {
+#pragma unroll
+          for (int e = 0; e < EPG; ++e)
+            w[e] = fmaxf(0.0f, s_p[stage_index(g, e, EPG)] - cres * s_q[stage_index(g, e, EPG)]);
+          return;
         }
-      } else if (nz_w) {  // rounding: the last thread with mass, its last positive weight
-        wsel = 31 - __clz(nz_w);
-        lsel = 31 - __clz(s_pos[wsel]);
-      }
-      if (warp == wsel) {
-        const int tsel = wsel * 32 + lsel;
-        const int a = min(hi, lo + tsel * P.seg), len = min(hi, a + P.seg) - a;
-        const float Mtc = Mt * c, Mdc = Md * c;
-        float run = 0.0f;
-        int pick = -1, lastp = -1;
-        for (int o0 = 0; o0 < len; o0 += 32) {
-          const int o = o0 + lane;
-          float w = 0.0f;
-          if (o < len) {
-            if (staged) {
-              w = fmaxf(0.0f, s_p[o * kTreeThreads + tsel] - cres * s_q[o * kTreeThreads + tsel]);
-            } else {
-              w = ex2(fmaf(load_one<DT>(trow, a + o), c, -Mtc)) * iSt;
-              if (cres > 0.0f)
-                w = fmaxf(0.0f, w - cres * (ex2(fmaf(load_one<DT>(drow, a + o), c, -Mdc)) * iSd));
-            }
-          }
-          const float inc = warp_inclusive_scan(w, lane);
-          const unsigned hit = __ballot_sync(0xffffffffu, w > 0.0f && run + inc > thr_local);
-          const unsigned pos = __ballot_sync(0xffffffffu, w > 0.0f);
-          if (pos) lastp = o0 + 31 - __clz(pos);
-          if (hit) {
-            pick = o0 + __ffs(hit) - 1;
-            break;
-          }
-          run += __shfl_sync(0xffffffffu, inc, 31);
+        float t[EPG];
+        unpack16<DT>(load_group<DT, VEC>(trow, lo + g * EPG, hi), t);
+#pragma unroll
+        for (int e = 0; e < EPG; ++e) w[e] = ex2(fmaf(t[e], c, -Mtc)) * iSt;
+        if (cres > 0.0f) {
+          float d[EPG];
+          unpack16<DT>(load_group<DT, VEC>(drow, lo + g * EPG, hi), d);
+#pragma unroll
+          for (int e = 0; e < EPG; ++e) w[e] = fmaxf(0.0f, w[e] - cres * (ex2(fmaf(d[e], c, -Mdc)) * iSd));
         }
-        if (pick < 0) pick = lastp;
-        if (lane == 0) s_final = pick >= 0 ? a + pick : cta_it;
-      } else if (wsel < 0 && tid == 0) {
-        s_final = cta_it;  // no positive weight left in the slice (underflow only)
-      }
-      __syncthreads();
-      final_tok = s_final;
+      });
     }
     break;
   }
@@ -560,10 +427,12 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
 
 // Dynamic shared memory of the walk: parents, tokens, children and the
 // children's two token logits (5 words per node), the uniforms (N + 1), plus
-// the staged p and q of the CTA's segments when staging is on.
+// the staged p and q of the CTA's slice (every lane's groups) when staging
+// is on.
 size_t tree_dynamic_smem(const TreeParams &P) {
+  const size_t epg = P.dtype == SPEC_DTYPE_F32 ? 4 : 8;
   return sizeof(int) * (6 * static_cast<size_t>(P.N) + 1) +
-         (P.stage ? 2 * sizeof(float) * static_cast<size_t>(P.seg) * kTreeThreads : 0);
+         (P.stage ? 2 * sizeof(float) * static_cast<size_t>(P.groups) * epg * kTreeThreads : 0);
 }
 
 template <int DT, bool VEC, bool GREEDY>

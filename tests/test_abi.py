@@ -45,6 +45,16 @@ def test_header_constants_match_binding():
     assert int(consts["SPEC_ECUDA"]) == api.SPEC_ECUDA
     assert int(consts["SPEC_DTYPE_BF16"]) == api.DTYPE_BF16
     assert int(consts["SPEC_STATUS_BAD_TREE"]) == api.STATUS_BAD_TREE
+    assert (int(consts["SPEC_CHAIN_AUTO"]), int(consts["SPEC_CHAIN_TWO_PASS"]), int(consts["SPEC_CHAIN_FUSED"])) == \
+        (api.CHAIN_AUTO, api.CHAIN_TWO_PASS, api.CHAIN_FUSED)
+
+
+def test_chain_path_switch(L):
+    L.spec_set_chain_path.argtypes = [ctypes.c_int]
+    for bad in (-1, 3, 1 << 20):
+        assert L.spec_set_chain_path(bad) == -1          # SPEC_EINVAL
+    for good in (2, 1, 0):
+        assert L.spec_set_chain_path(good) == 0
 
 
 FAKE = ctypes.c_void_p(0x10000)   # never dereferenced: every call below fails validation

@@ -2,7 +2,9 @@
 
 Greedy outputs and accept counts are compared bit for bit.  Sampled
 decisions follow the rule in tests/parity.py (near-threshold cases counted),
-per-token probabilities within 1e-5 absolute.
+per-token probabilities within 1e-5 absolute.  Every test runs once on each
+chain path (two-pass and fused; a fused call whose clusters cannot all be
+resident runs two-pass).
 """
 import numpy as np
 import pytest
@@ -19,6 +21,13 @@ pytestmark = pytest.mark.gpu
 def _built():
     import __graft_entry__
     __graft_entry__.build()
+
+
+@pytest.fixture(scope="module", autouse=True, params=["two_pass", "fused"])
+def chain_path(request, _built):
+    api.set_chain_path(api.CHAIN_TWO_PASS if request.param == "two_pass" else api.CHAIN_FUSED)
+    yield request.param
+    api.set_chain_path(api.CHAIN_AUTO)
 
 
 def _greedy_drafts(target_bits_or_f32, rng, accept_prob=0.7):
