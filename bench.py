@@ -441,6 +441,8 @@ def run_ours(args):
     import __graft_entry__
     __graft_entry__.build()
     from speculative_decoding_verification_02_gb300 import api
+    api.set_chain_path({"auto": api.CHAIN_AUTO, "two_pass": api.CHAIN_TWO_PASS,
+                        "fused": api.CHAIN_FUSED}[args.chain_path])
 
     wl = WORKLOADS[args.workload](args.workload)
     # rotating input sets: one cycle reads more than twice the L2
@@ -582,7 +584,7 @@ def run_ours(args):
                        "parallelism": f"replicas x{ws}",
                        "l2": f"inputs rotate over {nsets} resident sets ({nsets * wl.set_bytes / 2**20:.0f} MiB, "
                              f"more than twice the L2 between reuses)",
-                       "launch": f"CUDA graph of {nsets} calls"},
+                       "launch": f"CUDA graph of {nsets} calls", "chain_path": args.chain_path},
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
                          "traffic": profiled_traffic(dom, args.workload, wl.kind),
@@ -609,6 +611,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="vocab248k", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--chain-path", choices=["auto", "two_pass", "fused"], default="auto",
+                    help="chain verification path (same results; for profiling one path)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":

@@ -40,9 +40,11 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 constexpr long long kSmCount = 152;
 
 // Chain path (spec_set_chain_path).  In AUTO the fused kernel takes
-// vocabularies up to kFusedAutoMaxV, where it is as fast as the two-pass path.
+// vocabularies up to kFusedAutoMaxV: 0, since with the cluster accept kernel
+// the two-pass path measures faster on every shape tried (B=1..64,
+// V=2,048..248,320).
 std::atomic<int> g_chain_path{SPEC_CHAIN_AUTO};
-constexpr int kFusedAutoMaxV = 8192;
+constexpr int kFusedAutoMaxV = 0;
 
 int stream_chunk(int dtype, long long rows_total, int V) {
   const long long es = elem_size(dtype);
@@ -100,22 +102,6 @@ void tree_geometry(int B, int V, int &cluster, int &slice) {
   cluster = V >= 16 * 2048 ? 16 : V >= 8 * 2048 ? 8 : (V >= 4 * 2048 ? 4 : (V >= 2 * 2048 ? 2 : 1));
   while (cluster > 1 && static_cast<long long>(B) * cluster > kSmCount) cluster /= 2;
   slice = ((V + cluster - 1) / cluster + 7) / 8 * 8;
-}
-
-// Sampling accept kernel: one cluster of up to 16 CTAs (1024 threads, 16
-// logits each) per request when V fits and all the clusters fit in one wave
-// of the 152 SMs (one such CTA fills an SM); otherwise the chunked accept
-// kernel, whose small CTAs share SMs.
-void cluster_geometry(int B, int V, int &cluster, int &slice) {
-  const int per_cta = 1024 * 16;
-  const int n = (V + per_cta - 1) / per_cta;
-  if (n > 16 || static_cast<long long>(B) * n > kSmCount) {
-    cluster = 0;
-    slice = 0;
-    return;
-  }
-  cluster = n;
-  slice = ((V + n - 1) / n + 15) / 16 * 16;
 }
 
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
@@ -342,9 +328,9 @@ static int chain_common(bool sample, const void *target, int64_t t_req, const vo
   if (want_fused && chain_fused_plan(P, sample, fvec)) {
     e = launch_chain_fused(P, sample, fvec, as_stream(stream));
   } else {
-    cluster_geometry(B, V, P.cluster, P.slice);
-    if (!sample) P.cluster = 0;
-    e = launch_chain(P, sample, vec, as_stream(stream));
+    // two-pass: the cluster accept kernel when every request's cluster is resident
+    if (!(sample && chain_accept_plan(P, fvec))) P.cluster = 0;
+    e = launch_chain(P, sample, vec, fvec, as_stream(stream));
   }
   return e == cudaSuccess ? SPEC_OK : fail_cuda(e, sample ? "spec_verify_sample" : "spec_verify_greedy");
 }

@@ -26,7 +26,9 @@
 //                     kernel zeroed, so the workspace needs no
 //                     initialisation) picks the chunk where u * R falls and
 //                     scans it: a draw from norm(max(0, p - q)).
-// Both accept kernels read their inputs before waiting on the stats grid.
+//     When every request's thread-block cluster fits on the GPU at once,
+//     the cluster accept kernel (chain_fused.cu) replaces it.
+// The accept kernels read their inputs before waiting on the stats grid.
 // No kernel waits on another CTA.
 #include <cooperative_groups.h>
 
@@ -424,207 +426,6 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
   }
 }
 
-// ------------------------------------------------------- cluster accept
-
-// Sampling accept with one thread-block cluster per request (used when V fits
-// the cluster: V <= 16 CTAs x 1024 threads x 16 logits).  Every CTA merges
-// the request's partials and reaches the same decision.  The final draw
-// then needs one pass over V of the weights w_v -- max(0, p_m - q_m) after a
-// rejection, p_L after a full accept -- and nothing else: each thread
-// computes the weights of its 16 contiguous logits and keeps them in
-// registers, the CTA scans the thread sums, the CTAs swap their slice totals
-// through distributed shared memory, and the CTA whose slice holds u * total
-// finds the token from its threads' registers.  No atomics, no second pass.
-constexpr int kClusterThreads = 1024;
-constexpr int kClusterWarps = kClusterThreads / 32;
-constexpr int kSegment = 16;  // contiguous logits per thread
-constexpr int kMaxCluster = 16;
-
-// Inclusive scan of one value per thread over a 1024-thread block.  Returns
-// the thread's exclusive prefix; `total` receives the block sum.
-__device__ __forceinline__ float block_exclusive_scan_1024(float v, float &total) {
-  __shared__ float s_w[kClusterWarps];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const float incl = warp_inclusive_scan(v, lane);
-  if (lane == 31) s_w[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const float t = s_w[lane];
-    const float ti = warp_inclusive_scan(t, lane);
-    s_w[lane] = ti - t;  // exclusive prefix of each warp
-  }
-  __syncthreads();
-  float tot = 0.0f;
-  // the block total is the last warp's exclusive prefix plus its own total
-  const float last_incl = __shfl_sync(0xffffffffu, incl, 31);
-  const float warp_base = s_w[warp];
-  if (warp == kClusterWarps - 1) tot = warp_base + last_incl;
-  __shared__ float s_total;
-  if (threadIdx.x == kClusterThreads - 1) s_total = tot;
-  __syncthreads();
-  total = s_total;
-  const float ex = warp_base + incl - v;
-  __syncthreads();
-  return ex;
-}
-
-template <int DT, bool VEC>
-__global__ void __launch_bounds__(kClusterThreads) chain_sample_accept_cluster_kernel(const ChainParams P) {
-  cg::cluster_group cluster = cg::this_cluster();
-  const int CS = P.cluster;
-  const int rank = static_cast<int>(cluster.block_rank());
-  const int b = blockIdx.x / CS;
-  const int k = P.k, rows = 2 * k + 1, nc = P.nc;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  __shared__ float sM[kMaxRows], sS[kMaxRows], sX[kMaxRows];
-  __shared__ int sTok[SPEC_MAX_K];
-  __shared__ float sU[SPEC_MAX_K + 1], sP[SPEC_MAX_K], sQ[SPEC_MAX_K];
-  __shared__ float s_slot[2], s_tots[kMaxCluster];
-  __shared__ int s_m, s_wpick[kClusterWarps], s_wlast[kClusterWarps];
-
-  const Prologue pr = read_request(P, b, sTok, sU, true);
-  pdl_wait();
-  if (pr.bad) {  // every CTA of the cluster leaves here; no shared memory was exchanged
-    if (rank == 0) write_common<true>(P, b, pr.bad, pr.L, 0, 0, sTok, sP, sQ, true, -1);
-    return;
-  }
-  const int L = pr.L;
-  const int nrr = 2 * L + 1;
-  const Partial *base = P.part + static_cast<int64_t>(b) * rows * nc;
-  auto row_of = [&](int rr) { return rr <= L ? rr : (k + 1) + (rr - L - 1); };
-  auto tok_chunk = [&](int rr) {
-    const int pos = rr <= L ? rr : rr - L - 1;
-    return pos < L ? sTok[pos] / P.chunk : -1;
-  };
-  for (int rr = warp; rr < nrr; rr += 2 * kClusterWarps) {
-    const int rr2 = rr + kClusterWarps;
-    RowStats a, bb;
-    warp_merge_two_rows<true>(base + static_cast<int64_t>(row_of(rr)) * nc,
-                              rr2 < nrr ? base + static_cast<int64_t>(row_of(rr2)) * nc : nullptr, nc, P.c,
-                              tok_chunk(rr), rr2 < nrr ? tok_chunk(rr2) : -1, a, bb);
-    if (lane == 0) {
-      sM[rr] = a.M;
-      sS[rr] = a.S;
-      sX[rr] = a.X;
-      if (rr2 < nrr) {
-        sM[rr2] = bb.M;
-        sS[rr2] = bb.S;
-        sX[rr2] = bb.X;
-      }
-    }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int m = 0;
-    for (int i = 0; i < L; ++i) {
-      const float p = ex2((sX[i] - sM[i]) * P.c) / sS[i];
-      const float q = ex2((sX[L + 1 + i] - sM[L + 1 + i]) * P.c) / sS[L + 1 + i];
-      sP[i] = p;
-      sQ[i] = q;
-      if (m == i && sU[i] * q < p) m = i + 1;
-    }
-    s_m = m;
-  }
-  __syncthreads();
-  const int m = s_m;
-  const int ne = max(0, min(m + 1, pr.cap));
-  if (rank == 0) write_common<true>(P, b, 0, L, m, ne, sTok, sP, sQ, false, -1);
-
-  // weights of this thread's 16 logits: the residual after a rejection,
-  // p_L after a full accept
-  Weights W = m < L
-                  ? Weights{row_ptr<DT>(P.target, P.t_req, P.row, b, m), row_ptr<DT>(P.draftl, P.d_req, P.row, b, m),
-                            sM[m], sM[L + 1 + m], 1.0f / sS[m], 1.0f / sS[L + 1 + m], P.c}
-                  : Weights{row_ptr<DT>(P.target, P.t_req, P.row, b, L), nullptr, sM[L], 0.0f, 1.0f / sS[L], 0.0f,
-                            P.c};
-  const int lo = min(P.V, rank * P.slice), hi = min(P.V, lo + P.slice);
-  const int v0 = lo + tid * kSegment;
-  const float u_final = sU[k];
-  int phase = 0;
-  for (int attempt = 0; attempt < 2; ++attempt) {
-    float w[kSegment];
-    weights8<DT, VEC>(W, v0, hi, w);
-    weights8<DT, VEC>(W, v0 + 8, hi, w + 8);
-    float seg = 0.0f;
-#pragma unroll
-    for (int e = 0; e < kSegment; ++e) seg += w[e];
-    float cta_total;
-    const float ex = block_exclusive_scan_1024(seg, cta_total);
-    // swap slice totals through distributed shared memory: thread r fetches
-    // rank r's total, so the remote loads are in flight together
-    if (tid == 0) s_slot[phase & 1] = cta_total;
-    cluster.sync();
-    if (tid < CS) s_tots[tid] = *cluster.map_shared_rank(&s_slot[phase & 1], tid);
-    __syncthreads();
-    float total = 0.0f, rbase = 0.0f, thr = 0.0f;
-    int rsel = -1, rlast = 0;
-    for (int r = 0; r < CS; ++r) total += s_tots[r];
-    thr = u_final * total;
-    {
-      float cum = 0.0f;
-      for (int r = 0; r < CS; ++r) {
-        const float t = s_tots[r];
-        if (t > 0.0f) rlast = r;
-        if (rsel < 0 && cum + t > thr) {
-          rsel = r;
-          rbase = cum;
-        }
-        cum += t;
-      }
-    }
-    __syncthreads();
-    ++phase;
-    if (!(total > 0.0f) && m < L && attempt == 0) {
-      // zero residual mass (only through rounding): draw from p_m instead
-      W.b = nullptr;
-      W.beta = 0.0f;
-      continue;
-    }
-    cluster_arrive();  // this CTA reads no other CTA's shared memory from here on
-    const int owner = rsel >= 0 ? rsel : rlast;
-    if (rank == owner) {
-      // the first thread whose running prefix passes the threshold holds the
-      // token; each warp proposes its first such lane, thread 0 takes the
-      // first proposing warp
-      const float tl = rsel >= 0 ? thr - rbase : INFINITY;
-      int lastp = -1;
-#pragma unroll
-      for (int e = 0; e < kSegment; ++e)
-        if (w[e] > 0.0f) lastp = v0 + e;
-      const unsigned cross = __ballot_sync(0xffffffffu, ex + seg > tl);
-      int pick = -1;
-      if (cross && lane == __ffs(cross) - 1) {
-        float run = ex;
-#pragma unroll
-        for (int e = 0; e < kSegment; ++e) {
-          run += w[e];
-          if (pick < 0 && run > tl) pick = v0 + e;
-        }
-        if (pick < 0) pick = lastp;
-      }
-      if (cross) pick = __shfl_sync(0xffffffffu, pick, __ffs(cross) - 1);
-      for (int o = 16; o > 0; o >>= 1) lastp = max(lastp, __shfl_xor_sync(0xffffffffu, lastp, o));
-      if (lane == 0) {
-        s_wpick[warp] = cross ? pick : -1;
-        s_wlast[warp] = lastp;
-      }
-      __syncthreads();
-      if (tid == 0) {
-        int tok = -1, last = -1;
-        for (int i = 0; i < kClusterWarps; ++i) {
-          if (tok < 0 && s_wpick[i] >= 0) tok = s_wpick[i];
-          last = max(last, s_wlast[i]);
-        }
-        if (tok < 0) tok = last;
-        if (m < ne) P.out_tokens[static_cast<int64_t>(b) * (k + 1) + m] = tok;
-        if (P.resid_mass) P.resid_mass[b] = (m < L && W.b != nullptr) ? total : 0.0f;
-      }
-    }
-    break;
-  }
-  cluster_wait();  // no CTA leaves while another may still read its slots
-}
-
 // ------------------------------------------------------------------- host
 
 // Launch with programmatic stream serialisation: the kernel may start while
@@ -645,7 +446,7 @@ static cudaError_t launch_dependent(K kern, unsigned grid, cudaStream_t st, cons
   return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
-template <int DT, bool VEC>
+template <int DT, bool VEC, bool CVEC>
 static cudaError_t launch_chain_t(const ChainParams &P, bool sample, cudaStream_t st) {
   const int rows = sample ? 2 * P.k + 1 : P.k + 1;
   const unsigned grid1 = static_cast<unsigned>(static_cast<long long>(P.B) * rows * P.nc);
@@ -654,27 +455,7 @@ static cudaError_t launch_chain_t(const ChainParams &P, bool sample, cudaStream_
       chain_stats_kernel<DT, true, VEC><<<grid1, kThreads, 0, st>>>(P);
     });
     if (e != cudaSuccess) return e;
-    if (P.cluster > 0) {
-      auto kern = chain_sample_accept_cluster_kernel<DT, VEC>;
-      if (P.cluster > 8) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-      }
-      cudaLaunchConfig_t cfg{};
-      cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(P.B) * P.cluster));
-      cfg.blockDim = dim3(kClusterThreads);
-      cfg.stream = st;
-      cudaLaunchAttribute attr[2];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = P.cluster;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-      attr[1].val.programmaticStreamSerializationAllowed = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = trace_enabled() ? 1 : 2;
-      return trace_launch_ex("chain_sample_accept_cluster", st, [&] { return cudaLaunchKernelEx(&cfg, kern, P); });
-    }
+    if (P.cluster > 0) return launch_chain_accept_cluster(P, CVEC, st);
     const unsigned grid2 = static_cast<unsigned>(static_cast<long long>(P.B) * P.nc2);
     return trace_launch_ex("chain_sample_accept", st, [&] {
       return launch_dependent(chain_sample_accept_kernel<DT, VEC>, grid2, st, P);
@@ -689,12 +470,15 @@ static cudaError_t launch_chain_t(const ChainParams &P, bool sample, cudaStream_
   });
 }
 
-cudaError_t launch_chain(const ChainParams &P, bool sample, bool vec, cudaStream_t st) {
+cudaError_t launch_chain(const ChainParams &P, bool sample, bool vec, bool cvec, cudaStream_t st) {
+  // (cvec implies vec: it adds V a multiple of a 16-byte group)
   if (P.dtype == SPEC_DTYPE_BF16)
-    return vec ? launch_chain_t<SPEC_DTYPE_BF16, true>(P, sample, st)
-               : launch_chain_t<SPEC_DTYPE_BF16, false>(P, sample, st);
-  return vec ? launch_chain_t<SPEC_DTYPE_F32, true>(P, sample, st)
-             : launch_chain_t<SPEC_DTYPE_F32, false>(P, sample, st);
+    return vec ? (cvec ? launch_chain_t<SPEC_DTYPE_BF16, true, true>(P, sample, st)
+                       : launch_chain_t<SPEC_DTYPE_BF16, true, false>(P, sample, st))
+               : launch_chain_t<SPEC_DTYPE_BF16, false, false>(P, sample, st);
+  return vec ? (cvec ? launch_chain_t<SPEC_DTYPE_F32, true, true>(P, sample, st)
+                     : launch_chain_t<SPEC_DTYPE_F32, true, false>(P, sample, st))
+             : launch_chain_t<SPEC_DTYPE_F32, false, false>(P, sample, st);
 }
 
 }  // namespace sv

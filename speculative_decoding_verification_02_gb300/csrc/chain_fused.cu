@@ -12,8 +12,8 @@
 // loads stay coalesced):
 //   1. rows are streamed kRowBatch at a time with all their loads in flight;
 //      each lane folds its groups of each row into (max, sum
-//      2^((x - max) c), first argmax) and warps merge those with redux and
-//      shuffle reductions;
+//      2^((x - max) c)) -- greedy mode: (max, first argmax) -- and warps
+//      merge those with redux and shuffle reductions;
 //   2. warp w merges rows w, w + 16, ... over the CTA's warps and pushes the
 //      CTA's statistics of the row into every CTA of the cluster
 //      (distributed shared memory); after one cluster barrier every CTA
@@ -84,8 +84,17 @@ __device__ __forceinline__ float lane_weight_sum(const Weights &W, int lo, int h
   return acc;
 }
 
-template <int DT, bool VEC, bool SAMPLE>
-__global__ void __launch_bounds__(kFusedThreads) chain_fused_kernel(const ChainParams P) {
+// The streaming pass's statistics of one (request, row, chunk).
+__device__ __forceinline__ float4 ld_part(const Partial *p) { return __ldcg(reinterpret_cast<const float4 *>(p)); }
+
+// ACCEPT: the second launch of the two-pass path.  The row statistics are
+// not streamed here but merged from the partials the streaming pass wrote
+// (every CTA merges all of its request's rows, so no exchange is needed for
+// them); the decision and the final draw are the same.  Its CTAs are small
+// enough to share SMs with the streaming pass, so they start early and wait
+// for it (programmatic dependent launch).
+template <int DT, bool VEC, bool SAMPLE, bool ACCEPT>
+__global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_kernel(const ChainParams P) {
   cg::cluster_group cluster = cg::this_cluster();
   constexpr int EPG = Elems<DT>::kPerGroup;
   const int CS = P.cluster;
@@ -103,9 +112,10 @@ __global__ void __launch_bounds__(kFusedThreads) chain_fused_kernel(const ChainP
   __shared__ float s_red[kFusedWarps], s_z[2][kFusedMaxCluster];
   const RowPart kEmpty{-INFINITY, 0.0f, kNoIndex, 0.0f};
 
-  pdl_wait();  // the inputs may be the previous kernel's outputs
+  if (!ACCEPT) pdl_wait();  // the inputs may be the previous kernel's outputs
   pdl_launch_dependents();
   const Prologue pr = read_request(P, b, sTok, sU, SAMPLE);
+  if (ACCEPT) pdl_wait();  // the streaming pass's partials
   if (pr.bad) {  // every CTA of the cluster leaves here; no shared memory was exchanged
     if (rank == 0) write_common<SAMPLE>(P, b, pr.bad, pr.L, 0, 0, sTok, sP, sQ, true, -1);
     return;
@@ -117,59 +127,84 @@ __global__ void __launch_bounds__(kFusedThreads) chain_fused_kernel(const ChainP
                    : row_ptr<DT>(P.draftl, P.d_req, P.row, b, rr - L - 1);
   };
   const float c = P.c;
-  // the drafted tokens' logits (thread rr reads row rr's), in flight with the stream
-  float xtok = -INFINITY;
-  if (SAMPLE && tid < nrows) {
-    const int pos = tid <= L ? tid : tid - L - 1;
-    if (pos < L) xtok = load_one<DT>(row_of(tid), sTok[pos]);
-  }
   const int lo = min(P.V, rank * P.slice), hi = min(P.V, lo + P.slice);
   const int G = P.groups;  // rounds of 16-byte groups per lane
-
-  // ---- 1. row statistics over the slice, kRowBatch rows at a time
-  for (int rr0 = 0; rr0 < nrows; rr0 += kRowBatch) {
-    RowStats R[kRowBatch];
-    const char *rp[kRowBatch];
-#pragma unroll
-    for (int r = 0; r < kRowBatch; ++r) {
-      R[r] = row_stats_empty();
-      rp[r] = rr0 + r < nrows ? row_of(rr0 + r) : nullptr;
-    }
-    lane_rows_stats<DT, SAMPLE, VEC, kRowBatch>(rp, lo, hi, G, c, R);
-#pragma unroll
-    for (int r = 0; r < kRowBatch; ++r) {
-      if (rr0 + r < nrows) {
-        float m = R[r].m, s = R[r].s.x + R[r].s.y;
-        int i = R[r].i;
-        if (SAMPLE) warp_allmerge<true>(m, s, i, c);
-        else warp_allargmax(m, i);
-        if (lane == 0) s_wpart[warp * rows_max + rr0 + r] = RowPart{m, s, i, 0.0f};
+  if (ACCEPT) {
+    // ---- 1-2. merge the streaming pass's partials of each row (warp w: rows w, w + 16, ...)
+    const int nc = P.nc;
+    const Partial *base = P.part + static_cast<int64_t>(b) * (2 * k + 1) * nc;
+    for (int rr = warp; rr < nrows; rr += kFusedWarps) {
+      const int r = rr <= L ? rr : (k + 1) + (rr - L - 1);  // the streaming pass's row numbering
+      const Partial *rp = base + static_cast<int64_t>(r) * nc;
+      float m = -INFINITY, s = 0.0f;
+      int unused = kNoIndex;
+      for (int j = lane; j < nc; j += 32) {
+        const float4 q = ld_part(rp + j);
+        merge_stats(m, s, unused, q.x, q.y, kNoIndex, c);
+      }
+      warp_allmerge<false>(m, s, unused, c);
+      const int pos = rr <= L ? rr : rr - L - 1;
+      const float x = pos < L ? ld_part(rp + sTok[pos] / P.chunk).w : -INFINITY;  // the drafted token's logit
+      if (lane == 0) {
+        sM[rr] = m;
+        sS[rr] = s;
+        sX[rr] = x;
       }
     }
-  }
-  if (SAMPLE && tid < nrows) sX[tid] = xtok;
-  __syncthreads();
-
-  // ---- 2. the CTA's statistics of each row, pushed into every CTA
-  for (int rr = warp; rr < nrows; rr += kFusedWarps) {
-    RowPart x = lane < kFusedWarps ? s_wpart[lane * rows_max + rr] : kEmpty;
-    if (SAMPLE) warp_allmerge<true>(x.m, x.s, x.i, c);
-    else warp_allargmax(x.m, x.i);
-    if (lane < CS) *cluster.map_shared_rank(&s_cpart[rank * rows_max + rr], lane) = x;
-  }
-  cluster.sync();
-  // every CTA merges the slices (lane r holds rank r) and decides alike
-  for (int rr = warp; rr < nrows; rr += kFusedWarps) {
-    RowPart x = lane < CS ? s_cpart[lane * rows_max + rr] : kEmpty;
-    if (SAMPLE) warp_allmerge<true>(x.m, x.s, x.i, c);
-    else warp_allargmax(x.m, x.i);
-    if (lane == 0) {
-      sM[rr] = x.m;
-      sS[rr] = x.s;
-      sA[rr] = x.i == kNoIndex ? 0 : x.i;
+    __syncthreads();
+  } else {
+    // the drafted tokens' logits (thread rr reads row rr's), in flight with the stream
+    float xtok = -INFINITY;
+    if (SAMPLE && tid < nrows) {
+      const int pos = tid <= L ? tid : tid - L - 1;
+      if (pos < L) xtok = load_one<DT>(row_of(tid), sTok[pos]);
     }
+
+    // ---- 1. row statistics over the slice, kRowBatch rows at a time
+    for (int rr0 = 0; rr0 < nrows; rr0 += kRowBatch) {
+      RowStats R[kRowBatch];
+      const char *rp[kRowBatch];
+#pragma unroll
+      for (int r = 0; r < kRowBatch; ++r) {
+        R[r] = row_stats_empty();
+        rp[r] = rr0 + r < nrows ? row_of(rr0 + r) : nullptr;
+      }
+      lane_rows_stats<DT, SAMPLE, VEC, kRowBatch>(rp, lo, hi, G, c, R);
+#pragma unroll
+      for (int r = 0; r < kRowBatch; ++r) {
+        if (rr0 + r < nrows) {
+          float m = R[r].m, s = R[r].s.x + R[r].s.y;
+          int i = R[r].i;
+          if (SAMPLE) warp_allmerge<false>(m, s, i, c);  // sampling needs no argmax
+          else warp_allargmax(m, i);
+          if (lane == 0) s_wpart[warp * rows_max + rr0 + r] = RowPart{m, s, i, 0.0f};
+        }
+      }
+    }
+    if (SAMPLE && tid < nrows) sX[tid] = xtok;
+    __syncthreads();
+
+    // ---- 2. the CTA's statistics of each row, pushed into every CTA
+    for (int rr = warp; rr < nrows; rr += kFusedWarps) {
+      RowPart x = lane < kFusedWarps ? s_wpart[lane * rows_max + rr] : kEmpty;
+      if (SAMPLE) warp_allmerge<false>(x.m, x.s, x.i, c);
+      else warp_allargmax(x.m, x.i);
+      if (lane < CS) *cluster.map_shared_rank(&s_cpart[rank * rows_max + rr], lane) = x;
+    }
+    cluster.sync();
+    // every CTA merges the slices (lane r holds rank r) and decides alike
+    for (int rr = warp; rr < nrows; rr += kFusedWarps) {
+      RowPart x = lane < CS ? s_cpart[lane * rows_max + rr] : kEmpty;
+      if (SAMPLE) warp_allmerge<false>(x.m, x.s, x.i, c);
+      else warp_allargmax(x.m, x.i);
+      if (lane == 0) {
+        sM[rr] = x.m;
+        sS[rr] = x.s;
+        sA[rr] = x.i == kNoIndex ? 0 : x.i;
+      }
+    }
+    __syncthreads();
   }
-  __syncthreads();
   if (tid < L) {
     if (SAMPLE) {
       const float p = ex2((sX[tid] - sM[tid]) * c) / sS[tid];
@@ -234,7 +269,8 @@ __global__ void __launch_bounds__(kFusedThreads) chain_fused_kernel(const ChainP
     draw_rank = pos_r ? 31 - __clz(pos_r) : 0;  // rounding: the last rank with mass
   }
   if (rank != draw_rank) return;  // no CTA touches another's shared memory from here on
-  const int tok = range_draw<kFusedThreads, EPG>(wmass, tl, lo, G, sA[m], [&](int g, float *w) {
+  // (the fallback `lo` is unreachable: the drawing rank has mass, so one of its warps has)
+  const int tok = range_draw<kFusedThreads, EPG>(wmass, tl, lo, G, lo, [&](int g, float *w) {
     float x[EPG], y[EPG];
     unpack16<DT>(load_group<DT, VEC>(W.a, lo + g * EPG, hi), x);
     if (W.b) unpack16<DT>(load_group<DT, VEC>(W.b, lo + g * EPG, hi), y);
@@ -249,14 +285,17 @@ __global__ void __launch_bounds__(kFusedThreads) chain_fused_kernel(const ChainP
 
 // ------------------------------------------------------------------- host
 
-size_t chain_fused_smem(int k, bool sample, int cluster) {
+constexpr int kAcceptMaxSlice = 16384;  // largest slice per CTA of the cluster accept kernel
+
+size_t chain_fused_smem(int k, bool sample, int cluster, bool accept) {
+  if (accept) return 0;  // the warp and slice statistics live in shared memory only when streamed here
   const int rows = sample ? 2 * k + 1 : k + 1;
   return sizeof(RowPart) * static_cast<size_t>(kFusedWarps + cluster) * rows;
 }
 
-template <int DT, bool VEC, bool SAMPLE>
+template <int DT, bool VEC, bool SAMPLE, bool ACCEPT>
 static cudaError_t prepare(int cluster, size_t smem) {
-  auto kern = chain_fused_kernel<DT, VEC, SAMPLE>;
+  auto kern = chain_fused_kernel<DT, VEC, SAMPLE, ACCEPT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e == cudaSuccess && cluster > 8) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return e;
@@ -279,11 +318,35 @@ static void cluster_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, i
   cfg.numAttrs = pdl ? 2 : 1;
 }
 
-// How many clusters of `cluster` CTAs of the fused kernel fit on the device
-// at once (cached per device and shape).
-static int resident_clusters(int dtype, bool vec, bool sample, int k, int cluster) {
+// Calls f.template operator()<DT, VEC, SAMPLE, ACCEPT>() for the runtime
+// choice (ACCEPT implies SAMPLE).
+template <class F>
+static cudaError_t dispatch(int dtype, bool vec, bool sample, bool accept, F &&f) {
+  if (dtype == SPEC_DTYPE_BF16) {
+    if (vec) {
+      if (accept) return f.template operator()<SPEC_DTYPE_BF16, true, true, true>();
+      return sample ? f.template operator()<SPEC_DTYPE_BF16, true, true, false>()
+                    : f.template operator()<SPEC_DTYPE_BF16, true, false, false>();
+    }
+    if (accept) return f.template operator()<SPEC_DTYPE_BF16, false, true, true>();
+    return sample ? f.template operator()<SPEC_DTYPE_BF16, false, true, false>()
+                  : f.template operator()<SPEC_DTYPE_BF16, false, false, false>();
+  }
+  if (vec) {
+    if (accept) return f.template operator()<SPEC_DTYPE_F32, true, true, true>();
+    return sample ? f.template operator()<SPEC_DTYPE_F32, true, true, false>()
+                  : f.template operator()<SPEC_DTYPE_F32, true, false, false>();
+  }
+  if (accept) return f.template operator()<SPEC_DTYPE_F32, false, true, true>();
+  return sample ? f.template operator()<SPEC_DTYPE_F32, false, true, false>()
+                : f.template operator()<SPEC_DTYPE_F32, false, false, false>();
+}
+
+// How many clusters of `cluster` CTAs of the kernel fit on the device at
+// once (cached per device and shape).
+static int resident_clusters(int dtype, bool vec, bool sample, bool accept, int k, int cluster) {
   struct Key {
-    int dev, dtype, vec, sample, k, cluster, n;
+    int dev, dtype, vec, sample, accept, k, cluster, n;
   };
   static std::mutex mu;
   static std::vector<Key> cache;
@@ -292,42 +355,39 @@ static int resident_clusters(int dtype, bool vec, bool sample, int k, int cluste
   {
     std::lock_guard<std::mutex> g(mu);
     for (const Key &q : cache)
-      if (q.dev == dev && q.dtype == dtype && q.vec == vec && q.sample == sample && q.k == k && q.cluster == cluster)
+      if (q.dev == dev && q.dtype == dtype && q.vec == vec && q.sample == sample && q.accept == accept &&
+          q.k == k && q.cluster == cluster)
         return q.n;
   }
-  const size_t smem = chain_fused_smem(k, sample, cluster);
+  const size_t smem = chain_fused_smem(k, sample, cluster, accept);
   int n = 0;
-  auto query = [&](auto kern, cudaError_t prep) {
-    if (prep != cudaSuccess) return;
-    cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[2];
-    cluster_config(cfg, attr, cluster, static_cast<unsigned>(cluster), smem, nullptr, false);
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
-  };
-#define SV_QUERY(DT, V, S) query(chain_fused_kernel<DT, V, S>, prepare<DT, V, S>(cluster, smem))
-  if (dtype == SPEC_DTYPE_BF16) {
-    if (vec) { if (sample) SV_QUERY(SPEC_DTYPE_BF16, true, true); else SV_QUERY(SPEC_DTYPE_BF16, true, false); }
-    else { if (sample) SV_QUERY(SPEC_DTYPE_BF16, false, true); else SV_QUERY(SPEC_DTYPE_BF16, false, false); }
-  } else {
-    if (vec) { if (sample) SV_QUERY(SPEC_DTYPE_F32, true, true); else SV_QUERY(SPEC_DTYPE_F32, true, false); }
-    else { if (sample) SV_QUERY(SPEC_DTYPE_F32, false, true); else SV_QUERY(SPEC_DTYPE_F32, false, false); }
-  }
-#undef SV_QUERY
+  dispatch(dtype, vec, sample, accept, [&]<int DT, bool VEC, bool SAMPLE, bool ACCEPT>() {
+    cudaError_t e = prepare<DT, VEC, SAMPLE, ACCEPT>(cluster, smem);
+    if (e == cudaSuccess) {
+      cudaLaunchConfig_t cfg;
+      cudaLaunchAttribute attr[2];
+      cluster_config(cfg, attr, cluster, static_cast<unsigned>(cluster), smem, nullptr, false);
+      e = cudaOccupancyMaxActiveClusters(&n, chain_fused_kernel<DT, VEC, SAMPLE, ACCEPT>, &cfg);
+    }
+    if (e != cudaSuccess) n = 0;
+    return e;
+  });
   cudaGetLastError();  // a refused query leaves no error behind
   std::lock_guard<std::mutex> g(mu);
-  cache.push_back(Key{dev, dtype, vec, sample, k, cluster, n});
+  cache.push_back(Key{dev, dtype, vec, sample, accept, k, cluster, n});
   return n;
 }
 
-bool chain_fused_plan(ChainParams &P, bool sample, bool vec) {
-  // at least kFusedMinSlice logits per CTA, at most 16 CTAs per request, and
-  // every request's cluster resident at once
+// Cluster geometry: the largest cluster (at most 16 CTAs, at least
+// kFusedMinSlice logits each, and for the accept kernel at most
+// kAcceptMaxSlice) for which every request's cluster is resident at once.
+static bool plan(ChainParams &P, bool sample, bool vec, bool accept) {
   int cs = (P.V + kFusedMinSlice - 1) / kFusedMinSlice;
   cs = cs < 1 ? 1 : (cs > kFusedMaxCluster ? kFusedMaxCluster : cs);
-  for (; cs >= 1; --cs) {
-    if (resident_clusters(P.dtype, vec, sample, P.k, cs) >= P.B) break;
-  }
-  if (cs < 1) return false;
+  const int cs_min = accept ? (P.V + kAcceptMaxSlice - 1) / kAcceptMaxSlice : 1;
+  for (; cs >= cs_min; --cs)
+    if (resident_clusters(P.dtype, vec, sample, accept, P.k, cs) >= P.B) break;
+  if (cs < cs_min || cs < 1) return false;
   P.cluster = cs;
   P.slice = ((P.V + cs - 1) / cs + 7) / 8 * 8;
   const int epg = P.dtype == SPEC_DTYPE_F32 ? 4 : 8;
@@ -335,29 +395,30 @@ bool chain_fused_plan(ChainParams &P, bool sample, bool vec) {
   return true;
 }
 
-template <int DT, bool VEC, bool SAMPLE>
-static cudaError_t launch_fused_t(const ChainParams &P, cudaStream_t st) {
-  const size_t smem = chain_fused_smem(P.k, SAMPLE, P.cluster);
-  cudaError_t e = prepare<DT, VEC, SAMPLE>(P.cluster, smem);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[2];
-  cluster_config(cfg, attr, P.cluster, static_cast<unsigned>(P.B * P.cluster), smem, st, !trace_enabled());
-  return trace_launch_ex(SAMPLE ? "chain_fused_sample" : "chain_fused_greedy", st,
-                         [&] { return cudaLaunchKernelEx(&cfg, chain_fused_kernel<DT, VEC, SAMPLE>, P); });
-}
+bool chain_fused_plan(ChainParams &P, bool sample, bool vec) { return plan(P, sample, vec, false); }
+bool chain_accept_plan(ChainParams &P, bool vec) { return plan(P, true, vec, true); }
 
-template <int DT, bool VEC>
-static cudaError_t launch_fused_mode(const ChainParams &P, bool sample, cudaStream_t st) {
-  return sample ? launch_fused_t<DT, VEC, true>(P, st) : launch_fused_t<DT, VEC, false>(P, st);
+static cudaError_t launch(const ChainParams &P, bool sample, bool vec, bool accept, cudaStream_t st) {
+  const size_t smem = chain_fused_smem(P.k, sample, P.cluster, accept);
+  return dispatch(P.dtype, vec, sample, accept, [&]<int DT, bool VEC, bool SAMPLE, bool ACCEPT>() {
+    cudaError_t e = prepare<DT, VEC, SAMPLE, ACCEPT>(P.cluster, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    cluster_config(cfg, attr, P.cluster, static_cast<unsigned>(P.B * P.cluster), smem, st, !trace_enabled());
+    const char *name = ACCEPT ? "chain_sample_accept_cluster" : SAMPLE ? "chain_fused_sample" : "chain_fused_greedy";
+    return trace_launch_ex(name, st, [&] {
+      return cudaLaunchKernelEx(&cfg, chain_fused_kernel<DT, VEC, SAMPLE, ACCEPT>, P);
+    });
+  });
 }
 
 cudaError_t launch_chain_fused(const ChainParams &P, bool sample, bool vec, cudaStream_t st) {
-  if (P.dtype == SPEC_DTYPE_BF16)
-    return vec ? launch_fused_mode<SPEC_DTYPE_BF16, true>(P, sample, st)
-               : launch_fused_mode<SPEC_DTYPE_BF16, false>(P, sample, st);
-  return vec ? launch_fused_mode<SPEC_DTYPE_F32, true>(P, sample, st)
-             : launch_fused_mode<SPEC_DTYPE_F32, false>(P, sample, st);
+  return launch(P, sample, vec, false, st);
+}
+
+cudaError_t launch_chain_accept_cluster(const ChainParams &P, bool vec, cudaStream_t st) {
+  return launch(P, true, vec, true, st);
 }
 
 }  // namespace sv

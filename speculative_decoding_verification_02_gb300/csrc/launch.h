@@ -58,12 +58,18 @@ struct NgramParams {
   int32_t *draft, *draft_len, *status;
 };
 
-cudaError_t launch_chain(const ChainParams &P, bool sample, bool vec, cudaStream_t st);
-// Fused chain kernel: chain_fused_plan picks the cluster geometry (cluster,
-// slice, groups) and returns false when the requests' clusters cannot all be
-// resident at once (then the two-kernel path runs).
+// Two-pass chain path: the streaming pass (16-byte loads when vec) and an
+// accept kernel -- the cluster accept kernel when P.cluster > 0 (its
+// 16-byte path when cvec), else the chunked or greedy accept kernel.
+cudaError_t launch_chain(const ChainParams &P, bool sample, bool vec, bool cvec, cudaStream_t st);
+// Cluster kernels (chain_fused.cu).  The plans pick the cluster geometry
+// (cluster, slice, groups) and return false when the requests' clusters
+// cannot all be resident at once.  chain_fused_plan: the fused one-launch
+// kernel; chain_accept_plan: the two-pass path's cluster accept kernel.
 bool chain_fused_plan(ChainParams &P, bool sample, bool vec);
+bool chain_accept_plan(ChainParams &P, bool vec);
 cudaError_t launch_chain_fused(const ChainParams &P, bool sample, bool vec, cudaStream_t st);
+cudaError_t launch_chain_accept_cluster(const ChainParams &P, bool vec, cudaStream_t st);
 cudaError_t launch_tree(const TreeParams &P, bool vec, cudaStream_t st);
 size_t tree_dynamic_smem(const TreeParams &P);
 cudaError_t launch_ngram(const NgramParams &P, cudaStream_t st);

@@ -105,28 +105,122 @@ __device__ __forceinline__ uint4 load_group(const char *row, int e, int hi) {
   }
 }
 
+// Max of the logits of the first n (<= kBatch) of the groups g.
+template <int DT>
+__device__ __forceinline__ float groups_max(const uint4 *g, int n) {
+  if (DT == SPEC_DTYPE_BF16) {
+    auto h2 = [](uint32_t w) { return *reinterpret_cast<const __nv_bfloat162 *>(&w); };
+    __nv_bfloat162 a = __hmax2(h2(g[0].x), h2(g[0].y)), b = __hmax2(h2(g[0].z), h2(g[0].w));
+#pragma unroll
+    for (int u = 1; u < kBatch; ++u) {
+      if (u < n) {
+        a = __hmax2(a, __hmax2(h2(g[u].x), h2(g[u].y)));
+        b = __hmax2(b, __hmax2(h2(g[u].z), h2(g[u].w)));
+      }
+    }
+    const __nv_bfloat162 mx = __hmax2(a, b);
+    return fmaxf(__low2float(mx), __high2float(mx));
+  }
+  float a = fmaxf(__uint_as_float(g[0].x), __uint_as_float(g[0].y));
+  float b = fmaxf(__uint_as_float(g[0].z), __uint_as_float(g[0].w));
+#pragma unroll
+  for (int u = 1; u < kBatch; ++u) {
+    if (u < n) {
+      a = fmaxf(a, fmaxf(__uint_as_float(g[u].x), __uint_as_float(g[u].y)));
+      b = fmaxf(b, fmaxf(__uint_as_float(g[u].z), __uint_as_float(g[u].w)));
+    }
+  }
+  return fmaxf(a, b);
+}
+
+// Adds 2^(x c - mc) over the logits of the first n groups into acc (one
+// packed FMA per two logits, one exponential per logit, one packed add per
+// two; consecutive groups alternate between two accumulators).
+template <int DT>
+__device__ __forceinline__ void groups_sumexp(const uint4 *g, int n, float c, float mc, float2 &acc) {
+  const float2 cc = make_float2(c, c), nm = make_float2(-mc, -mc);
+  float2 acc2 = make_float2(0.0f, 0.0f);
+  auto fold = [&](float2 &A, float a, float b) {
+    const float2 z = __ffma2_rn(make_float2(a, b), cc, nm);
+    A = __fadd2_rn(A, make_float2(ex2(z.x), ex2(z.y)));
+  };
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) {
+    if (u < n) {
+      float2 &A = (u & 1) ? acc2 : acc;
+      if (DT == SPEC_DTYPE_BF16) {
+        fold(A, bf16_lo(g[u].x), bf16_hi(g[u].x));
+        fold(A, bf16_lo(g[u].y), bf16_hi(g[u].y));
+        fold(A, bf16_lo(g[u].z), bf16_hi(g[u].z));
+        fold(A, bf16_lo(g[u].w), bf16_hi(g[u].w));
+      } else {
+        fold(A, __uint_as_float(g[u].x), __uint_as_float(g[u].y));
+        fold(A, __uint_as_float(g[u].z), __uint_as_float(g[u].w));
+      }
+    }
+  }
+  acc = __fadd2_rn(acc, acc2);
+}
+
+// First logit equal to bm among the first n groups, group u starting at
+// logit e0 + u * span; kNoIndex if none.
+template <int DT>
+__device__ __forceinline__ int groups_first(const uint4 *g, int n, float bm, int e0, int span) {
+  constexpr int EPG = Elems<DT>::kPerGroup;
+  int first = kNoIndex;
+#pragma unroll
+  for (int u = kBatch - 1; u >= 0; --u) {
+    if (u < n) {
+      float x[EPG];
+      unpack16<DT>(g[u], x);
+#pragma unroll
+      for (int e = EPG - 1; e >= 0; --e)
+        if (x[e] == bm) first = e0 + u * span + e;
+    }
+  }
+  return first;
+}
+
 // Folds this lane's groups (the lane_group split, G rounds) of NR rows into
 // R[r]; a null rows[r] is skipped.  kBatch rounds of every row are loaded
-// before any of them is folded.
+// before any of them is folded.  SOFTMAX: the running max and the sum of
+// 2^((x - max) c), rescaled once per batch when the batch raises the max
+// (R[r].i is not kept); otherwise the running max and its first index.
 template <int DT, bool SOFTMAX, bool VEC, int NR>
 __device__ __forceinline__ void lane_rows_stats(const char *const *rows, int lo, int hi, int G, float c,
                                                 RowStats *R) {
   constexpr int EPG = Elems<DT>::kPerGroup;
   constexpr uint32_t kNegInf = DT == SPEC_DTYPE_F32 ? 0xff800000u : 0xff80ff80u;  // -inf words
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float unused = 0.0f;
   for (int j0 = 0; j0 < G; j0 += kBatch) {
+    const int n = min(kBatch, G - j0);                        // rounds in this batch
     const int e0 = lo + lane_group(warp, j0, G, lane) * EPG;  // round j0 + u starts at e0 + u 32 EPG
     uint4 x[NR][kBatch];
 #pragma unroll
     for (int r = 0; r < NR; ++r)
 #pragma unroll
       for (int u = 0; u < kBatch; ++u)
-        x[r][u] = (rows[r] && j0 + u < G) ? load_group<DT, VEC>(rows[r], e0 + u * 32 * EPG, hi)
-                                          : make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
+        x[r][u] = (rows[r] && u < n) ? load_group<DT, VEC>(rows[r], e0 + u * 32 * EPG, hi)
+                                     : make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
 #pragma unroll
-    for (int r = 0; r < NR; ++r)
-      if (rows[r]) fold_batch<DT, SOFTMAX, 32>(x[r], e0, c, R[r].m, R[r].s, R[r].i, -1, unused);
+    for (int r = 0; r < NR; ++r) {
+      if (!rows[r]) continue;
+      const float bm = groups_max<DT>(x[r], n);
+      if (SOFTMAX) {
+        if (bm > R[r].m) {
+          if (R[r].m != -INFINITY) {
+            const float f = ex2((R[r].m - bm) * c);
+            R[r].s.x *= f;
+            R[r].s.y *= f;
+          }
+          R[r].m = bm;
+        }
+        if (R[r].m != -INFINITY) groups_sumexp<DT>(x[r], n, c, R[r].m * c, R[r].s);
+      } else if (bm > R[r].m) {
+        R[r].m = bm;
+        R[r].i = groups_first<DT>(x[r], n, bm, e0, 32 * EPG);
+      }
+    }
   }
 }
 

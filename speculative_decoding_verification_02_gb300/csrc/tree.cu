@@ -7,7 +7,8 @@
 // coalesced).  Only the rows of the nodes the walk visits are read.  Per
 // visited node u:
 //   1. one pass reduces t_u, and d_u when u has children, to (max, sum
-//      2^((x - max) c), first argmax), both rows' loads in flight together;
+//      2^((x - max) c)) -- greedy mode: (max, first argmax) of t_u -- both
+//      rows' loads in flight together;
 //      warps merge with redux and shuffle reductions, warp 0 merges the
 //      warps and pushes the CTA's statistics into every CTA of the cluster
 //      (distributed shared memory), and after one cluster barrier every CTA
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
       float dm = R[1].m, ds = R[1].s.x + R[1].s.y;
       int i = R[0].i, di = kNoIndex;
       if (GREEDY) warp_allargmax(w_m, i);
-      else warp_allmerge<true>(w_m, w_s, i, c);
+      else warp_allmerge<false>(w_m, w_s, i, c);  // sampling needs no argmax
       if (drow) warp_allmerge<false>(dm, ds, di, c);
       if (lane == 0) s_part[warp] = Slot{w_m, w_s, dm, ds, i, 0.0f, 0, 0};
     }
@@ -279,7 +280,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
       mine = lane < kTreeWarps ? s_part[lane] : kEmpty;
       int di = kNoIndex;
       if (GREEDY) warp_allargmax(mine.mt, mine.it);
-      else warp_allmerge<true>(mine.mt, mine.st, mine.it, c);
+      else warp_allmerge<false>(mine.mt, mine.st, mine.it, c);
       if (drow) warp_allmerge<false>(mine.md, mine.sd, di, c);
     }
     const int ph = push_and_sync(mine);
@@ -314,11 +315,10 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
 
     // ---- sampling: the node's p and q statistics over the whole row
     float Mt = r.mt, St = r.st, Md = r.md, Sd = r.sd;
-    int it = r.it, id = kNoIndex;
-    warp_allmerge<true>(Mt, St, it, c);
-    if (drow) warp_allmerge<false>(Md, Sd, id, c);
+    int unused = kNoIndex;
+    warp_allmerge<false>(Mt, St, unused, c);
+    if (drow) warp_allmerge<false>(Md, Sd, unused, c);
     const float iSt = 1.0f / St, iSd = drow ? 1.0f / Sd : 0.0f;
-    const int cta_it = __shfl_sync(0xffffffffu, r.it, rank);  // this slice's argmax
     // lane r: rank r's share of the current draw distribution (p so far)
     float rmass = lane < ncl ? r.st * ex2((r.mt - Mt) * c) * iSt : 0.0f;
     float w_mass = -1.0f;  // this warp's share of it; < 0: p, from the warp's statistics
@@ -386,7 +386,8 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
       // the warp whose range holds the crossing, then that range
       const float mass = w_mass >= 0.0f ? w_mass : (w_m == -INFINITY ? 0.0f : w_s * ex2((w_m - Mt) * c) * iSt);
       const float Mtc = Mt * c, Mdc = Md * c;
-      final_tok = range_draw<kTreeThreads, EPG>(mass, tl, lo, G, cta_it, [&](int g, float *w) {
+      // (the fallback `lo` is unreachable: the drawing rank has mass, so one of its warps has)
+      final_tok = range_draw<kTreeThreads, EPG>(mass, tl, lo, G, lo, [&](int g, float *w) {
         if (staged) {
 #pragma unroll
           for (int e = 0; e < EPG; ++e)
