@@ -35,6 +35,7 @@
 #include "chain_common.cuh"
 #include "common.cuh"
 #include "launch.h"
+#include "segments.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -87,8 +88,9 @@ __global__ void __launch_bounds__(kThreads) chain_stats_kernel(const ChainParams
   const int tok = (SOFTMAX && pos < L) ? P.draft[static_cast<int64_t>(b) * P.k + pos] : -1;
   float m = -INFINITY, s = 0.0f, xt = -INFINITY;
   int idx = kNoIndex;
-  thread_chunk_stats<DT, SOFTMAX, VEC, kLoadStream>(row, v0, v1, P.c, m, s, idx, tok, xt);
-  block_merge<SOFTMAX>(m, s, idx, P.c, xt);
+  // (the argmax is only used by greedy verification)
+  thread_chunk_stats<DT, SOFTMAX, VEC, kLoadStream, kThreads, !SOFTMAX>(row, v0, v1, P.c, m, s, idx, tok, xt);
+  block_allmerge<SOFTMAX, !SOFTMAX, kThreads>(m, s, idx, P.c, xt);
   if (threadIdx.x == 0)
     *reinterpret_cast<float4 *>(P.part + (static_cast<int64_t>(b) * rows + r) * P.nc + j) =
         make_float4(m, s, __int_as_float(idx), xt);
@@ -102,13 +104,13 @@ constexpr int kMergeUnroll = 4;  // partials per lane whose loads are issued tog
 // max, sum 2^((x - max) c), first argmax, and the drafted token's logit
 // (tokchunk = the chunk holding the token, or -1).  The loads of the first
 // 32 * kMergeUnroll chunks of both rows are all issued before any is used.
-struct RowStats {
+struct MergedRow {
   float M, S, X;
   int A;
 };
 
 template <bool SOFTMAX>
-__device__ __forceinline__ RowStats merge_prefetched(const float4 *q, const Partial *pp, int nc, float c,
+__device__ __forceinline__ MergedRow merge_prefetched(const float4 *q, const Partial *pp, int nc, float c,
                                                      int tokchunk) {
   const int lane = threadIdx.x & 31;
   float m = -INFINITY, s = 0.0f, x = -INFINITY;
@@ -128,7 +130,7 @@ __device__ __forceinline__ RowStats merge_prefetched(const float4 *q, const Part
     if (j == tokchunk) x = r.x;
   }
   if (SOFTMAX) warp_merge_stats(m, s, idx, c); else warp_merge_argmax(m, idx);
-  RowStats out;
+  MergedRow out;
   out.M = m;
   out.S = s;
   out.A = idx == kNoIndex ? 0 : idx;  // an all -inf row: every index ties, take 0
@@ -138,7 +140,7 @@ __device__ __forceinline__ RowStats merge_prefetched(const float4 *q, const Part
 
 template <bool SOFTMAX>
 __device__ __forceinline__ void warp_merge_two_rows(const Partial *ppA, const Partial *ppB, int nc, float c,
-                                                    int tokA, int tokB, RowStats &a, RowStats &b) {
+                                                    int tokA, int tokB, MergedRow &a, MergedRow &b) {
   const int lane = threadIdx.x & 31;
   const float4 neutral = make_float4(-INFINITY, 0.0f, __int_as_float(kNoIndex), -INFINITY);
   float4 qa[kMergeUnroll], qb[kMergeUnroll];
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(kThreads) chain_greedy_accept_kernel(const Cha
   const Partial *base = P.part + static_cast<int64_t>(b) * rows * P.nc;
   for (int r = warp; r <= pr.L; r += 2 * kWarps) {
     const int r2 = r + kWarps;
-    RowStats a, bb;
+    MergedRow a, bb;
     warp_merge_two_rows<false>(base + static_cast<int64_t>(r) * P.nc,
                                r2 <= pr.L ? base + static_cast<int64_t>(r2) * P.nc : nullptr, P.nc, 1.0f, -1, -1,
                                a, bb);
@@ -292,7 +294,7 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
   };
   for (int rr = warp; rr < nrr; rr += 2 * kWarps) {
     const int rr2 = rr + kWarps;
-    RowStats a, bb;
+    MergedRow a, bb;
     warp_merge_two_rows<true>(base + static_cast<int64_t>(row_of(rr)) * nc,
                               rr2 < nrr ? base + static_cast<int64_t>(row_of(rr2)) * nc : nullptr, nc, P.c,
                               tok_chunk(rr), rr2 < nrr ? tok_chunk(rr2) : -1, a, bb);

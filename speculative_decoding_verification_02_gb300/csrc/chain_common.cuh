@@ -21,26 +21,30 @@ struct Prologue {
   int L, bad, cap;
 };
 
+// Validates a request whose draft length, emission cap and tokens are
+// already in shared memory (called by all threads).
+__device__ __forceinline__ Prologue check_request(const ChainParams &P, int L, int cap, const int *sTok) {
+  __shared__ int s_bad;
+  const int tid = threadIdx.x;
+  if (tid == 0) s_bad = (L >= 0 && L <= P.k) ? SPEC_STATUS_OK : SPEC_STATUS_BAD_LENGTH;
+  __syncthreads();
+  if (s_bad == SPEC_STATUS_OK && tid < L && (sTok[tid] < 0 || sTok[tid] >= P.V))
+    atomicMax(&s_bad, SPEC_STATUS_TOKEN_RANGE);
+  __syncthreads();
+  Prologue pr{L, s_bad, cap};
+  __syncthreads();
+  return pr;
+}
+
 __device__ __forceinline__ Prologue read_request(const ChainParams &P, int b, int *sTok, float *sU, bool sample) {
-  __shared__ int s_bad, s_L;
+  __shared__ int s_L, s_cap;
   const int tid = threadIdx.x, k = P.k;
-  __shared__ int s_cap;
-  if (tid == 0) {
-    const int L = P.draft_len ? P.draft_len[b] : k;
-    s_L = L;
-    s_bad = (L >= 0 && L <= k) ? SPEC_STATUS_OK : SPEC_STATUS_BAD_LENGTH;
-  }
+  if (tid == 0) s_L = P.draft_len ? P.draft_len[b] : k;
   if (tid == 32) s_cap = P.max_emit ? P.max_emit[b] : k + 1;
   if (tid < k) sTok[tid] = P.draft[static_cast<int64_t>(b) * k + tid];
   if (sample && tid >= 64 && tid <= 64 + k) sU[tid - 64] = P.uniforms[static_cast<int64_t>(b) * (k + 1) + tid - 64];
   __syncthreads();
-  const int L = s_L;
-  if (s_bad == SPEC_STATUS_OK && tid < L && (sTok[tid] < 0 || sTok[tid] >= P.V))
-    atomicMax(&s_bad, SPEC_STATUS_TOKEN_RANGE);
-  __syncthreads();
-  Prologue pr{L, s_bad, s_cap};
-  __syncthreads();
-  return pr;
+  return check_request(P, s_L, s_cap, sTok);
 }
 
 // The outputs that do not depend on the final draw (written once per request).

@@ -54,9 +54,10 @@ struct __align__(16) RowPart {
 };
 
 // This lane's sum of the draw weights W over its groups (lane_group split of
-// [lo, hi), G rounds; logits >= hi weigh 0).
+// [lo, hi), G rounds; logits >= hi weigh 0).  Each group's own sum goes to
+// gsum[g].
 template <int DT, bool VEC>
-__device__ __forceinline__ float lane_weight_sum(const Weights &W, int lo, int hi, int G) {
+__device__ __forceinline__ float lane_weight_sum(const Weights &W, int lo, int hi, int G, float *gsum) {
   constexpr int EPG = Elems<DT>::kPerGroup;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float acc = 0.0f;
@@ -76,8 +77,11 @@ __device__ __forceinline__ float lane_weight_sum(const Weights &W, int lo, int h
         float x[EPG], y[EPG];
         unpack16<DT>(xa[u], x);
         if (W.b) unpack16<DT>(xb[u], y);
+        float gs = 0.0f;
 #pragma unroll
-        for (int e = 0; e < EPG; ++e) acc += weight_at<DT>(W, x[e], W.b ? y[e] : 0.0f);
+        for (int e = 0; e < EPG; ++e) gs += weight_at<DT>(W, x[e], W.b ? y[e] : 0.0f);
+        gsum[g0 + 32 * u] = gs;
+        acc += gs;
       }
     }
   }
@@ -104,18 +108,57 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rows_max = SAMPLE ? 2 * k + 1 : k + 1;
   extern __shared__ RowPart dyn_parts[];
-  RowPart *s_wpart = dyn_parts;                           // [warp][row] warp statistics
-  RowPart *s_cpart = dyn_parts + kFusedWarps * rows_max;  // [rank][row] slice statistics
+  RowPart *s_wpart = dyn_parts;                           // [warp][row] warp statistics (streamed here)
+  RowPart *s_cpart = s_wpart + kFusedWarps * rows_max;    // [rank][row] slice statistics (streamed here)
+  float *s_gsum = reinterpret_cast<float *>(ACCEPT ? dyn_parts : s_cpart + kFusedMaxCluster * rows_max);
+  // s_gsum: [threads * groups] weight sum of each 16-byte group of the slice (sampling)
   __shared__ int sTok[SPEC_MAX_K], sOk[SPEC_MAX_K], sA[kFusedMaxRows];
   __shared__ float sU[SPEC_MAX_K + 1], sP[SPEC_MAX_K], sQ[SPEC_MAX_K];
   __shared__ float sM[kFusedMaxRows], sS[kFusedMaxRows], sX[kFusedMaxRows];
   __shared__ float s_red[kFusedWarps], s_z[2][kFusedMaxCluster];
   const RowPart kEmpty{-INFINITY, 0.0f, kNoIndex, 0.0f};
 
-  if (!ACCEPT) pdl_wait();  // the inputs may be the previous kernel's outputs
-  pdl_launch_dependents();
-  const Prologue pr = read_request(P, b, sTok, sU, SAMPLE);
-  if (ACCEPT) pdl_wait();  // the streaming pass's partials
+  const float c = P.c;
+  Prologue pr;
+  if (ACCEPT) {
+    // the request's inputs and every row's partials, loaded in one round trip:
+    // warp w merges rows w, w + 16, ... of the streaming pass's layout (target
+    // rows 0..k, draft rows k + 1..2k; rows the pass skipped are merged too and
+    // ignored); the drafted token's logit is the largest x over the chunks
+    // (the one chunk holding the token has it, the others -inf)
+    pdl_launch_dependents();
+    pdl_wait();  // the streaming pass's partials
+    __shared__ int s_L, s_cap;
+    if (tid == 0) s_L = P.draft_len ? P.draft_len[b] : k;
+    if (tid == 32) s_cap = P.max_emit ? P.max_emit[b] : k + 1;
+    if (tid < k) sTok[tid] = P.draft[static_cast<int64_t>(b) * k + tid];
+    if (tid >= 64 && tid <= 64 + k) sU[tid - 64] = P.uniforms[static_cast<int64_t>(b) * (k + 1) + tid - 64];
+    const int nc = P.nc;
+    const Partial *base = P.part + static_cast<int64_t>(b) * (2 * k + 1) * nc;
+    for (int r = warp; r < 2 * k + 1; r += kFusedWarps) {
+      const Partial *rp = base + static_cast<int64_t>(r) * nc;
+      float m = -INFINITY, s = 0.0f, x = -INFINITY;
+      int unused = kNoIndex;
+      for (int j = lane; j < nc; j += 32) {
+        const float4 q = ld_part(rp + j);
+        merge_stats(m, s, unused, q.x, q.y, kNoIndex, c);
+        x = fmaxf(x, q.w);
+      }
+      warp_allmerge<false>(m, s, unused, c);
+      x = warp_allmax(x);
+      if (lane == 0) {
+        sM[r] = m;
+        sS[r] = s;
+        sX[r] = x;
+      }
+    }
+    __syncthreads();
+    pr = check_request(P, s_L, s_cap, sTok);
+  } else {
+    pdl_wait();  // the inputs may be the previous kernel's outputs
+    pdl_launch_dependents();
+    pr = read_request(P, b, sTok, sU, SAMPLE);
+  }
   if (pr.bad) {  // every CTA of the cluster leaves here; no shared memory was exchanged
     if (rank == 0) write_common<SAMPLE>(P, b, pr.bad, pr.L, 0, 0, sTok, sP, sQ, true, -1);
     return;
@@ -126,33 +169,9 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
     return rr <= L ? row_ptr<DT>(P.target, P.t_req, P.row, b, rr)
                    : row_ptr<DT>(P.draftl, P.d_req, P.row, b, rr - L - 1);
   };
-  const float c = P.c;
   const int lo = min(P.V, rank * P.slice), hi = min(P.V, lo + P.slice);
   const int G = P.groups;  // rounds of 16-byte groups per lane
-  if (ACCEPT) {
-    // ---- 1-2. merge the streaming pass's partials of each row (warp w: rows w, w + 16, ...)
-    const int nc = P.nc;
-    const Partial *base = P.part + static_cast<int64_t>(b) * (2 * k + 1) * nc;
-    for (int rr = warp; rr < nrows; rr += kFusedWarps) {
-      const int r = rr <= L ? rr : (k + 1) + (rr - L - 1);  // the streaming pass's row numbering
-      const Partial *rp = base + static_cast<int64_t>(r) * nc;
-      float m = -INFINITY, s = 0.0f;
-      int unused = kNoIndex;
-      for (int j = lane; j < nc; j += 32) {
-        const float4 q = ld_part(rp + j);
-        merge_stats(m, s, unused, q.x, q.y, kNoIndex, c);
-      }
-      warp_allmerge<false>(m, s, unused, c);
-      const int pos = rr <= L ? rr : rr - L - 1;
-      const float x = pos < L ? ld_part(rp + sTok[pos] / P.chunk).w : -INFINITY;  // the drafted token's logit
-      if (lane == 0) {
-        sM[rr] = m;
-        sS[rr] = s;
-        sX[rr] = x;
-      }
-    }
-    __syncthreads();
-  } else {
+  if (!ACCEPT) {
     // the drafted tokens' logits (thread rr reads row rr's), in flight with the stream
     float xtok = -INFINITY;
     if (SAMPLE && tid < nrows) {
@@ -205,10 +224,13 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
     }
     __syncthreads();
   }
+  // the statistics of draft row i: after the target rows 0..L here, after
+  // rows 0..k in the streaming pass's layout
+  auto drow = [&](int i) { return (ACCEPT ? k : L) + 1 + i; };
   if (tid < L) {
     if (SAMPLE) {
       const float p = ex2((sX[tid] - sM[tid]) * c) / sS[tid];
-      const float q = ex2((sX[L + 1 + tid] - sM[L + 1 + tid]) * c) / sS[L + 1 + tid];
+      const float q = ex2((sX[drow(tid)] - sM[drow(tid)]) * c) / sS[drow(tid)];
       sP[tid] = p;
       sQ[tid] = q;
       sOk[tid] = sU[tid] * q < p;
@@ -230,12 +252,12 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
   if (!SAMPLE) return;
 
   // ---- 3. the final draw: residual after a rejection, p_L after a full accept
-  Weights W = m < L ? Weights{row_of(m), row_of(L + 1 + m), sM[m], sM[L + 1 + m], 1.0f / sS[m],
-                              1.0f / sS[L + 1 + m], c}
+  Weights W = m < L ? Weights{row_of(m), row_of(L + 1 + m), sM[m], sM[drow(m)], 1.0f / sS[m],
+                              1.0f / sS[drow(m)], c}
                     : Weights{row_of(L), nullptr, sM[L], 0.0f, 1.0f / sS[L], 0.0f, c};
   float wmass = 0.0f, rmass = 0.0f, total = 0.0f;
   for (int attempt = 0; attempt < 2; ++attempt) {
-    wmass = warp_sum(lane_weight_sum<DT, VEC>(W, lo, hi, G));  // this warp's range
+    wmass = warp_sum(lane_weight_sum<DT, VEC>(W, lo, hi, G, s_gsum));  // this warp's range
     const float ws = wmass;
     if (lane == 0) s_red[warp] = ws;
     __syncthreads();
@@ -270,7 +292,7 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
   }
   if (rank != draw_rank) return;  // no CTA touches another's shared memory from here on
   // (the fallback `lo` is unreachable: the drawing rank has mass, so one of its warps has)
-  const int tok = range_draw<kFusedThreads, EPG>(wmass, tl, lo, G, lo, [&](int g, float *w) {
+  const int tok = range_draw<kFusedThreads, EPG>(wmass, tl, lo, G, lo, s_gsum, [&](int g, float *w) {
     float x[EPG], y[EPG];
     unpack16<DT>(load_group<DT, VEC>(W.a, lo + g * EPG, hi), x);
     if (W.b) unpack16<DT>(load_group<DT, VEC>(W.b, lo + g * EPG, hi), y);
@@ -287,10 +309,18 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
 
 constexpr int kAcceptMaxSlice = 16384;  // largest slice per CTA of the cluster accept kernel
 
-size_t chain_fused_smem(int k, bool sample, int cluster, bool accept) {
-  if (accept) return 0;  // the warp and slice statistics live in shared memory only when streamed here
+// Dynamic shared memory: the warp and slice statistics of every row (only
+// when streamed here), then the draw's group sums (sampling).
+size_t chain_fused_smem(int k, bool sample, bool accept, int groups) {
   const int rows = sample ? 2 * k + 1 : k + 1;
-  return sizeof(RowPart) * static_cast<size_t>(kFusedWarps + cluster) * rows;
+  const size_t parts = accept ? 0 : sizeof(RowPart) * static_cast<size_t>(kFusedWarps + kFusedMaxCluster) * rows;
+  return parts + (sample ? sizeof(float) * static_cast<size_t>(kFusedThreads) * groups : 0);
+}
+
+static int lane_groups(int V, int dtype, int cluster) {
+  const int slice = ((V + cluster - 1) / cluster + 7) / 8 * 8;
+  const int epg = dtype == SPEC_DTYPE_F32 ? 4 : 8;
+  return ((slice + epg - 1) / epg + kFusedThreads - 1) / kFusedThreads;
 }
 
 template <int DT, bool VEC, bool SAMPLE, bool ACCEPT>
@@ -344,9 +374,9 @@ static cudaError_t dispatch(int dtype, bool vec, bool sample, bool accept, F &&f
 
 // How many clusters of `cluster` CTAs of the kernel fit on the device at
 // once (cached per device and shape).
-static int resident_clusters(int dtype, bool vec, bool sample, bool accept, int k, int cluster) {
+static int resident_clusters(int dtype, bool vec, bool sample, bool accept, int k, int V, int cluster) {
   struct Key {
-    int dev, dtype, vec, sample, accept, k, cluster, n;
+    int dev, dtype, vec, sample, accept, k, V, cluster, n;
   };
   static std::mutex mu;
   static std::vector<Key> cache;
@@ -356,10 +386,10 @@ static int resident_clusters(int dtype, bool vec, bool sample, bool accept, int 
     std::lock_guard<std::mutex> g(mu);
     for (const Key &q : cache)
       if (q.dev == dev && q.dtype == dtype && q.vec == vec && q.sample == sample && q.accept == accept &&
-          q.k == k && q.cluster == cluster)
+          q.k == k && q.V == V && q.cluster == cluster)
         return q.n;
   }
-  const size_t smem = chain_fused_smem(k, sample, cluster, accept);
+  const size_t smem = chain_fused_smem(k, sample, accept, lane_groups(V, dtype, cluster));
   int n = 0;
   dispatch(dtype, vec, sample, accept, [&]<int DT, bool VEC, bool SAMPLE, bool ACCEPT>() {
     cudaError_t e = prepare<DT, VEC, SAMPLE, ACCEPT>(cluster, smem);
@@ -374,7 +404,7 @@ static int resident_clusters(int dtype, bool vec, bool sample, bool accept, int 
   });
   cudaGetLastError();  // a refused query leaves no error behind
   std::lock_guard<std::mutex> g(mu);
-  cache.push_back(Key{dev, dtype, vec, sample, accept, k, cluster, n});
+  cache.push_back(Key{dev, dtype, vec, sample, accept, k, V, cluster, n});
   return n;
 }
 
@@ -386,12 +416,11 @@ static bool plan(ChainParams &P, bool sample, bool vec, bool accept) {
   cs = cs < 1 ? 1 : (cs > kFusedMaxCluster ? kFusedMaxCluster : cs);
   const int cs_min = accept ? (P.V + kAcceptMaxSlice - 1) / kAcceptMaxSlice : 1;
   for (; cs >= cs_min; --cs)
-    if (resident_clusters(P.dtype, vec, sample, accept, P.k, cs) >= P.B) break;
+    if (resident_clusters(P.dtype, vec, sample, accept, P.k, P.V, cs) >= P.B) break;
   if (cs < cs_min || cs < 1) return false;
   P.cluster = cs;
   P.slice = ((P.V + cs - 1) / cs + 7) / 8 * 8;
-  const int epg = P.dtype == SPEC_DTYPE_F32 ? 4 : 8;
-  P.groups = ((P.slice + epg - 1) / epg + kFusedThreads - 1) / kFusedThreads;
+  P.groups = lane_groups(P.V, P.dtype, cs);
   return true;
 }
 
@@ -399,7 +428,7 @@ bool chain_fused_plan(ChainParams &P, bool sample, bool vec) { return plan(P, sa
 bool chain_accept_plan(ChainParams &P, bool vec) { return plan(P, true, vec, true); }
 
 static cudaError_t launch(const ChainParams &P, bool sample, bool vec, bool accept, cudaStream_t st) {
-  const size_t smem = chain_fused_smem(P.k, sample, P.cluster, accept);
+  const size_t smem = chain_fused_smem(P.k, sample, accept, P.groups);
   return dispatch(P.dtype, vec, sample, accept, [&]<int DT, bool VEC, bool SAMPLE, bool ACCEPT>() {
     cudaError_t e = prepare<DT, VEC, SAMPLE, ACCEPT>(P.cluster, smem);
     if (e != cudaSuccess) return e;

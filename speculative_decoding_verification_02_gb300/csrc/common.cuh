@@ -346,8 +346,9 @@ __device__ __forceinline__ float group_logit(const uint4 &g, unsigned off) {
 
 // Folds one batch into the running (m, two-lane sum, idx), and picks up the
 // logit at index `tok` (-1: none) into xt.  The batch's groups start at
-// logits first_elem + u * NT * EPG, u < kBatch.
-template <int DT, bool SOFTMAX, int NT = kThreads>
+// logits first_elem + u * NT * EPG, u < kBatch.  IDX = false leaves idx
+// alone (no first-index search when the batch raises the max).
+template <int DT, bool SOFTMAX, int NT = kThreads, bool IDX = true>
 __device__ __forceinline__ void fold_batch(const uint4 *g, int first_elem, float c, float &m, float2 &s2,
                                            int &idx, int tok, float &xt) {
   constexpr int EPG = Elems<DT>::kPerGroup;
@@ -369,16 +370,18 @@ __device__ __forceinline__ void fold_batch(const uint4 *g, int first_elem, float
       s2.y *= f;
     }
     m = bm;
-    int first = kNoIndex;
+    if (IDX) {
+      int first = kNoIndex;
 #pragma unroll
-    for (int u = kBatch - 1; u >= 0; --u) {
-      float x[EPG];
-      unpack16<DT>(g[u], x);
+      for (int u = kBatch - 1; u >= 0; --u) {
+        float x[EPG];
+        unpack16<DT>(g[u], x);
 #pragma unroll
-      for (int e = EPG - 1; e >= 0; --e)
-        if (x[e] == bm) first = first_elem + u * kSpan + e;
+        for (int e = EPG - 1; e >= 0; --e)
+          if (x[e] == bm) first = first_elem + u * kSpan + e;
+      }
+      idx = first;
     }
-    idx = first;
   }
   if (SOFTMAX && m != -INFINITY) batch_sumexp<DT>(g, c, m * c, s2);
 }
@@ -389,7 +392,7 @@ __device__ __forceinline__ void fold_batch(const uint4 *g, int first_elem, float
 // none).  Full batches are loaded without predicates at fixed offsets from a
 // pointer that advances by one batch stride; two batches are in flight
 // (ping-pong), the last, partial batch is loaded with bounds checks.
-template <int DT, bool SOFTMAX, bool VEC, int LD, int NT = kThreads>
+template <int DT, bool SOFTMAX, bool VEC, int LD, int NT = kThreads, bool IDX = true>
 __device__ __forceinline__ void thread_chunk_stats(const char *row, int v0, int v1, float c,
                                                    float &m, float &s, int &idx, int tok, float &xt) {
   constexpr int EPG = Elems<DT>::kPerGroup;
@@ -414,15 +417,15 @@ __device__ __forceinline__ void thread_chunk_stats(const char *row, int v0, int 
     if (nfull > 0) load_batch(ga, p);
     for (; i + 2 <= nfull; i += 2) {
       load_batch(gb, p + kStride);
-      fold_batch<DT, SOFTMAX, NT>(ga, e0, c, m, s2, idx, tok, xt);
+      fold_batch<DT, SOFTMAX, NT, IDX>(ga, e0, c, m, s2, idx, tok, xt);
       e0 += kStride * EPG;
       if (i + 2 < nfull) load_batch(ga, p + 2 * kStride);
-      fold_batch<DT, SOFTMAX, NT>(gb, e0, c, m, s2, idx, tok, xt);
+      fold_batch<DT, SOFTMAX, NT, IDX>(gb, e0, c, m, s2, idx, tok, xt);
       e0 += kStride * EPG;
       p += 2 * kStride;
     }
     if (i < nfull) {  // an odd full batch is already in ga
-      fold_batch<DT, SOFTMAX, NT>(ga, e0, c, m, s2, idx, tok, xt);
+      fold_batch<DT, SOFTMAX, NT, IDX>(ga, e0, c, m, s2, idx, tok, xt);
       e0 += kStride * EPG;
       p += kStride;
       ++i;
@@ -432,7 +435,7 @@ __device__ __forceinline__ void thread_chunk_stats(const char *row, int v0, int 
 #pragma unroll
       for (int u = 0; u < kBatch; ++u)
         ga[u] = u < rest ? load16<LD>(p + u * NT) : make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
-      fold_batch<DT, SOFTMAX, NT>(ga, e0, c, m, s2, idx, tok, xt);
+      fold_batch<DT, SOFTMAX, NT, IDX>(ga, e0, c, m, s2, idx, tok, xt);
     }
     vtail = v0 + ng * EPG;
   }
@@ -443,7 +446,7 @@ __device__ __forceinline__ void thread_chunk_stats(const char *row, int v0, int 
     if (x > m) {
       if (SOFTMAX) s *= ex2((m - x) * c);
       m = x;
-      idx = v;
+      if (IDX) idx = v;
     }
     if (SOFTMAX && m != -INFINITY) s += ex2((x - m) * c);
   }

@@ -45,6 +45,36 @@ __device__ __forceinline__ void warp_allargmax(float &m, int &i) {
   m = M;
 }
 
+// Block-wide merge of every thread's (m, s, i) and of the max xt; the
+// result is valid in warp 0.  SOFTMAX: (max, sum rescaled to it, first
+// index of the max when IDX); otherwise (max, first index).
+template <bool SOFTMAX, bool IDX, int NT>
+__device__ __forceinline__ void block_allmerge(float &m, float &s, int &i, float c, float &xt) {
+  constexpr int NW = NT / 32;
+  __shared__ float sm[NW], ss[NW], sx[NW];
+  __shared__ int si[NW];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (SOFTMAX) warp_allmerge<IDX>(m, s, i, c);
+  else warp_allargmax(m, i);
+  xt = warp_allmax(xt);
+  if (lane == 0) {
+    sm[warp] = m;
+    ss[warp] = s;
+    si[warp] = i;
+    sx[warp] = xt;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    m = lane < NW ? sm[lane] : -INFINITY;
+    s = lane < NW ? ss[lane] : 0.0f;
+    i = lane < NW ? si[lane] : kNoIndex;
+    xt = lane < NW ? sx[lane] : -INFINITY;
+    if (SOFTMAX) warp_allmerge<IDX>(m, s, i, c);
+    else warp_allargmax(m, i);
+    xt = warp_allmax(xt);
+  }
+}
+
 // ------------------------------------------------------ per-lane work
 
 // Running statistics of one row over a lane's groups.
@@ -228,15 +258,19 @@ __device__ __forceinline__ void lane_rows_stats(const char *const *rows, int lo,
 // (the lane_group split).  `wmass` is the calling warp's sum of weights
 // (the same in all its lanes); the drawn logit is the first whose running
 // sum over the slice passes tl (tl = INFINITY: the last positive weight).
-// A scan of the warp masses finds the warp whose range holds the crossing;
-// that warp walks its range 32 groups at a time (a lane scan, then one lane
-// scans its group).  group_weights(g, w) writes the EPG weights of group g
-// (0 for logits >= hi).  Rounding between the scans falls back to the last
+// A scan of the warp masses finds the warp whose range holds the crossing.
+// With gsum (gsum[g] = the weight sum of group g, in the same summation
+// order as group_weights), that warp finds the group by one lane scan over
+// its range's group sums (lane l taking G consecutive groups of the range)
+// and reads only that group; without, it walks its range 32 groups at a
+// time.  group_weights(g, w) writes the EPG weights of group g (0 for
+// logits >= hi).  Rounding between the scans falls back to the last
 // positive weight of the last warp with mass; `fallback` is returned when
 // no warp has any.  Called by all NT threads; returns the token in every
 // thread.
 template <int NT, int EPG, class GroupWeights>
-__device__ int range_draw(float wmass, float tl, int lo, int G, int fallback, GroupWeights &&group_weights) {
+__device__ int range_draw(float wmass, float tl, int lo, int G, int fallback, const float *gsum,
+                          GroupWeights &&group_weights) {
   constexpr int NW = NT / 32;
   __shared__ float s_wsum[NW];
   __shared__ int s_tok;
@@ -257,46 +291,97 @@ __device__ int range_draw(float wmass, float tl, int lo, int G, int fallback, Gr
     wsel = 31 - __clz(pos_w);
   }
   if (warp == wsel) {
-    float run = 0.0f;
     int pick = -1, lastp = -1;
-    for (int j = 0; j < G; ++j) {
-      const int g = lane_group(wsel, j, G, lane);
+    // the crossing within group g, given the running sum `run` before it
+    auto scan_group = [&](int g, float run, bool cross) {
       float w[EPG];
       group_weights(g, w);
-      float lm = 0.0f;
-      int le = -1;  // this lane's last positive weight
+      int pe = -1, le = -1;
 #pragma unroll
       for (int e = 0; e < EPG; ++e) {
-        lm += w[e];
-        if (w[e] > 0.0f) le = e;
+        run += w[e];
+        if (w[e] > 0.0f) {
+          le = e;
+          if (cross && pe < 0 && run > thr_local) pe = e;
+        }
       }
-      const float incl = warp_inclusive_scan(lm, lane);
+      if (pe < 0) pe = le;  // rounding inside the group: its last positive weight
+      return pe < 0 ? -1 : g * EPG + pe;
+    };
+    if (gsum != nullptr) {
+      const int g0 = wsel * 32 * G;  // the range's first group
+      float ls = 0.0f;
+      for (int t = 0; t < G; ++t) ls += gsum[g0 + lane * G + t];
+      const float incl = warp_inclusive_scan(ls, lane);
       float excl = __shfl_up_sync(0xffffffffu, incl, 1);
       if (lane == 0) excl = 0.0f;
-      const unsigned hit = __ballot_sync(0xffffffffu, lm > 0.0f && run + incl > thr_local);
-      const unsigned pos = __ballot_sync(0xffffffffu, lm > 0.0f);
-      if (pos) {
-        const int hl = 31 - __clz(pos);
-        lastp = (g - lane + hl) * EPG + __shfl_sync(0xffffffffu, le, hl);
+      const unsigned hit = __ballot_sync(0xffffffffu, ls > 0.0f && incl > thr_local);
+      const unsigned pos = __ballot_sync(0xffffffffu, ls > 0.0f);
+      const int lh = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+      if (lh >= 0 && lane == lh) {  // this lane's G groups hold the crossing (or the last mass)
+        float run = excl;
+        int gsel = -1, glast = -1;
+        float base = excl, blast = excl;
+        for (int t = 0; t < G; ++t) {
+          const float gs = gsum[g0 + lane * G + t];
+          if (gs > 0.0f) {
+            glast = g0 + lane * G + t;
+            blast = run;
+            if (hit && gsel < 0 && run + gs > thr_local) {
+              gsel = glast;
+              base = run;
+            }
+          }
+          run += gs;
+        }
+        if (gsel < 0) {
+          gsel = glast;
+          base = blast;
+        }
+        pick = scan_group(gsel, base, hit != 0u);
       }
-      if (hit) {
-        const int lh = __ffs(hit) - 1;
-        int pe = le;  // rounding inside the lane: its last positive weight
-        float r = run + excl;
+      if (lh >= 0) pick = __shfl_sync(0xffffffffu, pick, lh);
+    } else {
+      float run = 0.0f;
+      for (int j = 0; j < G; ++j) {
+        const int g = lane_group(wsel, j, G, lane);
+        float w[EPG];
+        group_weights(g, w);
+        float lm = 0.0f;
+        int le = -1;  // this lane's last positive weight
 #pragma unroll
         for (int e = 0; e < EPG; ++e) {
-          r += w[e];
-          if (w[e] > 0.0f && r > thr_local) {
-            pe = e;
-            break;
-          }
+          lm += w[e];
+          if (w[e] > 0.0f) le = e;
         }
-        pick = (g - lane + lh) * EPG + __shfl_sync(0xffffffffu, pe, lh);
-        break;
+        const float incl = warp_inclusive_scan(lm, lane);
+        float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+        if (lane == 0) excl = 0.0f;
+        const unsigned hit = __ballot_sync(0xffffffffu, lm > 0.0f && run + incl > thr_local);
+        const unsigned pos = __ballot_sync(0xffffffffu, lm > 0.0f);
+        if (pos) {
+          const int hl = 31 - __clz(pos);
+          lastp = (g - lane + hl) * EPG + __shfl_sync(0xffffffffu, le, hl);
+        }
+        if (hit) {
+          const int lh = __ffs(hit) - 1;
+          int pe = le;  // rounding inside the lane: its last positive weight
+          float r = run + excl;
+#pragma unroll
+          for (int e = 0; e < EPG; ++e) {
+            r += w[e];
+            if (w[e] > 0.0f && r > thr_local) {
+              pe = e;
+              break;
+            }
+          }
+          pick = (g - lane + lh) * EPG + __shfl_sync(0xffffffffu, pe, lh);
+          break;
+        }
+        run += __shfl_sync(0xffffffffu, incl, 31);
       }
-      run += __shfl_sync(0xffffffffu, incl, 31);
+      if (pick < 0) pick = lastp;
     }
-    if (pick < 0) pick = lastp;
     if (lane == 0) s_tok = pick >= 0 ? lo + pick : fallback;
   } else if (wsel < 0 && threadIdx.x == 0) {
     s_tok = fallback;  // no positive weight in the slice (underflow only)

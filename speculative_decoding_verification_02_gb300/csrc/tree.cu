@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
       const float mass = w_mass >= 0.0f ? w_mass : (w_m == -INFINITY ? 0.0f : w_s * ex2((w_m - Mt) * c) * iSt);
       const float Mtc = Mt * c, Mdc = Md * c;
       // (the fallback `lo` is unreachable: the drawing rank has mass, so one of its warps has)
-      final_tok = range_draw<kTreeThreads, EPG>(mass, tl, lo, G, lo, [&](int g, float *w) {
+      final_tok = range_draw<kTreeThreads, EPG>(mass, tl, lo, G, lo, nullptr, [&](int g, float *w) {
         if (staged) {
 #pragma unroll
           for (int e = 0; e < EPG; ++e)
