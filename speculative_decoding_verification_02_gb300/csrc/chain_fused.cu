@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
 
 // ------------------------------------------------------------------- host
 
-constexpr int kAcceptMaxSlice = 16384;  // largest slice per CTA of the cluster accept kernel
+constexpr int kAcceptMaxSlice = 32768;  // largest slice per CTA of the cluster accept kernel
 
 // Dynamic shared memory: the warp and slice statistics of every row (only
 // when streamed here), then the draw's group sums (sampling).

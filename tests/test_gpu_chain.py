@@ -274,18 +274,53 @@ def test_workspace_reuse_and_graph_replay():
         check_chain_sample(prob, host(o), r)
 
 
-@pytest.mark.parametrize("seed,B,k,V,dtype,T", [(21, 160, 4, 3001, "bf16", 0.9), (22, 170, 3, 2500, "fp32", 1.0),
-                                               (23, 2, 4, 300_000, "bf16", 1.0), (24, 200, 6, 40_003, "bf16", 1.1)])
-def test_sample_parity_chunked_accept_path(seed, B, k, V, dtype, T):
-    """Shapes that take the chunked accept kernel (too many requests for one
-    wave of clusters, or V beyond a cluster's reach)."""
+@pytest.mark.parametrize("seed,B,k,V,dtype,T", [(21, 400, 4, 3001, "bf16", 0.9), (22, 420, 3, 2500, "fp32", 1.0),
+                                               (23, 2, 4, 600_000, "bf16", 1.0), (24, 200, 6, 40_003, "bf16", 1.1)])
+def test_sample_parity_chunked_accept_path(seed, B, k, V, dtype, T, chain_path):
+    """Shapes that take the chunked accept kernel: more requests than one
+    wave of cluster-accept CTAs (two 512-thread CTAs per SM on 152 SMs), or
+    V beyond 16 CTAs of 32,768 logits."""
     prob = workloads.chain_problem(seed, B, k, V, dtype, T, target_std=1.5,
                                    noise_std=np.linspace(0.3, 2.0, B).astype(np.float32))
     rng = np.random.default_rng(seed)
     draft_len = rng.integers(0, k + 1, B).astype(np.int32)
     max_emit = rng.integers(1, k + 2, B).astype(np.int32)
-    g = _run_sample(prob, draft_len, max_emit)
+    api.trace_enable(True)
+    api.trace_collect()
+    try:
+        g = _run_sample(prob, draft_len, max_emit)
+        launched = api.trace_collect()
+    finally:
+        api.trace_enable(False)
+    if chain_path == "two_pass":
+        assert "chain_sample_accept" in launched, launched
     r = _oracle_sample(prob, draft_len, max_emit)
     stats = check_chain_sample(prob, g, r, draft_len=draft_len)
     print("near-threshold", stats)
     assert (r["accepted"] < draft_len).any() and (r["accepted"] == draft_len).any()
+
+
+@pytest.mark.parametrize("seed,B,k,V,dtype,T", [(31, 160, 4, 3001, "bf16", 0.9), (32, 2, 4, 300_000, "bf16", 1.0),
+                                               (33, 24, 5, 40_003, "fp32", 1.2)])
+def test_sample_parity_cluster_accept_path(seed, B, k, V, dtype, T, chain_path):
+    """Shapes whose two-pass path ends in the cluster accept kernel (every
+    request's cluster resident at once, slices of at most 32,768 logits)."""
+    prob = workloads.chain_problem(seed, B, k, V, dtype, T, target_std=1.5,
+                                   noise_std=np.linspace(0.3, 2.0, B).astype(np.float32))
+    rng = np.random.default_rng(seed)
+    draft_len = rng.integers(0, k + 1, B).astype(np.int32)
+    max_emit = rng.integers(1, k + 2, B).astype(np.int32)
+    api.trace_enable(True)
+    api.trace_collect()
+    try:
+        g = _run_sample(prob, draft_len, max_emit)
+        launched = api.trace_collect()
+    finally:
+        api.trace_enable(False)
+    if chain_path == "two_pass":
+        assert "chain_sample_accept_cluster" in launched, launched
+    r = _oracle_sample(prob, draft_len, max_emit)
+    stats = check_chain_sample(prob, g, r, draft_len=draft_len)
+    print("near-threshold", stats)
+    if B >= 16:  # enough requests that some are rejected
+        assert (r["accepted"] < draft_len).any()
