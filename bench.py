@@ -49,9 +49,11 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 126 * 1024 * 1024
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 CSRC = "speculative_decoding_verification_02_gb300/csrc"
-KERNEL_SOURCES = {"chain": [f"{CSRC}/chain.cu", f"{CSRC}/common.cuh"],
-                  "tree": [f"{CSRC}/tree.cu", f"{CSRC}/common.cuh"],
-                  "ngram": [f"{CSRC}/ngram.cu", f"{CSRC}/chain.cu", f"{CSRC}/common.cuh"]}
+_CHAIN = [f"{CSRC}/chain.cu", f"{CSRC}/chain_fused.cu", f"{CSRC}/chain_common.cuh", f"{CSRC}/common.cuh",
+          f"{CSRC}/segments.cuh"]
+KERNEL_SOURCES = {"chain": _CHAIN,
+                  "tree": [f"{CSRC}/tree.cu", f"{CSRC}/common.cuh", f"{CSRC}/segments.cuh"],
+                  "ngram": [f"{CSRC}/ngram.cu"] + _CHAIN}
 
 
 # ----------------------------------------------------------------- helpers
