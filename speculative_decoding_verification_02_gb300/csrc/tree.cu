@@ -44,7 +44,6 @@ namespace sv {
 
 constexpr int kMaxCluster = 16;
 constexpr int kTreeWarps = kTreeThreads / 32;
-constexpr int kPrefetchKids = 2;  // children whose slices are fetched into L2 while the node is decided
 
 struct __align__(16) Slot {
   float mt, st, md, sd;  // slice statistics of the target and draft rows
@@ -57,13 +56,6 @@ template <int DT>
 __device__ __forceinline__ const char *node_row(const char *base, int64_t req, int64_t row, int b,
                                                 int u) {
   return base + (static_cast<int64_t>(b) * req + static_cast<int64_t>(u) * row) * Elems<DT>::kSize;
-}
-
-// Asks L2 to fetch [p, p + bytes) ahead of use (no completion to wait for).
-// p must be 16-byte aligned; bytes is rounded down to a multiple of 16.
-__device__ __forceinline__ void prefetch_l2(const char *p, int bytes) {
-  bytes &= ~15;
-  if (bytes > 0) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // Where p_v, q_v of element e of group g are staged: the slice's groups in
@@ -209,6 +201,8 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
     return warp_sum(part_of_lane);
   };
   // Children of `node` in increasing id order into s_kids; their number.
+  // (The walk uses this only when node's candidates need more than one
+  // sweep of the block; see the loop below.)
   auto children = [&](int node) {
     int nk = 0;
     for (int base = node + 1; base < N; base += kTreeThreads) {
@@ -230,38 +224,66 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
   int node = 0, nacc = 0, final_tok = -1, draw_rank = 0;
   if (tid == 0) s_path[0] = 0;
   for (;;) {
-    const int nkids = children(node);
+    // children of `node`, in increasing id order
+    int nkids, my_pos = -1, my_kid = -1;
+    const bool one_sweep = N - node - 1 <= kTreeThreads;
+    if (one_sweep) {
+      // thread t looks at node + 1 + t; a thread that finds a child keeps its
+      // slot and loads its token logits itself, and fills s_kids, s_kt, s_kd
+      // after the statistics pass (one barrier fewer than the general sweep)
+      const int cidx = node + 1 + tid;
+      const bool is_kid = cidx < N && s_par[cidx] == node;
+      const unsigned bal = __ballot_sync(0xffffffffu, is_kid);
+      if (lane == 0) s_cnt[warp] = __popc(bal);
+      __syncthreads();
+      const int cw = lane < kTreeWarps ? s_cnt[lane] : 0;
+      const int before = __reduce_add_sync(0xffffffffu, lane < warp ? cw : 0);
+      nkids = __reduce_add_sync(0xffffffffu, cw);
+      if (is_kid) {
+        my_pos = before + __popc(bal & ((1u << lane) - 1u));
+        my_kid = cidx;
+      }
+    } else {
+      nkids = children(node);
+    }
     const char *trow = node_row<DT>(P.target, P.t_req, P.row, b, node);
     const char *drow = (!GREEDY && nkids > 0) ? node_row<DT>(P.draftl, P.d_req, P.row, b, node) : nullptr;
-    // the walk is likely to continue at the first children: have L2 fetch
-    // this CTA's slice of their rows while the current node is worked on
-    if (VEC && tid < min(nkids, kPrefetchKids) && hi > lo) {
-      const int ch = s_kids[tid];
-      const int64_t off = static_cast<int64_t>(lo) * Elems<DT>::kSize;
-      const int bytes = (hi - lo) * Elems<DT>::kSize;
-      prefetch_l2(node_row<DT>(P.target, P.t_req, P.row, b, ch) + off, bytes);
-      if (!GREEDY) prefetch_l2(node_row<DT>(P.draftl, P.d_req, P.row, b, ch) + off, bytes);
-    }
     // the children's token logits: loaded now, stored after the statistics pass
     float kt0 = 0.0f, kd0 = 0.0f;
     if (drow) {
-      if (tid < nkids) {
-        const int x = s_tok[s_kids[tid]];
-        kt0 = load_one<DT>(trow, x);
-        kd0 = load_one<DT>(drow, x);
-      }
-      for (int i = tid + kTreeThreads; i < nkids; i += kTreeThreads) {
-        const int x = s_tok[s_kids[i]];
-        s_kt[i] = load_one<DT>(trow, x);
-        s_kd[i] = load_one<DT>(drow, x);
+      if (one_sweep) {
+        if (my_pos >= 0) {
+          const int x = s_tok[my_kid];
+          kt0 = load_one<DT>(trow, x);
+          kd0 = load_one<DT>(drow, x);
+        }
+      } else {
+        if (tid < nkids) {
+          const int x = s_tok[s_kids[tid]];
+          kt0 = load_one<DT>(trow, x);
+          kd0 = load_one<DT>(drow, x);
+        }
+        for (int i = tid + kTreeThreads; i < nkids; i += kTreeThreads) {
+          const int x = s_tok[s_kids[i]];
+          s_kt[i] = load_one<DT>(trow, x);
+          s_kd[i] = load_one<DT>(drow, x);
+        }
       }
     }
+    asm volatile("" ::: "memory");  // the logit loads go out before the pass's loads
 
     // ---- row statistics: lane pass, warp merge, block merge, exchange
     RowStats R[2] = {row_stats_empty(), row_stats_empty()};
     const char *rows[2] = {trow, drow};
     lane_rows_stats<DT, !GREEDY, VEC, 2>(rows, lo, hi, G, c, R);
-    if (drow && tid < nkids) {
+    asm volatile("" ::: "memory");  // and are stored only after it
+    if (one_sweep) {
+      if (my_pos >= 0) {
+        s_kids[my_pos] = my_kid;
+        s_kt[my_pos] = kt0;
+        s_kd[my_pos] = kd0;
+      }
+    } else if (drow && tid < nkids) {
       s_kt[tid] = kt0;
       s_kd[tid] = kd0;
     }
