@@ -63,6 +63,11 @@ __device__ __forceinline__ Partial ld_partial(const Partial *p) {
 
 template <int DT, bool SOFTMAX, bool VEC>
 __global__ void __launch_bounds__(kThreads) chain_stats_kernel(const ChainParams P) {
+  // Launched early behind the previous kernel in the stream: wait for it
+  // before reading, and only then let the accept kernel start (it reads the
+  // request's inputs, which that previous kernel may have written, before
+  // its own wait).
+  pdl_wait();
   pdl_launch_dependents();
   const int rows = SOFTMAX ? 2 * P.k + 1 : P.k + 1;
   const int per_req = rows * P.nc;
@@ -435,6 +440,8 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
 // griddepcontrol.wait before touching its results.
 template <class K>
 static cudaError_t launch_dependent(K kern, unsigned grid, cudaStream_t st, const ChainParams &P) {
+  // (every kernel of the library waits with griddepcontrol.wait before it
+  // reads anything the previous kernel in the stream may have written)
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -453,8 +460,8 @@ static cudaError_t launch_chain_t(const ChainParams &P, bool sample, cudaStream_
   const int rows = sample ? 2 * P.k + 1 : P.k + 1;
   const unsigned grid1 = static_cast<unsigned>(static_cast<long long>(P.B) * rows * P.nc);
   if (sample) {
-    cudaError_t e = trace_launch("chain_stats_sample", st, [&] {
-      chain_stats_kernel<DT, true, VEC><<<grid1, kThreads, 0, st>>>(P);
+    cudaError_t e = trace_launch_ex("chain_stats_sample", st, [&] {
+      return launch_dependent(chain_stats_kernel<DT, true, VEC>, grid1, st, P);
     });
     if (e != cudaSuccess) return e;
     if (P.cluster > 0) return launch_chain_accept_cluster(P, CVEC, st);
@@ -463,8 +470,8 @@ static cudaError_t launch_chain_t(const ChainParams &P, bool sample, cudaStream_
       return launch_dependent(chain_sample_accept_kernel<DT, VEC>, grid2, st, P);
     });
   }
-  cudaError_t e = trace_launch("chain_stats_greedy", st, [&] {
-    chain_stats_kernel<DT, false, VEC><<<grid1, kThreads, 0, st>>>(P);
+  cudaError_t e = trace_launch_ex("chain_stats_greedy", st, [&] {
+    return launch_dependent(chain_stats_kernel<DT, false, VEC>, grid1, st, P);
   });
   if (e != cudaSuccess) return e;
   return trace_launch_ex("chain_greedy_accept", st, [&] {

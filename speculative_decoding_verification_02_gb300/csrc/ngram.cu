@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(kNgramThreads) ngram_kernel(const NgramParams 
   __shared__ int s_key[SPEC_MAX_WINDOW];
   __shared__ int s_wbest[kNgramWarps];
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_launch_dependents();
+  pdl_wait();  // launched early behind the previous kernel in the stream: wait before reading
   const int n = P.hist_len[b], w = P.window, k = P.k;
   const int32_t *h = P.history + static_cast<int64_t>(b) * P.hist_stride;
   int32_t *d = P.draft + static_cast<int64_t>(b) * k;
@@ -79,7 +81,16 @@ __global__ void __launch_bounds__(kNgramThreads) ngram_kernel(const NgramParams 
 }
 
 cudaError_t launch_ngram(const NgramParams &P, cudaStream_t st) {
-  return trace_launch("ngram_draft", st, [&] { ngram_kernel<<<P.B, kNgramThreads, 0, st>>>(P); });
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(P.B));
+  cfg.blockDim = dim3(kNgramThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = trace_enabled() ? 0 : 1;
+  return trace_launch_ex("ngram_draft", st, [&] { return cudaLaunchKernelEx(&cfg, ngram_kernel, P); });
 }
 
 }  // namespace sv
