@@ -52,7 +52,9 @@ def test_ngram_exhaustive_small():
         _eq(_run(h, lens, w, k), oracle.ngram_draft(h, lens, w, k))
 
 
-@pytest.mark.parametrize("H,V,w,k", [(10000, 50, 3, 8), (5000, 3, 5, 4), (20000, 32000, 2, 6), (3, 5, 3, 4)])
+@pytest.mark.parametrize("H,V,w,k", [(10000, 50, 3, 8), (5000, 3, 5, 4), (20000, 32000, 2, 6), (3, 5, 3, 4),
+                                     (5003, 7, 4, 3),      # odd stride: 16-byte and 4-byte aligned rows mixed
+                                     (9000, 1000, 64, 8)])  # the longest window (a match is planted)
 def test_ngram_long_and_ragged(H, V, w, k):
     rng = np.random.default_rng(H + V)
     B = 24
