@@ -60,6 +60,7 @@ def _load():
                                           P, P, P, P, P, P, P, I, I, P]
         lib.orc_verify_tree.argtypes = [P, I64, P, I64, I64, I, I, I, I, D, P, P, P, I,
                                         P, P, P, P, P, I, I, P]
+        lib.orc_tree_rerank.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, P, P]
         lib.orc_max_threads.argtypes = []
         _lib = lib
         return lib
@@ -248,4 +249,29 @@ def verify_tree(target, draft_logits, parents, node_tok, uniforms, T: float, max
         _ptr(out["n_emit"]), _ptr(out["status"]), int(variant), int(threads), _ptr(degen)),
         "verify_tree")
     out["degenerate"] = int(degen[0])
+    return out
+
+
+def tree_rerank(parents, conf, m: int, max_depth: int = 64, node_tok=None, mask: bool = True):
+    """EAGLE-2 post-processing of candidate trees.  parents: [B, N] int32
+    (parents[0] = -1, parents[i] < i); conf: [B, N] fp32 draft confidences in
+    [0, 1] (conf[:, 0] unused); node_tok: [B, N] or None.  Returns the kept
+    nodes in flattened order with their flattened parents, depths, values,
+    tokens, the [B, m, m] attention mask, n_sel and status."""
+    parents = _i32(parents, None)
+    B, N = parents.shape
+    conf = np.ascontiguousarray(conf, dtype=np.float32)
+    if conf.shape != (B, N):
+        raise ValueError(f"conf must be {(B, N)}")
+    if node_tok is not None:
+        node_tok = _i32(node_tok, (B, N))
+    out = dict(sel_nodes=np.empty((B, m), np.int32), sel_parents=np.empty((B, m), np.int32),
+               sel_depth=np.empty((B, m), np.int32), sel_value=np.empty((B, m), np.float32),
+               sel_tok=np.empty((B, m), np.int32) if node_tok is not None else None,
+               mask=np.empty((B, m, m), np.uint8) if mask else None,
+               n_sel=np.empty(B, np.int32), status=np.empty(B, np.int32))
+    _check(_load().orc_tree_rerank(
+        _ptr(parents), _ptr(conf), _ptr(node_tok), B, N, int(m), int(max_depth), _ptr(out["sel_nodes"]),
+        _ptr(out["sel_parents"]), _ptr(out["sel_depth"]), _ptr(out["sel_value"]), _ptr(out["sel_tok"]),
+        _ptr(out["mask"]), _ptr(out["n_sel"]), _ptr(out["status"])), "tree_rerank")
     return out

@@ -31,6 +31,12 @@
  *   n-gram draft   take the last `window` tokens, find the same segment
  *                  earlier in the history, propose what followed it
  *                  ("第 13 篇", 逐行要点, the 草稿器.猜 line)
+ *   tree rerank    EAGLE-2's post-processing of a candidate tree: value =
+ *                  product of the draft confidences along the path, keep
+ *                  the m best (ties: shallower first), flatten by depth,
+ *                  each node attending to its ancestors ("Speculative
+ *                  Decoding II", section "Context-Aware Dynamic Draft Tree"
+ *                  and its worked example)
  *
  * Readings where the pages are silent (all listed in the design doc):
  *   - the uniform u_i tests draft position i; u_k (the last one) drives the
@@ -569,6 +575,131 @@ int orc_verify_tree(const void *target, int64_t t_req, const void *draft_logits,
     if (degenerate)
         *degenerate += degen;
     return fail ? ORC_ENOMEM : ORC_OK;
+}
+
+/* ----------------------------------------------------------- tree rerank */
+
+/* One candidate node: its value, depth and id. */
+typedef struct {
+    float v;
+    int depth, id;
+} rr_node;
+
+/* Rerank order: larger value first; equal values, the shallower node
+ * ("Speculative Decoding II", Context-Aware Dynamic Draft Tree: nodes of
+ * equal value are taken shallower first, so the kept nodes form a tree);
+ * equal value and depth, the lower id. */
+static int rr_rank_cmp(const void *pa, const void *pb)
+{
+    const rr_node *a = (const rr_node *)pa, *b = (const rr_node *)pb;
+    if (a->v != b->v)
+        return a->v > b->v ? -1 : 1;
+    if (a->depth != b->depth)
+        return a->depth < b->depth ? -1 : 1;
+    return a->id < b->id ? -1 : (a->id > b->id);
+}
+
+/* Flattened order: by depth, then id (the page's [I, do, make, it, this, a,
+ * now, plan] with relative positions [0, 1, 1, 2, 2, 2, 3, 3]). */
+static int rr_flat_cmp(const void *pa, const void *pb)
+{
+    const rr_node *a = (const rr_node *)pa, *b = (const rr_node *)pb;
+    if (a->depth != b->depth)
+        return a->depth < b->depth ? -1 : 1;
+    return a->id < b->id ? -1 : (a->id > b->id);
+}
+
+/*
+ * EAGLE-2 post-processing of a candidate draft tree ("Speculative Decoding
+ * II", section "Context-Aware Dynamic Draft Tree" and its worked example).
+ *   value    V(root) = 1, V(i) = V(parent(i)) * c_i: the product of the draft
+ *            confidences along the path, multiplied from the root down as the
+ *            page does (V = 0.60 x 0.80 = 0.48).  It is computed in binary32,
+ *            the library's precision, because it decides the ranking below
+ *            (an integer result) and both sides must decide alike;
+ *   rerank   keep the m nodes of largest V (rr_rank_cmp);
+ *   flatten  the kept nodes in rr_flat_cmp order; relative position = depth;
+ *            the mask row of a node marks itself and its ancestors.
+ * parents [B, N]: parents[0] = -1, 0 <= parents[i] < i; conf [B, N]: c_i in
+ * [0, 1] (conf[0] is not read); node_tok [B, N] or NULL.  Outputs, n_sel =
+ * min(m, N) entries per request then padding (-1; values -1; mask 0):
+ * sel_nodes, sel_parents (flattened index of the parent, -1 for the root),
+ * sel_depth, sel_value, sel_tok (when node_tok is given), mask [B, m, m]
+ * (NULL to skip), n_sel, status (ST_BAD_TREE for a malformed parent array, a
+ * depth beyond max_depth, or a confidence outside [0, 1]; such a request
+ * keeps nothing).
+ */
+int orc_tree_rerank(const int32_t *parents, const float *conf, const int32_t *node_tok, int B, int N,
+                    int m, int max_depth, int32_t *sel_nodes, int32_t *sel_parents, int32_t *sel_depth,
+                    float *sel_value, int32_t *sel_tok, uint8_t *mask, int32_t *n_sel, int32_t *status)
+{
+    if (B < 0 || N < 1 || m < 1 || max_depth < 0 || !parents || !conf || !sel_nodes || !sel_parents ||
+        !sel_depth || !n_sel || !status)
+        return ORC_EINVAL;
+    rr_node *nodes = (rr_node *)malloc(sizeof(rr_node) * (size_t)N);
+    int *depth = (int *)malloc(sizeof(int) * (size_t)N), *pos = (int *)malloc(sizeof(int) * (size_t)N);
+    float *val = (float *)malloc(sizeof(float) * (size_t)N);
+    if (!nodes || !depth || !pos || !val) {
+        free(nodes), free(depth), free(pos), free(val);
+        return ORC_ENOMEM;
+    }
+    for (int b = 0; b < B; ++b) {
+        const int32_t *par = parents + (int64_t)b * N;
+        const float *c = conf + (int64_t)b * N;
+        int32_t *o_node = sel_nodes + (int64_t)b * m, *o_par = sel_parents + (int64_t)b * m;
+        int32_t *o_dep = sel_depth + (int64_t)b * m;
+        for (int j = 0; j < m; ++j) {
+            o_node[j] = o_par[j] = o_dep[j] = -1;
+            if (sel_value) sel_value[(int64_t)b * m + j] = -1.0f;
+            if (sel_tok) sel_tok[(int64_t)b * m + j] = -1;
+        }
+        if (mask) memset(mask + (int64_t)b * m * m, 0, (size_t)m * (size_t)m);
+        n_sel[b] = 0;
+        /* the tree, its depths and values, from the root down (parents[i] < i) */
+        int bad = par[0] != -1;
+        depth[0] = 0;
+        val[0] = 1.0f;
+        for (int i = 1; i < N && !bad; ++i) {
+            if (par[i] < 0 || par[i] >= i || !(c[i] >= 0.0f && c[i] <= 1.0f)) {
+                bad = 1;
+                break;
+            }
+            depth[i] = depth[par[i]] + 1;
+            if (depth[i] > max_depth) bad = 1;
+            val[i] = val[par[i]] * c[i];
+        }
+        if (bad) {
+            status[b] = ST_BAD_TREE;
+            continue;
+        }
+        for (int i = 0; i < N; ++i) {
+            nodes[i].v = val[i];
+            nodes[i].depth = depth[i];
+            nodes[i].id = i;
+        }
+        qsort(nodes, (size_t)N, sizeof(rr_node), rr_rank_cmp);
+        const int n = m < N ? m : N;
+        qsort(nodes, (size_t)n, sizeof(rr_node), rr_flat_cmp);
+        for (int i = 0; i < N; ++i) pos[i] = -1;
+        for (int j = 0; j < n; ++j) pos[nodes[j].id] = j;
+        for (int j = 0; j < n; ++j) {
+            const int u = nodes[j].id;
+            o_node[j] = u;
+            o_par[j] = u == 0 ? -1 : pos[par[u]];
+            o_dep[j] = nodes[j].depth;
+            if (sel_value) sel_value[(int64_t)b * m + j] = nodes[j].v;
+            if (sel_tok) sel_tok[(int64_t)b * m + j] = node_tok ? node_tok[(int64_t)b * N + u] : -1;
+            if (mask) {
+                uint8_t *row = mask + ((int64_t)b * m + j) * m;
+                for (int a = u; a >= 0; a = a == 0 ? -1 : par[a])
+                    if (pos[a] >= 0) row[pos[a]] = 1;
+            }
+        }
+        n_sel[b] = n;
+        status[b] = ST_OK;
+    }
+    free(nodes), free(depth), free(pos), free(val);
+    return ORC_OK;
 }
 
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
