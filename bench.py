@@ -1,7 +1,8 @@
 """Benchmark of the verify-and-accept step on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload vocab248k|batch64|small|tree60|ngram]
+                    [--workload vocab248k|batch64|small|tree60|ngram|eagle2]
+                    [--chain-path auto|two_pass|fused]
 
 One step is one pass of the path over one batch:
   vocab248k  spec_verify_sample, B=1, k=4, V=248,320 bf16 (the default: the
@@ -12,6 +13,8 @@ One step is one pass of the path over one batch:
              (960 node rows per step)
   ngram      spec_ngram_draft on 64 histories of 4,096 tokens, then
              spec_verify_greedy of the drafts, V=32,000 fp32 (320 rows)
+  eagle2     spec_tree_rerank on 16 EAGLE-2-shaped candidate trees of 511
+             nodes, keeping 60 (value = candidate nodes per second)
 Inputs rotate over enough resident copies that one cycle reads more than
 twice the 126 MB L2, so no step finds its logits in L2; the calls are
 replayed from a CUDA graph.
@@ -53,7 +56,8 @@ _CHAIN = [f"{CSRC}/chain.cu", f"{CSRC}/chain_fused.cu", f"{CSRC}/chain_common.cu
           f"{CSRC}/segments.cuh"]
 KERNEL_SOURCES = {"chain": _CHAIN,
                   "tree": [f"{CSRC}/tree.cu", f"{CSRC}/common.cuh", f"{CSRC}/segments.cuh"],
-                  "ngram": [f"{CSRC}/ngram.cu"] + _CHAIN}
+                  "ngram": [f"{CSRC}/ngram.cu"] + _CHAIN,
+                  "rerank": [f"{CSRC}/rerank.cu", f"{CSRC}/common.cuh"]}
 
 
 # ----------------------------------------------------------------- helpers
@@ -318,6 +322,48 @@ class TreeWorkload:
         return reps * self.B * self.N
 
 
+class EagleWorkload:
+    """spec_tree_rerank on 16 EAGLE-2-shaped candidate trees of 511 nodes."""
+    kind = "rerank"
+    metric = "EAGLE-2 candidate-tree nodes post-processed per second (value, top-60 rerank, flatten, mask)"
+    unit = "nodes/s"
+
+    def __init__(self, name):
+        from speculative_decoding_verification_02_gb300 import workloads as W
+        self.prob = W.eagle2_candidates()
+        self.m = 60
+        p = self.prob
+        self.B, self.N = p["parents"].shape
+        self.desc = (f"EAGLE-2 tree post-processing, B={self.B} candidate trees of {self.N} nodes (depth 6, "
+                     f"10 nodes expanded per layer, 10 children each), keep m={self.m}, uint8 mask")
+        self.rows_per_step = self.B * self.N
+        self.set_bytes = self.B * self.N * 12
+        self.logits = "none"
+
+    def device_set(self, dev, i):
+        p = self.prob
+        return dict(P=to_dev(p["parents"], dev), C=to_dev(p["conf"], dev), X=to_dev(p["node_tok"], dev))
+
+    def call(self, s, out, stream):
+        from speculative_decoding_verification_02_gb300 import api
+        return api.spec_tree_rerank(s["P"], s["C"], self.m, node_tok=s["X"], out=out, stream=stream)
+
+    result_keys = ("sel_nodes", "sel_parents", "sel_depth", "sel_tok", "n_sel", "status")
+
+    def kernel_bytes(self, name, outs):
+        """Inputs (parents, confidences, tokens) and outputs (five int32/fp32
+        values per kept node, the m x m mask)."""
+        return self.B * (self.N * 12 + self.m * 20 + self.m * self.m)
+
+    def oracle_call(self, n, threads):
+        import oracle
+        p = self.prob
+        reps = max(1, -(-n // self.B))
+        for _ in range(reps):
+            oracle.tree_rerank(p["parents"], p["conf"], self.m, node_tok=p["node_tok"])
+        return reps * self.rows_per_step
+
+
 class NgramWorkload:
     """spec_ngram_draft, then spec_verify_greedy of its drafts."""
     kind = "ngram"
@@ -371,7 +417,7 @@ class NgramWorkload:
 
 
 WORKLOADS = {"vocab248k": ChainWorkload, "batch64": ChainWorkload, "small": ChainWorkload,
-             "tree60": TreeWorkload, "ngram": NgramWorkload}
+             "tree60": TreeWorkload, "ngram": NgramWorkload, "eagle2": EagleWorkload}
 
 
 def oracle_rate(wl, target_seconds: float):
@@ -416,14 +462,16 @@ def run_reference(args):
             break
     dt = time.perf_counter() - t0
     value = rows / dt
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
+    unit = getattr(wl, "unit", "rows/s")
+    line = {"impl": "reference", "metric": getattr(wl, "metric", METRIC), "value": value, "unit": unit,
+            "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / steps_done,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": wl.desc, "rows_per_step": wl.rows_per_step},
-            "cpu_baseline": {"kind": "oracle", "value": value, "unit": "rows/s", "cores": threads,
+            "cpu_baseline": {"kind": "oracle", "value": value, "unit": unit, "cores": threads,
                              "sample": f"{steps_done} of {args.steps} steps timed (cap {budget:.0f} s), "
                                        f"one batch of the workload each"},
-            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -573,19 +621,22 @@ def run_ours(args):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         rate, threads, nrows, dt = oracle_rate(wl, float(os.environ.get("SPEC_CPU_SECONDS", "10")))
-        cpu = {"value": rate, "unit": "rows/s", "cores": threads, "kind": "oracle",
+        cpu = {"value": rate, "unit": getattr(wl, "unit", "rows/s"), "cores": threads, "kind": "oracle",
                "sample": f"{nrows} rows of the workload's requests through the oracle ({dt:.1f} s, fp64, "
                          f"OpenMP over requests)"}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
+            "metric": getattr(wl, "metric", METRIC), "value": value, "unit": getattr(wl, "unit", "rows/s"),
+            "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": wl.desc, "rows_per_step": wl.rows_per_step, "logits": wl.logits,
                        "parallelism": f"replicas x{ws}",
-                       "l2": f"inputs rotate over {nsets} resident sets ({nsets * wl.set_bytes / 2**20:.0f} MiB, "
-                             f"more than twice the L2 between reuses)",
+                       "l2": (f"inputs rotate over {nsets} resident sets ({nsets * wl.set_bytes / 2**20:.0f} MiB, "
+                              f"more than twice the L2 between reuses)" if nsets * wl.set_bytes > 2 * L2_BYTES else
+                              f"inputs L2-resident ({nsets} sets, {nsets * wl.set_bytes / 2**20:.1f} MiB): a "
+                              f"latency-bound workload with little data"),
                        "launch": f"CUDA graph of {nsets} calls", "chain_path": args.chain_path},
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
@@ -594,7 +645,8 @@ def run_ours(args):
                          "algorithmic_bytes_per_launch": kernels[dom]["algorithmic_bytes_per_launch"],
                          "kernels": kernels},
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "e2e": {"value": e2e_value, "unit": getattr(wl, "unit", "rows/s"), "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h,
                     "steps": steps_e2e},
             "gpu_launches": int(launches_per_call * args.steps),
             "clocks": clocks,

@@ -238,6 +238,47 @@ int spec_verify_sample_noalloc(const void *target, int64_t target_req_stride,
                                float *resid_mass, int32_t *status, void *stream);
 
 /*
+ * spec_tree_rerank -- EAGLE-2 post-processing of candidate draft trees.
+ * ("Speculative Decoding II", section "Context-Aware Dynamic Draft Tree"
+ * and its worked example: a node's value is the product of the draft
+ * model's confidences along its path from the root; the m most valuable
+ * nodes are kept, equal values going to the shallower node, which keeps the
+ * kept nodes a tree rooted at the root; they are flattened for the target's
+ * forward, each node attending only to itself and its ancestors.)
+ *
+ *   parents      int32 [B, N]: parents[0] = -1, 0 <= parents[i] < i.
+ *   conf         fp32 [B, N]: c_i in [0, 1], the draft model's probability
+ *                of node i's token given its parent (conf[b][0] is not read;
+ *                the root's value is 1).
+ *   node_tok     int32 [B, N], or NULL when sel_tok is NULL.
+ *   N            in [1, SPEC_MAX_NODES]; m in [1, SPEC_MAX_NODES]: nodes to
+ *                keep (all N when m >= N).
+ *   max_depth    in [0, SPEC_MAX_DEPTH]: a deeper tree is malformed.
+ *   sel_nodes    out int32 [B, m]: the kept nodes' ids, flattened (by depth,
+ *                then id).
+ *   sel_parents  out int32 [B, m]: each kept node's parent as an index into
+ *                the flattened order, -1 for the root.
+ *   sel_depth    out int32 [B, m]: depths (the relative positions).
+ *   sel_value    out fp32 [B, m] or NULL: values, computed from the root down
+ *                in fp32 (V(i) = V(parent) * c_i).
+ *   sel_tok      out int32 [B, m] or NULL: node_tok in the flattened order.
+ *   mask         out uint8 [B, m, m] or NULL: mask[b][i][j] = 1 iff
+ *                flattened node j is node i or one of its ancestors.
+ *   n_sel        out int32 [B]: min(m, N), or 0 for a malformed tree.
+ *   status       out int32 [B] or NULL: SPEC_STATUS_BAD_TREE for a malformed
+ *                parent array, a depth beyond max_depth, or a confidence
+ *                outside [0, 1] (NaN included).
+ * Entries from n_sel on are -1 (values -1.0, mask rows and columns 0).
+ * Ties in value go to the shallower node, then to the lower id.  sel_parents
+ * and sel_tok describe a tree that spec_verify_tree accepts (node 0 the
+ * root, every parent before its child).  No workspace.
+ */
+int spec_tree_rerank(const int32_t *parents, const float *conf, const int32_t *node_tok, int B, int N,
+                     int m, int max_depth, int32_t *sel_nodes, int32_t *sel_parents, int32_t *sel_depth,
+                     float *sel_value, int32_t *sel_tok, uint8_t *mask, int32_t *n_sel, int32_t *status,
+                     void *stream);
+
+/*
  * spec_workspace_size -- bytes of workspace a call needs.
  *   op = SPEC_OP_*; rows_per_req = k for chains, N for trees.
  *   Returns 0 for invalid arguments and for ops that need none.

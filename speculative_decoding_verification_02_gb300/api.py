@@ -62,6 +62,7 @@ def lib():
         L.spec_launch_count.argtypes = []
         L.spec_launch_count.restype = ctypes.c_int64
         L.spec_set_chain_path.argtypes = [I]
+        L.spec_tree_rerank.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, P, P, P]
         _lib = L
         return L
 
@@ -286,6 +287,33 @@ def spec_verify_tree(target: torch.Tensor, draft_logits, parents: torch.Tensor, 
                                 _p(o["path_nodes"]), _p(o["out_tokens"]), _p(o["n_emit"]),
                                 _p(o["status"]), None, 0, _stream(stream, dev))
     _check(rc, "spec_verify_tree")
+    return o
+
+
+def spec_tree_rerank(parents: torch.Tensor, conf: torch.Tensor, m: int, max_depth: int = 64, node_tok=None, *,
+                     mask: bool = True, out=None, stream=None) -> dict:
+    """parents int32 [B, N], conf fp32 [B, N] (node_tok int32 [B, N] or None)
+    -> sel_nodes, sel_parents, sel_depth, sel_value, sel_tok (with node_tok),
+    mask uint8 [B, m, m] (unless mask=False), n_sel, status."""
+    dev = parents.device
+    if parents.dim() != 2:
+        raise ValueError("parents must be [B, N]")
+    B, N = parents.shape
+    parents = _i32(parents, (B, N), "parents", dev)
+    conf = _f32(conf, (B, N), "conf", dev)
+    node_tok = _i32(node_tok, (B, N), "node_tok", dev) if node_tok is not None else None
+    i32 = dict(dtype=torch.int32, device=dev)
+    o = out or dict(sel_nodes=torch.empty((B, m), **i32), sel_parents=torch.empty((B, m), **i32),
+                    sel_depth=torch.empty((B, m), **i32),
+                    sel_value=torch.empty((B, m), dtype=torch.float32, device=dev),
+                    sel_tok=torch.empty((B, m), **i32) if node_tok is not None else None,
+                    mask=torch.empty((B, m, m), dtype=torch.uint8, device=dev) if mask else None,
+                    n_sel=torch.empty(B, **i32), status=torch.empty(B, **i32))
+    rc = lib().spec_tree_rerank(_p(parents), _p(conf), _p(node_tok), B, N, int(m), int(max_depth),
+                                _p(o["sel_nodes"]), _p(o["sel_parents"]), _p(o["sel_depth"]),
+                                _p(o.get("sel_value")), _p(o.get("sel_tok")), _p(o.get("mask")),
+                                _p(o["n_sel"]), _p(o.get("status")), _stream(stream, dev))
+    _check(rc, "spec_tree_rerank")
     return o
 
 

@@ -358,6 +358,22 @@ int spec_verify_sample(const void *target, int64_t target_req_stride, const void
                       workspace, workspace_bytes, stream);
 }
 
+int spec_tree_rerank(const int32_t *parents, const float *conf, const int32_t *node_tok, int B, int N,
+                     int m, int max_depth, int32_t *sel_nodes, int32_t *sel_parents, int32_t *sel_depth,
+                     float *sel_value, int32_t *sel_tok, uint8_t *mask, int32_t *n_sel, int32_t *status,
+                     void *stream) {
+  if (B < 0 || N < 1 || N > SPEC_MAX_NODES || m < 1 || m > SPEC_MAX_NODES || max_depth < 0 ||
+      max_depth > SPEC_MAX_DEPTH)
+    return SPEC_EINVAL;
+  if (B == 0) return SPEC_OK;
+  if (!parents || !conf || !sel_nodes || !sel_parents || !sel_depth || !n_sel || (sel_tok && !node_tok))
+    return SPEC_EINVAL;
+  RerankParams P{parents, conf, node_tok, B, N, m, max_depth, sel_nodes, sel_parents, sel_depth,
+                 sel_value, sel_tok, mask, n_sel, status};
+  const cudaError_t e = launch_tree_rerank(P, as_stream(stream));
+  return e == cudaSuccess ? SPEC_OK : fail_cuda(e, "spec_tree_rerank");
+}
+
 int spec_verify_tree(const void *target, int64_t target_req_stride, const void *draft_logits,
                      int64_t draft_req_stride, int64_t row_stride, int dtype, int B, int N,
                      int V, float temperature, const int32_t *parents, const int32_t *node_tok,

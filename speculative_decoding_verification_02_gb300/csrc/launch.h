@@ -74,6 +74,19 @@ cudaError_t launch_tree(const TreeParams &P, bool vec, cudaStream_t st);
 size_t tree_dynamic_smem(const TreeParams &P);
 cudaError_t launch_ngram(const NgramParams &P, cudaStream_t st);
 
+struct RerankParams {
+  const int32_t *parents;
+  const float *conf;
+  const int32_t *node_tok;
+  int B, N, m, max_depth;
+  int32_t *sel_nodes, *sel_parents, *sel_depth;
+  float *sel_value;
+  int32_t *sel_tok;
+  uint8_t *mask;
+  int32_t *n_sel, *status;
+};
+cudaError_t launch_tree_rerank(const RerankParams &P, cudaStream_t st);
+
 // Tracing hooks (api.cu).  trace_begin returns a slot (or -1 when tracing is
 // off); trace_end records the closing event of that slot.
 int trace_begin(const char *name, cudaStream_t st);

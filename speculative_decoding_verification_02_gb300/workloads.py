@@ -21,6 +21,15 @@ Workload recipes (stddev convention: N(mu, s) means standard deviation s):
   tree60        B=16, N=60 nodes (root included), depth 6, <=10 children,
                 V=128256 bf16 target/draft rows per node drawn as in
                 chain_vocab248k, child tokens i.i.d. from the parent's q, T=1
+  eagle2_candidates  B=16 candidate trees grown layer by layer as in
+                EAGLE-2's expansion stage: the root gets `branch` children,
+                then for depth-1 more layers `expand` nodes of the newest
+                layer each get `branch` children (the expanded nodes are a
+                random subset here); a node's confidences are the sorted
+                first `branch` weights of a Dirichlet(0.5) draw over
+                branch + 1 outcomes (the last standing for the rest of the
+                vocabulary), tokens uniform over [0, V).  Defaults: depth 6,
+                expand 10, branch 10 -> N = 511 nodes; m = 60 kept
 """
 from __future__ import annotations
 
@@ -211,3 +220,30 @@ def ngram_problem(seed: int, B: int = 64, H: int = 4096, V: int = 32000, k: int 
                     target[b, i, planted_next[b, i]] += np.float32(boost)
     return dict(history=hist, hist_len=hist_len, target=target, window=window, k=k, V=V,
                 planted_next=planted_next, B=B, H=H)
+
+
+def eagle2_candidates(seed: int = SEED_BASE + 6, B: int = 16, depth: int = 6, expand: int = 10,
+                      branch: int = 10, V: int = 128256) -> dict:
+    """Candidate draft trees shaped like EAGLE-2's expansion stage (see the
+    module docstring): parents [B, N] int32 (creation order, parents[0] =
+    -1), conf [B, N] fp32 (conf[:, 0] = 1), node_tok [B, N] int32."""
+    r_tree, r_conf, r_tok = _rngs(seed, 3)
+    N = 1 + branch + (depth - 1) * expand * branch
+    parents = np.full((B, N), -1, np.int32)
+    conf = np.ones((B, N), np.float32)
+    for b in range(B):
+        nxt, layer = 1, [0]
+        for d in range(depth):
+            grow = layer if d == 0 else np.sort(r_tree.choice(layer, size=min(expand, len(layer)), replace=False))
+            new = []
+            for u in grow:
+                w = np.sort(r_conf.dirichlet(np.full(branch + 1, 0.5))[:branch])[::-1].astype(np.float32)
+                for c in w:
+                    parents[b, nxt] = u
+                    conf[b, nxt] = c
+                    new.append(nxt)
+                    nxt += 1
+            layer = new
+        assert nxt == N
+    node_tok = r_tok.integers(0, V, (B, N)).astype(np.int32)
+    return dict(parents=parents, conf=conf, node_tok=node_tok, V=V, depth=depth)

@@ -139,3 +139,20 @@ def test_status_strings(L):
     assert b"workspace" in L.spec_status_string(-3)
     assert b"tree" in L.spec_status_string(102)
     assert L.spec_last_error() is not None
+
+
+def test_tree_rerank_argument_checks(L):
+    P_ = ctypes.c_void_p
+    L.spec_tree_rerank.argtypes = [P_, P_, P_, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int] + [P_] * 9
+    def call(parents=FAKE, conf=FAKE, tok=None, B=2, N=8, m=4, depth=8, nodes=FAKE, par=FAKE, dep=FAKE,
+             val=None, stok=None, mask=None, nsel=FAKE, st=None):
+        return L.spec_tree_rerank(parents, conf, tok, B, N, m, depth, nodes, par, dep, val, stok, mask, nsel, st,
+                                  None)
+    assert call(N=0) == -1 and call(N=4097) == -1
+    assert call(m=0) == -1 and call(m=4097) == -1
+    assert call(depth=-1) == -1 and call(depth=65) == -1
+    assert call(B=-1) == -1
+    assert call(B=0) == 0                       # nothing to do, nothing launched
+    for kw in ("parents", "conf", "nodes", "par", "dep", "nsel"):
+        assert call(**{kw: None}) == -1, kw
+    assert call(stok=FAKE) == -1                # tokens out without tokens in
