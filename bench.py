@@ -325,6 +325,7 @@ class TreeWorkload:
 class EagleWorkload:
     """spec_tree_rerank on 16 EAGLE-2-shaped candidate trees of 511 nodes."""
     kind = "rerank"
+    oracle_threads = 1  # the oracle's rerank runs on one thread
     metric = "EAGLE-2 candidate-tree nodes post-processed per second (value, top-60 rerank, flatten, mask)"
     unit = "nodes/s"
 
@@ -425,7 +426,7 @@ def oracle_rate(wl, target_seconds: float):
     the workload: whole requests, in rounds whose size grows until the timed
     rounds together last about target_seconds."""
     import oracle
-    threads = oracle.max_threads()
+    threads = getattr(wl, "oracle_threads", None) or oracle.max_threads()
     wl.oracle_call(1, threads)            # untimed: thread pool and caches warm
     n, rows, dt = max(1, threads), 0, 0.0
     while dt < target_seconds:
@@ -446,7 +447,7 @@ def run_reference(args):
         return 0
     import oracle
     wl = WORKLOADS[args.workload](args.workload)
-    threads = min(oracle.max_threads(), wl.B)  # the oracle parallelises over requests
+    threads = getattr(wl, "oracle_threads", None) or min(oracle.max_threads(), wl.B)  # over requests
     budget = float(os.environ.get("SPEC_REF_SECONDS", "60"))
     t_start = time.perf_counter()
     for _ in range(args.warmup):
@@ -622,8 +623,9 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         rate, threads, nrows, dt = oracle_rate(wl, float(os.environ.get("SPEC_CPU_SECONDS", "10")))
         cpu = {"value": rate, "unit": getattr(wl, "unit", "rows/s"), "cores": threads, "kind": "oracle",
-               "sample": f"{nrows} rows of the workload's requests through the oracle ({dt:.1f} s, fp64, "
-                         f"OpenMP over requests)"}
+               "sample": f"{nrows} {getattr(wl, 'unit', 'rows/s').split('/')[0]} of the workload's requests "
+                         f"through the oracle ({dt:.1f} s, fp64"
+                         f"{', OpenMP over requests' if threads > 1 else ', one thread'})"}
 
     if rank == 0:
         line = {
