@@ -70,6 +70,7 @@ extern "C" {
 #define SPEC_OP_GREEDY 1
 #define SPEC_OP_SAMPLE 2
 #define SPEC_OP_TREE 3
+#define SPEC_OP_DRAW 4
 
 /* Limits checked on the host. */
 #define SPEC_MAX_K 64        /* draft length of a chain */
@@ -236,6 +237,29 @@ int spec_verify_sample_noalloc(const void *target, int64_t target_req_stride,
                                const int32_t *max_emit, const float *uniforms, int32_t *accepted,
                                int32_t *out_tokens, int32_t *n_emit, float *p_tok, float *q_tok,
                                float *resid_mass, int32_t *status, void *stream);
+
+/*
+ * spec_sample -- draw one token from each row's softmax: the drafter's side
+ * of speculative sampling, x ~ q.  ("投机解码:为什么一个字都不改", 改进方案:
+ * the draft model proposes x by sampling its own distribution
+ * q = softmax(draft logits / T), and verification later needs q(x); the
+ * draw is the one the verify step uses for its final token.)
+ *
+ *   logits       request b's row starts at element b*req_stride (V logits,
+ *                contiguous); dtype SPEC_DTYPE_F32 or SPEC_DTYPE_BF16.
+ *   temperature  T > 0 (finite).
+ *   uniforms     fp32 [B] in [0, 1).
+ *   tokens       out int32 [B]: the smallest v whose inclusive prefix sum of
+ *                softmax(row / T) exceeds u_b (if rounding leaves none, the
+ *                last v with positive probability).
+ *   probs        out fp32 [B] or NULL: the probability of tokens[b].
+ *   status       out int32 [B] or NULL.
+ *   workspace    size from spec_workspace_size(SPEC_OP_DRAW, B, 0, V, dtype);
+ *                needs no initialisation.
+ */
+int spec_sample(const void *logits, int64_t req_stride, int dtype, int B, int V, float temperature,
+                const float *uniforms, int32_t *tokens, float *probs, int32_t *status, void *workspace,
+                size_t workspace_bytes, void *stream);
 
 /*
  * spec_tree_rerank -- EAGLE-2 post-processing of candidate draft trees.

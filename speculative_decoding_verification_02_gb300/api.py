@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libspecverify.so")
 SPEC_OK, SPEC_EINVAL, SPEC_EDTYPE, SPEC_EWORKSPACE, SPEC_ECUDA = 0, -1, -2, -3, -4
 STATUS_OK, STATUS_TOKEN_RANGE, STATUS_BAD_TREE, STATUS_BAD_LENGTH = 0, 1, 2, 3
 DTYPE_F32, DTYPE_BF16 = 0, 1
-OP_NGRAM, OP_GREEDY, OP_SAMPLE, OP_TREE = 0, 1, 2, 3
+OP_NGRAM, OP_GREEDY, OP_SAMPLE, OP_TREE, OP_DRAW = 0, 1, 2, 3, 4
 CHAIN_AUTO, CHAIN_TWO_PASS, CHAIN_FUSED = 0, 1, 2
 
 _lock = threading.Lock()
@@ -63,6 +63,7 @@ def lib():
         L.spec_launch_count.restype = ctypes.c_int64
         L.spec_set_chain_path.argtypes = [I]
         L.spec_tree_rerank.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, P, P, P]
+        L.spec_sample.argtypes = [P, I64, I, I, I, F, P, P, P, P, P, Z, P]
         _lib = L
         return L
 
@@ -287,6 +288,33 @@ def spec_verify_tree(target: torch.Tensor, draft_logits, parents: torch.Tensor, 
                                 _p(o["path_nodes"]), _p(o["out_tokens"]), _p(o["n_emit"]),
                                 _p(o["status"]), None, 0, _stream(stream, dev))
     _check(rc, "spec_verify_tree")
+    return o
+
+
+def spec_sample(logits: torch.Tensor, uniforms: torch.Tensor, temperature: float = 1.0, *, probs: bool = True,
+                out=None, ws=None, stream=None) -> dict:
+    """logits [B, V] (fp32 or bf16, each row contiguous), uniforms fp32 [B]
+    -> tokens int32 [B] drawn from softmax(logits / T), probs fp32 [B] (the
+    drawn tokens' probabilities), status."""
+    if not isinstance(logits, torch.Tensor) or logits.dim() != 2:
+        raise ValueError("logits must be a [B, V] tensor")
+    if logits.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("logits must be float32 or bfloat16")
+    if logits.stride(1) != 1:
+        logits = logits.contiguous()
+    dev = logits.device
+    B, V = logits.shape
+    uniforms = _f32(uniforms, (B,), "uniforms", dev)
+    dt = _dtype_code(logits)
+    need = spec_workspace_size(OP_DRAW, B, 0, V, dt)
+    ws = ws if ws is not None else workspace(need, dev, stream)
+    o = out or dict(tokens=torch.empty(B, dtype=torch.int32, device=dev),
+                    probs=torch.empty(B, dtype=torch.float32, device=dev) if probs else None,
+                    status=torch.empty(B, dtype=torch.int32, device=dev))
+    rc = lib().spec_sample(_p(logits), logits.stride(0), dt, B, V, float(temperature), _p(uniforms),
+                           _p(o["tokens"]), _p(o.get("probs")), _p(o["status"]), _p(ws), ws.numel(),
+                           _stream(stream, dev))
+    _check(rc, "spec_sample")
     return o
 
 

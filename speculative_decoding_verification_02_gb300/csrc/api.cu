@@ -164,6 +164,14 @@ bool trace_enabled() {
 
 using namespace sv;
 
+// spec_sample runs the sampling chain with k = 0 (the draw from row 0 with
+// uniform 0 is the bonus draw); the accept counts it does not return live
+// after the chain's workspace.
+static size_t draw_workspace(int B, int V, int dtype) {
+  const size_t chain = chain_layout(true, B, 0, V, dtype).total;
+  return chain + round_up(2 * sizeof(int32_t) * static_cast<size_t>(B), 256);
+}
+
 extern "C" {
 
 size_t spec_workspace_size(int op, int B, int rows_per_req, int V, int dtype) {
@@ -172,6 +180,7 @@ size_t spec_workspace_size(int op, int B, int rows_per_req, int V, int dtype) {
   switch (op) {
     case SPEC_OP_GREEDY: return chain_layout(false, B, rows_per_req, V, dtype).total;
     case SPEC_OP_SAMPLE: return chain_layout(true, B, rows_per_req, V, dtype).total;
+    case SPEC_OP_DRAW: return draw_workspace(B, V, dtype);
     default: return 0;  // n-gram and tree walks need no workspace
   }
 }
@@ -271,7 +280,8 @@ static int chain_common(bool sample, const void *target, int64_t t_req, const vo
                         const int32_t *draft, const int32_t *draft_len, const int32_t *max_emit,
                         const float *uniforms, int32_t *accepted, int32_t *out_tokens,
                         int32_t *n_emit, float *p_tok, float *q_tok, float *resid_mass,
-                        int32_t *status, void *workspace, size_t workspace_bytes, void *stream) {
+                        int32_t *status, void *workspace, size_t workspace_bytes, void *stream,
+                        float *final_prob = nullptr) {
   if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_EDTYPE;
   if (B < 0 || k < 0 || k > SPEC_MAX_K || V <= 0 || t_req < 0 || d_req < 0 || row < 0)
     return SPEC_EINVAL;
@@ -318,6 +328,7 @@ static int chain_common(bool sample, const void *target, int64_t t_req, const vo
   P.p_tok = p_tok;
   P.q_tok = q_tok;
   P.resid_mass = resid_mass;
+  P.final_prob = final_prob;
   P.counter2 = reinterpret_cast<int *>(ws + L.counter2);
   P.part = reinterpret_cast<Partial *>(ws + L.part);
   P.part2 = reinterpret_cast<float *>(ws + L.part2);
@@ -333,6 +344,23 @@ static int chain_common(bool sample, const void *target, int64_t t_req, const vo
     e = launch_chain(P, sample, vec, fvec, as_stream(stream));
   }
   return e == cudaSuccess ? SPEC_OK : fail_cuda(e, sample ? "spec_verify_sample" : "spec_verify_greedy");
+}
+
+int spec_sample(const void *logits, int64_t req_stride, int dtype, int B, int V, float temperature,
+                const float *uniforms, int32_t *tokens, float *probs, int32_t *status, void *workspace,
+                size_t workspace_bytes, void *stream) {
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_EDTYPE;
+  if (B < 0 || V <= 0 || req_stride < 0 || !(temperature > 0.0f && std::isfinite(temperature))) return SPEC_EINVAL;
+  if (B == 0) return SPEC_OK;
+  if (!logits || !uniforms || !tokens) return SPEC_EINVAL;
+  const size_t need = draw_workspace(B, V, dtype);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return SPEC_EWORKSPACE;
+  const size_t chain = chain_layout(true, B, 0, V, dtype).total;
+  int32_t *accepted = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + chain);
+  return chain_common(true, logits, req_stride, nullptr, 0, 0, dtype, B, 0, V, temperature, nullptr, nullptr,
+                      nullptr, uniforms, accepted, tokens, accepted + B, nullptr, nullptr, nullptr, status,
+                      workspace, chain, stream, probs);
 }
 
 int spec_verify_greedy(const void *target, int64_t target_req_stride, int64_t row_stride,

@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
   __shared__ float s_sub[kWarps][kMaxSubs];
   __shared__ float s_wcache[kPickCache];
   __shared__ int s_last, s_j, s_m;
-  __shared__ float s_thr, s_tot;
+  __shared__ float s_thr, s_tot, s_drawn;
   __shared__ bool s_fallback;
   const int nc = P.nc;
   const int b = blockIdx.x / P.nc2, j = blockIdx.x - b * P.nc2;
@@ -406,12 +406,14 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
       float tp;
       warp_pick([&](int jj) { const Partial q = ld_partial(p1 + jj); return q.s * ex2((q.m - M) * c); }, nc,
                 u_final, s_wcache, kPickCache, js, th, tp);
+      tot = tp;
     }
     if (lane == 0) {
       s_j = js;
       s_thr = th;
-      s_tot = tot;
+      s_tot = fallback ? 0.0f : tot;  // the residual mass (0 after the fallback)
       s_fallback = fallback;
+      s_drawn = tot;                   // the mass of the distribution the token is drawn from
     }
   }
   __syncthreads();
@@ -430,6 +432,8 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
   if (tid == 0) {
     if (m < ne) P.out_tokens[static_cast<int64_t>(b) * (k + 1) + m] = tok;
     if (P.resid_mass) P.resid_mass[b] = (m < L && !s_fallback) ? s_tot : 0.0f;
+    if (P.final_prob)
+      P.final_prob[b] = weight_at<DT>(W, load_one<DT>(W.a, tok), W.b ? load_one<DT>(W.b, tok) : 0.0f) / s_drawn;
   }
 }
 

@@ -302,6 +302,8 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
   if (tid == 0) {
     if (m < ne) P.out_tokens[static_cast<int64_t>(b) * (k + 1) + m] = tok;
     if (P.resid_mass) P.resid_mass[b] = (m < L && W.b != nullptr) ? total : 0.0f;
+    if (P.final_prob)
+      P.final_prob[b] = weight_at<DT>(W, load_one<DT>(W.a, tok), W.b ? load_one<DT>(W.b, tok) : 0.0f) / total;
   }
 }
 

@@ -25,6 +25,7 @@ struct ChainParams {
   const float *uniforms;
   int32_t *accepted, *out_tokens, *n_emit, *status;
   float *p_tok, *q_tok, *resid_mass;
+  float *final_prob;  // or null: the final token's probability under the distribution it was drawn from
   Partial *part;     // [B][rows][nc] streaming-pass statistics
   float *part2;      // [B][nsub] mass of the final draw's weights per sub-chunk
   int *counter2;     // [B] arrival counter of the residual pass

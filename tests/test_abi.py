@@ -156,3 +156,21 @@ def test_tree_rerank_argument_checks(L):
     for kw in ("parents", "conf", "nodes", "par", "dep", "nsel"):
         assert call(**{kw: None}) == -1, kw
     assert call(stok=FAKE) == -1                # tokens out without tokens in
+
+
+def test_sample_draw_argument_checks(L):
+    P_ = ctypes.c_void_p
+    L.spec_sample.argtypes = [P_, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                              P_, P_, P_, P_, P_, ctypes.c_size_t, P_]
+    L.spec_workspace_size.restype = ctypes.c_size_t
+    need = L.spec_workspace_size(4, 8, 0, 1000, 1)
+    assert need > 0 and need >= L.spec_workspace_size(2, 8, 0, 1000, 1)
+    ws = ctypes.c_void_p(0x100000)
+    def call(logits=FAKE, stride=1000, dtype=1, B=8, V=1000, T=1.0, u=FAKE, tok=FAKE, w=ws, wsb=need):
+        return L.spec_sample(logits, stride, dtype, B, V, T, u, tok, None, None, w, wsb, None)
+    assert call(dtype=7) == -2
+    assert call(B=-1) == -1 and call(V=0) == -1 and call(stride=-1) == -1
+    assert call(T=0.0) == -1 and call(T=float("inf")) == -1 and call(T=float("nan")) == -1
+    assert call(logits=None) == -1 and call(u=None) == -1 and call(tok=None) == -1
+    assert call(wsb=need - 1) == -3 and call(w=None) == -3 and call(w=ctypes.c_void_p(0x100010)) == -3
+    assert call(B=0) == 0
