@@ -27,7 +27,8 @@ _lib = None
 
 ST_OK, ST_TOKEN_RANGE, ST_BAD_TREE, ST_BAD_LENGTH = 0, 1, 2, 3
 VARIANT_LOSSLESS, VARIANT_RESAMPLE_FROM_P, VARIANT_NAIVE_EQUAL = 0, 1, 2
-TREE_VARIANT_NO_RESIDUAL_UPDATE = 1
+TREE_VARIANT_NO_RESIDUAL_UPDATE = 1   # planted mistake
+TREE_VARIANT_WITHOUT_REPLACEMENT = 2  # siblings drawn from q without replacement
 
 
 def build(force: bool = False) -> str:

@@ -27,7 +27,12 @@
  *                  the children in turn and replacing p by the normalised
  *                  residual after every rejected child ("Speculative Decoding
  *                  II", EAGLE section, the paragraph on verifying the draft
- *                  tree with tree attention, "consistent with SpecInfer")
+ *                  tree with tree attention, "consistent with SpecInfer");
+ *                  variant 2, for siblings drawn from q WITHOUT replacement,
+ *                  also removes each rejected sibling's token from q and
+ *                  renormalises it, since the next sibling was drawn from
+ *                  that distribution (a reading; the pages name SpecInfer
+ *                  only)
  *   n-gram draft   take the last `window` tokens, find the same segment
  *                  earlier in the history, propose what followed it
  *                  ("第 13 篇", 逐行要点, the 草稿器.猜 line)
@@ -461,7 +466,7 @@ int orc_verify_tree(const void *target, int64_t t_req, const void *draft_logits,
                     int32_t *status, int variant, int threads, int64_t *degenerate)
 {
     if (!target || B < 0 || N < 1 || V <= 0 || max_depth < 0 ||
-        (dtype != 0 && dtype != 1) || variant < 0 || variant > 1)
+        (dtype != 0 && dtype != 1) || variant < 0 || variant > 2)
         return ORC_EINVAL;
     const int greedy = !(T > 0.0);
     if (!greedy && !draft_logits)
@@ -549,12 +554,23 @@ int orc_verify_tree(const void *target, int64_t t_req, const void *draft_logits,
                         continue;
                     if (accept_test((double)u[c], p[tok[c]], q[tok[c]])) {
                         next = c;
-                    } else if (variant == 0) {
+                    } else if (variant == 0 || variant == 2) {
                         double R = residual(p, q, V, r);
-                        if (R > 0.0)
+                        if (R > 0.0) {
                             memcpy(p, r, sizeof(double) * (size_t)V);
-                        else
-                            degen += 1; /* keep p: see the header */
+                            if (variant == 2) {
+                                /* siblings drawn without replacement: the next
+                                 * one came from q with this token removed */
+                                double Q = 0.0;
+                                q[tok[c]] = 0.0;
+                                for (int v = 0; v < V; ++v)
+                                    Q += q[v];
+                                for (int v = 0; v < V; ++v)
+                                    q[v] = Q > 0.0 ? q[v] / Q : 0.0;
+                            }
+                        } else {
+                            degen += 1; /* keep p (and q): see the header */
+                        }
                     }
                 }
                 if (next < 0)

@@ -8,7 +8,9 @@
   token is distributed exactly as p.  Each acceptance threshold and the final
   residual draw are measured by scanning one uniform over a 2^16 grid; the
   composition over both sibling tokens must equal p to ~1e-4, and the
-  planted mistake (no residual update between siblings) must not.
+  planted mistake (no residual update between siblings) must not.  With
+  three siblings drawn WITHOUT replacement, the rule that also removes each
+  rejected token from q emits exactly p, and the i.i.d. rule does not.
 - Malformed trees and out-of-range tokens are reported per request.
 """
 import numpy as np
@@ -96,39 +98,48 @@ def test_greedy_walk_on_worked_tree(branch, expect_tokens, expect_path):
     assert out["accepted_len"][0] == len(expect_path) - 1
 
 
-def _tree_first_token_law(lp, lq, variant):
-    """Root with two sibling leaves; first emitted token law, threshold by threshold."""
+def _tree_first_token_law(lp, lq, variant, n=2, replace=True):
+    """Root with n sibling leaves drawn from q (i.i.d., or without replacement);
+    the first emitted token's law, threshold by threshold: sibling j's
+    acceptance rate is measured by scanning u_j over a 2^16 grid with the
+    earlier siblings' uniforms set to reject, and the final draw by scanning
+    u_final with every sibling rejected."""
+    import itertools
     V = lp.size
-    N = 3
+    N = n + 1
     q = _softmax64(lq)
     grid = (np.arange(M, dtype=np.float64) / M).astype(np.float32)
-    target = np.broadcast_to(np.stack([lp, lp, lp]), (M, N, V))
-    dl = np.broadcast_to(np.stack([lq, lq, lq]), (M, N, V))
-    parents = np.broadcast_to(np.array([-1, 0, 0], np.int32), (M, N))
+    target = np.broadcast_to(np.stack([lp] * N), (M, N, V))
+    dl = np.broadcast_to(np.stack([lq] * N), (M, N, V))
+    parents = np.broadcast_to(np.array([-1] + [0] * n, np.int32), (M, N))
     law = np.zeros(V)
-
-    def run(x1, x2, u1, u2, uf):
-        tok = np.broadcast_to(np.array([0, x1, x2], np.int32), (M, N))
-        u = np.stack([np.zeros(M, np.float32), u1, u2, uf], 1).astype(np.float32)
-        return oracle.verify_tree(target, dl, parents, tok, u, 1.0, max_depth=1,
-                                  variant=variant, threads=4)
-
     half = np.full(M, 0.5, np.float32)
     rej = np.full(M, U_REJECT, np.float32)
-    for x1 in range(V):
-        for x2 in range(V):
-            w = q[x1] * q[x2]
-            a1 = (run(x1, x2, grid, half, half)["path_nodes"][:, 1] == 1).mean()
-            law[x1] += w * a1
-            if a1 == 1.0:
-                continue
-            a2 = (run(x1, x2, rej, grid, half)["path_nodes"][:, 1] == 2).mean()
-            law[x2] += w * (1 - a1) * a2
-            if a2 == 1.0:
-                continue
-            out = run(x1, x2, rej, rej, grid)
+
+    def run(xs, us):
+        tok = np.broadcast_to(np.array([0] + list(xs), np.int32), (M, N))
+        u = np.stack([np.zeros(M, np.float32)] + list(us), 1).astype(np.float32)
+        return oracle.verify_tree(target, dl, parents, tok, u, 1.0, max_depth=1, variant=variant, threads=4)
+
+    seqs = itertools.product(range(V), repeat=n) if replace else itertools.permutations(range(V), n)
+    for xs in seqs:
+        w, left = 1.0, 1.0
+        for x in xs:                       # the drafter's draws
+            w *= q[x] / left
+            if not replace:
+                left -= q[x]
+        reach = 1.0                        # probability that siblings 1..j-1 were all rejected
+        for j in range(n):
+            us = [rej] * j + [grid] + [half] * (n - j - 1) + [half]
+            a = (run(xs, us)["path_nodes"][:, 1] == j + 1).mean()
+            law[xs[j]] += w * reach * a
+            reach *= 1 - a
+            if reach == 0.0:
+                break
+        if reach > 0.0:
+            out = run(xs, [rej] * n + [grid])
             assert np.all(out["accepted_len"] == 0)
-            law += w * (1 - a1) * (1 - a2) * np.bincount(out["out_tokens"][:, 0], minlength=V) / M
+            law += w * reach * np.bincount(out["out_tokens"][:, 0], minlength=V) / M
     return law
 
 
@@ -199,3 +210,19 @@ def test_single_node_tree_draws_from_root_target():
     assert np.all(out["n_emit"] == 1) and np.all(out["accepted_len"] == 0)
     np.testing.assert_allclose(np.bincount(out["out_tokens"][:, 0], minlength=V) / n, _softmax64(l),
                                atol=5 * np.sqrt(0.25 / n))
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_siblings_without_replacement_first_token_is_exactly_p(seed):
+    """Three siblings drawn from q without replacement: the rule that removes
+    each rejected sibling's token from q (and renormalises it) emits exactly
+    p; the i.i.d. rule applied to such drafts does not."""
+    rng = np.random.default_rng(70 + seed)
+    V = 4
+    lp = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    lq = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    p = _softmax64(lp)
+    law = _tree_first_token_law(lp, lq, oracle.TREE_VARIANT_WITHOUT_REPLACEMENT, n=3, replace=False)
+    assert np.max(np.abs(law - p)) < 6.0 * V / M
+    bad = _tree_first_token_law(lp, lq, oracle.VARIANT_LOSSLESS, n=3, replace=False)
+    assert np.max(np.abs(bad - p)) > 5e-3
