@@ -1,7 +1,7 @@
 """Benchmark of the verify-and-accept step on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload vocab248k|batch64|small|tree60|ngram|eagle2]
+                    [--workload vocab248k|batch64|small|tree60|tree60wor|draw64|ngram|eagle2]
                     [--chain-path auto|two_pass|fused]
 
 One step is one pass of the path over one batch:
@@ -11,6 +11,9 @@ One step is one pass of the path over one batch:
   small      spec_verify_sample, B=4, k=4, V=2,048 fp32 (36 rows)
   tree60     spec_verify_tree, 16 trees of 60 nodes, V=128,256 bf16
              (960 node rows per step)
+  tree60wor  the same trees with siblings drafted without replacement,
+             spec_verify_tree_ex with SPEC_TREE_SIBLINGS_WITHOUT_REPLACEMENT
+  draw64     spec_sample (drafter-side draw), B=64 rows of V=128,256 bf16
   ngram      spec_ngram_draft on 64 histories of 4,096 tokens, then
              spec_verify_greedy of the drafts, V=32,000 fp32 (320 rows)
   eagle2     spec_tree_rerank on 16 EAGLE-2-shaped candidate trees of 511
@@ -57,6 +60,7 @@ _CHAIN = [f"{CSRC}/chain.cu", f"{CSRC}/chain_fused.cu", f"{CSRC}/chain_common.cu
 KERNEL_SOURCES = {"chain": _CHAIN,
                   "tree": [f"{CSRC}/tree.cu", f"{CSRC}/common.cuh", f"{CSRC}/segments.cuh"],
                   "ngram": [f"{CSRC}/ngram.cu"] + _CHAIN,
+                  "draw": _CHAIN,
                   "rerank": [f"{CSRC}/rerank.cu", f"{CSRC}/common.cuh"]}
 
 
@@ -141,15 +145,38 @@ def barrier():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons every 200 ms while running.
+
+    A timed region of a few milliseconds falls between two samples, so the
+    caller keeps the GPU under the same (untimed) load before and after it
+    until samples have landed (keep_busy); the summary gives the samples
+    inside the timed region when there are any, else those of the load
+    around it, and says which."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        self.window = None  # (start, end) of the timed region, wall clock
+
+    def count(self) -> int:
+        try:
+            with open(self.path) as f:
+                return sum(1 for _ in f)
+        except OSError:
+            return 0
+
+    def keep_busy(self, work, new_samples: int, max_seconds: float):
+        """Runs work() repeatedly until new_samples more samples are written
+        (or max_seconds pass)."""
+        if self.proc is None:
+            return
+        c0, t0 = self.count(), time.time()
+        while self.count() < c0 + new_samples and time.time() - t0 < max_seconds:
+            work()
 
     def __enter__(self):
         try:
@@ -174,24 +201,30 @@ class ClockSampler:
     def summary(self) -> dict:
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sms, maxs, reasons = [], [], set()
+        import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sms.append(float(parts[1]))
-                maxs.append(float(parts[2]))
+                sm, mx = float(parts[1]), float(parts[2])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sms:
+            try:
+                ts = datetime.datetime.strptime(parts[9], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None
+            rows.append((ts, sm, mx, {n for n, v in zip(names, parts[5:9]) if v.lower() == "active"}))
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs), "reasons": sorted(reasons),
-                "samples": len(sms)}
+        inside = [r for r in rows if self.window and r[0] is not None and
+                  self.window[0] <= r[0] <= self.window[1]]
+        use = inside or rows
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": sorted(set().union(*(r[3] for r in use))), "samples": len(use),
+                "window": "timed region" if inside else "the same load just before and after the timed region"}
 
 
 # --------------------------------------------------------------- workloads
@@ -220,6 +253,8 @@ class ChainWorkload:
         self.rows_per_step = self.B * (2 * self.k + 1)
         self.set_bytes = self.rows_per_step * self.V * self.es
         self.logits = "bf16" if self.es == 2 else "fp32"
+        if name != "vocab248k":
+            self.metric = f"verified logit rows/sec at V={self.V:,}; achieved HBM GB/s vs GB300 peak"
 
     def device_set(self, dev, i):
         import torch
@@ -269,18 +304,78 @@ class ChainWorkload:
         return reps * self.B * (2 * self.k + 1)
 
 
+class DrawWorkload:
+    """spec_sample: the drafter-side draw x ~ softmax(d/T) with its
+    probability, on the first draft row of each batch64 request."""
+    kind = "draw"
+    unit = "rows/s"
+
+    def __init__(self, name):
+        from speculative_decoding_verification_02_gb300 import workloads as W
+        p = W.chain_batch64()
+        self.rows = np.ascontiguousarray(p["draft_logits"][:, 0])
+        self.T = p["T"]
+        self.B, self.V = self.rows.shape
+        self.u = np.random.default_rng(W.SEED_BASE + 7).random(self.B, dtype=np.float32)
+        self.desc = ("drafter-side draw x ~ softmax(d/T) with q(x), B=64 rows of V=128,256 bf16 "
+                     "(batch64's first draft rows: d=t+N(0,s), t~N(0,2.5)), T=0.7")
+        self.metric = f"drawn logit rows/sec at V={self.V:,}; achieved HBM GB/s vs GB300 peak"
+        self.es = 2
+        self.rows_per_step = self.B
+        self.set_bytes = self.B * self.V * self.es
+        self.logits = "bf16"
+
+    def device_set(self, dev, i):
+        import torch
+        g = torch.Generator().manual_seed(2000 + i)
+        u = torch.rand(self.B, generator=g).clamp_(max=1 - 2 ** -24) if i else torch.from_numpy(self.u)
+        return dict(L=to_dev(self.rows, dev), U=u.to(dev))
+
+    def call(self, s, out, stream):
+        from speculative_decoding_verification_02_gb300 import api
+        return api.spec_sample(s["L"], s["U"], self.T, out=out, stream=stream)
+
+    result_keys = ("tokens", "probs", "status")
+
+    def kernel_bytes(self, name, outs):
+        """The statistics pass reads every row once; the draw re-reads (at
+        most) the row it draws from."""
+        if name.startswith("chain_stats") or name.startswith("chain_fused"):
+            return self.set_bytes
+        if name.startswith("chain_sample_accept"):
+            return self.B * self.V * self.es
+        return None
+
+    def oracle_call(self, n, threads):
+        """At least n draws through the oracle (verification with no draft)."""
+        import oracle
+        reps = max(1, -(-n // self.B))
+        empty = np.zeros((self.B, 0, self.V), self.rows.dtype)
+        for _ in range(reps):
+            oracle.verify_sample(self.rows[:, None], empty, np.zeros((self.B, 0), np.int32), self.u[:, None], self.T,
+                                 threads=threads)
+        return reps * self.B
+
+
 class TreeWorkload:
     """spec_verify_tree on 16 draft trees of 60 nodes."""
     kind = "tree"
 
     def __init__(self, name):
+        from speculative_decoding_verification_02_gb300 import api
         from speculative_decoding_verification_02_gb300 import workloads as W
-        self.prob = W.tree60()
+        self.wor = name == "tree60wor"
+        self.flags = api.TREE_SIBLINGS_WITHOUT_REPLACEMENT if self.wor else 0
+        self.prob = (W.tree_problem(W.SEED_BASE + 5, 16, 60, 6, 10, 128256, "bf16", 1.0, siblings="without_replacement")
+                     if self.wor else W.tree60())
         self.desc = ("EAGLE-style tree verify, B=16, 60-node trees of depth 6 with <=10 children, "
-                     "V=128,256 bf16 (t~N(0,3) with 5 ids +8, d=0.8t+N(0,1)), T=1")
+                     "V=128,256 bf16 (t~N(0,3) with 5 ids +8, d=0.8t+N(0,1)), T=1" +
+                     (", siblings drawn from q without replacement and verified with the matching rule"
+                      if self.wor else ""))
         p = self.prob
         self.B, self.N, self.V = p["target"].shape
         self.es = 2
+        self.metric = f"verified tree-node logit rows/sec at V={self.V:,}; achieved HBM GB/s vs GB300 peak"
         self.rows_per_step = self.B * self.N
         self.set_bytes = 2 * self.B * self.N * self.V * self.es
         self.logits = "bf16"
@@ -294,7 +389,7 @@ class TreeWorkload:
     def call(self, s, out, stream):
         from speculative_decoding_verification_02_gb300 import api
         return api.spec_verify_tree(s["T"], s["D"], s["P"], s["X"], s["U"], self.prob["T"], self.prob["depth"],
-                                    out=out, stream=stream)
+                                    flags=self.flags, out=out, stream=stream)
 
     result_keys = ("accepted_len", "path_nodes", "out_tokens", "n_emit", "status")
 
@@ -318,7 +413,8 @@ class TreeWorkload:
         reps = max(1, -(-n // self.B))
         for _ in range(reps):
             oracle.verify_tree(p["target"], p["draft_logits"], p["parents"], p["node_tok"], p["uniforms"], p["T"],
-                               p["depth"], threads=threads)
+                               p["depth"], threads=threads,
+                               variant=oracle.TREE_VARIANT_WITHOUT_REPLACEMENT if self.wor else 0)
         return reps * self.B * self.N
 
 
@@ -379,6 +475,7 @@ class NgramWorkload:
         self.k, self.V, self.w = p["k"], p["V"], p["window"]
         self.es = 4
         self.rows_per_step = self.B * (self.k + 1)
+        self.metric = f"drafted and greedily verified logit rows/sec at V={self.V:,}; achieved HBM GB/s vs GB300 peak"
         self.set_bytes = self.rows_per_step * self.V * 4 + self.B * self.H * 4
         self.logits = "fp32"
 
@@ -418,7 +515,7 @@ class NgramWorkload:
 
 
 WORKLOADS = {"vocab248k": ChainWorkload, "batch64": ChainWorkload, "small": ChainWorkload,
-             "tree60": TreeWorkload, "ngram": NgramWorkload, "eagle2": EagleWorkload}
+             "tree60": TreeWorkload, "tree60wor": TreeWorkload, "draw64": DrawWorkload, "ngram": NgramWorkload, "eagle2": EagleWorkload}
 
 
 def oracle_rate(wl, target_seconds: float):
@@ -535,9 +632,18 @@ def run_ours(args):
             for i in range(args.warmup % nsets):
                 wl.call(sets[i], outs[i], stream)
         torch.cuda.synchronize(dev)
+
+        def load():  # untimed replays of the same graph, so clock samples see the step's load
+            with torch.cuda.stream(stream):
+                for _ in range(8):
+                    graph.replay()
+            torch.cuda.synchronize(dev)
+
+        sampler.keep_busy(load, 2, 3.0)
         barrier()
         torch.cuda.synchronize(dev)
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_start = time.time()
         ev0.record(stream)
         with torch.cuda.stream(stream):
             for _ in range(args.steps // nsets):
@@ -546,8 +652,10 @@ def run_ours(args):
                 graph_rem.replay()
         ev1.record(stream)
         torch.cuda.synchronize(dev)
+        sampler.window = (t_start, time.time())
         barrier()
         ms = ev0.elapsed_time(ev1)
+        sampler.keep_busy(load, 1, 1.5)
     clocks = sampler.summary()
     ms_max = reduce_max(ms, dev)
     total_rows = reduce_sum(args.steps * wl.rows_per_step, dev)

@@ -200,6 +200,32 @@ int spec_verify_tree(const void *target, int64_t target_req_stride, const void *
                      int32_t *path_nodes, int32_t *out_tokens, int32_t *n_emit,
                      int32_t *status, void *workspace, size_t workspace_bytes, void *stream);
 
+/* Flags of spec_verify_tree_ex. */
+#define SPEC_TREE_SIBLINGS_WITHOUT_REPLACEMENT 1
+
+/*
+ * spec_verify_tree_ex -- spec_verify_tree with flags (bitwise OR; 0 gives
+ * spec_verify_tree exactly; an unknown bit is SPEC_EINVAL).
+ *
+ *   SPEC_TREE_SIBLINGS_WITHOUT_REPLACEMENT: the drafter drew the children of
+ *   a node from q one after another WITHOUT replacement, each from q with the
+ *   earlier children's tokens removed and q renormalised.  Then after a
+ *   rejected child x, besides p <- norm(max(0, p - q)), q <- q with x zeroed,
+ *   renormalised (a rejected child's q(x) = 0 from then on, and a child whose
+ *   q(x) = 0 is accepted iff p(x) > 0).  With this reading the walk keeps the
+ *   target's distribution for such drafts, where the default rule assumes
+ *   the children were drawn independently from q ("Speculative Decoding II",
+ *   EAGLE section, the tree verified as in SpecInfer; the without-replacement
+ *   variant is a reading of that rule for drafts drawn so).  Ignored when
+ *   T <= 0.
+ */
+int spec_verify_tree_ex(const void *target, int64_t target_req_stride, const void *draft_logits,
+                        int64_t draft_req_stride, int64_t row_stride, int dtype, int B, int N,
+                        int V, float temperature, const int32_t *parents, const int32_t *node_tok,
+                        const float *uniforms, int max_depth, int flags, int32_t *accepted_len,
+                        int32_t *path_nodes, int32_t *out_tokens, int32_t *n_emit,
+                        int32_t *status, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Size of the scratch array behind spec_verify_sample_noalloc (4 MiB). */
 #define SPEC_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
 

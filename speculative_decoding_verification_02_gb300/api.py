@@ -23,6 +23,7 @@ STATUS_OK, STATUS_TOKEN_RANGE, STATUS_BAD_TREE, STATUS_BAD_LENGTH = 0, 1, 2, 3
 DTYPE_F32, DTYPE_BF16 = 0, 1
 OP_NGRAM, OP_GREEDY, OP_SAMPLE, OP_TREE, OP_DRAW = 0, 1, 2, 3, 4
 CHAIN_AUTO, CHAIN_TWO_PASS, CHAIN_FUSED = 0, 1, 2
+TREE_SIBLINGS_WITHOUT_REPLACEMENT = 1
 
 _lock = threading.Lock()
 _lib = None
@@ -51,6 +52,8 @@ def lib():
                                          P, P, P, P, P, Z, P]
         L.spec_verify_tree.argtypes = [P, I64, P, I64, I64, I, I, I, I, F, P, P, P, I, P, P, P, P,
                                        P, P, Z, P]
+        L.spec_verify_tree_ex.argtypes = [P, I64, P, I64, I64, I, I, I, I, F, P, P, P, I, I, P, P, P, P,
+                                          P, P, Z, P]
         L.spec_workspace_size.argtypes = [I, I, I, I, I]
         L.spec_workspace_size.restype = Z
         L.spec_status_string.argtypes = [I]
@@ -256,10 +259,11 @@ def spec_verify_sample(target: torch.Tensor, draft_logits: torch.Tensor, draft: 
 
 
 def spec_verify_tree(target: torch.Tensor, draft_logits, parents: torch.Tensor, node_tok: torch.Tensor,
-                     uniforms: torch.Tensor, temperature: float, max_depth: int, *, out=None,
+                     uniforms: torch.Tensor, temperature: float, max_depth: int, *, flags: int = 0, out=None,
                      stream=None) -> dict:
     """target/draft_logits [B, N, V], parents/node_tok int32 [B, N], uniforms fp32 [B, N+1]
-    -> accepted_len, path_nodes, out_tokens, n_emit, status.  temperature <= 0: greedy."""
+    -> accepted_len, path_nodes, out_tokens, n_emit, status.  temperature <= 0: greedy.
+    flags != 0 (TREE_SIBLINGS_WITHOUT_REPLACEMENT) goes through spec_verify_tree_ex."""
     target = _logits3(target, "target")
     dev = target.device
     B, N, V = target.shape
@@ -282,12 +286,16 @@ def spec_verify_tree(target: torch.Tensor, draft_logits, parents: torch.Tensor, 
                     n_emit=torch.empty(B, dtype=torch.int32, device=dev),
                     status=torch.empty(B, dtype=torch.int32, device=dev))
     d_req = draft_logits.stride(0) if draft_logits is not None else 0
-    rc = lib().spec_verify_tree(_p(target), target.stride(0), _p(draft_logits), d_req, target.stride(1),
-                                _dtype_code(target), B, N, V, float(temperature), _p(parents),
-                                _p(node_tok), _p(uniforms), int(max_depth), _p(o["accepted_len"]),
-                                _p(o["path_nodes"]), _p(o["out_tokens"]), _p(o["n_emit"]),
-                                _p(o["status"]), None, 0, _stream(stream, dev))
-    _check(rc, "spec_verify_tree")
+    head = (_p(target), target.stride(0), _p(draft_logits), d_req, target.stride(1), _dtype_code(target), B, N,
+            V, float(temperature), _p(parents), _p(node_tok), _p(uniforms), int(max_depth))
+    tail = (_p(o["accepted_len"]), _p(o["path_nodes"]), _p(o["out_tokens"]), _p(o["n_emit"]), _p(o["status"]),
+            None, 0, _stream(stream, dev))
+    if flags:
+        rc = lib().spec_verify_tree_ex(*head, int(flags), *tail)
+        _check(rc, "spec_verify_tree_ex")
+    else:
+        rc = lib().spec_verify_tree(*head, *tail)
+        _check(rc, "spec_verify_tree")
     return o
 
 

@@ -408,8 +408,20 @@ int spec_verify_tree(const void *target, int64_t target_req_stride, const void *
                      const float *uniforms, int max_depth, int32_t *accepted_len,
                      int32_t *path_nodes, int32_t *out_tokens, int32_t *n_emit,
                      int32_t *status, void *workspace, size_t workspace_bytes, void *stream) {
+  return spec_verify_tree_ex(target, target_req_stride, draft_logits, draft_req_stride, row_stride, dtype, B, N, V,
+                             temperature, parents, node_tok, uniforms, max_depth, 0, accepted_len, path_nodes,
+                             out_tokens, n_emit, status, workspace, workspace_bytes, stream);
+}
+
+int spec_verify_tree_ex(const void *target, int64_t target_req_stride, const void *draft_logits,
+                        int64_t draft_req_stride, int64_t row_stride, int dtype, int B, int N,
+                        int V, float temperature, const int32_t *parents, const int32_t *node_tok,
+                        const float *uniforms, int max_depth, int flags, int32_t *accepted_len,
+                        int32_t *path_nodes, int32_t *out_tokens, int32_t *n_emit,
+                        int32_t *status, void *workspace, size_t workspace_bytes, void *stream) {
   (void)workspace;
   (void)workspace_bytes;
+  if (flags & ~SPEC_TREE_SIBLINGS_WITHOUT_REPLACEMENT) return SPEC_EINVAL;
   if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_EDTYPE;
   if (std::isnan(temperature)) return SPEC_EINVAL;
   const bool greedy = !(temperature > 0.0f);
@@ -444,6 +456,7 @@ int spec_verify_tree(const void *target, int64_t target_req_stride, const void *
   if (tree_dynamic_smem(P) > 200 * 1024) P.stage = 0;  // very large V: re-read the slice instead
   P.c = greedy ? 1.0f : static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   P.greedy = greedy ? 1 : 0;
+  P.wor = !greedy && (flags & SPEC_TREE_SIBLINGS_WITHOUT_REPLACEMENT) ? 1 : 0;
   P.parents = parents;
   P.node_tok = node_tok;
   P.uniforms = uniforms;
@@ -454,7 +467,7 @@ int spec_verify_tree(const void *target, int64_t target_req_stride, const void *
   P.status = status;
   // the cluster kernels' 16-byte path also wants V a multiple of a group
   const cudaError_t e = launch_tree(P, vec && V % (16 / es) == 0, as_stream(stream));
-  return e == cudaSuccess ? SPEC_OK : fail_cuda(e, "spec_verify_tree");
+  return e == cudaSuccess ? SPEC_OK : fail_cuda(e, "spec_verify_tree_ex");
 }
 
 }  // extern "C"

@@ -48,6 +48,7 @@ struct TreeParams {
   int stage;       // 1: the first rejection at a node stages p and q of the slice in shared memory
   float c;         // log2(e) / T; unused when greedy
   int greedy;
+  int wor;         // siblings drawn without replacement: rejected tokens leave q
   const int32_t *parents, *node_tok;
   const float *uniforms;
   int32_t *accepted_len, *path_nodes, *out_tokens, *n_emit, *status;

@@ -30,6 +30,12 @@
 //      crossing is found from the per-rank masses already exchanged; in that
 //      CTA a scan of the per-warp masses finds the warp whose range holds
 //      it, and that warp walks its range.
+// Siblings drawn without replacement (P.wor): a rejected sibling's token is
+// also removed from q (q renormalised), since the next sibling was drawn from
+// that distribution; then c_{j+1} = c_j + Z_j / Q_j with Q_j the q mass not
+// yet removed, the acceptance test is u q(x) Z_j < max(0, p(x) - c_j q(x)) Q_j,
+// and a removed token's residual keeps the coefficient of its removal (a
+// correction per removed token, in the lane owning it).
 // Greedy mode (T <= 0): per node one argmax exchange, then the first child
 // whose token equals the argmax.
 #include <cooperative_groups.h>
@@ -123,7 +129,8 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
   float *s_uni = reinterpret_cast<float *>(dyn + 5 * N);  // [N + 1] the request's uniforms
   constexpr int EPG = Elems<DT>::kPerGroup;
   const int G = P.groups;                                 // rounds of 16-byte groups per lane
-  float *s_p = s_uni + N + 1;                             // [G * EPG * threads] staged p (stage_index)
+  float *s_kc = s_uni + N + 1;                            // [N] removed children's coefficients (P.wor)
+  float *s_p = s_kc + N;                                  // [G * EPG * threads] staged p (stage_index)
   float *s_q = s_p + static_cast<size_t>(G) * EPG * kTreeThreads;  // staged q
   __shared__ Slot s_all[2][kMaxCluster];  // [exchange parity][source rank]
   __shared__ Slot s_part[kTreeWarps];
@@ -345,19 +352,49 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
     float rmass = lane < ncl ? r.st * ex2((r.mt - Mt) * c) * iSt : 0.0f;
     float w_mass = -1.0f;  // this warp's share of it; < 0: p, from the warp's statistics
 
-    float cres = 0.0f, Z = 1.0f;
+    // the p and q of child i's token (from the children's token logits)
+    auto pq_of = [&](int i, float &pv, float &qv) {
+      pv = ex2((s_kt[i] - Mt) * c) * iSt;
+      qv = ex2((s_kd[i] - Md) * c) * iSd;
+    };
+    // the same, rounded as the sweeps over the slice round them
+    auto pq_sweep = [&](int i, float &pv, float &qv) {
+      pv = ex2(fmaf(s_kt[i], c, -Mt * c)) * iSt;
+      qv = ex2(fmaf(s_kd[i], c, -Md * c)) * iSd;
+    };
+    // Siblings drawn without replacement (P.wor): each rejected sibling's
+    // token is removed from q.  A removed token's residual keeps the
+    // coefficient it had at its removal, s_kc[i] for child i (-1: child i
+    // removed nothing); Qrem is the q mass not removed.  Every token never
+    // removed shares the coefficient cres.
+    auto removed_coef = [&](int x, int upto) {
+      float a = -1.0f;
+      for (int i = 0; i < upto; ++i)
+        if (s_kc[i] >= 0.0f && s_tok[s_kids[i]] == x) a = s_kc[i];
+      return a;
+    };
+    float cres = 0.0f, Z = 1.0f, Qrem = 1.0f;
     bool staged = false;  // s_p / s_q hold this node's slice
     int next = -1;
     for (int ki = 0; ki < nkids; ++ki) {
-      const int ch = s_kids[ki];
-      const float pt = ex2((s_kt[ki] - Mt) * c) * iSt;
-      const float qt = ex2((s_kd[ki] - Md) * c) * iSd;
-      if (s_uni[ch] * qt * Z < fmaxf(0.0f, pt - cres * qt)) {
+      const int ch = s_kids[ki], x = s_tok[ch];
+      float pt, qt;
+      pq_of(ki, pt, qt);
+      const float ax = P.wor ? removed_coef(x, ki) : -1.0f;
+      // a removed token, or every q mass removed: q_j(x) = 0, accepted iff p_j(x) > 0
+      const bool accept = ax >= 0.0f            ? pt - ax * qt > 0.0f
+                          : P.wor && !(Qrem > 0.0f) ? pt - cres * qt > 0.0f
+                                                    : s_uni[ch] * qt * Z < fmaxf(0.0f, pt - cres * qt) * Qrem;
+      if (accept) {
         next = ch;
         break;
       }
-      // rejected: next residual  max(0, p - (cres + Z) q), its mass over the cluster
-      const float cnew = cres + Z;
+      if (P.wor && !(Qrem > 0.0f)) {  // q_j has no mass left: the residual is p_j itself
+        s_kc[ki] = -1.0f;
+        continue;
+      }
+      // rejected: the next residual max(0, p - cnew q), its mass over the cluster
+      const float cnew = cres + (P.wor ? Z / Qrem : Z);
       float part = 0.0f;
       if (staged) {
         for (int j = 0; j < G; ++j) {
@@ -372,9 +409,25 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
       } else {
         part = lane_residual<DT, VEC, false>(trow, drow, lo, hi, G, Mt * c, Md * c, c, iSt, iSd, cnew, s_p, s_q);
       }
+      if (P.wor) {
+        // tokens removed earlier keep their own coefficient: the lane owning
+        // such a token's group corrects its part
+        for (int i = 0; i < ki; ++i) {
+          const int y = s_tok[s_kids[i]];
+          if (s_kc[i] < 0.0f || y < lo || y >= hi) continue;
+          const int gy = (y - lo) / EPG;
+          if (lane != (gy & 31) || warp != (gy >> 5) / G) continue;
+          float py, qy;
+          pq_sweep(i, py, qy);
+          part += fmaxf(0.0f, py - s_kc[i] * qy) - fmaxf(0.0f, py - cnew * qy);
+        }
+      }
       float zr, wz;
       const float Znew = cluster_sum(part, zr, wz);
-      if (Znew > 0.0f) {  // a zero-mass residual (rounding only) keeps the previous p
+      const bool moved = Znew > 0.0f;  // a zero-mass residual (rounding only) keeps the previous p and q
+      if (P.wor) s_kc[ki] = moved && ax < 0.0f ? cnew : -1.0f;  // (every thread writes the same value)
+      if (moved) {
+        if (P.wor && ax < 0.0f) Qrem = fmaxf(0.0f, Qrem - qt);
         cres = cnew;
         Z = Znew;
         rmass = zr;
@@ -414,17 +467,29 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
 #pragma unroll
           for (int e = 0; e < EPG; ++e)
             w[e] = fmaxf(0.0f, s_p[stage_index(g, e, EPG)] - cres * s_q[stage_index(g, e, EPG)]);
-          return;
+        } else {
+          float t[EPG];
+          unpack16<DT>(load_group<DT, VEC>(trow, lo + g * EPG, hi), t);
+#pragma unroll
+          for (int e = 0; e < EPG; ++e) w[e] = ex2(fmaf(t[e], c, -Mtc)) * iSt;
+          if (cres > 0.0f) {
+            float d[EPG];
+            unpack16<DT>(load_group<DT, VEC>(drow, lo + g * EPG, hi), d);
+#pragma unroll
+            for (int e = 0; e < EPG; ++e) w[e] = fmaxf(0.0f, w[e] - cres * (ex2(fmaf(d[e], c, -Mdc)) * iSd));
+          }
         }
-        float t[EPG];
-        unpack16<DT>(load_group<DT, VEC>(trow, lo + g * EPG, hi), t);
+        if (P.wor) {  // removed tokens keep the coefficient of their removal
+          for (int i = 0; i < nkids; ++i) {
+            const int y = s_tok[s_kids[i]] - lo - g * EPG;
+            if (s_kc[i] < 0.0f || y < 0 || y >= EPG) continue;
+            float py, qy;
+            pq_sweep(i, py, qy);
+            const float wy = fmaxf(0.0f, py - s_kc[i] * qy);
 #pragma unroll
-        for (int e = 0; e < EPG; ++e) w[e] = ex2(fmaf(t[e], c, -Mtc)) * iSt;
-        if (cres > 0.0f) {
-          float d[EPG];
-          unpack16<DT>(load_group<DT, VEC>(drow, lo + g * EPG, hi), d);
-#pragma unroll
-          for (int e = 0; e < EPG; ++e) w[e] = fmaxf(0.0f, w[e] - cres * (ex2(fmaf(d[e], c, -Mdc)) * iSd));
+            for (int e = 0; e < EPG; ++e)  // (no dynamic index into the register array)
+              if (e == y) w[e] = wy;
+          }
         }
       });
     }
@@ -448,13 +513,13 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
   }
 }
 
-// Dynamic shared memory of the walk: parents, tokens, children and the
-// children's two token logits (5 words per node), the uniforms (N + 1), plus
-// the staged p and q of the CTA's slice (every lane's groups) when staging
-// is on.
+// Dynamic shared memory of the walk: parents, tokens, children, the
+// children's two token logits and their coefficients (6 words per node), the
+// uniforms (N + 1), plus the staged p and q of the CTA's slice (every lane's
+// groups) when staging is on.
 size_t tree_dynamic_smem(const TreeParams &P) {
   const size_t epg = P.dtype == SPEC_DTYPE_F32 ? 4 : 8;
-  return sizeof(int) * (6 * static_cast<size_t>(P.N) + 1) +
+  return sizeof(int) * (7 * static_cast<size_t>(P.N) + 1) +
          (P.stage ? 2 * sizeof(float) * static_cast<size_t>(P.groups) * epg * kTreeThreads : 0);
 }
 

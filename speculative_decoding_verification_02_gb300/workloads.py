@@ -70,6 +70,17 @@ def gumbel_draw(rng, logits_row, T: float) -> int:
     return int(np.argmax(logits_as_f64(logits_row) / T - np.log(-np.log(u))))
 
 
+def gumbel_top(rng, logits_row, T: float, n: int) -> np.ndarray:
+    """n draws from softmax(logits/T) without replacement, in draw order: the
+    n largest of l/T + G (Gumbel-top-k), the largest first."""
+    if n > logits_row.shape[-1]:
+        raise ValueError("more draws without replacement than tokens")
+    u = rng.random(logits_row.shape[-1])
+    u = np.where(u <= 0.0, np.finfo(np.float64).tiny, u)
+    keys = logits_as_f64(logits_row) / T - np.log(-np.log(u))
+    return np.argsort(-keys, kind="stable")[:n].astype(np.int32)
+
+
 def uniforms(rng, shape) -> np.ndarray:
     """Caller-supplied uniforms in [0, 1), float32."""
     u = rng.random(shape, dtype=np.float32)
@@ -143,9 +154,13 @@ def random_tree(rng, N: int, depth: int, max_children: int) -> np.ndarray:
 def tree_problem(seed: int, B: int, N: int, depth: int, max_children: int, V: int,
                  dtype: str = "bf16", T: float = 1.0, target_std: float = 3.0,
                  draft_scale: float = 0.8, noise_std: float = 1.0, peaks: int = 5,
-                 peak_height: float = 8.0) -> dict:
+                 peak_height: float = 8.0, siblings: str = "iid") -> dict:
     """A tree-verification problem: per request a random tree, per node a target
-    and a draft row, child tokens drawn i.i.d. from the parent's draft q."""
+    and a draft row, child tokens drawn from the parent's draft q: i.i.d.
+    (siblings="iid"), or one after another without replacement, in id order
+    (siblings="without_replacement")."""
+    if siblings not in ("iid", "without_replacement"):
+        raise ValueError(siblings)
     r_tree, r_t, r_n, r_x, r_u, r_p = _rngs(seed, 6)
     store = np.uint16 if dtype == "bf16" else np.float32
     target = np.empty((B, N, V), dtype=store)
@@ -162,11 +177,18 @@ def tree_problem(seed: int, B: int, N: int, depth: int, max_children: int, V: in
             d = np.float32(draft_scale) * t + r_n.standard_normal(V, dtype=np.float32) * np.float32(noise_std)
             draft_logits[b, u] = _store(d, dtype)
         node_tok[b, 0] = int(r_x.integers(V))  # the last committed token
-        for c in range(1, N):
-            node_tok[b, c] = gumbel_draw(r_x, draft_logits[b, parents[b, c]], T if T > 0 else 1.0)
+        Tq = T if T > 0 else 1.0
+        if siblings == "iid":
+            for c in range(1, N):
+                node_tok[b, c] = gumbel_draw(r_x, draft_logits[b, parents[b, c]], Tq)
+        else:
+            for u in range(N):
+                kids = np.flatnonzero(parents[b] == u)
+                if kids.size:
+                    node_tok[b, kids] = gumbel_top(r_x, draft_logits[b, u], Tq, kids.size)
     return dict(target=target, draft_logits=draft_logits, parents=parents, node_tok=node_tok,
                 uniforms=uniforms(r_u, (B, N + 1)), T=float(T), B=B, N=N, V=V, depth=depth,
-                dtype=dtype)
+                dtype=dtype, siblings=siblings)
 
 
 def tree60(seed: int = SEED_BASE + 5, B: int = 16) -> dict:

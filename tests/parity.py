@@ -88,9 +88,10 @@ def check_chain_sample(prob, gpu: dict, orc: dict, draft_len=None, tol=TOL) -> d
     return dict(near_accept=near_accept, near_draw=near_draw)
 
 
-def check_tree(prob, gpu: dict, orc: dict, tol=TOL) -> dict:
+def check_tree(prob, gpu: dict, orc: dict, tol=TOL, without_replacement=False) -> dict:
     """Tree outputs must match the oracle exactly, except when a decision on the
-    oracle's own path was within tol of its fp64 threshold."""
+    oracle's own path was within tol of its fp64 threshold.  without_replacement:
+    the walk also removes each rejected sibling's token from q."""
     B, N = prob["parents"].shape
     T = prob["T"]
     near = 0
@@ -103,12 +104,12 @@ def check_tree(prob, gpu: dict, orc: dict, tol=TOL) -> dict:
         if same:
             continue
         assert T > 0, f"greedy tree walk differs on request {b}"
-        assert _tree_near_threshold(prob, b, gpu, orc, tol), f"tree request {b} differs"
+        assert _tree_near_threshold(prob, b, gpu, orc, tol, without_replacement), f"tree request {b} differs"
         near += 1
     return dict(near=near)
 
 
-def _tree_near_threshold(prob, b, gpu, orc, tol):
+def _tree_near_threshold(prob, b, gpu, orc, tol, without_replacement=False):
     """Replays the oracle's walk in fp64 up to the first divergence and checks
     that the diverging decision was within tol of its threshold."""
     par, tok, u = prob["parents"][b], prob["node_tok"][b], prob["uniforms"][b]
@@ -122,7 +123,7 @@ def _tree_near_threshold(prob, b, gpu, orc, tol):
         nxt = -1
         for c in kids:
             x = tok[c]
-            thr = min(1.0, p[x] / q[x]) if q[x] > 0 else 1.0
+            thr = min(1.0, p[x] / q[x]) if q[x] > 0 else float(p[x] > 0)
             if abs(float(u[c]) - thr) < tol:
                 return True
             if u[c] < thr:
@@ -131,6 +132,11 @@ def _tree_near_threshold(prob, b, gpu, orc, tol):
             r, R = oracle.residual(p, q)
             if R > 0:
                 p = r
+                if without_replacement:
+                    q = q.copy()
+                    q[x] = 0.0
+                    Q = q.sum()
+                    q = q / Q if Q > 0 else np.zeros_like(q)
         g_next = int(gpu["path_nodes"][b, depth + 1]) if depth + 1 < gpu["path_nodes"].shape[1] else -1
         if nxt < 0:
             a, bb = int(gpu["out_tokens"][b, depth]), int(orc["out_tokens"][b, depth])

@@ -45,6 +45,7 @@ def test_header_constants_match_binding():
     assert int(consts["SPEC_ECUDA"]) == api.SPEC_ECUDA
     assert int(consts["SPEC_DTYPE_BF16"]) == api.DTYPE_BF16
     assert int(consts["SPEC_STATUS_BAD_TREE"]) == api.STATUS_BAD_TREE
+    assert int(consts["SPEC_TREE_SIBLINGS_WITHOUT_REPLACEMENT"]) == api.TREE_SIBLINGS_WITHOUT_REPLACEMENT
     assert (int(consts["SPEC_CHAIN_AUTO"]), int(consts["SPEC_CHAIN_TWO_PASS"]), int(consts["SPEC_CHAIN_FUSED"])) == \
         (api.CHAIN_AUTO, api.CHAIN_TWO_PASS, api.CHAIN_FUSED)
 
@@ -111,6 +112,16 @@ def test_greedy_tree_ngram_argument_checks(L):
     assert tree(par=None) == api.SPEC_EINVAL
     assert tree(dt=9) == api.SPEC_EDTYPE
     assert tree(B=0) == api.SPEC_OK
+    tree_ex = lambda **kw: L.spec_verify_tree_ex(*dict(dict(t=FAKE, tr=0, d=FAKE, dr=0, r=64, dt=0, B=1, N=4, V=64,
+                                                            T=1.0, par=FAKE, tok=FAKE, u=FAKE, md=3, fl=1, al=FAKE,
+                                                            pn=FAKE, ot=FAKE, ne=FAKE, st=FAKE, ws=None, wb=0,
+                                                            s=None), **kw).values())
+    assert tree_ex(fl=2) == api.SPEC_EINVAL            # unknown flag bit
+    assert tree_ex(fl=-1) == api.SPEC_EINVAL
+    assert tree_ex(N=0) == api.SPEC_EINVAL
+    assert tree_ex(d=None) == api.SPEC_EINVAL
+    assert tree_ex(B=0) == api.SPEC_OK
+    assert tree_ex(B=0, fl=0) == api.SPEC_OK
     ng = lambda **kw: L.spec_ngram_draft(*dict(dict(h=FAKE, hl=FAKE, B=2, hs=16, w=3, k=4, d=FAKE, dl=FAKE,
                                                     st=None, s=None), **kw).values())
     assert ng(w=0) == api.SPEC_EINVAL

@@ -62,3 +62,24 @@ def test_two_rank_reductions_gloo():
         assert p.exitcode == 0
     # timing is the max over ranks, rows add up: value = sum(rows) / max(time)
     assert res == [(0, 2, 20.0, 18.0), (1, 2, 20.0, 18.0)]
+
+
+def test_clock_summary_prefers_samples_inside_the_timed_region(tmp_path):
+    import datetime
+    s = bench.ClockSampler(0)
+    s.path = str(tmp_path / "clocks.csv")
+    s.proc = object()                       # as if nvidia-smi had been started
+    t0 = datetime.datetime(2026, 1, 2, 3, 4, 5)
+    rows = [(0.0, 1500, "Not Active"), (0.2, 2070, "Not Active"), (0.4, 2055, "Active"), (0.6, 1200, "Not Active")]
+    with open(s.path, "w") as f:
+        for dt, mhz, cap in rows:
+            ts = (t0 + datetime.timedelta(seconds=dt)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+            f.write(f"0, {mhz}, 2070, 900.1, 0x4, Not Active, Not Active, Not Active, {cap}, {ts}\n")
+    base = t0.timestamp()
+    s.window = (base + 0.1, base + 0.5)
+    c = s.summary()
+    assert c["window"] == "timed region" and c["samples"] == 2
+    assert c["sm_mhz"] == 2062.5 and c["sm_max_mhz"] == 2070 and c["reasons"] == ["sw_power_cap"]
+    s.window = (base + 5.0, base + 5.1)     # a region between samples: the load around it
+    c = s.summary()
+    assert c["samples"] == 4 and c["window"].startswith("the same load")

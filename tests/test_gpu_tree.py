@@ -1,5 +1,8 @@
 """GPU parity of tree verification against the oracle (greedy: bit for bit;
-sampling: bit for bit except decisions within 1e-5 of their fp64 threshold)."""
+sampling: bit for bit except decisions within 1e-5 of their fp64 threshold),
+with the default rule and with siblings drawn without replacement
+(spec_verify_tree_ex, SPEC_TREE_SIBLINGS_WITHOUT_REPLACEMENT, against the
+oracle's without-replacement variant)."""
 import numpy as np
 import pytest
 import torch
@@ -17,22 +20,24 @@ def _built():
     __graft_entry__.build()
 
 
-def _run_tree(prob, max_depth=None, greedy=False):
+def _run_tree(prob, max_depth=None, greedy=False, wor=False):
     T = -1.0 if greedy else prob["T"]
     md = prob["depth"] if max_depth is None else max_depth
     args = (to_dev(prob["target"]), None if greedy else to_dev(prob["draft_logits"]),
             to_dev(prob["parents"]), to_dev(prob["node_tok"]), to_dev(prob["uniforms"]), T, md)
-    o = api.spec_verify_tree(*args)
+    flags = api.TREE_SIBLINGS_WITHOUT_REPLACEMENT if wor else 0
+    o = api.spec_verify_tree(*args, flags=flags)
     poison_like(o)
-    o = api.spec_verify_tree(*args, out=o)
+    o = api.spec_verify_tree(*args, flags=flags, out=o)
     torch.cuda.synchronize()
     return host(o)
 
 
-def _oracle_tree(prob, max_depth=None, greedy=False):
+def _oracle_tree(prob, max_depth=None, greedy=False, wor=False):
     return oracle.verify_tree(prob["target"], None if greedy else prob["draft_logits"], prob["parents"],
                               prob["node_tok"], prob["uniforms"], -1.0 if greedy else prob["T"],
                               prob["depth"] if max_depth is None else max_depth,
+                              variant=oracle.TREE_VARIANT_WITHOUT_REPLACEMENT if wor else oracle.VARIANT_LOSSLESS,
                               threads=oracle.max_threads())
 
 
@@ -103,3 +108,52 @@ def test_tree_bad_inputs_are_flagged():
     for b in range(1, 5):
         assert g["n_emit"][b] == 0 and np.all(g["out_tokens"][b] == -1) and np.all(g["path_nodes"][b] == -1)
     check_tree(prob, g, r)
+
+
+# ------------------------------------------------ siblings without replacement
+
+def test_tree60_without_replacement_full_size():
+    """The 16 x 60-node, V=128,256 bf16 trees with siblings drafted without
+    replacement, verified with the matching rule."""
+    prob = workloads.tree_problem(workloads.SEED_BASE + 5, 16, 60, 6, 10, 128256, "bf16", 1.0,
+                                  siblings="without_replacement")
+    g, r = _run_tree(prob, wor=True), _oracle_tree(prob, wor=True)
+    print("near-threshold", check_tree(prob, g, r, without_replacement=True), "mean accepted",
+          r["accepted_len"].mean())
+
+
+@pytest.mark.parametrize("seed,B,N,depth,kids,V,dtype,T", [
+    (11, 24, 12, 3, 4, 3000, "bf16", 1.0), (12, 24, 30, 5, 6, 20011, "fp32", 0.8),
+    (13, 30, 20, 2, 8, 17, "fp32", 1.0), (14, 12, 40, 4, 12, 70000, "bf16", 1.2),
+    (15, 40, 9, 1, 8, 10, "fp32", 0.5), (16, 10, 100, 10, 12, 8192, "bf16", 1.0)])
+def test_tree_without_replacement_parity(seed, B, N, depth, kids, V, dtype, T):
+    """Small vocabularies with many siblings remove most of q's mass; the
+    target sharpened towards one peak makes removals and rejections common."""
+    prob = workloads.tree_problem(seed, B, N, depth, kids, V, dtype, T, target_std=1.5, noise_std=1.0,
+                                  peaks=2 if V > 16 else 0, siblings="without_replacement")
+    g, r = _run_tree(prob, wor=True), _oracle_tree(prob, wor=True)
+    print("near-threshold", check_tree(prob, g, r, without_replacement=True))
+    # greedy walks ignore the flag
+    gg, rg = _run_tree(prob, greedy=True, wor=True), _oracle_tree(prob, greedy=True)
+    check_tree(dict(prob, T=-1.0), gg, rg)
+
+
+def test_without_replacement_rule_differs_from_default():
+    """Same inputs, both rules: the walks differ on some requests (the rule is
+    in effect), and each matches its own oracle variant."""
+    prob = workloads.tree_problem(17, 64, 20, 2, 8, 12, "fp32", 1.0, target_std=1.5, noise_std=1.0, peaks=0,
+                                  siblings="without_replacement")
+    g0, r0 = _run_tree(prob), _oracle_tree(prob)
+    g2, r2 = _run_tree(prob, wor=True), _oracle_tree(prob, wor=True)
+    check_tree(prob, g0, r0)
+    check_tree(prob, g2, r2, without_replacement=True)
+    assert (r0["out_tokens"] != r2["out_tokens"]).any(axis=1).sum() >= 3
+
+
+def test_without_replacement_duplicate_and_exhausted_tokens():
+    """Siblings drawn i.i.d. over V=3 repeat tokens and can remove all of q's
+    mass; the rule still applies: a removed token has q = 0 and is accepted
+    iff its residual p is positive."""
+    prob = workloads.tree_problem(18, 48, 16, 1, 15, 3, "fp32", 1.0, target_std=1.0, noise_std=1.5, peaks=0)
+    g, r = _run_tree(prob, wor=True), _oracle_tree(prob, wor=True)
+    check_tree(prob, g, r, without_replacement=True)

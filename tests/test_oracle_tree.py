@@ -226,3 +226,22 @@ def test_siblings_without_replacement_first_token_is_exactly_p(seed):
     assert np.max(np.abs(law - p)) < 6.0 * V / M
     bad = _tree_first_token_law(lp, lq, oracle.VARIANT_LOSSLESS, n=3, replace=False)
     assert np.max(np.abs(bad - p)) > 5e-3
+
+
+def test_gumbel_top_draws_without_replacement():
+    """The drafts that exercise the without-replacement rule: the first two of
+    l + G (Gumbel-top-k) follow sequential sampling without replacement,
+    P(x, y) = q(x) q(y) / (1 - q(x))."""
+    V, n = 4, 200_000
+    rng = np.random.default_rng(21)
+    l = (rng.standard_normal(V) * 1.2).astype(np.float32)
+    q = _softmax64(l)
+    pairs = np.array([workloads.gumbel_top(rng, l, 1.0, 2) for _ in range(n)])
+    assert np.all(pairs[:, 0] != pairs[:, 1])
+    freq = np.zeros((V, V))
+    np.add.at(freq, (pairs[:, 0], pairs[:, 1]), 1.0 / n)
+    law = q[:, None] * q[None, :] / (1.0 - q[:, None])
+    np.fill_diagonal(law, 0.0)
+    assert np.max(np.abs(freq - law)) < 5 * np.sqrt(0.25 / n)
+    with pytest.raises(ValueError):
+        workloads.gumbel_top(rng, l, 1.0, V + 1)
