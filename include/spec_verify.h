@@ -395,6 +395,41 @@ int64_t spec_launch_count(void);
 #define SPEC_CHAIN_GRID 3
 int spec_set_chain_path(int path);
 
+/*
+ * Host analysis helpers, for choosing the draft length k from measured
+ * acceptance ("投机解码:为什么一个字都不改", the bookkeeping section: with
+ * every position accepted independently with probability alpha a round
+ * yields (1 - alpha^(k+1)) / (1 - alpha) tokens; its experiments weigh the
+ * draft's cost c against k, and it points to Leviathan et al., appendix A.1
+ * and theorem 3.8, for the best k under that cost).  These run on the host:
+ * their pointers are HOST memory, they launch nothing and return SPEC_OK or
+ * SPEC_EINVAL (alpha outside [0, 1], k < 0, c < 0 or not finite, a null
+ * output).
+ *
+ *   spec_expected_tokens  *out = 1 + alpha + ... + alpha^k, the expected
+ *                         tokens per round (k + 1 at alpha = 1).
+ *   spec_speedup          *out = expected tokens / (k c + 1): a round costs
+ *                         k draft forwards of c target forwards each plus
+ *                         one target forward (the verify step's own time is
+ *                         not counted).
+ *   spec_best_k           the k in [0, k_max] with the largest speedup
+ *                         (k = 0: plain decoding, speedup 1; ties keep the
+ *                         smaller k), and that speedup (speedup_out may be
+ *                         NULL).
+ *   spec_alpha_estimate   alpha from n observed rounds: accepted[r] (the m a
+ *                         verify call returned) and draft_len[r] (NULL: all
+ *                         k).  A round tested m + 1 positions when m < L and
+ *                         m when m = L, m of them accepted; the estimate is
+ *                         sum(m) / sum(tested), NaN when nothing was tested.
+ *                         *tests_out (may be NULL) = sum(tested).
+ *                         SPEC_EINVAL also when some m > L or L < 0.
+ */
+int spec_expected_tokens(double alpha, int k, double *out);
+int spec_speedup(double alpha, int k, double draft_cost, double *out);
+int spec_best_k(double alpha, double draft_cost, int k_max, int *k_out, double *speedup_out);
+int spec_alpha_estimate(const int32_t *accepted, const int32_t *draft_len, int n, int k, double *alpha_out,
+                        int64_t *tests_out);
+
 #ifdef __cplusplus
 }
 #endif

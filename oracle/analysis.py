@@ -1,6 +1,6 @@
 """Host-side helpers of the oracle (plain Python) -- TEST INFRASTRUCTURE.
 
-These restate the pages' bookkeeping and the closed form; they never touch
+These restate the pages' bookkeeping, the closed form and the choice of k; they never touch
 logits.  The decode loop takes its drafter and verifier as callables so the
 same host loop can drive the oracle and, in the GPU tests, the library.
 """
@@ -63,3 +63,33 @@ def speculative_generate(next_logits: Callable[[list], np.ndarray], prompt: Sequ
         accepted.append(len(emitted) - 1)
         out.extend(emitted)
     return out[len(prompt):len(prompt) + n_new], accepted
+
+
+def speedup(alpha: float, k: int, draft_cost: float) -> float:
+    """Walltime speedup of speculative decoding over plain decoding when one
+    draft forward costs `draft_cost` target forwards: a round runs k draft
+    forwards and one target forward and yields the expected tokens per round
+    ("投机解码:为什么一个字都不改", the bookkeeping experiments weighing the
+    draft's cost against k)."""
+    return expected_tokens_per_round(alpha, k) / (k * draft_cost + 1.0)
+
+
+def best_k(alpha: float, draft_cost: float, k_max: int):
+    """The draft length in 0..k_max with the largest speedup, by trying each
+    (k = 0 is plain decoding, speedup 1; a tie keeps the smaller k)."""
+    best, best_s = 0, 1.0
+    for k in range(1, k_max + 1):
+        s = speedup(alpha, k, draft_cost)
+        if s > best_s:
+            best, best_s = k, s
+    return best, best_s
+
+
+def alpha_estimate(accepted: Sequence[int], draft_len: Sequence[int] | None = None, k: int = 0):
+    """Acceptance rate from observed rounds: a round that accepted m of L
+    drafted tokens tested m + 1 positions if m < L (the last one rejected)
+    and L if m = L; alpha = accepted positions / tested positions."""
+    lens = [k] * len(accepted) if draft_len is None else list(draft_len)
+    acc = sum(int(m) for m in accepted)
+    tests = sum(int(m) + (1 if int(m) < int(L) else 0) for m, L in zip(accepted, lens))
+    return (acc / tests if tests else float("nan")), tests

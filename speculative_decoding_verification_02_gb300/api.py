@@ -67,6 +67,11 @@ def lib():
         L.spec_set_chain_path.argtypes = [I]
         L.spec_tree_rerank.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, P, P, P]
         L.spec_sample.argtypes = [P, I64, I, I, I, F, P, P, P, P, P, Z, P]
+        D = ctypes.c_double
+        L.spec_expected_tokens.argtypes = [D, I, P]
+        L.spec_speedup.argtypes = [D, I, D, P]
+        L.spec_best_k.argtypes = [D, D, I, P, P]
+        L.spec_alpha_estimate.argtypes = [P, P, I, I, P, P]
         _lib = L
         return L
 
@@ -390,3 +395,45 @@ def spec_verify_sample_noalloc(target: torch.Tensor, draft_logits: torch.Tensor,
             _p(o.get("q_tok")), _p(o.get("resid_mass")), _p(o["status"]), _stream(stream, dev))
     _check(rc, "spec_verify_sample_noalloc")
     return o
+
+
+# ------------------------------------------------------- host analysis helpers
+# Host-side (no GPU): the choice of the draft length from measured acceptance.
+
+def expected_tokens(alpha: float, k: int) -> float:
+    """Expected tokens per round, 1 + alpha + ... + alpha^k."""
+    out = ctypes.c_double()
+    _check(lib().spec_expected_tokens(float(alpha), int(k), ctypes.byref(out)), "spec_expected_tokens")
+    return out.value
+
+
+def speedup(alpha: float, k: int, draft_cost: float) -> float:
+    """Expected tokens per round over the round's cost k c + 1 (in target forwards)."""
+    out = ctypes.c_double()
+    _check(lib().spec_speedup(float(alpha), int(k), float(draft_cost), ctypes.byref(out)), "spec_speedup")
+    return out.value
+
+
+def best_k(alpha: float, draft_cost: float, k_max: int) -> tuple:
+    """(k in [0, k_max] with the largest speedup, that speedup)."""
+    k = ctypes.c_int()
+    s = ctypes.c_double()
+    _check(lib().spec_best_k(float(alpha), float(draft_cost), int(k_max), ctypes.byref(k), ctypes.byref(s)),
+           "spec_best_k")
+    return k.value, s.value
+
+
+def alpha_estimate(accepted, draft_len=None, k: int = 0) -> tuple:
+    """(alpha, positions tested) from rounds' accepted counts (host arrays or
+    tensors, copied to the host) and draft lengths (None: all k)."""
+    import numpy as np
+    acc = np.ascontiguousarray(torch.as_tensor(accepted).cpu().numpy(), dtype=np.int32).reshape(-1)
+    dl = None if draft_len is None else np.ascontiguousarray(torch.as_tensor(draft_len).cpu().numpy(),
+                                                             dtype=np.int32).reshape(-1)
+    if dl is not None and dl.size != acc.size:
+        raise ValueError("draft_len must match accepted")
+    a = ctypes.c_double()
+    t = ctypes.c_int64()
+    _check(lib().spec_alpha_estimate(acc.ctypes.data, None if dl is None else dl.ctypes.data, acc.size, int(k),
+                                     ctypes.byref(a), ctypes.byref(t)), "spec_alpha_estimate")
+    return a.value, t.value
