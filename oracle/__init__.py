@@ -57,8 +57,9 @@ def _load():
         lib.orc_residual.restype = D
         lib.orc_ngram_draft.argtypes = [P, P, I, I, I, I, P, P, P]
         lib.orc_verify_greedy.argtypes = [P, I, I, I, I, I64, I64, P, P, P, P, P, P, P]
-        lib.orc_verify_sample.argtypes = [P, I64, P, I64, I64, I, I, I, I, D, P, P, P, P,
+        lib.orc_verify_sample.argtypes = [P, I64, P, I64, I64, I, I, I, I, D, I, D, P, P, P, P,
                                           P, P, P, P, P, P, P, I, I, P]
+        lib.orc_filter_row.argtypes = [P, I, I, D, I, D, P, P, P]
         lib.orc_verify_tree.argtypes = [P, I64, P, I64, I64, I, I, I, I, D, P, P, P, I,
                                         P, P, P, P, P, I, I, P]
         lib.orc_tree_rerank.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, P, P]
@@ -178,12 +179,14 @@ def verify_greedy(target, draft, draft_len=None, max_emit=None):
 
 
 def verify_sample(target, draft_logits, draft, uniforms, T: float = 1.0, draft_len=None,
-                  max_emit=None, variant: int = VARIANT_LOSSLESS, threads: int = 1):
+                  max_emit=None, variant: int = VARIANT_LOSSLESS, threads: int = 1, top_k: int = 0,
+                  top_p: float = 1.0):
     """Sampling chain verification.
 
     target: [B, k+1, V], draft_logits: [B, k, V] (fp32 or bf16 bits; request
     strides may be 0 to broadcast one problem), draft: [B, k] int32,
-    uniforms: [B, k+1] float32.
+    uniforms: [B, k+1] float32.  top_k / top_p filter p and q alike before
+    verification (0 / 1.0: off; see filter_row).
     """
     target, code = _logits(target)
     draft_logits, code_d = _logits(draft_logits)
@@ -208,13 +211,30 @@ def verify_sample(target, draft_logits, draft, uniforms, T: float = 1.0, draft_l
                resid_mass=np.empty(B), status=np.empty(B, np.int32))
     degen = np.zeros(1, dtype=np.int64)
     _check(_load().orc_verify_sample(
-        _ptr(target), t_req, _ptr(draft_logits), d_req, row, code, B, k, V, float(T),
+        _ptr(target), t_req, _ptr(draft_logits), d_req, row, code, B, k, V, float(T), int(top_k), float(top_p),
         _ptr(draft), _ptr(_i32(draft_len, (B,))), _ptr(_i32(max_emit, (B,))), _ptr(uniforms),
         _ptr(out["accepted"]), _ptr(out["out_tokens"]), _ptr(out["n_emit"]),
         _ptr(out["p_tok"]), _ptr(out["q_tok"]), _ptr(out["resid_mass"]), _ptr(out["status"]),
         int(variant), int(threads), _ptr(degen)), "verify_sample")
     out["degenerate"] = int(degen[0])
     return out
+
+
+def filter_row(row, T: float = 1.0, top_k: int = 0, top_p: float = 1.0):
+    """Top-k then top-p filtering of one logit row (fp32 or bf16 bits), in
+    fp64: (p' [V] float64, theta = the smallest kept logit, kept count).
+    top_k keeps every logit >= the top_k-th largest; top_p then keeps, over
+    those renormalised, the smallest descending prefix whose mass reaches
+    top_p, ties at its last logit included."""
+    row, code = _logits(row)
+    row = np.ascontiguousarray(row).reshape(-1)
+    V = row.size
+    p = np.empty(V)
+    theta = ctypes.c_double()
+    kept = ctypes.c_int32()
+    _check(_load().orc_filter_row(_ptr(row), code, V, float(T), int(top_k), float(top_p), _ptr(p),
+                                  ctypes.byref(theta), ctypes.byref(kept)), "filter_row")
+    return p, theta.value, kept.value
 
 
 def verify_tree(target, draft_logits, parents, node_tok, uniforms, T: float, max_depth: int,

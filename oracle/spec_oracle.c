@@ -109,6 +109,104 @@ static void softmax_row(const void *row, int dtype, int V, double T, double *p)
         p[v] /= S;
 }
 
+/* ------------------------------------------------- top-k / top-p filtering
+ *
+ * A sampling variant the pages defer to another lesson ("投机解码", the
+ * section that sets temperature, top-k and top-p aside): verification stays
+ * lossless against the FILTERED target when both p and q are filtered the
+ * same way and the drafter drew from the filtered q.  The plainest reading,
+ * applied in this order:
+ *   1. p = softmax(x / T);
+ *   2. top-k (0 < top_k < V): theta_k = the top_k-th largest logit (counting
+ *      repeats); keep every v with x_v >= theta_k (ties at the cut stay);
+ *   3. top-p (top_p < 1): over the kept tokens in descending logit order,
+ *      with p renormalised to them, the smallest prefix whose mass reaches
+ *      top_p; theta_p = the logit of its last token; keep every kept v with
+ *      x_v >= theta_p;
+ *   4. p' = p renormalised over the kept tokens, 0 elsewhere.
+ * theta = the smallest kept logit.  top_k <= 0 or >= V, and top_p >= 1,
+ * switch their filter off. */
+
+typedef struct {
+    double x;
+    int v;
+} orc_keyed;
+
+static int keyed_desc(const void *pa, const void *pb)
+{
+    const orc_keyed *a = pa, *b = pb;
+    if (a->x != b->x)
+        return a->x > b->x ? -1 : 1;
+    return a->v < b->v ? -1 : (a->v > b->v);
+}
+
+/* p' of one row (written to p), the threshold logit and the kept count. */
+static int filter_row(const void *row, int dtype, int V, double T, int top_k, double top_p,
+                      double *p, double *theta_out, int *kept_out)
+{
+    softmax_row(row, dtype, V, T, p);
+    double theta = -INFINITY;
+    int use_k = top_k > 0 && top_k < V, use_p = top_p < 1.0;
+    if (use_k || use_p) {
+        orc_keyed *ord = malloc(sizeof(orc_keyed) * (size_t)V);
+        if (!ord)
+            return ORC_ENOMEM;
+        for (int v = 0; v < V; ++v) {
+            ord[v].x = logit_at(row, dtype, v);
+            ord[v].v = v;
+        }
+        qsort(ord, (size_t)V, sizeof *ord, keyed_desc);
+        int n = V; /* kept tokens form the prefix ord[0..n) */
+        if (use_k) {
+            theta = ord[top_k - 1].x;
+            n = top_k;
+            while (n < V && ord[n].x >= theta)
+                ++n;
+        }
+        if (use_p) {
+            double SK = 0.0, cum = 0.0;
+            for (int j = 0; j < n; ++j)
+                SK += p[ord[j].v];
+            int j = 0;
+            for (; j < n; ++j) {
+                cum += p[ord[j].v] / SK;
+                if (cum >= top_p)
+                    break;
+            }
+            if (j == n) /* rounding: the mass never reached top_p, keep all */
+                j = n - 1;
+            if (ord[j].x > theta)
+                theta = ord[j].x;
+        }
+        free(ord);
+    }
+    double S = 0.0;
+    int kept = 0;
+    for (int v = 0; v < V; ++v) {
+        if (logit_at(row, dtype, v) >= theta) {
+            S += p[v];
+            ++kept;
+        } else {
+            p[v] = 0.0;
+        }
+    }
+    for (int v = 0; v < V; ++v)
+        p[v] /= S;
+    if (theta == -INFINITY) {
+        theta = INFINITY; /* no filter: the smallest logit */
+        for (int v = 0; v < V; ++v) {
+            double x = logit_at(row, dtype, v);
+            if (x < theta)
+                theta = x;
+        }
+    }
+    if (theta_out)
+        *theta_out = theta;
+    if (kept_out)
+        *kept_out = kept;
+    return ORC_OK;
+}
+
 /* Index of the largest logit; ties go to the lowest index. */
 static int argmax_row(const void *row, int dtype, int V)
 {
@@ -310,9 +408,21 @@ int orc_verify_greedy(const void *target, int dtype, int B, int k, int V,
  * i < draft_len (else -1); resid_mass [B] = sum max(0, p_m - q_m) at the
  * rejected position (0 when every draft token was accepted).
  * degenerate (may be NULL): incremented once per zero-mass residual. */
+int orc_filter_row(const void *row, int dtype, int V, double T, int top_k, double top_p,
+                   double *p, double *theta, int32_t *kept)
+{
+    if (!row || !p || V <= 0 || !(T > 0.0) || (dtype != 0 && dtype != 1) || !(top_p > 0.0))
+        return ORC_EINVAL;
+    int n = 0;
+    int rc = filter_row(row, dtype, V, T, top_k, top_p, p, theta, &n);
+    if (kept)
+        *kept = n;
+    return rc;
+}
+
 int orc_verify_sample(const void *target, int64_t t_req, const void *draft_logits,
                       int64_t d_req, int64_t row, int dtype, int B, int k, int V,
-                      double T, const int32_t *draft, const int32_t *draft_len,
+                      double T, int top_k, double top_p, const int32_t *draft, const int32_t *draft_len,
                       const int32_t *max_emit, const float *uniforms,
                       int32_t *accepted, int32_t *out_tokens, int32_t *n_emit,
                       double *p_tok, double *q_tok, double *resid_mass,
@@ -320,7 +430,7 @@ int orc_verify_sample(const void *target, int64_t t_req, const void *draft_logit
                       int64_t *degenerate)
 {
     if (!target || !draft_logits || B < 0 || k < 0 || V <= 0 || !(T > 0.0) ||
-        (dtype != 0 && dtype != 1) || variant < 0 || variant > 2)
+        (dtype != 0 && dtype != 1) || variant < 0 || variant > 2 || !(top_p > 0.0))
         return ORC_EINVAL;
     const size_t es = dtype == 0 ? 4 : 2;
     int64_t degen = 0;
@@ -373,8 +483,8 @@ int orc_verify_sample(const void *target, int64_t t_req, const void *draft_logit
 
         /* the per-position probabilities of the drafted tokens */
         for (int i = 0; i < L; ++i) {
-            softmax_row(tb + (int64_t)i * row * es, dtype, V, T, p);
-            softmax_row(db + (int64_t)i * row * es, dtype, V, T, q);
+            fail |= filter_row(tb + (int64_t)i * row * es, dtype, V, T, top_k, top_p, p, NULL, NULL);
+            fail |= filter_row(db + (int64_t)i * row * es, dtype, V, T, top_k, top_p, q, NULL, NULL);
             if (p_tok)
                 p_tok[(int64_t)b * k + i] = p[x[i]];
             if (q_tok)
@@ -384,12 +494,12 @@ int orc_verify_sample(const void *target, int64_t t_req, const void *draft_logit
         /* left to right: accept, or stop at the first rejection */
         int m = 0, final_tok = -1;
         for (; m < L; ++m) {
-            softmax_row(tb + (int64_t)m * row * es, dtype, V, T, p);
+            fail |= filter_row(tb + (int64_t)m * row * es, dtype, V, T, top_k, top_p, p, NULL, NULL);
             int acc;
             if (variant == 2) {
                 acc = inverse_cdf(p, V, (double)u[m]) == x[m];
             } else {
-                softmax_row(db + (int64_t)m * row * es, dtype, V, T, q);
+                fail |= filter_row(db + (int64_t)m * row * es, dtype, V, T, top_k, top_p, q, NULL, NULL);
                 acc = accept_test((double)u[m], p[x[m]], q[x[m]]);
             }
             if (!acc)
@@ -414,7 +524,7 @@ int orc_verify_sample(const void *target, int64_t t_req, const void *draft_logit
             }
         } else {
             /* all L accepted: the bonus token comes from p_L */
-            softmax_row(tb + (int64_t)L * row * es, dtype, V, T, p);
+            fail |= filter_row(tb + (int64_t)L * row * es, dtype, V, T, top_k, top_p, p, NULL, NULL);
             final_tok = inverse_cdf(p, V, (double)u[k]);
         }
         int cap = max_emit ? max_emit[b] : k + 1;
