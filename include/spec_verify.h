@@ -79,6 +79,7 @@ extern "C" {
 #define SPEC_OP_SAMPLE 2
 #define SPEC_OP_TREE 3
 #define SPEC_OP_DRAW 4
+#define SPEC_OP_FILTER 5 /* spec_filter_rows: B = rows */
 
 /* Limits checked on the host. */
 #define SPEC_MAX_K 64        /* draft length of a chain */
@@ -294,6 +295,55 @@ int spec_verify_sample_noalloc(const void *target, int64_t target_req_stride,
 int spec_sample(const void *logits, int64_t req_stride, int dtype, int B, int V, float temperature,
                 const float *uniforms, int32_t *tokens, float *probs, int32_t *status, void *workspace,
                 size_t workspace_bytes, void *stream);
+
+/*
+ * Top-k / top-p filtered sampling.  The pages leave temperature, top-k and
+ * top-p to another lesson ("投机解码:为什么一个字都不改", the section that sets
+ * them aside); verification stays lossless against the FILTERED target when
+ * the target's and the draft's distributions are filtered alike and the
+ * drafter drew from the filtered q.  The filter of one row, in this order:
+ *   p = softmax(x / T);
+ *   top_k (0 < top_k < V): keep every v whose logit is >= the top_k-th
+ *     largest logit (repeats counted; ties at the cut are all kept);
+ *   top_p (top_p < 1): over the kept logits in descending order, with p
+ *     renormalised to them, keep the smallest prefix whose mass reaches
+ *     top_p, and every logit equal to its last one;
+ *   p' = p renormalised over the kept logits, 0 elsewhere.
+ * top_k = 0 (or >= V) and top_p = 1 switch a filter off; top_k < 0, or
+ * top_p outside (0, 1], is SPEC_EINVAL.  A kept set is always {v : x_v >=
+ * theta} for one threshold theta, the smallest kept logit.  Rows of more
+ * than 16 x 96 KB of logits (V > 786,432 bf16 or 393,216 fp32) are
+ * SPEC_EINVAL.  The top-p cut adds masses in 2^-44 fixed point, so it is
+ * the same on every run; against exact arithmetic it can differ only where
+ * the mass at the cut is within about 1e-7 of top_p.
+ *
+ * spec_verify_sample_topkp -- spec_verify_sample with p and q filtered: the
+ *   acceptance test, p_tok / q_tok, the residual and the bonus draw all use
+ *   p' and q'.  A drafted token that q' excludes has q'(x) = 0 and is
+ *   accepted iff p'(x) > 0.  Same arguments and workspace
+ *   (SPEC_OP_SAMPLE) as spec_verify_sample, plus top_k and top_p.  With
+ *   both filters off it is spec_verify_sample.
+ * spec_sample_topkp -- spec_sample from the filtered rows (the drafter's
+ *   draw from q'); probs gets q'(x).  Workspace as spec_sample.
+ * spec_filter_rows -- the filter alone, for R rows of V logits (row r at
+ *   r * row_stride): theta fp32 [R] (the smallest kept logit; with both
+ *   filters off, the smallest logit) and kept int32 [R] or NULL (the kept
+ *   count).  workspace: spec_workspace_size(SPEC_OP_FILTER, R, 0, V, dtype)
+ *   bytes.
+ */
+int spec_verify_sample_topkp(const void *target, int64_t target_req_stride, const void *draft_logits,
+                             int64_t draft_req_stride, int64_t row_stride, int dtype, int B, int k, int V,
+                             float temperature, int top_k, float top_p, const int32_t *draft,
+                             const int32_t *draft_len, const int32_t *max_emit, const float *uniforms,
+                             int32_t *accepted, int32_t *out_tokens, int32_t *n_emit, float *p_tok, float *q_tok,
+                             float *resid_mass, int32_t *status, void *workspace, size_t workspace_bytes,
+                             void *stream);
+int spec_sample_topkp(const void *logits, int64_t req_stride, int dtype, int B, int V, float temperature,
+                      int top_k, float top_p, const float *uniforms, int32_t *tokens, float *probs,
+                      int32_t *status, void *workspace, size_t workspace_bytes, void *stream);
+int spec_filter_rows(const void *logits, int64_t row_stride, int dtype, int R, int V, float temperature, int top_k,
+                     float top_p, float *theta, int32_t *kept, void *workspace, size_t workspace_bytes,
+                     void *stream);
 
 /*
  * spec_tree_rerank -- EAGLE-2 post-processing of candidate draft trees.

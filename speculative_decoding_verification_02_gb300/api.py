@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libspecverify.so")
 SPEC_OK, SPEC_EINVAL, SPEC_EDTYPE, SPEC_EWORKSPACE, SPEC_ECUDA = 0, -1, -2, -3, -4
 STATUS_OK, STATUS_TOKEN_RANGE, STATUS_BAD_TREE, STATUS_BAD_LENGTH, STATUS_SYNC_TIMEOUT = 0, 1, 2, 3, 4
 DTYPE_F32, DTYPE_BF16 = 0, 1
-OP_NGRAM, OP_GREEDY, OP_SAMPLE, OP_TREE, OP_DRAW = 0, 1, 2, 3, 4
+OP_NGRAM, OP_GREEDY, OP_SAMPLE, OP_TREE, OP_DRAW, OP_FILTER = 0, 1, 2, 3, 4, 5
 CHAIN_AUTO, CHAIN_TWO_PASS, CHAIN_FUSED, CHAIN_GRID = 0, 1, 2, 3
 TREE_SIBLINGS_WITHOUT_REPLACEMENT = 1
 
@@ -67,6 +67,10 @@ def lib():
         L.spec_set_chain_path.argtypes = [I]
         L.spec_tree_rerank.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, P, P, P]
         L.spec_sample.argtypes = [P, I64, I, I, I, F, P, P, P, P, P, Z, P]
+        L.spec_verify_sample_topkp.argtypes = [P, I64, P, I64, I64, I, I, I, I, F, I, F, P, P, P, P, P, P, P, P,
+                                               P, P, P, P, Z, P]
+        L.spec_sample_topkp.argtypes = [P, I64, I, I, I, F, I, F, P, P, P, P, P, Z, P]
+        L.spec_filter_rows.argtypes = [P, I64, I, I, I, F, I, F, P, P, P, Z, P]
         D = ctypes.c_double
         L.spec_expected_tokens.argtypes = [D, I, P]
         L.spec_speedup.argtypes = [D, I, D, P]
@@ -224,9 +228,11 @@ def spec_verify_greedy(target: torch.Tensor, draft: torch.Tensor, draft_len=None
 
 def spec_verify_sample(target: torch.Tensor, draft_logits: torch.Tensor, draft: torch.Tensor,
                        uniforms: torch.Tensor, temperature: float = 1.0, draft_len=None,
-                       max_emit=None, *, probs: bool = True, out=None, ws=None, stream=None) -> dict:
+                       max_emit=None, *, probs: bool = True, top_k: int = 0, top_p: float = 1.0, out=None,
+                       ws=None, stream=None) -> dict:
     """target [B, k+1, V], draft_logits [B, k, V] (same dtype), draft int32 [B, k],
-    uniforms fp32 [B, k+1] -> accepted, out_tokens, n_emit, p_tok, q_tok, resid_mass, status."""
+    uniforms fp32 [B, k+1] -> accepted, out_tokens, n_emit, p_tok, q_tok, resid_mass, status.
+    top_k / top_p (0 / 1.0: off) filter p and q alike (spec_verify_sample_topkp)."""
     target = _logits3(target, "target")
     draft_logits = _logits3(draft_logits, "draft_logits")
     dev = target.device
@@ -253,13 +259,15 @@ def spec_verify_sample(target: torch.Tensor, draft_logits: torch.Tensor, draft: 
             o.update(p_tok=torch.empty((B, k), dtype=torch.float32, device=dev),
                      q_tok=torch.empty((B, k), dtype=torch.float32, device=dev),
                      resid_mass=torch.empty(B, dtype=torch.float32, device=dev))
-    rc = lib().spec_verify_sample(_p(target), target.stride(0), _p(draft_logits), draft_logits.stride(0),
-                                  target.stride(1), dt, B, k, V, float(temperature), _p(draft),
-                                  _p(draft_len), _p(max_emit), _p(uniforms), _p(o["accepted"]),
-                                  _p(o["out_tokens"]), _p(o["n_emit"]), _p(o.get("p_tok")),
-                                  _p(o.get("q_tok")), _p(o.get("resid_mass")), _p(o["status"]),
-                                  _p(ws), ws.numel(), _stream(stream, dev))
-    _check(rc, "spec_verify_sample")
+    head = (_p(target), target.stride(0), _p(draft_logits), draft_logits.stride(0), target.stride(1), dt, B, k, V,
+            float(temperature))
+    tail = (_p(draft), _p(draft_len), _p(max_emit), _p(uniforms), _p(o["accepted"]), _p(o["out_tokens"]),
+            _p(o["n_emit"]), _p(o.get("p_tok")), _p(o.get("q_tok")), _p(o.get("resid_mass")), _p(o["status"]),
+            _p(ws), ws.numel(), _stream(stream, dev))
+    if top_k or top_p != 1.0:
+        _check(lib().spec_verify_sample_topkp(*head, int(top_k), float(top_p), *tail), "spec_verify_sample_topkp")
+    else:
+        _check(lib().spec_verify_sample(*head, *tail), "spec_verify_sample")
     return o
 
 
@@ -305,10 +313,11 @@ def spec_verify_tree(target: torch.Tensor, draft_logits, parents: torch.Tensor, 
 
 
 def spec_sample(logits: torch.Tensor, uniforms: torch.Tensor, temperature: float = 1.0, *, probs: bool = True,
-                out=None, ws=None, stream=None) -> dict:
+                top_k: int = 0, top_p: float = 1.0, out=None, ws=None, stream=None) -> dict:
     """logits [B, V] (fp32 or bf16, each row contiguous), uniforms fp32 [B]
     -> tokens int32 [B] drawn from softmax(logits / T), probs fp32 [B] (the
-    drawn tokens' probabilities), status."""
+    drawn tokens' probabilities), status.  top_k / top_p (0 / 1.0: off):
+    draw from the filtered rows (spec_sample_topkp)."""
     if not isinstance(logits, torch.Tensor) or logits.dim() != 2:
         raise ValueError("logits must be a [B, V] tensor")
     if logits.dtype not in (torch.float32, torch.bfloat16):
@@ -324,10 +333,36 @@ def spec_sample(logits: torch.Tensor, uniforms: torch.Tensor, temperature: float
     o = out or dict(tokens=torch.empty(B, dtype=torch.int32, device=dev),
                     probs=torch.empty(B, dtype=torch.float32, device=dev) if probs else None,
                     status=torch.empty(B, dtype=torch.int32, device=dev))
-    rc = lib().spec_sample(_p(logits), logits.stride(0), dt, B, V, float(temperature), _p(uniforms),
-                           _p(o["tokens"]), _p(o.get("probs")), _p(o["status"]), _p(ws), ws.numel(),
-                           _stream(stream, dev))
-    _check(rc, "spec_sample")
+    tail = (_p(uniforms), _p(o["tokens"]), _p(o.get("probs")), _p(o["status"]), _p(ws), ws.numel(),
+            _stream(stream, dev))
+    if top_k or top_p != 1.0:
+        rc = lib().spec_sample_topkp(_p(logits), logits.stride(0), dt, B, V, float(temperature), int(top_k),
+                                     float(top_p), *tail)
+        _check(rc, "spec_sample_topkp")
+    else:
+        _check(lib().spec_sample(_p(logits), logits.stride(0), dt, B, V, float(temperature), *tail), "spec_sample")
+    return o
+
+
+def spec_filter_rows(logits: torch.Tensor, temperature: float = 1.0, top_k: int = 0, top_p: float = 1.0, *,
+                     out=None, stream=None) -> dict:
+    """logits [R, V] (fp32 or bf16, each row contiguous) -> theta fp32 [R]
+    (the smallest logit the top-k / top-p filter keeps) and kept int32 [R]."""
+    if not isinstance(logits, torch.Tensor) or logits.dim() != 2:
+        raise ValueError("logits must be a [R, V] tensor")
+    if logits.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("logits must be float32 or bfloat16")
+    if logits.stride(1) != 1:
+        logits = logits.contiguous()
+    dev = logits.device
+    R, V = logits.shape
+    dt = _dtype_code(logits)
+    ws = workspace(spec_workspace_size(OP_FILTER, R, 0, V, dt), dev, stream)
+    o = out or dict(theta=torch.empty(R, dtype=torch.float32, device=dev),
+                    kept=torch.empty(R, dtype=torch.int32, device=dev))
+    _check(lib().spec_filter_rows(_p(logits), logits.stride(0), dt, R, V, float(temperature), int(top_k),
+                                  float(top_p), _p(o["theta"]), _p(o.get("kept")), _p(ws), ws.numel(),
+                                  _stream(stream, dev)), "spec_filter_rows")
     return o
 
 

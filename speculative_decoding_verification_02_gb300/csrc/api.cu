@@ -79,7 +79,7 @@ int sub_chunk(int dtype) { return 256 * (16 / elem_size(dtype)); }
 // path.
 struct ChainLayout {
   int nc, chunk, nc2, chunk2, nsub;
-  size_t sync, part, part2, counter2, total;
+  size_t sync, part, part2, counter2, theta, total;
 };
 
 ChainLayout chain_layout(bool sample, int B, int k, int V, int dtype) {
@@ -103,6 +103,8 @@ ChainLayout chain_layout(bool sample, int B, int k, int V, int dtype) {
   off = round_up(off + sizeof(float) * std::max(sample ? B * static_cast<size_t>(L.nsub) : 0, grid_mass), 256);
   L.counter2 = off;
   off = round_up(off + (sample ? sizeof(int) * B : 0), 256);
+  L.theta = off;  // top-k / top-p: each row's threshold
+  off = round_up(off + (sample ? sizeof(float) * B * rows : 0), 256);
   L.total = off;
   return L;
 }
@@ -221,6 +223,7 @@ size_t spec_workspace_size(int op, int B, int rows_per_req, int V, int dtype) {
     case SPEC_OP_GREEDY: return chain_layout(false, B, rows_per_req, V, dtype).total;
     case SPEC_OP_SAMPLE: return chain_layout(true, B, rows_per_req, V, dtype).total;
     case SPEC_OP_DRAW: return draw_workspace(B, V, dtype);
+    case SPEC_OP_FILTER: return round_up(sizeof(Partial) * static_cast<size_t>(B), 256);
     default: return 0;  // n-gram and tree walks need no workspace
   }
 }
@@ -323,11 +326,13 @@ static int chain_common(bool sample, const void *target, int64_t t_req, const vo
                         const float *uniforms, int32_t *accepted, int32_t *out_tokens,
                         int32_t *n_emit, float *p_tok, float *q_tok, float *resid_mass,
                         int32_t *status, void *workspace, size_t workspace_bytes, void *stream,
-                        float *final_prob = nullptr) {
+                        float *final_prob = nullptr, int top_k = 0, float top_p = 1.0f) {
   if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_EDTYPE;
   if (B < 0 || k < 0 || k > SPEC_MAX_K || V <= 0 || t_req < 0 || d_req < 0 || row < 0)
     return SPEC_EINVAL;
   if (sample && !(T > 0.0f && std::isfinite(T))) return SPEC_EINVAL;
+  if (top_k < 0 || !(top_p > 0.0f && top_p <= 1.0f)) return SPEC_EINVAL;
+  const bool filtered = sample && ((top_k > 0 && top_k < V) || top_p < 1.0f);
   if (B == 0) return SPEC_OK;
   if (!target || !accepted || !out_tokens || !n_emit || (k > 0 && !draft)) return SPEC_EINVAL;
   if (sample && (!uniforms || (k > 0 && !draftl))) return SPEC_EINVAL;
@@ -380,7 +385,22 @@ static int chain_common(bool sample, const void *target, int64_t t_req, const vo
   const int path = g_chain_path.load(std::memory_order_relaxed);
   const bool want_grid = path == SPEC_CHAIN_GRID || (path == SPEC_CHAIN_AUTO && kGridAuto);
   const bool want_fused = path == SPEC_CHAIN_FUSED || (path == SPEC_CHAIN_AUTO && V <= kFusedAutoMaxV);
-  if (want_grid && chain_grid_plan(P, sample, fvec)) {
+  if (filtered) {
+    // the filter kernel replaces the streaming pass: one partial per row
+    // (statistics over the kept logits) and each row's threshold, then the
+    // accept kernel with the thresholds as masks
+    P.top_k = top_k;
+    P.top_p = top_p;
+    P.theta = reinterpret_cast<float *>(ws + L.theta);
+    P.nc = 1;
+    P.chunk = V;
+    if (!chain_filter_plan(P)) return SPEC_EINVAL;  // a row longer than 16 slices of 96 KB
+    e = launch_chain_filter(P, fvec, as_stream(stream));
+    if (e == cudaSuccess) {
+      if (!chain_accept_plan(P, fvec)) P.cluster = 0;
+      e = launch_chain(P, true, vec, fvec, as_stream(stream), false);
+    }
+  } else if (want_grid && chain_grid_plan(P, sample, fvec)) {
     e = ensure_sync_zero(ws + L.sync, as_stream(stream));
     if (e == cudaSuccess) e = launch_chain_grid(P, sample, fvec, as_stream(stream));
   } else if (want_fused && chain_fused_plan(P, sample, fvec)) {
@@ -408,6 +428,67 @@ int spec_sample(const void *logits, int64_t req_stride, int dtype, int B, int V,
   return chain_common(true, logits, req_stride, nullptr, 0, 0, dtype, B, 0, V, temperature, nullptr, nullptr,
                       nullptr, uniforms, accepted, tokens, accepted + B, nullptr, nullptr, nullptr, status,
                       workspace, chain, stream, probs);
+}
+
+int spec_sample_topkp(const void *logits, int64_t req_stride, int dtype, int B, int V, float temperature,
+                      int top_k, float top_p, const float *uniforms, int32_t *tokens, float *probs,
+                      int32_t *status, void *workspace, size_t workspace_bytes, void *stream) {
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_EDTYPE;
+  if (B < 0 || V <= 0 || req_stride < 0 || !(temperature > 0.0f && std::isfinite(temperature))) return SPEC_EINVAL;
+  if (top_k < 0 || !(top_p > 0.0f && top_p <= 1.0f)) return SPEC_EINVAL;
+  if (B == 0) return SPEC_OK;
+  if (!logits || !uniforms || !tokens) return SPEC_EINVAL;
+  const size_t need = draw_workspace(B, V, dtype);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return SPEC_EWORKSPACE;
+  const size_t chain = chain_layout(true, B, 0, V, dtype).total;
+  int32_t *accepted = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + chain);
+  return chain_common(true, logits, req_stride, nullptr, 0, 0, dtype, B, 0, V, temperature, nullptr, nullptr,
+                      nullptr, uniforms, accepted, tokens, accepted + B, nullptr, nullptr, nullptr, status,
+                      workspace, chain, stream, probs, top_k, top_p);
+}
+
+int spec_filter_rows(const void *logits, int64_t row_stride, int dtype, int R, int V, float temperature, int top_k,
+                     float top_p, float *theta, int32_t *kept, void *workspace, size_t workspace_bytes,
+                     void *stream) {
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_EDTYPE;
+  if (R < 0 || V <= 0 || row_stride < 0 || !(temperature > 0.0f && std::isfinite(temperature))) return SPEC_EINVAL;
+  if (top_k < 0 || !(top_p > 0.0f && top_p <= 1.0f)) return SPEC_EINVAL;
+  if (R == 0) return SPEC_OK;
+  if (!logits || !theta) return SPEC_EINVAL;
+  const size_t need = round_up(sizeof(Partial) * static_cast<size_t>(R), 256);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return SPEC_EWORKSPACE;
+  const int es = elem_size(dtype);
+  ChainParams P{};
+  P.target = static_cast<const char *>(logits);
+  P.t_req = row_stride;  // each row is a request with one position
+  P.dtype = dtype;
+  P.B = R;
+  P.k = 0;
+  P.V = V;
+  P.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  P.top_k = top_k;
+  P.top_p = top_p;
+  P.theta = theta;
+  P.kept = kept;
+  P.part = static_cast<Partial *>(workspace);
+  if (!chain_filter_plan(P)) return SPEC_EINVAL;
+  const bool vec = aligned16(logits) && (row_stride * es) % 16 == 0 && V % (16 / es) == 0;
+  const cudaError_t e = launch_chain_filter(P, vec, as_stream(stream));
+  return e == cudaSuccess ? SPEC_OK : fail_cuda(e, "spec_filter_rows");
+}
+
+int spec_verify_sample_topkp(const void *target, int64_t target_req_stride, const void *draft_logits,
+                             int64_t draft_req_stride, int64_t row_stride, int dtype, int B, int k, int V,
+                             float temperature, int top_k, float top_p, const int32_t *draft,
+                             const int32_t *draft_len, const int32_t *max_emit, const float *uniforms,
+                             int32_t *accepted, int32_t *out_tokens, int32_t *n_emit, float *p_tok, float *q_tok,
+                             float *resid_mass, int32_t *status, void *workspace, size_t workspace_bytes,
+                             void *stream) {
+  return chain_common(true, target, target_req_stride, draft_logits, draft_req_stride, row_stride, dtype, B, k, V,
+                      temperature, draft, draft_len, max_emit, uniforms, accepted, out_tokens, n_emit, p_tok, q_tok,
+                      resid_mass, status, workspace, workspace_bytes, stream, nullptr, top_k, top_p);
 }
 
 int spec_verify_greedy(const void *target, int64_t target_req_stride, int64_t row_stride,

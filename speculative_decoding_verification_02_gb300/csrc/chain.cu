@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kThreads) chain_greedy_accept_kernel(const Cha
 
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const ChainParams P) {
-  __shared__ float sM[kMaxRows], sS[kMaxRows], sX[kMaxRows];
+  __shared__ float sM[kMaxRows], sS[kMaxRows], sX[kMaxRows], sTh[kMaxRows];
   __shared__ int sTok[SPEC_MAX_K];
   __shared__ float sU[SPEC_MAX_K + 1], sP[SPEC_MAX_K], sQ[SPEC_MAX_K];
   __shared__ float s_sub[kWarps][kMaxSubs];
@@ -307,10 +307,12 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
       sM[rr] = a.M;
       sS[rr] = a.S;
       sX[rr] = a.X;
+      sTh[rr] = row_theta(P.theta, static_cast<int64_t>(b) * rows + row_of(rr));
       if (rr2 < nrr) {
         sM[rr2] = bb.M;
         sS[rr2] = bb.S;
         sX[rr2] = bb.X;
+        sTh[rr2] = row_theta(P.theta, static_cast<int64_t>(b) * rows + row_of(rr2));
       }
     }
   }
@@ -318,8 +320,10 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
   if (tid == 0) {
     int m = 0;
     for (int i = 0; i < L; ++i) {
-      const float p = ex2((sX[i] - sM[i]) * P.c) / sS[i];
-      const float q = ex2((sX[L + 1 + i] - sM[L + 1 + i]) * P.c) / sS[L + 1 + i];
+      // (a drafted token below its row's threshold has probability 0)
+      const float p = sX[i] >= sTh[i] ? ex2((sX[i] - sM[i]) * P.c) / sS[i] : 0.0f;
+      const float q = sX[L + 1 + i] >= sTh[L + 1 + i] ? ex2((sX[L + 1 + i] - sM[L + 1 + i]) * P.c) / sS[L + 1 + i]
+                                                      : 0.0f;
       sP[i] = p;
       sQ[i] = q;
       if (m == i && sU[i] * q < p) m = i + 1;
@@ -337,9 +341,9 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
   // arrive picks the chunk where u * total falls and scans it
   Weights W = m < L
                   ? Weights{row_ptr<DT>(P.target, P.t_req, P.row, b, m), row_ptr<DT>(P.draftl, P.d_req, P.row, b, m),
-                            sM[m], sM[L + 1 + m], 1.0f / sS[m], 1.0f / sS[L + 1 + m], P.c}
+                            sM[m], sM[L + 1 + m], 1.0f / sS[m], 1.0f / sS[L + 1 + m], P.c, sTh[m], sTh[L + 1 + m]}
                   : Weights{row_ptr<DT>(P.target, P.t_req, P.row, b, L), nullptr, sM[L], 0.0f, 1.0f / sS[L], 0.0f,
-                            P.c};
+                            P.c, sTh[L], -INFINITY};
   // Per sub-chunk of kThreads 16-byte groups (each thread adds up its one
   // group of it), so the last CTA only has to scan one sub-chunk.
   constexpr int EPG = Elems<DT>::kPerGroup;
@@ -460,13 +464,15 @@ static cudaError_t launch_dependent(K kern, unsigned grid, cudaStream_t st, cons
 }
 
 template <int DT, bool VEC, bool CVEC>
-static cudaError_t launch_chain_t(const ChainParams &P, bool sample, cudaStream_t st) {
+static cudaError_t launch_chain_t(const ChainParams &P, bool sample, bool stats, cudaStream_t st) {
   const int rows = sample ? 2 * P.k + 1 : P.k + 1;
   const unsigned grid1 = static_cast<unsigned>(static_cast<long long>(P.B) * rows * P.nc);
   if (sample) {
-    cudaError_t e = trace_launch_ex("chain_stats_sample", st, [&] {
-      return launch_dependent(chain_stats_kernel<DT, true, VEC>, grid1, st, P);
-    });
+    cudaError_t e = cudaSuccess;
+    if (stats)
+      e = trace_launch_ex("chain_stats_sample", st, [&] {
+        return launch_dependent(chain_stats_kernel<DT, true, VEC>, grid1, st, P);
+      });
     if (e != cudaSuccess) return e;
     if (P.cluster > 0) return launch_chain_accept_cluster(P, CVEC, st);
     const unsigned grid2 = static_cast<unsigned>(static_cast<long long>(P.B) * P.nc2);
@@ -483,15 +489,15 @@ static cudaError_t launch_chain_t(const ChainParams &P, bool sample, cudaStream_
   });
 }
 
-cudaError_t launch_chain(const ChainParams &P, bool sample, bool vec, bool cvec, cudaStream_t st) {
+cudaError_t launch_chain(const ChainParams &P, bool sample, bool vec, bool cvec, cudaStream_t st, bool stats) {
   // (cvec implies vec: it adds V a multiple of a 16-byte group)
   if (P.dtype == SPEC_DTYPE_BF16)
-    return vec ? (cvec ? launch_chain_t<SPEC_DTYPE_BF16, true, true>(P, sample, st)
-                       : launch_chain_t<SPEC_DTYPE_BF16, true, false>(P, sample, st))
-               : launch_chain_t<SPEC_DTYPE_BF16, false, false>(P, sample, st);
-  return vec ? (cvec ? launch_chain_t<SPEC_DTYPE_F32, true, true>(P, sample, st)
-                     : launch_chain_t<SPEC_DTYPE_F32, true, false>(P, sample, st))
-             : launch_chain_t<SPEC_DTYPE_F32, false, false>(P, sample, st);
+    return vec ? (cvec ? launch_chain_t<SPEC_DTYPE_BF16, true, true>(P, sample, stats, st)
+                       : launch_chain_t<SPEC_DTYPE_BF16, true, false>(P, sample, stats, st))
+               : launch_chain_t<SPEC_DTYPE_BF16, false, false>(P, sample, stats, st);
+  return vec ? (cvec ? launch_chain_t<SPEC_DTYPE_F32, true, true>(P, sample, stats, st)
+                     : launch_chain_t<SPEC_DTYPE_F32, true, false>(P, sample, stats, st))
+             : launch_chain_t<SPEC_DTYPE_F32, false, false>(P, sample, stats, st);
 }
 
 }  // namespace sv

@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
   // s_gsum: [threads * groups] weight sum of each 16-byte group of the slice (sampling)
   __shared__ int sTok[SPEC_MAX_K], sOk[SPEC_MAX_K], sA[kFusedMaxRows];
   __shared__ float sU[SPEC_MAX_K + 1], sP[SPEC_MAX_K], sQ[SPEC_MAX_K];
-  __shared__ float sM[kFusedMaxRows], sS[kFusedMaxRows], sX[kFusedMaxRows];
+  __shared__ float sM[kFusedMaxRows], sS[kFusedMaxRows], sX[kFusedMaxRows], sTh[kFusedMaxRows];
   __shared__ float s_red[kFusedWarps], s_z[2][kFusedMaxCluster];
   const RowPart kEmpty{-INFINITY, 0.0f, kNoIndex, 0.0f};
 
@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
         sM[r] = m;
         sS[r] = s;
         sX[r] = x;
+        sTh[r] = row_theta(P.theta, static_cast<int64_t>(b) * (2 * k + 1) + r);
       }
     }
     __syncthreads();
@@ -227,10 +228,14 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
   // the statistics of draft row i: after the target rows 0..L here, after
   // rows 0..k in the streaming pass's layout
   auto drow = [&](int i) { return (ACCEPT ? k : L) + 1 + i; };
+  if (!ACCEPT && tid < nrows) sTh[tid] = -INFINITY;  // the fused path streams unfiltered rows
+  if (!ACCEPT) __syncthreads();
   if (tid < L) {
     if (SAMPLE) {
-      const float p = ex2((sX[tid] - sM[tid]) * c) / sS[tid];
-      const float q = ex2((sX[drow(tid)] - sM[drow(tid)]) * c) / sS[drow(tid)];
+      // (a drafted token below its row's threshold has probability 0)
+      const float p = sX[tid] >= sTh[tid] ? ex2((sX[tid] - sM[tid]) * c) / sS[tid] : 0.0f;
+      const float q = sX[drow(tid)] >= sTh[drow(tid)] ? ex2((sX[drow(tid)] - sM[drow(tid)]) * c) / sS[drow(tid)]
+                                                      : 0.0f;
       sP[tid] = p;
       sQ[tid] = q;
       sOk[tid] = sU[tid] * q < p;
@@ -253,8 +258,8 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
 
   // ---- 3. the final draw: residual after a rejection, p_L after a full accept
   Weights W = m < L ? Weights{row_of(m), row_of(L + 1 + m), sM[m], sM[drow(m)], 1.0f / sS[m],
-                              1.0f / sS[drow(m)], c}
-                    : Weights{row_of(L), nullptr, sM[L], 0.0f, 1.0f / sS[L], 0.0f, c};
+                              1.0f / sS[drow(m)], c, sTh[m], sTh[drow(m)]}
+                    : Weights{row_of(L), nullptr, sM[L], 0.0f, 1.0f / sS[L], 0.0f, c, sTh[L], -INFINITY};
   float wmass = 0.0f, rmass = 0.0f, total = 0.0f;
   for (int attempt = 0; attempt < 2; ++attempt) {
     wmass = warp_sum(lane_weight_sum<DT, VEC>(W, lo, hi, G, s_gsum));  // this warp's range

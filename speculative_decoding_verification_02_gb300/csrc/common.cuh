@@ -152,19 +152,26 @@ __device__ __forceinline__ float warp_inclusive_scan(float v, int lane) {
 // --------------------------------------------------- weighted row selection
 
 // Weight of element v in an inverse-CDF draw over one row (a) or a row pair
-// (a, b):  w_v = max(0, alpha * 2^((a_v - Ma) c) - beta * 2^((b_v - Mb) c)).
-// beta = 0 (and b = nullptr) draws from the row's own softmax.
+// (a, b):  w_v = max(0, alpha * 2^((a_v - Ma) c) [a_v >= ta] - beta * 2^((b_v
+// - Mb) c) [b_v >= tb]).  beta = 0 (and b = nullptr) draws from the row's own
+// softmax; ta, tb are the rows' top-k / top-p thresholds (-inf: unfiltered).
 struct Weights {
   const char *a;
   const char *b;
   float Ma, Mb, alpha, beta, c;
+  float ta, tb;
 };
 
 template <int DT>
 __device__ __forceinline__ float weight_at(const Weights &W, float a, float b) {
-  float w = W.alpha * ex2((a - W.Ma) * W.c);
-  if (W.b != nullptr) w -= W.beta * ex2((b - W.Mb) * W.c);
+  float w = a >= W.ta ? W.alpha * ex2((a - W.Ma) * W.c) : 0.0f;
+  if (W.b != nullptr && b >= W.tb) w -= W.beta * ex2((b - W.Mb) * W.c);
   return fmaxf(w, 0.0f);
+}
+
+// A row's filter threshold (the smallest kept logit), -inf when unfiltered.
+__device__ __forceinline__ float row_theta(const float *theta, int64_t row) {
+  return theta ? __ldcg(theta + row) : -INFINITY;
 }
 
 // The eight weights of elements [v0, v0 + 8) (those >= hi are 0).

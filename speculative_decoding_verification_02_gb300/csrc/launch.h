@@ -36,6 +36,13 @@ struct ChainParams {
   // chunks per slice row, register slots per warp, and the barrier counter
   int grid_ctas, grid_gps, grid_cpr, grid_slots;
   unsigned *grid_sync;
+  // top-k / top-p filtering (filter.cu): the filter, and per partial row its
+  // threshold (the smallest kept logit) and kept count.  theta == nullptr:
+  // unfiltered (the accept kernels keep every logit).
+  int top_k;
+  float top_p;
+  float *theta;
+  int32_t *kept;
 };
 
 // The grid kernel's limits, which the workspace layout also needs: CTAs
@@ -72,7 +79,9 @@ struct NgramParams {
 // Two-pass chain path: the streaming pass (16-byte loads when vec) and an
 // accept kernel -- the cluster accept kernel when P.cluster > 0 (its
 // 16-byte path when cvec), else the chunked or greedy accept kernel.
-cudaError_t launch_chain(const ChainParams &P, bool sample, bool vec, bool cvec, cudaStream_t st);
+// stats = false (sampling only): the accept kernel alone, on partials the
+// filter kernel wrote.
+cudaError_t launch_chain(const ChainParams &P, bool sample, bool vec, bool cvec, cudaStream_t st, bool stats = true);
 // Cluster kernels (chain_fused.cu).  The plans pick the cluster geometry
 // (cluster, slice, groups) and return false when the requests' clusters
 // cannot all be resident at once.  chain_fused_plan: the fused one-launch
@@ -87,6 +96,13 @@ cudaError_t launch_chain_accept_cluster(const ChainParams &P, bool vec, cudaStre
 // partials for one launch) or cooperative launches are unavailable.  The
 // launch needs *grid_sync == 0 and leaves it 0.
 bool chain_grid_plan(ChainParams &P, bool sample, bool vec);
+// Top-k / top-p filter of every partial row (filter.cu): writes the row's
+// statistics over its kept logits as partial P.part[row] (one chunk per row)
+// and its threshold P.theta[row].  The plan picks the cluster geometry
+// (cluster, slice) and returns false when a row is too long (more than 16
+// slices of 96 KB).
+bool chain_filter_plan(ChainParams &P);
+cudaError_t launch_chain_filter(const ChainParams &P, bool vec, cudaStream_t st);
 cudaError_t launch_chain_grid(const ChainParams &P, bool sample, bool vec, cudaStream_t st);
 cudaError_t launch_tree(const TreeParams &P, bool vec, cudaStream_t st);
 size_t tree_dynamic_smem(const TreeParams &P);

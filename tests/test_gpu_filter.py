@@ -1,0 +1,279 @@
+"""GPU parity of top-k / top-p filtering and filtered verification against
+the oracle.
+
+- spec_filter_rows: the threshold and the kept count are the oracle's,
+  exactly for top-k; for top-p the cut may sit one value group off only where
+  the oracle's cumulative mass at that cut is within 1e-6 of top_p (counted).
+- spec_verify_sample_topkp: outputs under the chain decision rule of
+  tests/parity.py against the oracle's filtered verification (requests whose
+  GPU filter cut differs from the oracle's in some row -- only allowed where
+  the cut's mass is within 1e-6 of top_p -- are counted and skipped), on the
+  headline shape, bf16 ties at the top-k cut, masked logits, drafts outside
+  the filtered q, lengths, caps and bad tokens; both filters off reproduce
+  spec_verify_sample bit for bit.
+- spec_sample_topkp: tokens and q'(x) against the oracle, and 200,000 draws
+  from one row follow the filtered distribution.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_verification_02_gb300 import api, workloads
+from tests.parity import TOL, _near_draw, check_chain_sample, host, poison_like, to_dev
+
+pytestmark = pytest.mark.gpu
+NEAR = 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _cut_ok(row, T, top_k, top_p, theta_g):
+    """True when the GPU's kept set {x >= theta_g} is the oracle's, or a top-p
+    cut the oracle's fp64 masses put within NEAR of top_p."""
+    x = workloads.logits_as_f64(row).reshape(-1)
+    _, theta_o, _ = oracle.filter_row(row, T, top_k, top_p)
+    if theta_g == theta_o:
+        return True, False
+    if top_p >= 1.0:
+        return False, False
+    z = x / T
+    p = np.exp(z - z.max())
+    vals = np.unique(x)[::-1]
+    if 0 < top_k < x.size:
+        tk = np.sort(x)[::-1][top_k - 1]
+        vals = vals[vals >= tk]
+        keep = x >= tk
+    else:
+        keep = np.ones(x.size, bool)
+    SK = p[keep].sum()
+    cum = np.array([p[x >= v].sum() for v in vals]) / SK
+    i_o = int(np.flatnonzero(vals == theta_o)[0])
+    i_g = np.flatnonzero(vals == theta_g)
+    if i_g.size == 0:
+        return False, False
+    i_g = int(i_g[0])
+    lo = min(i_o, i_g)
+    return abs(i_o - i_g) == 1 and abs(cum[lo] - top_p) < NEAR, True
+
+
+@pytest.mark.parametrize("seed,R,V,dtype,T,top_k,top_p", [
+    (1, 9, 248_320, "bf16", 1.0, 50, 1.0), (2, 9, 248_320, "bf16", 1.0, 0, 0.9),
+    (3, 9, 248_320, "bf16", 0.7, 40, 0.8), (4, 16, 32_000, "fp32", 1.0, 100, 0.95),
+    (5, 32, 3001, "fp32", 1.3, 7, 1.0), (6, 32, 3001, "bf16", 1.0, 0, 0.5),
+    (7, 8, 128_256, "bf16", 1.0, 1, 1.0), (8, 12, 9, "fp32", 1.0, 3, 0.6),
+    (9, 4, 5000, "fp32", 1.0, 0, 1.0), (10, 6, 393_216, "fp32", 1.0, 20, 0.9)])
+def test_filter_rows_match_oracle(seed, R, V, dtype, T, top_k, top_p):
+    rng = np.random.default_rng(seed)
+    x = (rng.standard_normal((R, V)) * 3).astype(np.float32)
+    for r in range(R):
+        x[r, rng.choice(V, min(5, V), replace=False)] += 8.0
+    rows = workloads.bf16_bits(x) if dtype == "bf16" else x
+    g = host(api.spec_filter_rows(to_dev(rows), T, top_k, top_p))
+    near = 0
+    for r in range(R):
+        pf, theta_o, kept_o = oracle.filter_row(rows[r], T, top_k, top_p)
+        ok, was_near = _cut_ok(rows[r], T, top_k, top_p, float(g["theta"][r]))
+        assert ok, (r, g["theta"][r], theta_o, g["kept"][r], kept_o)
+        if was_near:
+            near += 1
+        else:
+            assert g["kept"][r] == kept_o, (r, g["kept"][r], kept_o)
+    assert near <= R // 4
+    print("near-cut rows", near)
+
+
+def test_filter_rows_ties_and_masks():
+    """bf16 rows with the maximum and the cut value repeated, -inf logits,
+    an all-equal row, and -0 next to +0."""
+    rng = np.random.default_rng(21)
+    V = 70_000
+    x = rng.integers(-4, 4, (6, V)).astype(np.float32)
+    x[1, rng.random(V) < 0.5] = -np.inf
+    x[2] = 1.5
+    x[3, :10] = 0.0
+    x[3, 10:20] = -0.0
+    x[3, 20:] = -5.0
+    rows = workloads.bf16_bits(x)
+    for top_k, top_p in [(1, 1.0), (100, 1.0), (25_000, 1.0), (15, 1.0), (0, 0.3), (0, 0.99), (5000, 0.7)]:
+        g = host(api.spec_filter_rows(to_dev(rows), 1.0, top_k, top_p))
+        for r in range(6):
+            _, theta_o, kept_o = oracle.filter_row(rows[r], 1.0, top_k, top_p)
+            ok, was_near = _cut_ok(rows[r], 1.0, top_k, top_p, float(g["theta"][r]))
+            assert ok and (was_near or g["kept"][r] == kept_o), (top_k, top_p, r, g["theta"][r], theta_o,
+                                                                   g["kept"][r], kept_o)
+
+
+def _filtered_chain(seed, B, k, V, dtype, T, top_k, top_p, draft_from_filtered=True):
+    prob = workloads.chain_problem(seed, B, k, V, dtype, T, target_std=1.5,
+                                   noise_std=np.linspace(0.3, 1.5, B).astype(np.float32))
+    rng = np.random.default_rng(seed + 1)
+    if draft_from_filtered and k:
+        for b in range(B):
+            for i in range(k):
+                qf = oracle.filter_row(prob["draft_logits"][b, i], T, top_k, top_p)[0]
+                prob["draft"][b, i] = rng.choice(V, p=qf / qf.sum())
+    return prob
+
+
+def _mismatch_requests(prob, top_k, top_p):
+    """Requests with a row whose GPU filter cut differs from the oracle's; each
+    such cut must be a top-p cut within NEAR of top_p in exact arithmetic.
+    (spec_filter_rows runs the same filter kernel, with the same slices and
+    arithmetic, as the filtered verification.)"""
+    B, R, V = prob["target"].shape
+    rows = np.concatenate([prob["target"].reshape(B * R, V), prob["draft_logits"].reshape(B * (R - 1), V)])
+    g = host(api.spec_filter_rows(to_dev(rows), prob["T"], top_k, top_p))
+    out = set()
+    for j in range(rows.shape[0]):
+        _, theta_o, _ = oracle.filter_row(rows[j], prob["T"], top_k, top_p)
+        if float(g["theta"][j]) != theta_o:
+            ok, _ = _cut_ok(rows[j], prob["T"], top_k, top_p, float(g["theta"][j]))
+            assert ok, (j, g["theta"][j], theta_o)
+            out.add(j // R if j < B * R else (j - B * R) // (R - 1))
+    return out
+
+
+def _run(prob, top_k, top_p, draft_len=None, max_emit=None):
+    args = dict(draft_len=None if draft_len is None else to_dev(draft_len),
+                max_emit=None if max_emit is None else to_dev(max_emit), top_k=top_k, top_p=top_p)
+    T, D = to_dev(prob["target"]), to_dev(prob["draft_logits"])
+    x, u = to_dev(prob["draft"]), to_dev(prob["uniforms"])
+    o = api.spec_verify_sample(T, D, x, u, prob["T"], **args)
+    poison_like(o)
+    o = api.spec_verify_sample(T, D, x, u, prob["T"], out=o, **args)
+    torch.cuda.synchronize()
+    return host(o)
+
+
+def _check(prob, g, r, top_k, top_p, draft_len=None):
+    skip = _mismatch_requests(prob, top_k, top_p)
+    keep = np.array([b for b in range(prob["target"].shape[0]) if b not in skip], dtype=np.int64)
+    assert len(skip) <= max(1, len(keep) // 8), skip
+    if skip:
+        print("requests with a near top-p cut", sorted(skip))
+    sub = lambda d: {kk: (v[keep] if isinstance(v, np.ndarray) and v.ndim and v.shape[0] == len(keep) + len(skip)
+                          else v) for kk, v in d.items()}
+    # the decision rule's near-threshold replay uses the filtered distributions
+    p2 = dict(prob, target=prob["target"][keep], draft_logits=prob["draft_logits"][keep],
+              draft=prob["draft"][keep], uniforms=prob["uniforms"][keep])
+    return check_chain_sample_filtered(p2, sub(g), sub(r), top_k, top_p,
+                                       None if draft_len is None else draft_len[keep])
+
+
+def check_chain_sample_filtered(prob, g, r, top_k, top_p, draft_len=None):
+    """check_chain_sample with the near-threshold replays on filtered p and q."""
+    B, R, V = prob["target"].shape
+    k = R - 1
+    np.testing.assert_array_equal(g["status"], r["status"])
+    near = 0
+    for b in range(B):
+        L = k if draft_len is None else int(draft_len[b])
+        if r["status"][b] != 0:
+            assert g["n_emit"][b] == 0
+            continue
+        pt, qt = r["p_tok"][b], r["q_tok"][b]
+        assert np.all(np.abs(g["p_tok"][b, :L] - pt[:L]) <= TOL) and np.all(np.abs(g["q_tok"][b, :L] - qt[:L]) <= TOL)
+        mg, mo = int(g["accepted"][b]), int(r["accepted"][b])
+        if mg != mo:
+            i = min(mg, mo)
+            thr = min(1.0, pt[i] / qt[i]) if qt[i] > 0 else float(pt[i] > 0)
+            assert abs(float(prob["uniforms"][b, i]) - thr) < TOL, (b, mg, mo)
+            near += 1
+            continue
+        np.testing.assert_array_equal(g["out_tokens"][b, :mo], r["out_tokens"][b, :mo])
+        assert g["n_emit"][b] == r["n_emit"][b]
+        assert abs(g["resid_mass"][b] - r["resid_mass"][b]) <= TOL
+        ne = int(r["n_emit"][b])
+        if mo < ne and g["out_tokens"][b, mo] != r["out_tokens"][b, mo]:
+            pf = oracle.filter_row(prob["target"][b, mo], prob["T"], top_k, top_p)[0]
+            if mo < L:
+                qf = oracle.filter_row(prob["draft_logits"][b, mo], prob["T"], top_k, top_p)[0]
+                dist, Rm = oracle.residual(pf, qf)
+                if Rm <= 0:
+                    dist = pf
+            else:
+                dist = pf
+            assert _near_draw(dist, float(prob["uniforms"][b, k]), int(g["out_tokens"][b, mo]),
+                              int(r["out_tokens"][b, mo])), (b, "final token")
+            near += 1
+    return near
+
+
+@pytest.mark.parametrize("seed,B,k,V,dtype,T,top_k,top_p", [
+    (1, 1, 4, 248_320, "bf16", 1.0, 50, 1.0), (2, 2, 4, 248_320, "bf16", 1.0, 0, 0.6),
+    (3, 16, 4, 3000, "fp32", 1.0, 20, 0.9), (4, 64, 3, 2048, "bf16", 0.8, 0, 0.95),
+    (5, 400, 2, 4000, "bf16", 1.0, 40, 0.9), (6, 8, 6, 40_003, "bf16", 1.2, 100, 1.0),
+    (7, 4, 0, 50_000, "fp32", 1.0, 10, 0.8)])
+def test_filtered_verification_parity(seed, B, k, V, dtype, T, top_k, top_p):
+    """B=400 takes the chunked accept kernel; the others the cluster accept kernel."""
+    prob = _filtered_chain(seed, B, k, V, dtype, T, top_k, top_p)
+    g = _run(prob, top_k, top_p)
+    r = oracle.verify_sample(prob["target"], prob["draft_logits"], prob["draft"], prob["uniforms"], T,
+                             top_k=top_k, top_p=top_p, threads=oracle.max_threads())
+    print("near", _check(prob, g, r, top_k, top_p))
+
+
+def test_filtered_drafts_outside_the_filter_lengths_caps():
+    """Drafts drawn from the unfiltered q (some fall outside q'), variable
+    lengths, caps and a bad token, masked logits."""
+    B, k, V, top_k, top_p = 24, 5, 6000, 30, 0.9
+    prob = _filtered_chain(31, B, k, V, "bf16", 1.0, top_k, top_p, draft_from_filtered=False)
+    rng = np.random.default_rng(5)
+    t = workloads.bf16_to_f32(prob["target"]).copy()
+    t[rng.random(t.shape) < 0.2] = -np.inf
+    prob["target"] = workloads.bf16_bits(t)
+    draft_len = rng.integers(0, k + 1, B).astype(np.int32)
+    draft_len[0] = -1
+    prob["draft"][1, 0] = V
+    draft_len[1] = 2
+    max_emit = rng.integers(0, k + 2, B).astype(np.int32)
+    g = _run(prob, top_k, top_p, draft_len, max_emit)
+    r = oracle.verify_sample(prob["target"], prob["draft_logits"], prob["draft"], prob["uniforms"], 1.0,
+                             draft_len=draft_len, max_emit=max_emit, top_k=top_k, top_p=top_p,
+                             threads=oracle.max_threads())
+    _check(prob, g, r, top_k, top_p, draft_len)
+    assert list(g["status"][:2]) == [3, 1]
+    assert (r["q_tok"][r["status"] == 0] == 0).any()      # some drafts lie outside q'
+
+
+def test_filters_off_is_the_unfiltered_path():
+    prob = workloads.chain_problem(41, 16, 4, 30_000, "bf16", 1.0, target_std=1.5, noise_std=0.8)
+    a = _run(prob, 0, 1.0)
+    b = _run(prob, 30_000, 1.0)   # top_k = V: off
+    for key in a:
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+
+
+def test_filtered_draws_and_their_distribution():
+    rng = np.random.default_rng(9)
+    B, V, T, top_k, top_p = 6, 50_000, 0.9, 200, 0.85
+    x = workloads.bf16_bits((rng.standard_normal((B, V)) * 2).astype(np.float32))
+    u = rng.random(B, dtype=np.float32)
+    g = host(api.spec_sample(to_dev(x), to_dev(u), T, top_k=top_k, top_p=top_p))
+    for b in range(B):
+        pf = oracle.filter_row(x[b], T, top_k, top_p)[0]
+        r = oracle.verify_sample(np.ascontiguousarray(x[b:b + 1, None]), np.zeros((1, 0, V), x.dtype),
+                                 np.zeros((1, 0), np.int32), u[b:b + 1, None], T, top_k=top_k, top_p=top_p)
+        rt, gt = int(r["out_tokens"][0, 0]), int(g["tokens"][b])
+        assert rt == gt or _near_draw(pf, float(u[b]), rt, gt)
+        assert abs(g["probs"][b] - pf[gt]) <= TOL
+    # 200,000 draws from one filtered row (a V=2048 row, broadcast)
+    row = workloads.chain_small()["draft_logits"][0, 0]
+    n = 200_000
+    pf = oracle.filter_row(row, 1.0, 64, 0.9)[0]
+    uu = np.random.default_rng(10).random(n, dtype=np.float32)
+    g = host(api.spec_sample(to_dev(row)[None].expand(n, row.size), to_dev(uu), 1.0, top_k=64, top_p=0.9))
+    counts = np.bincount(g["tokens"], minlength=row.size)
+    kept = pf > 0
+    assert counts[~kept].sum() == 0
+    # Pearson chi-square over the kept tokens: dof = kept - 1 for a correct
+    # sampler, its standard deviation sqrt(2 dof); a bound of 6 standard deviations
+    chi2 = np.sum((counts[kept] - n * pf[kept]) ** 2 / (n * pf[kept]))
+    dof = kept.sum() - 1
+    assert chi2 < dof + 6 * np.sqrt(2 * dof), (chi2, dof)
+    print("kept", kept.sum(), "chi2", chi2, "dof", dof)
