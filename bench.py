@@ -1,13 +1,15 @@
 """Benchmark of the verify-and-accept step on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload vocab248k|batch64|small|tree60|tree60wor|draw64|ngram|eagle2]
+                    [--workload vocab248k|batch64|topkp64|small|tree60|tree60wor|draw64|ngram|eagle2]
                     [--chain-path auto|two_pass|fused|grid]
 
 One step is one pass of the path over one batch:
   vocab248k  spec_verify_sample, B=1, k=4, V=248,320 bf16 (the default: the
              workload the headline metric is quoted on; 9 rows per step)
   batch64    spec_verify_sample, B=64, k=8, V=128,256 bf16 (1,088 rows)
+  topkp64    the batch64 rows verified with top_k=50, top_p=0.9 (drafts from
+             the drafter's own top-50; spec_verify_sample_topkp)
   small      spec_verify_sample, B=4, k=4, V=2,048 fp32 (36 rows)
   tree60     spec_verify_tree, 16 trees of 60 nodes, V=128,256 bf16
              (960 node rows per step)
@@ -58,6 +60,7 @@ CSRC = "speculative_decoding_verification_02_gb300/csrc"
 _CHAIN = [f"{CSRC}/chain.cu", f"{CSRC}/chain_fused.cu", f"{CSRC}/chain_common.cuh", f"{CSRC}/common.cuh",
           f"{CSRC}/segments.cuh"]
 KERNEL_SOURCES = {"chain": _CHAIN,
+                  "filter": _CHAIN + [f"{CSRC}/filter.cu"],
                   "tree": [f"{CSRC}/tree.cu", f"{CSRC}/common.cuh", f"{CSRC}/segments.cuh"],
                   "ngram": [f"{CSRC}/ngram.cu"] + _CHAIN,
                   "draw": _CHAIN,
@@ -230,8 +233,10 @@ class ClockSampler:
 # --------------------------------------------------------------- workloads
 
 class ChainWorkload:
-    """spec_verify_sample on one chain problem."""
+    """spec_verify_sample on one chain problem (filtered when top_k / top_p
+    are set)."""
     kind = "chain"
+    top_k, top_p = 0, 1.0
 
     def __init__(self, name):
         from speculative_decoding_verification_02_gb300 import workloads as W
@@ -243,6 +248,12 @@ class ChainWorkload:
             self.prob = W.chain_batch64()
             self.desc = ("chain sampling verify, B=64, k=8, V=128,256 bf16 "
                          "(t~N(0,2.5), d=t+N(0,s), s in {0.3,1,2}, T=0.7)")
+        elif name == "topkp64":
+            self.top_k, self.top_p = 50, 0.9
+            self.kind = "filter"
+            self.prob = W.chain_batch64_topk(top_k=self.top_k)
+            self.desc = ("top-k / top-p filtered chain sampling verify, top_k=50, top_p=0.9, B=64, k=8, "
+                         "V=128,256 bf16 (the batch64 rows, T=0.7; drafts from the drafter's own top-50)")
         else:
             self.prob = W.chain_small()
             self.desc = "chain sampling verify, B=4, k=4, V=2048 fp32 (t~N(0,2), d=t+N(0,0.5), T=1)"
@@ -267,7 +278,8 @@ class ChainWorkload:
 
     def call(self, s, out, stream):
         from speculative_decoding_verification_02_gb300 import api
-        return api.spec_verify_sample(s["T"], s["D"], s["X"], s["U"], self.prob["T"], out=out, stream=stream)
+        return api.spec_verify_sample(s["T"], s["D"], s["X"], s["U"], self.prob["T"], top_k=self.top_k,
+                                      top_p=self.top_p, out=out, stream=stream)
 
     result_keys = ("accepted", "out_tokens", "n_emit", "status")
 
@@ -275,7 +287,7 @@ class ChainWorkload:
         """Algorithmic bytes of one launch of kernel `name`, averaged over the
         rotating sets (the draw's bytes depend on where each call stopped)."""
         row = self.V * self.es
-        if name.startswith(("chain_stats", "chain_fused", "chain_grid")):
+        if name.startswith(("chain_stats", "chain_fused", "chain_grid", "chain_filter")):
             return self.set_bytes  # every row once (the fused kernel's draw re-reads two from L2)
         if name.startswith("chain_sample_accept"):
             tot = 0.0
@@ -296,11 +308,13 @@ class ChainWorkload:
             tgt = np.broadcast_to(p["target"][:1], (n,) + p["target"].shape[1:])
             dl = np.broadcast_to(p["draft_logits"][:1], (n,) + p["draft_logits"].shape[1:])
             idx = np.zeros(n, dtype=np.int64)
-            oracle.verify_sample(tgt, dl, p["draft"][idx], p["uniforms"][idx], p["T"], threads=threads)
+            oracle.verify_sample(tgt, dl, p["draft"][idx], p["uniforms"][idx], p["T"], top_k=self.top_k,
+                                 top_p=self.top_p, threads=threads)
             return n * (2 * self.k + 1)
         reps = max(1, -(-n // self.B))
         for _ in range(reps):
-            oracle.verify_sample(p["target"], p["draft_logits"], p["draft"], p["uniforms"], p["T"], threads=threads)
+            oracle.verify_sample(p["target"], p["draft_logits"], p["draft"], p["uniforms"], p["T"], top_k=self.top_k,
+                                 top_p=self.top_p, threads=threads)
         return reps * self.B * (2 * self.k + 1)
 
 
@@ -514,7 +528,7 @@ class NgramWorkload:
         return reps * self.rows_per_step
 
 
-WORKLOADS = {"vocab248k": ChainWorkload, "batch64": ChainWorkload, "small": ChainWorkload,
+WORKLOADS = {"vocab248k": ChainWorkload, "batch64": ChainWorkload, "small": ChainWorkload, "topkp64": ChainWorkload,
              "tree60": TreeWorkload, "tree60wor": TreeWorkload, "draw64": DrawWorkload, "ngram": NgramWorkload, "eagle2": EagleWorkload}
 
 

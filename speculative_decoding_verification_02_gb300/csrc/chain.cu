@@ -351,40 +351,45 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
   const int sub = kThreads * EPG;
   const int v0 = j * P.chunk2, v1 = min(P.V, v0 + P.chunk2);
   const int nsub = (v1 - v0 + sub - 1) / sub;  // <= kMaxSubs by the choice of chunk2
-  for (int i0 = 0; i0 < nsub; i0 += kSubBatch) {
-    uint4 A[kSubBatch], Bv[kSubBatch];
-    bool full[kSubBatch];
+  // (FILT = false when neither row has a threshold: no mask in the loop)
+  auto weight_pass = [&]<bool FILT>() {
+    for (int i0 = 0; i0 < nsub; i0 += kSubBatch) {
+      uint4 A[kSubBatch], Bv[kSubBatch];
+      bool full[kSubBatch];
 #pragma unroll
-    for (int q = 0; q < kSubBatch; ++q) {
-      const int gv = v0 + ((i0 + q) * kThreads + tid) * EPG;  // first logit of this thread's group
-      full[q] = VEC && i0 + q < nsub && gv + EPG <= v1;
-      if (full[q]) {
-        A[q] = __ldcg(reinterpret_cast<const uint4 *>(W.a + static_cast<int64_t>(gv) * ES));
-        if (W.b != nullptr) Bv[q] = __ldcg(reinterpret_cast<const uint4 *>(W.b + static_cast<int64_t>(gv) * ES));
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < kSubBatch; ++q) {
-      if (i0 + q >= nsub) break;
-      const int gv = v0 + ((i0 + q) * kThreads + tid) * EPG;
-      float ws = 0.0f;
-      if (full[q]) {
-        float a[EPG], bb[EPG];
-        unpack16<DT>(A[q], a);
-        if (W.b != nullptr) unpack16<DT>(Bv[q], bb);
-#pragma unroll
-        for (int e = 0; e < EPG; ++e) ws += weight_at<DT>(W, a[e], bb[e]);
-      } else {
-        for (int e = 0; e < EPG; ++e) {
-          const int v = gv + e;
-          if (v < v1)
-            ws += weight_at<DT>(W, load_one<DT>(W.a, v), W.b != nullptr ? load_one<DT>(W.b, v) : -INFINITY);
+      for (int q = 0; q < kSubBatch; ++q) {
+        const int gv = v0 + ((i0 + q) * kThreads + tid) * EPG;  // first logit of this thread's group
+        full[q] = VEC && i0 + q < nsub && gv + EPG <= v1;
+        if (full[q]) {
+          A[q] = __ldcg(reinterpret_cast<const uint4 *>(W.a + static_cast<int64_t>(gv) * ES));
+          if (W.b != nullptr) Bv[q] = __ldcg(reinterpret_cast<const uint4 *>(W.b + static_cast<int64_t>(gv) * ES));
         }
       }
-      ws = warp_sum(ws);
-      if (lane == 0) s_sub[warp][i0 + q] = ws;
+#pragma unroll
+      for (int q = 0; q < kSubBatch; ++q) {
+        if (i0 + q >= nsub) break;
+        const int gv = v0 + ((i0 + q) * kThreads + tid) * EPG;
+        float ws = 0.0f;
+        if (full[q]) {
+          float a[EPG], bb[EPG];
+          unpack16<DT>(A[q], a);
+          if (W.b != nullptr) unpack16<DT>(Bv[q], bb);
+#pragma unroll
+          for (int e = 0; e < EPG; ++e) ws += weight_at<DT, FILT>(W, a[e], bb[e]);
+        } else {
+          for (int e = 0; e < EPG; ++e) {
+            const int v = gv + e;
+            if (v < v1)
+              ws += weight_at<DT, FILT>(W, load_one<DT>(W.a, v), W.b != nullptr ? load_one<DT>(W.b, v) : -INFINITY);
+          }
+        }
+        ws = warp_sum(ws);
+        if (lane == 0) s_sub[warp][i0 + q] = ws;
+      }
     }
-  }
+  };
+  if (weights_filtered(W)) weight_pass.template operator()<true>();
+  else weight_pass.template operator()<false>();
   __syncthreads();
   const int nsub_all = P.nsub;
   float *part2 = P.part2 + static_cast<int64_t>(b) * nsub_all;

@@ -56,7 +56,7 @@ struct __align__(16) RowPart {
 // This lane's sum of the draw weights W over its groups (lane_group split of
 // [lo, hi), G rounds; logits >= hi weigh 0).  Each group's own sum goes to
 // gsum[g].
-template <int DT, bool VEC>
+template <int DT, bool VEC, bool FILT>
 __device__ __forceinline__ float lane_weight_sum(const Weights &W, int lo, int hi, int G, float *gsum) {
   constexpr int EPG = Elems<DT>::kPerGroup;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -79,7 +79,7 @@ __device__ __forceinline__ float lane_weight_sum(const Weights &W, int lo, int h
         if (W.b) unpack16<DT>(xb[u], y);
         float gs = 0.0f;
 #pragma unroll
-        for (int e = 0; e < EPG; ++e) gs += weight_at<DT>(W, x[e], W.b ? y[e] : 0.0f);
+        for (int e = 0; e < EPG; ++e) gs += weight_at<DT, FILT>(W, x[e], W.b ? y[e] : 0.0f);
         gsum[g0 + 32 * u] = gs;
         acc += gs;
       }
@@ -262,7 +262,9 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
                     : Weights{row_of(L), nullptr, sM[L], 0.0f, 1.0f / sS[L], 0.0f, c, sTh[L], -INFINITY};
   float wmass = 0.0f, rmass = 0.0f, total = 0.0f;
   for (int attempt = 0; attempt < 2; ++attempt) {
-    wmass = warp_sum(lane_weight_sum<DT, VEC>(W, lo, hi, G, s_gsum));  // this warp's range
+    // (only the accept kernel's rows can carry top-k / top-p thresholds)
+    wmass = warp_sum(ACCEPT && weights_filtered(W) ? lane_weight_sum<DT, VEC, true>(W, lo, hi, G, s_gsum)
+                                                   : lane_weight_sum<DT, VEC, false>(W, lo, hi, G, s_gsum));
     const float ws = wmass;
     if (lane == 0) s_red[warp] = ws;
     __syncthreads();

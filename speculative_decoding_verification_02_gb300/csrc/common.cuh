@@ -162,12 +162,17 @@ struct Weights {
   float ta, tb;
 };
 
-template <int DT>
+// FILT = false compiles the thresholds out: the unfiltered rows' loops keep
+// their instruction count (the masks cost a compare and a select per logit).
+template <int DT, bool FILT = true>
 __device__ __forceinline__ float weight_at(const Weights &W, float a, float b) {
-  float w = a >= W.ta ? W.alpha * ex2((a - W.Ma) * W.c) : 0.0f;
-  if (W.b != nullptr && b >= W.tb) w -= W.beta * ex2((b - W.Mb) * W.c);
+  float w = (!FILT || a >= W.ta) ? W.alpha * ex2((a - W.Ma) * W.c) : 0.0f;
+  if (W.b != nullptr && (!FILT || b >= W.tb)) w -= W.beta * ex2((b - W.Mb) * W.c);
   return fmaxf(w, 0.0f);
 }
+
+// True when either row of W has a top-k / top-p threshold.
+__device__ __forceinline__ bool weights_filtered(const Weights &W) { return W.ta > -INFINITY || W.tb > -INFINITY; }
 
 // A row's filter threshold (the smallest kept logit), -inf when unfiltered.
 __device__ __forceinline__ float row_theta(const float *theta, int64_t row) {
@@ -486,44 +491,5 @@ __device__ __forceinline__ void block_merge(float &m, float &s, int &idx, float 
     for (int o = 16; o > 0; o >>= 1) xt = fmaxf(xt, __shfl_xor_sync(0xffffffffu, xt, o));
   }
 }
-
-template <int DT, bool VEC, int LD, int NT = kThreads>
-__device__ __forceinline__ float thread_chunk_weight_sum(const Weights &W, int v0, int v1) {
-  constexpr int EPG = Elems<DT>::kPerGroup;
-  constexpr int ES = Elems<DT>::kSize;
-  float acc = 0.0f;
-  int vtail = v0;
-  if (VEC) {
-    const int ng = (v1 - v0) / EPG;
-    const uint4 *ga = reinterpret_cast<const uint4 *>(W.a + static_cast<int64_t>(v0) * ES);
-    const uint4 *gb = W.b != nullptr ? reinterpret_cast<const uint4 *>(W.b + static_cast<int64_t>(v0) * ES) : nullptr;
-    for (int g0 = threadIdx.x; g0 < ng; g0 += NT * kBatch) {
-      uint4 A[kBatch], Bv[kBatch];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int gi = g0 + u * NT;
-        if (gi < ng) {
-          A[u] = load16<LD>(ga + gi);
-          if (W.b != nullptr) Bv[u] = load16<LD>(gb + gi);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        if (g0 + u * NT < ng) {
-          float a[EPG], bb[EPG];
-          unpack16<DT>(A[u], a);
-          if (W.b != nullptr) unpack16<DT>(Bv[u], bb);
-#pragma unroll
-          for (int e = 0; e < EPG; ++e) acc += weight_at<DT>(W, a[e], bb[e]);
-        }
-      }
-    }
-    vtail = v0 + ng * EPG;
-  }
-  for (int v = vtail + threadIdx.x; v < v1; v += NT)
-    acc += weight_at<DT>(W, load_one<DT>(W.a, v), W.b != nullptr ? load_one<DT>(W.b, v) : -INFINITY);
-  return acc;
-}
-
 
 }  // namespace sv

@@ -70,6 +70,16 @@ def gumbel_draw(rng, logits_row, T: float) -> int:
     return int(np.argmax(logits_as_f64(logits_row) / T - np.log(-np.log(u))))
 
 
+def gumbel_draw_top_k(rng, logits_row, T: float, top_k: int) -> int:
+    """A drafter that samples from its own top-k: Gumbel-max over the top_k
+    largest logits (by position among equal logits at the cut)."""
+    l64 = logits_as_f64(logits_row)
+    cand = np.argpartition(-l64, top_k - 1)[:top_k]
+    u = rng.random(top_k)
+    u = np.where(u <= 0.0, np.finfo(np.float64).tiny, u)
+    return int(cand[np.argmax(l64[cand] / T - np.log(-np.log(u)))])
+
+
 def gumbel_top(rng, logits_row, T: float, n: int) -> np.ndarray:
     """n draws from softmax(logits/T) without replacement, in draw order: the
     n largest of l/T + G (Gumbel-top-k), the largest first."""
@@ -129,6 +139,17 @@ def chain_vocab248k(seed: int = SEED_BASE + 3, B: int = 1) -> dict:
 def chain_batch64(seed: int = SEED_BASE + 4, B: int = 64) -> dict:
     sig = np.array([(0.3, 1.0, 2.0)[b % 3] for b in range(B)], dtype=np.float32)
     return chain_problem(seed, B, 8, 128256, "bf16", 0.7, target_std=2.5, noise_std=sig)
+
+
+def chain_batch64_topk(seed: int = SEED_BASE + 8, B: int = 64, top_k: int = 50) -> dict:
+    """The batch64 rows with each draft token redrawn by a drafter sampling
+    from its own top-k (for top-k / top-p filtered verification)."""
+    p = chain_batch64(B=B)
+    rng = np.random.default_rng(seed)
+    for b in range(p["B"]):
+        for i in range(p["k"]):
+            p["draft"][b, i] = gumbel_draw_top_k(rng, p["draft_logits"][b, i], p["T"], top_k)
+    return p
 
 
 # ------------------------------------------------------------------- trees
