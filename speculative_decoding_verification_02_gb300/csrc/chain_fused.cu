@@ -97,7 +97,10 @@ __device__ __forceinline__ float4 ld_part(const Partial *p) { return __ldcg(rein
 // them); the decision and the final draw are the same.  Its CTAs are small
 // enough to share SMs with the streaming pass, so they start early and wait
 // for it (programmatic dependent launch).
-template <int DT, bool VEC, bool SAMPLE, bool ACCEPT>
+// FILT (accept kernel only): the rows carry top-k / top-p thresholds, which
+// mask the drafted tokens' probabilities and the draw weights; without it
+// the kernel reads and applies none.
+template <int DT, bool VEC, bool SAMPLE, bool ACCEPT, bool FILT = false>
 __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_kernel(const ChainParams P) {
   cg::cluster_group cluster = cg::this_cluster();
   constexpr int EPG = Elems<DT>::kPerGroup;
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
         sM[r] = m;
         sS[r] = s;
         sX[r] = x;
-        sTh[r] = row_theta(P.theta, static_cast<int64_t>(b) * (2 * k + 1) + r);
+        if (FILT) sTh[r] = row_theta(P.theta, static_cast<int64_t>(b) * (2 * k + 1) + r);
       }
     }
     __syncthreads();
@@ -228,14 +231,13 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
   // the statistics of draft row i: after the target rows 0..L here, after
   // rows 0..k in the streaming pass's layout
   auto drow = [&](int i) { return (ACCEPT ? k : L) + 1 + i; };
-  if (!ACCEPT && tid < nrows) sTh[tid] = -INFINITY;  // the fused path streams unfiltered rows
-  if (!ACCEPT) __syncthreads();
   if (tid < L) {
     if (SAMPLE) {
       // (a drafted token below its row's threshold has probability 0)
-      const float p = sX[tid] >= sTh[tid] ? ex2((sX[tid] - sM[tid]) * c) / sS[tid] : 0.0f;
-      const float q = sX[drow(tid)] >= sTh[drow(tid)] ? ex2((sX[drow(tid)] - sM[drow(tid)]) * c) / sS[drow(tid)]
-                                                      : 0.0f;
+      const float p = !FILT || sX[tid] >= sTh[tid] ? ex2((sX[tid] - sM[tid]) * c) / sS[tid] : 0.0f;
+      const float q = !FILT || sX[drow(tid)] >= sTh[drow(tid)]
+                          ? ex2((sX[drow(tid)] - sM[drow(tid)]) * c) / sS[drow(tid)]
+                          : 0.0f;
       sP[tid] = p;
       sQ[tid] = q;
       sOk[tid] = sU[tid] * q < p;
@@ -258,13 +260,12 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
 
   // ---- 3. the final draw: residual after a rejection, p_L after a full accept
   Weights W = m < L ? Weights{row_of(m), row_of(L + 1 + m), sM[m], sM[drow(m)], 1.0f / sS[m],
-                              1.0f / sS[drow(m)], c, sTh[m], sTh[drow(m)]}
-                    : Weights{row_of(L), nullptr, sM[L], 0.0f, 1.0f / sS[L], 0.0f, c, sTh[L], -INFINITY};
+                              1.0f / sS[drow(m)], c, FILT ? sTh[m] : -INFINITY, FILT ? sTh[drow(m)] : -INFINITY}
+                    : Weights{row_of(L), nullptr, sM[L], 0.0f, 1.0f / sS[L], 0.0f, c, FILT ? sTh[L] : -INFINITY,
+                              -INFINITY};
   float wmass = 0.0f, rmass = 0.0f, total = 0.0f;
   for (int attempt = 0; attempt < 2; ++attempt) {
-    // (only the accept kernel's rows can carry top-k / top-p thresholds)
-    wmass = warp_sum(ACCEPT && weights_filtered(W) ? lane_weight_sum<DT, VEC, true>(W, lo, hi, G, s_gsum)
-                                                   : lane_weight_sum<DT, VEC, false>(W, lo, hi, G, s_gsum));
+    wmass = warp_sum(lane_weight_sum<DT, VEC, FILT>(W, lo, hi, G, s_gsum));  // this warp's range
     const float ws = wmass;
     if (lane == 0) s_red[warp] = ws;
     __syncthreads();
@@ -304,13 +305,13 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
     unpack16<DT>(load_group<DT, VEC>(W.a, lo + g * EPG, hi), x);
     if (W.b) unpack16<DT>(load_group<DT, VEC>(W.b, lo + g * EPG, hi), y);
 #pragma unroll
-    for (int e = 0; e < EPG; ++e) w[e] = weight_at<DT>(W, x[e], W.b ? y[e] : 0.0f);
+    for (int e = 0; e < EPG; ++e) w[e] = weight_at<DT, FILT>(W, x[e], W.b ? y[e] : 0.0f);
   });
   if (tid == 0) {
     if (m < ne) P.out_tokens[static_cast<int64_t>(b) * (k + 1) + m] = tok;
     if (P.resid_mass) P.resid_mass[b] = (m < L && W.b != nullptr) ? total : 0.0f;
     if (P.final_prob)
-      P.final_prob[b] = weight_at<DT>(W, load_one<DT>(W.a, tok), W.b ? load_one<DT>(W.b, tok) : 0.0f) / total;
+      P.final_prob[b] = weight_at<DT, FILT>(W, load_one<DT>(W.a, tok), W.b ? load_one<DT>(W.b, tok) : 0.0f) / total;
   }
 }
 
@@ -332,9 +333,9 @@ static int lane_groups(int V, int dtype, int cluster) {
   return ((slice + epg - 1) / epg + kFusedThreads - 1) / kFusedThreads;
 }
 
-template <int DT, bool VEC, bool SAMPLE, bool ACCEPT>
+template <int DT, bool VEC, bool SAMPLE, bool ACCEPT, bool FILT>
 static cudaError_t prepare(int cluster, size_t smem) {
-  auto kern = chain_fused_kernel<DT, VEC, SAMPLE, ACCEPT>;
+  auto kern = chain_fused_kernel<DT, VEC, SAMPLE, ACCEPT, FILT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e == cudaSuccess && cluster > 8) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return e;
@@ -357,35 +358,43 @@ static void cluster_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, i
   cfg.numAttrs = pdl ? 2 : 1;
 }
 
-// Calls f.template operator()<DT, VEC, SAMPLE, ACCEPT>() for the runtime
-// choice (ACCEPT implies SAMPLE).
+// Calls f.template operator()<DT, VEC, SAMPLE, ACCEPT, FILT>() for the
+// runtime choice (ACCEPT implies SAMPLE; FILT only with ACCEPT).
 template <class F>
-static cudaError_t dispatch(int dtype, bool vec, bool sample, bool accept, F &&f) {
+static cudaError_t dispatch(int dtype, bool vec, bool sample, bool accept, bool filt, F &&f) {
   if (dtype == SPEC_DTYPE_BF16) {
     if (vec) {
-      if (accept) return f.template operator()<SPEC_DTYPE_BF16, true, true, true>();
-      return sample ? f.template operator()<SPEC_DTYPE_BF16, true, true, false>()
-                    : f.template operator()<SPEC_DTYPE_BF16, true, false, false>();
+      if (accept)
+        return filt ? f.template operator()<SPEC_DTYPE_BF16, true, true, true, true>()
+                    : f.template operator()<SPEC_DTYPE_BF16, true, true, true, false>();
+      return sample ? f.template operator()<SPEC_DTYPE_BF16, true, true, false, false>()
+                    : f.template operator()<SPEC_DTYPE_BF16, true, false, false, false>();
     }
-    if (accept) return f.template operator()<SPEC_DTYPE_BF16, false, true, true>();
-    return sample ? f.template operator()<SPEC_DTYPE_BF16, false, true, false>()
-                  : f.template operator()<SPEC_DTYPE_BF16, false, false, false>();
+    if (accept)
+      return filt ? f.template operator()<SPEC_DTYPE_BF16, false, true, true, true>()
+                  : f.template operator()<SPEC_DTYPE_BF16, false, true, true, false>();
+    return sample ? f.template operator()<SPEC_DTYPE_BF16, false, true, false, false>()
+                  : f.template operator()<SPEC_DTYPE_BF16, false, false, false, false>();
   }
   if (vec) {
-    if (accept) return f.template operator()<SPEC_DTYPE_F32, true, true, true>();
-    return sample ? f.template operator()<SPEC_DTYPE_F32, true, true, false>()
-                  : f.template operator()<SPEC_DTYPE_F32, true, false, false>();
+    if (accept)
+      return filt ? f.template operator()<SPEC_DTYPE_F32, true, true, true, true>()
+                  : f.template operator()<SPEC_DTYPE_F32, true, true, true, false>();
+    return sample ? f.template operator()<SPEC_DTYPE_F32, true, true, false, false>()
+                  : f.template operator()<SPEC_DTYPE_F32, true, false, false, false>();
   }
-  if (accept) return f.template operator()<SPEC_DTYPE_F32, false, true, true>();
-  return sample ? f.template operator()<SPEC_DTYPE_F32, false, true, false>()
-                : f.template operator()<SPEC_DTYPE_F32, false, false, false>();
+  if (accept)
+    return filt ? f.template operator()<SPEC_DTYPE_F32, false, true, true, true>()
+                : f.template operator()<SPEC_DTYPE_F32, false, true, true, false>();
+  return sample ? f.template operator()<SPEC_DTYPE_F32, false, true, false, false>()
+                : f.template operator()<SPEC_DTYPE_F32, false, false, false, false>();
 }
 
 // How many clusters of `cluster` CTAs of the kernel fit on the device at
 // once (cached per device and shape).
-static int resident_clusters(int dtype, bool vec, bool sample, bool accept, int k, int V, int cluster) {
+static int resident_clusters(int dtype, bool vec, bool sample, bool accept, bool filt, int k, int V, int cluster) {
   struct Key {
-    int dev, dtype, vec, sample, accept, k, V, cluster, n;
+    int dev, dtype, vec, sample, accept, filt, k, V, cluster, n;
   };
   static std::mutex mu;
   static std::vector<Key> cache;
@@ -395,25 +404,25 @@ static int resident_clusters(int dtype, bool vec, bool sample, bool accept, int 
     std::lock_guard<std::mutex> g(mu);
     for (const Key &q : cache)
       if (q.dev == dev && q.dtype == dtype && q.vec == vec && q.sample == sample && q.accept == accept &&
-          q.k == k && q.V == V && q.cluster == cluster)
+          q.filt == filt && q.k == k && q.V == V && q.cluster == cluster)
         return q.n;
   }
   const size_t smem = chain_fused_smem(k, sample, accept, lane_groups(V, dtype, cluster));
   int n = 0;
-  dispatch(dtype, vec, sample, accept, [&]<int DT, bool VEC, bool SAMPLE, bool ACCEPT>() {
-    cudaError_t e = prepare<DT, VEC, SAMPLE, ACCEPT>(cluster, smem);
+  dispatch(dtype, vec, sample, accept, filt, [&]<int DT, bool VEC, bool SAMPLE, bool ACCEPT, bool FILT>() {
+    cudaError_t e = prepare<DT, VEC, SAMPLE, ACCEPT, FILT>(cluster, smem);
     if (e == cudaSuccess) {
       cudaLaunchConfig_t cfg;
       cudaLaunchAttribute attr[2];
       cluster_config(cfg, attr, cluster, static_cast<unsigned>(cluster), smem, nullptr, false);
-      e = cudaOccupancyMaxActiveClusters(&n, chain_fused_kernel<DT, VEC, SAMPLE, ACCEPT>, &cfg);
+      e = cudaOccupancyMaxActiveClusters(&n, chain_fused_kernel<DT, VEC, SAMPLE, ACCEPT, FILT>, &cfg);
     }
     if (e != cudaSuccess) n = 0;
     return e;
   });
   cudaGetLastError();  // a refused query leaves no error behind
   std::lock_guard<std::mutex> g(mu);
-  cache.push_back(Key{dev, dtype, vec, sample, accept, k, V, cluster, n});
+  cache.push_back(Key{dev, dtype, vec, sample, accept, filt, k, V, cluster, n});
   return n;
 }
 
@@ -421,11 +430,12 @@ static int resident_clusters(int dtype, bool vec, bool sample, bool accept, int 
 // kFusedMinSlice logits each, and for the accept kernel at most
 // kAcceptMaxSlice) for which every request's cluster is resident at once.
 static bool plan(ChainParams &P, bool sample, bool vec, bool accept) {
+  const bool filt = accept && P.theta != nullptr;
   int cs = (P.V + kFusedMinSlice - 1) / kFusedMinSlice;
   cs = cs < 1 ? 1 : (cs > kFusedMaxCluster ? kFusedMaxCluster : cs);
   const int cs_min = accept ? (P.V + kAcceptMaxSlice - 1) / kAcceptMaxSlice : 1;
   for (; cs >= cs_min; --cs)
-    if (resident_clusters(P.dtype, vec, sample, accept, P.k, P.V, cs) >= P.B) break;
+    if (resident_clusters(P.dtype, vec, sample, accept, filt, P.k, P.V, cs) >= P.B) break;
   if (cs < cs_min || cs < 1) return false;
   P.cluster = cs;
   P.slice = ((P.V + cs - 1) / cs + 7) / 8 * 8;
@@ -438,15 +448,16 @@ bool chain_accept_plan(ChainParams &P, bool vec) { return plan(P, true, vec, tru
 
 static cudaError_t launch(const ChainParams &P, bool sample, bool vec, bool accept, cudaStream_t st) {
   const size_t smem = chain_fused_smem(P.k, sample, accept, P.groups);
-  return dispatch(P.dtype, vec, sample, accept, [&]<int DT, bool VEC, bool SAMPLE, bool ACCEPT>() {
-    cudaError_t e = prepare<DT, VEC, SAMPLE, ACCEPT>(P.cluster, smem);
+  const bool filt = accept && P.theta != nullptr;
+  return dispatch(P.dtype, vec, sample, accept, filt, [&]<int DT, bool VEC, bool SAMPLE, bool ACCEPT, bool FILT>() {
+    cudaError_t e = prepare<DT, VEC, SAMPLE, ACCEPT, FILT>(P.cluster, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     cluster_config(cfg, attr, P.cluster, static_cast<unsigned>(P.B * P.cluster), smem, st, !trace_enabled());
     const char *name = ACCEPT ? "chain_sample_accept_cluster" : SAMPLE ? "chain_fused_sample" : "chain_fused_greedy";
     return trace_launch_ex(name, st, [&] {
-      return cudaLaunchKernelEx(&cfg, chain_fused_kernel<DT, VEC, SAMPLE, ACCEPT>, P);
+      return cudaLaunchKernelEx(&cfg, chain_fused_kernel<DT, VEC, SAMPLE, ACCEPT, FILT>, P);
     });
   });
 }

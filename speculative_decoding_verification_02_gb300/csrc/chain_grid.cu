@@ -168,9 +168,8 @@ __global__ void __launch_bounds__(kGridThreads, 1) chain_grid_kernel(const Chain
         if (SAMPLE) {
           const float M = warp_allmax(m);
           if (M != -INFINITY) {
-            const float Mc = M * c;
 #pragma unroll
-            for (int q = 0; q < EPG; ++q) sum += ex2(fmaf(x[q], c, -Mc));
+            for (int q = 0; q < EPG; ++q) sum += ex2((x[q] - M) * c);
           }
           sum = warp_sum(sum);
           m = M;
@@ -302,16 +301,16 @@ __global__ void __launch_bounds__(kGridThreads, 1) chain_grid_kernel(const Chain
     auto weights = [&](const Item &t, const uint4 &gt, const uint4 &gd, float *wr, float *wp) {
       const int b = t.b, m = s_m[b], rt = b * R + m, rd = b * R + K1 + m;
       const bool resid = m < s_L[b];
-      const float Mtc = s_M[rt] * c, iSt = 1.0f / s_S[rt];
-      const float Mdc = resid ? s_M[rd] * c : 0.0f, iSd = resid ? 1.0f / s_S[rd] : 0.0f;
+      const float Mt = s_M[rt], iSt = 1.0f / s_S[rt];
+      const float Md = resid ? s_M[rd] : 0.0f, iSd = resid ? 1.0f / s_S[rd] : 0.0f;
       float x[EPG], y[EPG];
       unpack16<DT>(gt, x);
       unpack16<DT>(gd, y);
 #pragma unroll
       for (int q = 0; q < EPG; ++q) {
-        const float p = ex2(fmaf(x[q], c, -Mtc)) * iSt;
+        const float p = ex2((x[q] - Mt) * c) * iSt;
         wp[q] = p;
-        wr[q] = resid ? fmaxf(0.0f, p - ex2(fmaf(y[q], c, -Mdc)) * iSd) : p;
+        wr[q] = resid ? fmaxf(0.0f, p - ex2((y[q] - Md) * c) * iSd) : p;
       }
     };
 #pragma unroll

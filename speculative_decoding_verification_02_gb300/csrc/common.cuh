@@ -324,13 +324,15 @@ __device__ __forceinline__ float batch_max(const uint4 *g) {
   return bm;
 }
 
-// Adds 2^(x c - mc) over the batch into the two-lane accumulator: one packed
-// FMA per two logits, one ex2 per logit, one packed add per two.
+// Adds 2^((x - m) c) over the batch into the two-lane accumulator: one
+// packed subtract and one packed multiply per two logits (x - m first, so a
+// large |m c| adds no rounding offset to every exponent), one ex2 per logit,
+// one packed add per two.
 template <int DT>
-__device__ __forceinline__ void batch_sumexp(const uint4 *g, float c, float mc, float2 &acc) {
-  const float2 cc = make_float2(c, c), nm = make_float2(-mc, -mc);
+__device__ __forceinline__ void batch_sumexp(const uint4 *g, float c, float m, float2 &acc) {
+  const float2 cc = make_float2(c, c), nm = make_float2(-m, -m);
   auto fold = [&](float a, float b) {
-    const float2 z = __ffma2_rn(make_float2(a, b), cc, nm);
+    const float2 z = __fmul2_rn(__fadd2_rn(make_float2(a, b), nm), cc);
     acc = __fadd2_rn(acc, make_float2(ex2(z.x), ex2(z.y)));
   };
 #pragma unroll
@@ -395,7 +397,7 @@ __device__ __forceinline__ void fold_batch(const uint4 *g, int first_elem, float
       idx = first;
     }
   }
-  if (SOFTMAX && m != -INFINITY) batch_sumexp<DT>(g, c, m * c, s2);
+  if (SOFTMAX && m != -INFINITY) batch_sumexp<DT>(g, c, m, s2);
 }
 
 // Statistics of row[v0, v1) for the calling thread (strided over the block):

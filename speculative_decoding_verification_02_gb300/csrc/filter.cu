@@ -22,6 +22,14 @@
 //     every CTA picks the same digit: the bin holding the top_k-th largest
 //     count, or the bin where the mass from the top reaches top_p times the
 //     kept mass.
+// Most rows never need the full radix walk.  When top-k is on, one pass
+// counts the logits in the top-byte bin of the row's max and in the bin
+// below it (packed bf16x2 compares), and copies the first bin's logits into
+// a short list in shared memory; when that window already holds top_k
+// logits (and each CTA's share fits the list), the radix walk and the top-p
+// walk run over the list alone, and the kept mass is added in 2^-44 fixed
+// point (so the list's order, which the appends leave unspecified, does not
+// matter).  Otherwise the walk runs over the whole slice as above.
 // The outputs are the chain verification's per-row statistics, as one
 // partial per row -- (max M, sum over kept logits of 2^((x - M) c), the
 // drafted token's logit) -- and theta, which the accept kernels apply as a
@@ -40,6 +48,7 @@ namespace sv {
 
 constexpr int kFilterThreads = 512;
 constexpr int kFilterWarps = kFilterThreads / 32;
+constexpr int kFilterListCap = 1024;             // candidate logits per CTA on the list path
 constexpr double kMassScale = 17592186044416.0;  // 2^44: fixed-point unit of the histogram masses
 
 // Order-preserving unsigned key of an fp32 value (its bits); -0 maps to +0.
@@ -60,21 +69,30 @@ __device__ __forceinline__ float prefix_value(uint32_t prefix, int levels) {
   return key_value((key & 0x80000000u) ? key : (key | 0xffffu));
 }
 
+// The smallest logit of the dtype whose key has top byte d (1 <= d <= 255):
+// x >= bin_floor(d) exactly when key(x) >> 24 >= d, for every non-NaN x.
+template <int DT>
+__device__ __forceinline__ float bin_floor(uint32_t d) {
+  if (d & 0x80u) return __uint_as_float((d & 0x7fu) << 24);
+  if (DT == SPEC_DTYPE_F32) return __uint_as_float(((~d & 0xffu) << 24) | 0xffffffu);
+  return __uint_as_float(((((~d & 0xffu) << 8) | 0xffu)) << 16);
+}
+
+// 0x0001 in each 16-bit half of a bf16 pair that is >= the pair t2.
+__device__ __forceinline__ uint32_t ge_pair(uint32_t w, uint32_t t2) {
+  return __hge2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&w), *reinterpret_cast<const __nv_bfloat162 *>(&t2)) &
+         0x00010001u;
+}
+
+// The fixed-point (2^-44) mass of one logit, 2^((x - M) c).
+__device__ __forceinline__ unsigned long long fixed_mass(float x, float c, float M) {
+  return static_cast<unsigned long long>(static_cast<double>(ex2((x - M) * c)) * kMassScale);
+}
+
 template <int DT>
 __device__ __forceinline__ uint32_t elem_bits(const void *s, int e) {
   if (DT == SPEC_DTYPE_F32) return reinterpret_cast<const uint32_t *>(s)[e];
   return static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(s)[e]) << 16;
-}
-
-// Cluster-wide sum of one value per CTA, added in rank order (the same
-// result in every CTA).  `slot` is a [kMaxCluster] array in shared memory.
-template <class T>
-__device__ __forceinline__ T cluster_sum_ranked(cg::cluster_group &cluster, T *slot, T v, int CS, int rank) {
-  if (threadIdx.x < CS) *cluster.map_shared_rank(&slot[rank], threadIdx.x) = v;
-  cluster.sync();
-  T s = T(0);
-  for (int q = 0; q < CS; ++q) s += slot[q];
-  return s;
 }
 
 template <int DT, bool VEC>
@@ -116,15 +134,32 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
 
   // ---- the slice into shared memory, and the slice max
   float mloc = -INFINITY;
+  const int ng = VEC ? n / EPG : 0;  // n is a multiple of EPG on the 16-byte path
   if (VEC) {
-    const int ng = n / EPG;  // n is a multiple of EPG on the 16-byte path
-    for (int g = tid; g < ng; g += kFilterThreads) {
-      const uint4 w = __ldg(reinterpret_cast<const uint4 *>(row + static_cast<int64_t>(lo + g * EPG) * ES));
-      reinterpret_cast<uint4 *>(s_row)[g] = w;
-      float x[EPG];
-      unpack16<DT>(w, x);
-#pragma unroll
-      for (int e = 0; e < EPG; ++e) mloc = fmaxf(mloc, x[e]);
+    // every 16-byte copy in flight at once, then one wait
+    const char *src = row + static_cast<int64_t>(lo) * ES;
+    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(s_row));
+    for (int g = tid; g < ng; g += kFilterThreads)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16u * g), "l"(src + 16 * static_cast<int64_t>(g))
+                   : "memory");
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    if (DT == SPEC_DTYPE_BF16) {
+      __nv_bfloat162 mx = __float2bfloat162_rn(-INFINITY);
+      for (int g = tid; g < ng; g += kFilterThreads) {
+        const uint4 w = reinterpret_cast<const uint4 *>(s_row)[g];
+        mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162 *>(&w.x));
+        mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162 *>(&w.y));
+        mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162 *>(&w.z));
+        mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162 *>(&w.w));
+      }
+      mloc = fmaxf(__low2float(mx), __high2float(mx));
+    } else {
+      for (int g = tid; g < ng; g += kFilterThreads) {
+        const uint4 w = reinterpret_cast<const uint4 *>(s_row)[g];
+        mloc = fmaxf(mloc, fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
+                                 fmaxf(__uint_as_float(w.z), __uint_as_float(w.w))));
+      }
     }
   } else {
     for (int e = tid; e < n; e += kFilterThreads) {
@@ -142,43 +177,170 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
   cluster.sync();
   float M = -INFINITY;
   for (int q = 0; q < CS; ++q) M = fmaxf(M, s_cf[q]);
-  const float Mc = M * c;
+
+  // ---- the list path (top-k on): the window of the max's top-byte bin, or
+  // of that bin and the one below, when the window holds top_k logits and
+  // each CTA's share fits the list
+  __shared__ uint32_t s_list[kFilterListCap];
+  __shared__ int s_nlist;
+  __shared__ uint32_t s_xc[2][kMaxCS];  // per rank: logits >= tau0, logits >= tau1
+  __shared__ uint32_t s_w0[kFilterWarps], s_w1[kFilterWarps];
+  bool use_list = false;  // the walk runs over s_union[0, nlist) in rank 0 alone
+  int nlist = 0;
+  uint32_t *s_union = s_list;
+  const uint32_t BM = order_key(__float_as_uint(M)) >> 24;
+  // (not for a max in the two bins at +0, whose floors +0 and the smallest
+  // normal would let a flushed subnormal compare on the wrong side)
+  if (P.top_k > 0 && P.top_k < V && BM >= 2u && (BM | 1u) != 0x81u) {
+    const float tau0 = bin_floor<DT>(BM), tau1 = bin_floor<DT>(BM - 1u);
+    // appends every logit >= tau to the list (up to its capacity); with
+    // COUNT, also counts the logits >= tau0 and >= tau1 (tau = tau0)
+    auto scan = [&]<bool COUNT>(float tau, uint32_t &c0, uint32_t &c1) {
+      auto append = [&](uint32_t bits) {
+        const int pos = atomicAdd(&s_nlist, 1);
+        if (pos < kFilterListCap) s_list[pos] = bits;
+      };
+      if (VEC && DT == SPEC_DTYPE_BF16) {
+        const uint32_t ta = (__float_as_uint(tau) >> 16) * 0x10001u;
+        const uint32_t t1 = (__float_as_uint(tau1) >> 16) * 0x10001u;
+        uint32_t p0 = 0u, p1 = 0u;  // two 16-bit counters each (at most 48 per half)
+        for (int g = tid; g < ng; g += kFilterThreads) {
+          const uint4 w = reinterpret_cast<const uint4 *>(s_row)[g];
+          const uint32_t a0 = ge_pair(w.x, ta), a1 = ge_pair(w.y, ta), a2 = ge_pair(w.z, ta), a3 = ge_pair(w.w, ta);
+          if (COUNT) {
+            p0 += a0 + a1 + a2 + a3;
+            p1 += ge_pair(w.x, t1) + ge_pair(w.y, t1) + ge_pair(w.z, t1) + ge_pair(w.w, t1);
+          }
+          if (a0 | a1 | a2 | a3) {
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+              const uint32_t bits = (h & 1) ? (ws[h >> 1] & 0xffff0000u) : (ws[h >> 1] << 16);
+              if (__uint_as_float(bits) >= tau) append(bits);
+            }
+          }
+        }
+        c0 = (p0 & 0xffffu) + (p0 >> 16);
+        c1 = (p1 & 0xffffu) + (p1 >> 16);
+      } else {
+        c0 = c1 = 0u;
+        for (int e = tid; e < n; e += kFilterThreads) {
+          const uint32_t bits = elem_bits<DT>(s_row, e);
+          const float x = __uint_as_float(bits);
+          if (COUNT) {
+            c0 += x >= tau0;
+            c1 += x >= tau1;
+          }
+          if (x >= tau) append(bits);
+        }
+      }
+    };
+    if (tid == 0) s_nlist = 0;
+    __syncthreads();
+    uint32_t c0, c1;
+    scan.template operator()<true>(tau0, c0, c1);
+    c0 = __reduce_add_sync(0xffffffffu, c0);
+    c1 = __reduce_add_sync(0xffffffffu, c1);
+    if (lane == 0) {
+      s_w0[warp] = c0;
+      s_w1[warp] = c1;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      c0 = __reduce_add_sync(0xffffffffu, lane < kFilterWarps ? s_w0[lane] : 0u);
+      c1 = __reduce_add_sync(0xffffffffu, lane < kFilterWarps ? s_w1[lane] : 0u);
+      if (lane < CS) {  // this CTA's counts, into every CTA of the cluster
+        *cluster.map_shared_rank(&s_xc[0][rank], lane) = c0;
+        *cluster.map_shared_rank(&s_xc[1][rank], lane) = c1;
+      }
+    }
+    cluster.sync();
+    uint32_t T0 = 0u, T1 = 0u, A0 = 0u, A1 = 0u;  // cluster totals, largest per-CTA counts
+    for (int q = 0; q < CS; ++q) {
+      T0 += s_xc[0][q];
+      T1 += s_xc[1][q];
+      A0 = max(A0, s_xc[0][q]);
+      A1 = max(A1, s_xc[1][q]);
+    }
+    const uint32_t K = static_cast<uint32_t>(P.top_k);
+    int win = -1;  // the window taken: 0 (>= tau0), 1 (>= tau1), -1 none
+    if (T0 >= K && A0 <= static_cast<uint32_t>(kFilterListCap)) {
+      win = 0;  // the lists hold every logit >= tau0
+    } else if (T1 >= K && A1 <= static_cast<uint32_t>(kFilterListCap)) {
+      if (tid == 0) s_nlist = 0;
+      __syncthreads();
+      scan.template operator()<false>(tau1, c0, c1);
+      win = 1;  // the lists hold every logit >= tau1
+      cluster.sync();  // every slice scan is over before rank 0's slice buffer is reused
+    }
+    if (win >= 0) {
+      // the union of the lists, in rank order, into rank 0's slice buffer (no
+      // slice is read again on this path; CS lists of at most kFilterListCap
+      // entries fit in any slice of a row that needs CS > 1); then rank 0
+      // goes on alone
+      use_list = true;
+      __syncthreads();
+      const int mine = min(s_nlist, kFilterListCap);
+      if (CS > 1) {
+        uint32_t off = 0u, total = 0u;
+        for (int q = 0; q < CS; ++q) {
+          const uint32_t cq = s_xc[win][q];
+          off += q < rank ? cq : 0u;
+          total += cq;
+        }
+        uint32_t *dst = cluster.map_shared_rank(reinterpret_cast<uint32_t *>(s_row), 0) + off;
+        for (int e = tid; e < mine; e += kFilterThreads) dst[e] = s_list[e];
+        cluster.sync();
+        if (rank != 0) return;  // (no CTA touches another's shared memory after this barrier)
+        s_union = reinterpret_cast<uint32_t *>(s_row);
+        nlist = static_cast<int>(total);
+      } else {
+        nlist = mine;
+      }
+    }
+  }
 
   // ---- radix selection: one level of the histogram walk.  Builds the
   // level's cluster-wide histogram of digit (key >> shift) & 255 over the
   // logits whose key >> (shift + 8) equals `prefix` (all logits at the first
-  // level) and >= floor; then warp 0 walks the bins from the top until the
-  // count (BY_MASS: the mass) reaches `need`.  Returns the digit; `rest`
-  // becomes need minus what the bins above the digit hold.
+  // level) and >= floor -- on the list path, the logits of the list (which
+  // holds every logit >= the answer); then warp 0 walks the bins from the top until the
+  // count (BY_MASS: the mass) reaches `need` -- or, with frac > 0, frac
+  // times the level's whole mass.  Returns the digit; `rest` becomes need
+  // minus what the bins above the digit hold.
   int level_no = 0;
   auto level = [&](int shift, uint32_t prefix, bool first, float floor, bool by_mass,
-                   unsigned long long need, unsigned long long &rest) -> uint32_t {
+                   unsigned long long need, unsigned long long &rest, float frac = 0.0f) -> uint32_t {
     const int buf = level_no++ & 1;  // the other buffer may still be read by other CTAs
     for (int d = tid; d < 256; d += kFilterThreads) {
       s_cnt[buf][d] = 0u;
       s_mass[buf][d] = 0ull;
     }
     __syncthreads();
-    for (int e = tid; e < n; e += kFilterThreads) {
-      const uint32_t bits = elem_bits<DT>(s_row, e);
+    const int ne = use_list ? nlist : n;
+    for (int e = tid; e < ne; e += kFilterThreads) {
+      const uint32_t bits = use_list ? s_union[e] : elem_bits<DT>(s_row, e);
       const uint32_t key = order_key(bits);
       if (!first && (key >> (shift + 8)) != prefix) continue;
       const float x = __uint_as_float(bits);
       if (!(x >= floor)) continue;
       const uint32_t d = (key >> shift) & 255u;
       atomicAdd(&s_cnt[buf][d], 1u);
-      if (by_mass) {
-        const double w = static_cast<double>(ex2(fmaf(x, c, -Mc))) * kMassScale;
-        atomicAdd(&s_mass[buf][d], static_cast<unsigned long long>(w));
-      }
+      if (by_mass) atomicAdd(&s_mass[buf][d], fixed_mass(x, c, M));
     }
-    cluster.sync();  // every CTA's histogram is complete
+    if (use_list) __syncthreads();  // rank 0 alone: its histogram is the row's
+    else cluster.sync();            // every CTA's histogram is complete
     for (int d = tid; d < 256; d += kFilterThreads) {
       uint32_t cnt = 0u;
       unsigned long long ms = 0ull;
-      for (int q = 0; q < CS; ++q) {
-        cnt += *cluster.map_shared_rank(&s_cnt[buf][d], q);
-        if (by_mass) ms += *cluster.map_shared_rank(&s_mass[buf][d], q);
+      if (use_list) {
+        cnt = s_cnt[buf][d];
+        ms = s_mass[buf][d];
+      } else {
+        for (int q = 0; q < CS; ++q) {
+          cnt += *cluster.map_shared_rank(&s_cnt[buf][d], q);
+          if (by_mass) ms += *cluster.map_shared_rank(&s_mass[buf][d], q);
+        }
       }
       t_cnt[d] = cnt;
       t_mass[d] = ms;
@@ -197,6 +359,11 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
       for (int o = 1; o < 32; o <<= 1) {
         const unsigned long long v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
+      }
+      if (frac > 0.0f) {
+        const unsigned long long total = __shfl_sync(0xffffffffu, incl, 31);
+        need = static_cast<unsigned long long>(static_cast<double>(frac) * static_cast<double>(total));
+        if (need == 0ull) need = 1ull;
       }
       const unsigned hit = __ballot_sync(0xffffffffu, lsum > 0ull && incl >= need);
       if (hit) {
@@ -261,84 +428,84 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
     uint32_t prefix = 0u;
     unsigned long long need = 0ull, rest = 0ull;
     for (int lv = 0; lv < kLevels; ++lv) {
-      const int shift = 24 - 8 * lv;
-      if (lv == 0) {
-        // the first level's histogram also gives the kept mass: need = top_p of it
-        // (a first pass with need = max makes the walk fall through; the histogram stays)
-        (void)level(shift, 0u, true, theta, true, ~0ull, rest);
-        unsigned long long total = 0ull;
-        for (int d = 0; d < 256; ++d) total += t_mass[d];
-        need = static_cast<unsigned long long>(static_cast<double>(P.top_p) * static_cast<double>(total));
-        if (need == 0ull) need = 1ull;
-        // pick the digit from the same histogram
-        if (tid == 0) {
-          unsigned long long run = 0ull;
-          int sel = -1, last = -1;
-          for (int d = 255; d >= 0; --d) {
-            if (t_cnt[d] == 0u) continue;
-            last = d;
-            if (run + t_mass[d] >= need) {
-              sel = d;
-              break;
-            }
-            run += t_mass[d];
-          }
-          if (sel < 0) {
-            sel = last < 0 ? 0 : last;
-            run = 0ull;
-            for (int d = 255; d > sel; --d) run += t_mass[d];
-          }
-          s_sel_digit = static_cast<uint32_t>(sel);
-          s_sel_rest = need > run ? need - run : 1ull;
-        }
-        __syncthreads();
-        prefix = s_sel_digit;
-        need = s_sel_rest;
-        __syncthreads();
-      } else {
-        const uint32_t d = level(shift, prefix, false, theta, true, need, rest);
-        prefix = (prefix << 8) | d;
-        need = rest;
-      }
+      // the first level's walk needs top_p of the kept mass it histograms
+      const uint32_t d = level(24 - 8 * lv, prefix, lv == 0, theta, true, need, rest, lv == 0 ? P.top_p : 0.0f);
+      prefix = (prefix << 8) | d;
+      need = rest;
     }
     theta = fmaxf(theta, prefix_value<DT>(prefix, kLevels));
   }
 
-  // ---- the kept logits: their mass, count and smallest value
+  // ---- the kept logits: their mass, count and smallest value.  On the list
+  // path the mass is added in 2^-44 fixed point (the list's order is not
+  // fixed); on the slice, in fp32 in thread order, then in warp, block and
+  // rank order.  Either way every run gives the same bits.
   float s_loc = 0.0f, mn = INFINITY;
+  unsigned long long f_loc = 0ull;
   uint32_t cnt = 0u;
-  for (int e = tid; e < n; e += kFilterThreads) {
-    const float x = __uint_as_float(elem_bits<DT>(s_row, e));
-    if (x >= theta) {
-      s_loc += ex2(fmaf(x, c, -Mc));
-      mn = fminf(mn, x);
-      ++cnt;
+  if (use_list) {
+    for (int e = tid; e < nlist; e += kFilterThreads) {
+      const float x = __uint_as_float(s_union[e]);
+      if (x >= theta) {
+        f_loc += fixed_mass(x, c, M);
+        mn = fminf(mn, x);
+        ++cnt;
+      }
+    }
+  } else {
+    for (int e = tid; e < n; e += kFilterThreads) {
+      const float x = __uint_as_float(elem_bits<DT>(s_row, e));
+      if (x >= theta) {
+        s_loc += ex2((x - M) * c);
+        mn = fminf(mn, x);
+        ++cnt;
+      }
     }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) f_loc += __shfl_xor_sync(0xffffffffu, f_loc, o);
   s_loc = warp_sum(s_loc);
   mn = -warp_allmax(-mn);
   cnt = __reduce_add_sync(0xffffffffu, cnt);
   __shared__ float s_mn[kFilterWarps];
+  __shared__ unsigned long long s_redf[kFilterWarps];
+  __shared__ float s_cmn[kMaxCS];
   if (lane == 0) {
     s_red[warp] = s_loc;
+    s_redf[warp] = f_loc;
     s_redu[warp] = cnt;
     s_mn[warp] = mn;
   }
   __syncthreads();
   if (warp == 0) {
     s_loc = warp_sum(lane < kFilterWarps ? s_red[lane] : 0.0f);
+    f_loc = lane < kFilterWarps ? s_redf[lane] : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) f_loc += __shfl_xor_sync(0xffffffffu, f_loc, o);
     cnt = __reduce_add_sync(0xffffffffu, lane < kFilterWarps ? s_redu[lane] : 0u);
     mn = -warp_allmax(-(lane < kFilterWarps ? s_mn[lane] : INFINITY));
+    if (!use_list && lane < CS) {  // this CTA's sums, into every CTA of the cluster
+      *cluster.map_shared_rank(&s_cs[rank], lane) = s_loc;
+      *cluster.map_shared_rank(&s_cu[rank], lane) = cnt;
+      *cluster.map_shared_rank(&s_cmn[rank], lane) = mn;
+    }
   }
-  __shared__ float s_cmn[kMaxCS];
-  if (tid == 0) s_red[0] = s_loc, s_redu[0] = cnt, s_mn[0] = mn;
-  __syncthreads();
-  if (tid < CS) *cluster.map_shared_rank(&s_cmn[rank], tid) = s_mn[0];
-  const float S = cluster_sum_ranked(cluster, s_cs, s_red[0], CS, rank);
-  const uint32_t kept = cluster_sum_ranked(cluster, s_cu, s_redu[0], CS, rank);
+  // (after this barrier no CTA touches another's shared memory)
+  if (!use_list) cluster.sync();
   if (rank == 0 && tid == 0) {
-    float smallest = INFINITY;
-    for (int q = 0; q < CS; ++q) smallest = fminf(smallest, s_cmn[q]);
+    float S = 0.0f, smallest = INFINITY;
+    uint32_t kept = 0u;
+    if (use_list) {  // rank 0 alone, over the whole row's list
+      S = static_cast<float>(static_cast<double>(f_loc) / kMassScale);
+      kept = cnt;
+      smallest = mn;
+    } else {
+      for (int q = 0; q < CS; ++q) {
+        S += s_cs[q];
+        kept += s_cu[q];
+        smallest = fminf(smallest, s_cmn[q]);
+      }
+    }
     float xtok = -INFINITY;
     if (i < L) {
       const int tok = P.draft[static_cast<int64_t>(b) * k + i];
@@ -348,7 +515,6 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
     P.theta[j] = smallest;
     if (P.kept) P.kept[j] = static_cast<int32_t>(kept);
   }
-  cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 // Cluster geometry: at most 16 CTAs, each slice at most 96 KB of logits.

@@ -163,15 +163,16 @@ __device__ __forceinline__ float groups_max(const uint4 *g, int n) {
   return fmaxf(a, b);
 }
 
-// Adds 2^(x c - mc) over the logits of the first n groups into acc (one
-// packed FMA per two logits, one exponential per logit, one packed add per
-// two; consecutive groups alternate between two accumulators).
+// Adds 2^((x - m) c) over the logits of the first n groups into acc (one
+// packed subtract and one packed multiply per two logits, one exponential
+// per logit, one packed add per two; consecutive groups alternate between
+// two accumulators).
 template <int DT>
-__device__ __forceinline__ void groups_sumexp(const uint4 *g, int n, float c, float mc, float2 &acc) {
-  const float2 cc = make_float2(c, c), nm = make_float2(-mc, -mc);
+__device__ __forceinline__ void groups_sumexp(const uint4 *g, int n, float c, float m, float2 &acc) {
+  const float2 cc = make_float2(c, c), nm = make_float2(-m, -m);
   float2 acc2 = make_float2(0.0f, 0.0f);
   auto fold = [&](float2 &A, float a, float b) {
-    const float2 z = __ffma2_rn(make_float2(a, b), cc, nm);
+    const float2 z = __fmul2_rn(__fadd2_rn(make_float2(a, b), nm), cc);
     A = __fadd2_rn(A, make_float2(ex2(z.x), ex2(z.y)));
   };
 #pragma unroll
@@ -245,7 +246,7 @@ __device__ __forceinline__ void lane_rows_stats(const char *const *rows, int lo,
           }
           R[r].m = bm;
         }
-        if (R[r].m != -INFINITY) groups_sumexp<DT>(x[r], n, c, R[r].m * c, R[r].s);
+        if (R[r].m != -INFINITY) groups_sumexp<DT>(x[r], n, c, R[r].m, R[r].s);
       } else if (bm > R[r].m) {
         R[r].m = bm;
         R[r].i = groups_first<DT>(x[r], n, bm, e0, 32 * EPG);

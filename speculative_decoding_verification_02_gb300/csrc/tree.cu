@@ -69,12 +69,12 @@ __device__ __forceinline__ const char *node_row(const char *base, int64_t req, i
 // consecutive lanes touch consecutive words.
 __device__ __forceinline__ int stage_index(int g, int e, int epg) { return (((g >> 5) * epg + e) << 5) + (g & 31); }
 
-// p_v = 2^(t_v c - Mtc) iSt and q_v = 2^(d_v c - Mdc) iSd over this lane's
+// p_v = 2^((t_v - Mt) c) iSt and q_v = 2^((d_v - Md) c) iSd over this lane's
 // groups (logits >= hi read as -inf, so give 0); returns the lane's sum of
 // max(0, p_v - cres q_v).  STORE also writes p_v, q_v to sp, sq.
 template <int DT, bool VEC, bool STORE>
 __device__ __forceinline__ float lane_residual(const char *trow, const char *drow, int lo, int hi, int G,
-                                               float Mtc, float Mdc, float c, float iSt, float iSd, float cres,
+                                               float Mt, float Md, float c, float iSt, float iSd, float cres,
                                                float *sp, float *sq) {
   constexpr int EPG = Elems<DT>::kPerGroup;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -97,8 +97,8 @@ __device__ __forceinline__ float lane_residual(const char *trow, const char *dro
         unpack16<DT>(xd[u], d);
 #pragma unroll
         for (int e = 0; e < EPG; ++e) {
-          const float pv = ex2(fmaf(t[e], c, -Mtc)) * iSt;
-          const float qv = ex2(fmaf(d[e], c, -Mdc)) * iSd;
+          const float pv = ex2((t[e] - Mt) * c) * iSt;
+          const float qv = ex2((d[e] - Md) * c) * iSd;
           if (STORE) {
             sp[stage_index(g0 + 32 * u, e, EPG)] = pv;
             sq[stage_index(g0 + 32 * u, e, EPG)] = qv;
@@ -352,15 +352,11 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
     float rmass = lane < ncl ? r.st * ex2((r.mt - Mt) * c) * iSt : 0.0f;
     float w_mass = -1.0f;  // this warp's share of it; < 0: p, from the warp's statistics
 
-    // the p and q of child i's token (from the children's token logits)
+    // the p and q of child i's token (from the children's token logits), rounded
+    // as the sweeps over the slice round them
     auto pq_of = [&](int i, float &pv, float &qv) {
       pv = ex2((s_kt[i] - Mt) * c) * iSt;
       qv = ex2((s_kd[i] - Md) * c) * iSd;
-    };
-    // the same, rounded as the sweeps over the slice round them
-    auto pq_sweep = [&](int i, float &pv, float &qv) {
-      pv = ex2(fmaf(s_kt[i], c, -Mt * c)) * iSt;
-      qv = ex2(fmaf(s_kd[i], c, -Md * c)) * iSd;
     };
     // Siblings drawn without replacement (P.wor): each rejected sibling's
     // token is removed from q.  A removed token's residual keeps the
@@ -404,10 +400,10 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
             part += fmaxf(0.0f, s_p[stage_index(g, e, EPG)] - cnew * s_q[stage_index(g, e, EPG)]);
         }
       } else if (P.stage) {
-        part = lane_residual<DT, VEC, true>(trow, drow, lo, hi, G, Mt * c, Md * c, c, iSt, iSd, cnew, s_p, s_q);
+        part = lane_residual<DT, VEC, true>(trow, drow, lo, hi, G, Mt, Md, c, iSt, iSd, cnew, s_p, s_q);
         staged = true;
       } else {
-        part = lane_residual<DT, VEC, false>(trow, drow, lo, hi, G, Mt * c, Md * c, c, iSt, iSd, cnew, s_p, s_q);
+        part = lane_residual<DT, VEC, false>(trow, drow, lo, hi, G, Mt, Md, c, iSt, iSd, cnew, s_p, s_q);
       }
       if (P.wor) {
         // tokens removed earlier keep their own coefficient: the lane owning
@@ -418,7 +414,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
           const int gy = (y - lo) / EPG;
           if (lane != (gy & 31) || warp != (gy >> 5) / G) continue;
           float py, qy;
-          pq_sweep(i, py, qy);
+          pq_of(i, py, qy);
           part += fmaxf(0.0f, py - s_kc[i] * qy) - fmaxf(0.0f, py - cnew * qy);
         }
       }
@@ -460,7 +456,6 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
     if (rank == draw_rank) {
       // the warp whose range holds the crossing, then that range
       const float mass = w_mass >= 0.0f ? w_mass : (w_m == -INFINITY ? 0.0f : w_s * ex2((w_m - Mt) * c) * iSt);
-      const float Mtc = Mt * c, Mdc = Md * c;
       // (the fallback `lo` is unreachable: the drawing rank has mass, so one of its warps has)
       final_tok = range_draw<kTreeThreads, EPG>(mass, tl, lo, G, lo, nullptr, [&](int g, float *w) {
         if (staged) {
@@ -471,12 +466,12 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
           float t[EPG];
           unpack16<DT>(load_group<DT, VEC>(trow, lo + g * EPG, hi), t);
 #pragma unroll
-          for (int e = 0; e < EPG; ++e) w[e] = ex2(fmaf(t[e], c, -Mtc)) * iSt;
+          for (int e = 0; e < EPG; ++e) w[e] = ex2((t[e] - Mt) * c) * iSt;
           if (cres > 0.0f) {
             float d[EPG];
             unpack16<DT>(load_group<DT, VEC>(drow, lo + g * EPG, hi), d);
 #pragma unroll
-            for (int e = 0; e < EPG; ++e) w[e] = fmaxf(0.0f, w[e] - cres * (ex2(fmaf(d[e], c, -Mdc)) * iSd));
+            for (int e = 0; e < EPG; ++e) w[e] = fmaxf(0.0f, w[e] - cres * (ex2((d[e] - Md) * c) * iSd));
           }
         }
         if (P.wor) {  // removed tokens keep the coefficient of their removal
@@ -484,7 +479,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
             const int y = s_tok[s_kids[i]] - lo - g * EPG;
             if (s_kc[i] < 0.0f || y < 0 || y >= EPG) continue;
             float py, qy;
-            pq_sweep(i, py, qy);
+            pq_of(i, py, qy);
             const float wy = fmaxf(0.0f, py - s_kc[i] * qy);
 #pragma unroll
             for (int e = 0; e < EPG; ++e)  // (no dynamic index into the register array)

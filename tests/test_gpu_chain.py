@@ -325,3 +325,24 @@ def test_sample_parity_cluster_accept_path(seed, B, k, V, dtype, T, chain_path):
     print("near-threshold", stats)
     if B >= 16:  # enough requests that some are rejected
         assert (r["accepted"] < draft_len).any()
+
+
+@pytest.mark.parametrize("dtype,offset", [("fp32", 40.0), ("bf16", 40.0), ("fp32", -300.0)])
+def test_sample_parity_large_logits_low_temperature(dtype, offset):
+    """Logits shifted to +40 (or -300) at T = 0.05, so |max| / T is above
+    1,000: every exponent must be formed as (x - max) / T.  Rounding max / T
+    on its own would shift all of them by up to 6e-5 and put p off by more
+    than the 1e-5 tolerance."""
+    rng = np.random.default_rng(61)
+    B, k, V, T = 24, 4, 30_000, 0.05
+    base = workloads.chain_problem(61, B, k, V, "fp32", 1.0, target_std=0.15,
+                                   noise_std=np.linspace(0.005, 0.05, B).astype(np.float32))
+    cast = workloads.bf16_bits if dtype == "bf16" else (lambda a: np.ascontiguousarray(a, np.float32))
+    prob = dict(base, target=cast(base["target"] + np.float32(offset)),
+                draft_logits=cast(base["draft_logits"] + np.float32(offset)), T=T, dtype=dtype)
+    for b in range(B):
+        for i in range(k):
+            prob["draft"][b, i] = workloads.gumbel_draw(rng, prob["draft_logits"][b, i], T)
+    g, r = _run_sample(prob), _oracle_sample(prob)
+    print("near-threshold", check_chain_sample(prob, g, r))
+    assert 0 < r["accepted"].mean() < k

@@ -277,3 +277,65 @@ def test_filtered_draws_and_their_distribution():
     dof = kept.sum() - 1
     assert chi2 < dof + 6 * np.sqrt(2 * dof), (chi2, dof)
     print("kept", kept.sum(), "chi2", chi2, "dof", dof)
+
+
+def _path_rows(kind, V, rng):
+    """Rows that steer the filter kernel down each of its paths (with top_k =
+    50): the max's top-byte bin holding >= 50 logits ("bin0"); fewer, with the
+    bin below completing them ("bin1"); a top bin too full for the per-CTA
+    list ("dense"); a negative max ("negative"); a max in the two lowest
+    bins, the window reaching bin 1 ("tiny"); a max of +0, where the window
+    is not tried ("zero")."""
+    x = (rng.standard_normal(V) * 0.3).astype(np.float32)
+    if kind == "bin0":
+        x = (rng.standard_normal(V) * 2.5).astype(np.float32)
+    elif kind == "bin1":
+        x[rng.choice(V, 300, replace=False)] = rng.uniform(2.5, 7.5, 300)
+        x[rng.choice(V, 3, replace=False)] = 20.0
+    elif kind == "dense":
+        x = rng.uniform(8.5, 30.0, V).astype(np.float32)
+    elif kind == "negative":
+        x = rng.uniform(-30.0, -1.5, V).astype(np.float32)
+    elif kind == "tiny":
+        x[:] = -np.inf
+        x[rng.choice(V, 60, replace=False)] = -1e38
+        x[rng.choice(V, 3, replace=False)] = -2e37
+    elif kind == "zero":
+        x = -np.abs(x)
+        x[rng.choice(V, 70, replace=False)] = 0.0
+    return x
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("top_p", [1.0, 0.7])
+def test_filter_paths(dtype, top_p):
+    """Every path of the filter kernel: the thresholds and kept counts of
+    spec_filter_rows, and filtered verification (p_tok, q_tok and the
+    residual mass test the kept mass) on requests made of the same rows."""
+    rng = np.random.default_rng(77)
+    V, top_k, T = 128_256, 50, 1.0
+    kinds = ["bin0", "bin1", "dense", "negative", "tiny", "zero"]
+    x = np.stack([_path_rows(kd, V, rng) for kd in kinds])
+    rows = workloads.bf16_bits(x) if dtype == "bf16" else x
+    g = host(api.spec_filter_rows(to_dev(rows), T, top_k, top_p))
+    for r in range(len(kinds)):
+        ok, was_near = _cut_ok(rows[r], T, top_k, top_p, float(g["theta"][r]))
+        _, theta_o, kept_o = oracle.filter_row(rows[r], T, top_k, top_p)
+        assert ok, (kinds[r], g["theta"][r], theta_o)
+        assert was_near or g["kept"][r] == kept_o, (kinds[r], g["kept"][r], kept_o)
+    # requests: target rows 0..k from one kind, draft rows = target + noise
+    B, k = len(kinds), 2
+    tgt = np.repeat(x[:, None, :], k + 1, axis=1).copy()
+    tgt[:, 1:] += (rng.standard_normal((B, k, V)) * 0.05).astype(np.float32)
+    dl = tgt[:, :k] + (rng.standard_normal((B, k, V)) * 0.2).astype(np.float32)
+    cast = workloads.bf16_bits if dtype == "bf16" else (lambda a: np.ascontiguousarray(a, np.float32))
+    prob = dict(target=cast(tgt), draft_logits=cast(dl), T=T, B=B, k=k, V=V, dtype=dtype,
+                draft=np.zeros((B, k), np.int32), uniforms=workloads.uniforms(rng, (B, k + 1)))
+    for b in range(B):
+        for i in range(k):
+            qf = oracle.filter_row(prob["draft_logits"][b, i], T, top_k, top_p)[0]
+            prob["draft"][b, i] = rng.choice(V, p=qf / qf.sum())
+    gv = _run(prob, top_k, top_p)
+    r = oracle.verify_sample(prob["target"], prob["draft_logits"], prob["draft"], prob["uniforms"], T,
+                             top_k=top_k, top_p=top_p, threads=oracle.max_threads())
+    _check(prob, gv, r, top_k, top_p)

@@ -157,3 +157,17 @@ def test_without_replacement_duplicate_and_exhausted_tokens():
     prob = workloads.tree_problem(18, 48, 16, 1, 15, 3, "fp32", 1.0, target_std=1.0, noise_std=1.5, peaks=0)
     g, r = _run_tree(prob, wor=True), _oracle_tree(prob, wor=True)
     check_tree(prob, g, r, without_replacement=True)
+
+
+@pytest.mark.parametrize("wor", [False, True])
+def test_tree_parity_large_logits_low_temperature(wor):
+    """Tree walks on logits shifted to +40 at T = 0.05 (|max| / T above 800):
+    the sweeps form every exponent as (x - max) / T."""
+    prob = workloads.tree_problem(62, 8, 20, 4, 4, 20_000, "fp32", 0.05, target_std=0.15, draft_scale=1.0,
+                                  noise_std=0.03, peaks=0,
+                                  siblings="without_replacement" if wor else "iid")
+    prob["target"] = prob["target"] + np.float32(40.0)
+    prob["draft_logits"] = prob["draft_logits"] + np.float32(40.0)
+    g, r = _run_tree(prob, wor=wor), _oracle_tree(prob, wor=wor)
+    print("near-threshold", check_tree(prob, g, r, without_replacement=wor), "mean accepted",
+          r["accepted_len"].mean())
