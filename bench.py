@@ -675,18 +675,26 @@ def run_ours(args):
     total_rows = reduce_sum(args.steps * wl.rows_per_step, dev)
     value = total_rows / (ms_max / 1e3)
 
-    # kernel timing pass: the same calls eagerly, each kernel bracketed by
-    # CUDA events on the launching stream (dependent launches serialised)
+    # kernel timing pass: the same calls captured into a graph with every
+    # kernel bracketed by CUDA events on its launching stream (event-record
+    # nodes; dependent launches serialised), timed on the graph's last replay
     api.trace_enable(True)
     api.trace_collect()
     reps = max(1, min(4, 256 // nsets))
+    tgraph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
-        for r in range(reps):
-            for i in range(nsets):
-                wl.call(sets[i], outs[i], stream)
+        with torch.cuda.graph(tgraph, stream=stream):
+            for r in range(reps):
+                for i in range(nsets):
+                    wl.call(sets[i], outs[i], stream)
+    api.trace_enable(False)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            tgraph.replay()
     torch.cuda.synchronize(dev)
     trace = api.trace_collect()
-    api.trace_enable(False)
+    del tgraph
     peak, peak_kind = peak_hbm()
     kernels = {}
     for kname, (t_ms, cnt) in trace.items():

@@ -407,7 +407,12 @@ const char *spec_last_error(void);
  * elapsed time to its kernel's total, writes up to `cap` entries (kernel
  * name, total milliseconds, launch count) and clears the record.  It
  * returns the number of distinct kernels, or a negative SPEC_* code.
- * Tracing is process-wide and meant for eager (not graph-captured) runs.
+ * Tracing is process-wide.  Calls made while their stream is being captured
+ * into a CUDA graph put the events into the graph as event-record nodes:
+ * each replay of the graph stamps them again, so collect after the replay
+ * to be timed (the record keeps one pair per captured launch, whatever the
+ * number of replays).  Dependent launches are not chained while tracing is
+ * on, so each bracket holds one kernel.
  */
 int spec_trace_enable(int on);
 int spec_trace_collect(const char **names, double *total_ms, int64_t *launches, int cap);

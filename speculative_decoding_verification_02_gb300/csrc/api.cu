@@ -172,6 +172,19 @@ cudaEvent_t take_event() {
   return e;
 }
 
+// Records ev on st.  Under stream capture the record becomes an event-record
+// node of the graph (an ordinary record there only orders the capture), so
+// every replay of the graph stamps the event again.
+void record_event(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+    cudaGetLastError();  // (leave no error for the launch check that follows)
+    cs = cudaStreamCaptureStatusNone;
+  }
+  if (cs == cudaStreamCaptureStatusActive) cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+  else cudaEventRecord(ev, st);
+}
+
 }  // namespace
 
 int trace_begin(const char *name, cudaStream_t st) {
@@ -179,7 +192,7 @@ int trace_begin(const char *name, cudaStream_t st) {
   if (!g_trace_on) return -1;
   TraceRec r{name, take_event(), take_event()};
   if (!r.start || !r.stop) return -1;
-  cudaEventRecord(r.start, st);
+  record_event(r.start, st);
   g_trace.push_back(r);
   return static_cast<int>(g_trace.size()) - 1;
 }
@@ -187,7 +200,7 @@ int trace_begin(const char *name, cudaStream_t st) {
 void trace_end(int slot, cudaStream_t st) {
   if (slot < 0) return;
   std::lock_guard<std::mutex> g(g_trace_mu);
-  if (slot < static_cast<int>(g_trace.size())) cudaEventRecord(g_trace[slot].stop, st);
+  if (slot < static_cast<int>(g_trace.size())) record_event(g_trace[slot].stop, st);
 }
 
 void count_launch() {

@@ -10,7 +10,8 @@
 // A row is then described by its threshold: kept = {v : x_v >= theta}.
 //
 // One thread-block cluster per row; CTA r of the cluster holds slice r of
-// the row in shared memory.  Both thresholds are found by radix selection on
+// the row in shared memory (staged through registers, several 16-byte loads
+// in flight per thread).  Both thresholds are found by radix selection on
 // an order-preserving 32-bit key of each logit (bf16 logits differ only in
 // the top 16 bits: two 8-bit levels; fp32: four):
 //   - each level builds a 256-bin histogram of the next digit over the
@@ -49,6 +50,7 @@ namespace sv {
 constexpr int kFilterThreads = 512;
 constexpr int kFilterWarps = kFilterThreads / 32;
 constexpr int kFilterListCap = 1024;             // candidate logits per CTA on the list path
+constexpr int kFilterLoadBatch = 6;              // 16-byte loads each thread keeps in flight
 constexpr double kMassScale = 17592186044416.0;  // 2^44: fixed-point unit of the histogram masses
 
 // Order-preserving unsigned key of an fp32 value (its bits); -0 maps to +0.
@@ -118,6 +120,13 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
   if (r == 0 && rank == 0 && tid == 0 && P.counter2) P.counter2[b] = 0;  // for the chunked accept kernel
   const char *row = side ? row_ptr<DT>(P.draftl, P.d_req, P.row, b, i) : row_ptr<DT>(P.target, P.t_req, P.row, b, i);
   const int lo = min(V, rank * P.slice), hi = min(V, lo + P.slice), n = hi - lo;
+  // the drafted token's logit (rank 0 writes the partial), loaded now so the
+  // two dependent reads overlap the slice's
+  float xtok = -INFINITY;
+  if (rank == 0 && tid == 0 && i < L) {
+    const int tok = P.draft[static_cast<int64_t>(b) * k + i];
+    if (tok >= 0 && tok < V) xtok = load_one<DT>(row, tok);
+  }
 
   extern __shared__ __align__(16) unsigned char dyn_filter[];
   unsigned char *s_row = dyn_filter;  // [slice] the slice's logits
@@ -136,31 +145,34 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
   float mloc = -INFINITY;
   const int ng = VEC ? n / EPG : 0;  // n is a multiple of EPG on the 16-byte path
   if (VEC) {
-    // every 16-byte copy in flight at once, then one wait
-    const char *src = row + static_cast<int64_t>(lo) * ES;
-    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(s_row));
-    for (int g = tid; g < ng; g += kFilterThreads)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16u * g), "l"(src + 16 * static_cast<int64_t>(g))
-                   : "memory");
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    __syncthreads();
-    if (DT == SPEC_DTYPE_BF16) {
-      __nv_bfloat162 mx = __float2bfloat162_rn(-INFINITY);
-      for (int g = tid; g < ng; g += kFilterThreads) {
-        const uint4 w = reinterpret_cast<const uint4 *>(s_row)[g];
-        mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162 *>(&w.x));
-        mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162 *>(&w.y));
-        mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162 *>(&w.z));
-        mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162 *>(&w.w));
-      }
-      mloc = fmaxf(__low2float(mx), __high2float(mx));
-    } else {
-      for (int g = tid; g < ng; g += kFilterThreads) {
-        const uint4 w = reinterpret_cast<const uint4 *>(s_row)[g];
-        mloc = fmaxf(mloc, fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
-                                 fmaxf(__uint_as_float(w.z), __uint_as_float(w.w))));
+    // batches of kFilterLoadBatch 16-byte loads in flight per thread (into
+    // registers, then shared memory), the max folded in as they land
+    const uint4 *src = reinterpret_cast<const uint4 *>(row + static_cast<int64_t>(lo) * ES);
+    uint4 *dst = reinterpret_cast<uint4 *>(s_row);
+    __nv_bfloat162 mx2 = __float2bfloat162_rn(-INFINITY);
+    for (int g0 = tid; g0 < ng; g0 += kFilterThreads * kFilterLoadBatch) {
+      uint4 w[kFilterLoadBatch];
+#pragma unroll
+      for (int u = 0; u < kFilterLoadBatch; ++u)
+        if (g0 + u * kFilterThreads < ng) w[u] = ld_stream16(src + g0 + u * kFilterThreads);
+#pragma unroll
+      for (int u = 0; u < kFilterLoadBatch; ++u) {
+        if (g0 + u * kFilterThreads < ng) {
+          dst[g0 + u * kFilterThreads] = w[u];
+          if (DT == SPEC_DTYPE_BF16) {
+            mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162 *>(&w[u].x));
+            mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162 *>(&w[u].y));
+            mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162 *>(&w[u].z));
+            mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162 *>(&w[u].w));
+          } else {
+            mloc = fmaxf(mloc, fmaxf(fmaxf(__uint_as_float(w[u].x), __uint_as_float(w[u].y)),
+                                     fmaxf(__uint_as_float(w[u].z), __uint_as_float(w[u].w))));
+          }
+        }
       }
     }
+    if (DT == SPEC_DTYPE_BF16) mloc = fmaxf(__low2float(mx2), __high2float(mx2));
+    __syncthreads();  // the slice is in shared memory
   } else {
     for (int e = tid; e < n; e += kFilterThreads) {
       const float x = load_one<DT>(row, lo + e);
@@ -505,11 +517,6 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
         kept += s_cu[q];
         smallest = fminf(smallest, s_cmn[q]);
       }
-    }
-    float xtok = -INFINITY;
-    if (i < L) {
-      const int tok = P.draft[static_cast<int64_t>(b) * k + i];
-      if (tok >= 0 && tok < V) xtok = load_one<DT>(row, tok);
     }
     P.part[j] = Partial{M, S, kNoIndex, xtok};
     P.theta[j] = smallest;
