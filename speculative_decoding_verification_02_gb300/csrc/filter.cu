@@ -30,7 +30,12 @@
 // logits (and each CTA's share fits the list), the radix walk and the top-p
 // walk run over the list alone, and the kept mass is added in 2^-44 fixed
 // point (so the list's order, which the appends leave unspecified, does not
-// matter).  Otherwise the walk runs over the whole slice as above.
+// matter).  With several CTAs, each pushes its list into rank 0's shared
+// memory and leaves; rank 0 finishes the row alone.  Otherwise the walk runs
+// over the whole slice as above.
+// Row mode, for calls with at least two rows per SM and top-k on: one CTA
+// per row, no cluster and no staging; the passes read the row from global
+// memory (the same steps with a cluster of one).
 // The outputs are the chain verification's per-row statistics, as one
 // partial per row -- (max M, sum over kept logits of 2^((x - M) c), the
 // drafted token's logit) -- and theta, which the accept kernels apply as a
@@ -50,6 +55,8 @@ namespace sv {
 constexpr int kFilterThreads = 512;
 constexpr int kFilterWarps = kFilterThreads / 32;
 constexpr int kFilterListCap = 1024;             // candidate logits per CTA on the list path
+constexpr int kFilterRowListCap = 4096;          // the same in row mode (one CTA per row)
+constexpr int kFilterRowMinRows = 2 * 152;       // row mode from this many rows (two per SM of the 152)
 constexpr int kFilterLoadBatch = 6;              // 16-byte loads each thread keeps in flight
 constexpr double kMassScale = 17592186044416.0;  // 2^44: fixed-point unit of the histogram masses
 
@@ -97,14 +104,19 @@ __device__ __forceinline__ uint32_t elem_bits(const void *s, int e) {
   return static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(s)[e]) << 16;
 }
 
-template <int DT, bool VEC>
-__global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const ChainParams P) {
+// The filter of partial row j by the calling CTA (and, with STAGE, the
+// other CTAs of its cluster, one slice each).
+// STAGE = false (row mode): the CTA reads the whole row from global memory
+// instead of a staged slice -- the first pass (the max) from HBM, the later
+// ones from L2 -- with a longer list.
+template <int DT, bool VEC, bool STAGE>
+__device__ __forceinline__ void filter_row(const ChainParams &P, const int j) {
   cg::cluster_group cluster = cg::this_cluster();
   constexpr int EPG = Elems<DT>::kPerGroup, ES = Elems<DT>::kSize;
   constexpr int kLevels = DT == SPEC_DTYPE_F32 ? 4 : 2;
   constexpr int kMaxCS = 16;
-  const int CS = P.cluster, rank = static_cast<int>(cluster.block_rank());
-  const int j = blockIdx.x / CS;  // row of the partials layout: request b, row r
+  constexpr int kCap = STAGE ? kFilterListCap : kFilterRowListCap;
+  const int CS = STAGE ? P.cluster : 1, rank = STAGE ? static_cast<int>(cluster.block_rank()) : 0;
   const int k = P.k, K1 = k + 1, R = 2 * k + 1;
   const int b = j / R, r = j - b * R;
   const int side = r < K1 ? 0 : 1, i = side ? r - K1 : r;
@@ -112,14 +124,12 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
   const int V = P.V;
   const float c = P.c;
 
-  pdl_wait();  // the draft lengths and tokens may come from the previous kernel
-  pdl_launch_dependents();
   const int L = P.draft_len ? P.draft_len[b] : k;
   // the rows verification reads: targets 0..L, drafts 0..L-1 (the same in the whole cluster)
   if (L < 0 || L > k || (side == 0 ? i > L : i >= L)) return;
   if (r == 0 && rank == 0 && tid == 0 && P.counter2) P.counter2[b] = 0;  // for the chunked accept kernel
   const char *row = side ? row_ptr<DT>(P.draftl, P.d_req, P.row, b, i) : row_ptr<DT>(P.target, P.t_req, P.row, b, i);
-  const int lo = min(V, rank * P.slice), hi = min(V, lo + P.slice), n = hi - lo;
+  const int lo = STAGE ? min(V, rank * P.slice) : 0, hi = STAGE ? min(V, lo + P.slice) : V, n = hi - lo;
   // the drafted token's logit (rank 0 writes the partial), loaded now so the
   // two dependent reads overlap the slice's
   float xtok = -INFINITY;
@@ -129,7 +139,9 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
   }
 
   extern __shared__ __align__(16) unsigned char dyn_filter[];
-  unsigned char *s_row = dyn_filter;  // [slice] the slice's logits
+  unsigned char *s_row = dyn_filter;  // [slice] the slice's logits (STAGE)
+  // the logits every pass after the first reads: the staged slice, or the row
+  const unsigned char *src = STAGE ? s_row : reinterpret_cast<const unsigned char *>(row);
   __shared__ uint32_t s_cnt[2][256];
   __shared__ unsigned long long s_mass[2][256];
   __shared__ uint32_t t_cnt[256];
@@ -144,7 +156,36 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
   // ---- the slice into shared memory, and the slice max
   float mloc = -INFINITY;
   const int ng = VEC ? n / EPG : 0;  // n is a multiple of EPG on the 16-byte path
-  if (VEC) {
+  if (!STAGE) {
+    // row mode: the max only, batches of 16-byte loads in flight per thread
+    if (VEC) {
+      const uint4 *g16 = reinterpret_cast<const uint4 *>(row);
+      __nv_bfloat162 mx2 = __float2bfloat162_rn(-INFINITY);
+      for (int g0 = tid; g0 < ng; g0 += kFilterThreads * kFilterLoadBatch) {
+        uint4 w[kFilterLoadBatch];
+#pragma unroll
+        for (int u = 0; u < kFilterLoadBatch; ++u)
+          if (g0 + u * kFilterThreads < ng) w[u] = ld_stream16(g16 + g0 + u * kFilterThreads);
+#pragma unroll
+        for (int u = 0; u < kFilterLoadBatch; ++u) {
+          if (g0 + u * kFilterThreads < ng) {
+            if (DT == SPEC_DTYPE_BF16) {
+              mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162 *>(&w[u].x));
+              mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162 *>(&w[u].y));
+              mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162 *>(&w[u].z));
+              mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162 *>(&w[u].w));
+            } else {
+              mloc = fmaxf(mloc, fmaxf(fmaxf(__uint_as_float(w[u].x), __uint_as_float(w[u].y)),
+                                       fmaxf(__uint_as_float(w[u].z), __uint_as_float(w[u].w))));
+            }
+          }
+        }
+      }
+      if (DT == SPEC_DTYPE_BF16) mloc = fmaxf(__low2float(mx2), __high2float(mx2));
+    } else {
+      for (int e = tid; e < n; e += kFilterThreads) mloc = fmaxf(mloc, load_one<DT>(row, e));
+    }
+  } else if (VEC) {
     // batches of kFilterLoadBatch 16-byte loads in flight per thread (into
     // registers, then shared memory), the max folded in as they land
     const uint4 *src = reinterpret_cast<const uint4 *>(row + static_cast<int64_t>(lo) * ES);
@@ -193,7 +234,7 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
   // ---- the list path (top-k on): the window of the max's top-byte bin, or
   // of that bin and the one below, when the window holds top_k logits and
   // each CTA's share fits the list
-  __shared__ uint32_t s_list[kFilterListCap];
+  __shared__ uint32_t s_list[kCap];
   __shared__ int s_nlist;
   __shared__ uint32_t s_xc[2][kMaxCS];  // per rank: logits >= tau0, logits >= tau1
   __shared__ uint32_t s_w0[kFilterWarps], s_w1[kFilterWarps];
@@ -210,14 +251,14 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
     auto scan = [&]<bool COUNT>(float tau, uint32_t &c0, uint32_t &c1) {
       auto append = [&](uint32_t bits) {
         const int pos = atomicAdd(&s_nlist, 1);
-        if (pos < kFilterListCap) s_list[pos] = bits;
+        if (pos < kCap) s_list[pos] = bits;
       };
       if (VEC && DT == SPEC_DTYPE_BF16) {
         const uint32_t ta = (__float_as_uint(tau) >> 16) * 0x10001u;
         const uint32_t t1 = (__float_as_uint(tau1) >> 16) * 0x10001u;
         uint32_t p0 = 0u, p1 = 0u;  // two 16-bit counters each (at most 48 per half)
         for (int g = tid; g < ng; g += kFilterThreads) {
-          const uint4 w = reinterpret_cast<const uint4 *>(s_row)[g];
+          const uint4 w = reinterpret_cast<const uint4 *>(src)[g];
           const uint32_t a0 = ge_pair(w.x, ta), a1 = ge_pair(w.y, ta), a2 = ge_pair(w.z, ta), a3 = ge_pair(w.w, ta);
           if (COUNT) {
             p0 += a0 + a1 + a2 + a3;
@@ -237,7 +278,7 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
       } else {
         c0 = c1 = 0u;
         for (int e = tid; e < n; e += kFilterThreads) {
-          const uint32_t bits = elem_bits<DT>(s_row, e);
+          const uint32_t bits = elem_bits<DT>(src, e);
           const float x = __uint_as_float(bits);
           if (COUNT) {
             c0 += x >= tau0;
@@ -276,9 +317,9 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
     }
     const uint32_t K = static_cast<uint32_t>(P.top_k);
     int win = -1;  // the window taken: 0 (>= tau0), 1 (>= tau1), -1 none
-    if (T0 >= K && A0 <= static_cast<uint32_t>(kFilterListCap)) {
+    if (T0 >= K && A0 <= static_cast<uint32_t>(kCap)) {
       win = 0;  // the lists hold every logit >= tau0
-    } else if (T1 >= K && A1 <= static_cast<uint32_t>(kFilterListCap)) {
+    } else if (T1 >= K && A1 <= static_cast<uint32_t>(kCap)) {
       if (tid == 0) s_nlist = 0;
       __syncthreads();
       scan.template operator()<false>(tau1, c0, c1);
@@ -292,8 +333,8 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
       // goes on alone
       use_list = true;
       __syncthreads();
-      const int mine = min(s_nlist, kFilterListCap);
-      if (CS > 1) {
+      const int mine = min(s_nlist, kCap);
+      if (STAGE && CS > 1) {
         uint32_t off = 0u, total = 0u;
         for (int q = 0; q < CS; ++q) {
           const uint32_t cq = s_xc[win][q];
@@ -331,7 +372,7 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
     __syncthreads();
     const int ne = use_list ? nlist : n;
     for (int e = tid; e < ne; e += kFilterThreads) {
-      const uint32_t bits = use_list ? s_union[e] : elem_bits<DT>(s_row, e);
+      const uint32_t bits = use_list ? s_union[e] : elem_bits<DT>(src, e);
       const uint32_t key = order_key(bits);
       if (!first && (key >> (shift + 8)) != prefix) continue;
       const float x = __uint_as_float(bits);
@@ -466,7 +507,7 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
     }
   } else {
     for (int e = tid; e < n; e += kFilterThreads) {
-      const float x = __uint_as_float(elem_bits<DT>(s_row, e));
+      const float x = __uint_as_float(elem_bits<DT>(src, e));
       if (x >= theta) {
         s_loc += ex2((x - M) * c);
         mn = fminf(mn, x);
@@ -524,6 +565,17 @@ __global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const Chai
   }
 }
 
+// STAGE: one cluster per row.  Row mode (launched without clusters): one CTA
+// per row.  (Two CTAs per SM taking rows in turn measured slower, and the
+// loop alone raised the kernel to 60 registers, two CTAs per SM instead of
+// three.)
+template <int DT, bool VEC, bool STAGE>
+__global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const ChainParams P) {
+  pdl_wait();  // the draft lengths and tokens may come from the previous kernel
+  pdl_launch_dependents();
+  filter_row<DT, VEC, STAGE>(P, STAGE ? static_cast<int>(blockIdx.x) / P.cluster : static_cast<int>(blockIdx.x));
+}
+
 // Cluster geometry: at most 16 CTAs, each slice at most 96 KB of logits.
 constexpr int kFilterMaxSliceBytes = 96 * 1024;
 
@@ -540,29 +592,40 @@ bool chain_filter_plan(ChainParams &P) {
 
 cudaError_t launch_chain_filter(const ChainParams &P, bool vec, cudaStream_t st) {
   const int es = P.dtype == SPEC_DTYPE_F32 ? 4 : 2;
-  const size_t smem = static_cast<size_t>(P.slice) * es;
   const int rows = P.B * (2 * P.k + 1);
+  // row mode when top-k is on (its window needs it) and the rows alone fill
+  // the GPU; otherwise a cluster per row splits each row over several SMs
+  const bool row_mode = P.top_k > 0 && P.top_k < P.V && rows >= kFilterRowMinRows;
+  const int cs = row_mode ? 1 : P.cluster;
+  const size_t smem = row_mode ? 0 : static_cast<size_t>(P.slice) * es;
   auto go = [&](auto kern) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e == cudaSuccess && P.cluster > 8) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess && cs > 8) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>(rows * P.cluster));
+    cfg.gridDim = dim3(static_cast<unsigned>(rows * cs));
     cfg.blockDim = dim3(kFilterThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = P.cluster;
+    attr[0].val.clusterDim.x = cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return trace_launch_ex("chain_filter", st, [&] { return cudaLaunchKernelEx(&cfg, kern, P); });
+    return trace_launch_ex(row_mode ? "chain_filter_rows" : "chain_filter", st,
+                           [&] { return cudaLaunchKernelEx(&cfg, kern, P); });
   };
+  if (row_mode) {
+    if (P.dtype == SPEC_DTYPE_BF16)
+      return vec ? go(chain_filter_kernel<SPEC_DTYPE_BF16, true, false>)
+                 : go(chain_filter_kernel<SPEC_DTYPE_BF16, false, false>);
+    return vec ? go(chain_filter_kernel<SPEC_DTYPE_F32, true, false>) : go(chain_filter_kernel<SPEC_DTYPE_F32, false, false>);
+  }
   if (P.dtype == SPEC_DTYPE_BF16)
-    return vec ? go(chain_filter_kernel<SPEC_DTYPE_BF16, true>) : go(chain_filter_kernel<SPEC_DTYPE_BF16, false>);
-  return vec ? go(chain_filter_kernel<SPEC_DTYPE_F32, true>) : go(chain_filter_kernel<SPEC_DTYPE_F32, false>);
+    return vec ? go(chain_filter_kernel<SPEC_DTYPE_BF16, true, true>) : go(chain_filter_kernel<SPEC_DTYPE_BF16, false, true>);
+  return vec ? go(chain_filter_kernel<SPEC_DTYPE_F32, true, true>) : go(chain_filter_kernel<SPEC_DTYPE_F32, false, true>);
 }
 
 }  // namespace sv

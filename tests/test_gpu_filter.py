@@ -306,25 +306,30 @@ def _path_rows(kind, V, rng):
     return x
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-@pytest.mark.parametrize("top_p", [1.0, 0.7])
-def test_filter_paths(dtype, top_p):
+@pytest.mark.parametrize("dtype,top_p,reps", [("bf16", 1.0, 1), ("fp32", 1.0, 1), ("bf16", 0.7, 1), ("fp32", 0.7, 1),
+                                               ("bf16", 1.0, 52), ("bf16", 0.7, 52), ("fp32", 0.7, 52)])
+def test_filter_paths(dtype, top_p, reps):
     """Every path of the filter kernel: the thresholds and kept counts of
     spec_filter_rows, and filtered verification (p_tok, q_tok and the
-    residual mass test the kept mass) on requests made of the same rows."""
+    residual mass test the kept mass) on requests made of the same rows.
+    reps = 52 gives 312 rows and 66 requests of 5 verified rows, enough rows
+    for the kernel's row mode (one CTA per row, no staged slices)."""
     rng = np.random.default_rng(77)
     V, top_k, T = 128_256, 50, 1.0
-    kinds = ["bin0", "bin1", "dense", "negative", "tiny", "zero"]
+    kinds = ["bin0", "bin1", "dense", "negative", "tiny", "zero"] * reps
     x = np.stack([_path_rows(kd, V, rng) for kd in kinds])
     rows = workloads.bf16_bits(x) if dtype == "bf16" else x
     g = host(api.spec_filter_rows(to_dev(rows), T, top_k, top_p))
     for r in range(len(kinds)):
         ok, was_near = _cut_ok(rows[r], T, top_k, top_p, float(g["theta"][r]))
         _, theta_o, kept_o = oracle.filter_row(rows[r], T, top_k, top_p)
-        assert ok, (kinds[r], g["theta"][r], theta_o)
-        assert was_near or g["kept"][r] == kept_o, (kinds[r], g["kept"][r], kept_o)
+        assert ok, (r, kinds[r], g["theta"][r], theta_o)
+        assert was_near or g["kept"][r] == kept_o, (r, kinds[r], g["kept"][r], kept_o)
     # requests: target rows 0..k from one kind, draft rows = target + noise
-    B, k = len(kinds), 2
+    # (66 requests x 5 rows in the row-mode case)
+    if reps > 1:
+        x = x[:66]
+    B, k = x.shape[0], 2
     tgt = np.repeat(x[:, None, :], k + 1, axis=1).copy()
     tgt[:, 1:] += (rng.standard_normal((B, k, V)) * 0.05).astype(np.float32)
     dl = tgt[:, :k] + (rng.standard_normal((B, k, V)) * 0.2).astype(np.float32)
