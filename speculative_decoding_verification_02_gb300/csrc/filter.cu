@@ -157,15 +157,24 @@ __device__ __forceinline__ void filter_row(const ChainParams &P, const int j) {
   float mloc = -INFINITY;
   const int ng = VEC ? n / EPG : 0;  // n is a multiple of EPG on the 16-byte path
   if (!STAGE) {
-    // row mode: the max only, batches of 16-byte loads in flight per thread
+    // row mode: the max only, batches of 16-byte loads in flight per thread,
+    // marked evict-last in L2 so that the row is still there for the passes
+    // that read it again
     if (VEC) {
       const uint4 *g16 = reinterpret_cast<const uint4 *>(row);
+      unsigned long long keep;
+      asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
       __nv_bfloat162 mx2 = __float2bfloat162_rn(-INFINITY);
       for (int g0 = tid; g0 < ng; g0 += kFilterThreads * kFilterLoadBatch) {
         uint4 w[kFilterLoadBatch];
 #pragma unroll
         for (int u = 0; u < kFilterLoadBatch; ++u)
-          if (g0 + u * kFilterThreads < ng) w[u] = ld_stream16(g16 + g0 + u * kFilterThreads);
+          if (g0 + u * kFilterThreads < ng) {
+            const uint4 *a = g16 + g0 + u * kFilterThreads;
+            asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                : "=r"(w[u].x), "=r"(w[u].y), "=r"(w[u].z), "=r"(w[u].w)
+                : "l"(a), "l"(keep));
+          }
 #pragma unroll
         for (int u = 0; u < kFilterLoadBatch; ++u) {
           if (g0 + u * kFilterThreads < ng) {
