@@ -71,10 +71,11 @@ def gumbel_draw(rng, logits_row, T: float) -> int:
 
 
 def gumbel_draw_top_k(rng, logits_row, T: float, top_k: int) -> int:
-    """A drafter that samples from its own top-k: Gumbel-max over the top_k
-    largest logits (by position among equal logits at the cut)."""
+    """A drafter that samples from its own top-k: Gumbel-max over exactly
+    top_k logits, the largest (equal logits at the cut taken by position).
+    Without ties at the cut this is a draw from the top-k filtered softmax."""
     l64 = logits_as_f64(logits_row)
-    cand = np.argpartition(-l64, top_k - 1)[:top_k]
+    cand = np.argsort(-l64, kind="stable")[:top_k]
     u = rng.random(top_k)
     u = np.where(u <= 0.0, np.finfo(np.float64).tiny, u)
     return int(cand[np.argmax(l64[cand] / T - np.log(-np.log(u)))])

@@ -5,6 +5,7 @@ import json
 import os
 import socket
 
+import numpy as np
 import pytest
 import torch.distributed as dist
 import torch.multiprocessing as mp
@@ -83,3 +84,20 @@ def test_clock_summary_prefers_samples_inside_the_timed_region(tmp_path):
     s.window = (base + 5.0, base + 5.1)     # a region between samples: the load around it
     c = s.summary()
     assert c["samples"] == 4 and c["window"].startswith("the same load")
+
+
+def test_topkp64_workload_recipe():
+    """The filtered-verification bench workload: the batch64 rows with
+    top_k = 50, top_p = 0.9, every draft among its draft row's 50 largest
+    logits, and the filter kernel's algorithmic bytes = every row once."""
+    wl = bench.WORKLOADS["topkp64"]("topkp64")
+    p = wl.prob
+    assert (wl.top_k, wl.top_p, wl.kind) == (50, 0.9, "filter")
+    assert (wl.B, wl.k, wl.V) == (64, 8, 128_256) and wl.rows_per_step == 64 * 17
+    from speculative_decoding_verification_02_gb300 import workloads as W
+    for b in range(0, 64, 7):
+        for i in range(wl.k):
+            row = W.logits_as_f64(p["draft_logits"][b, i])
+            assert row[p["draft"][b, i]] >= np.sort(row)[-50]
+    assert wl.kernel_bytes("chain_filter_rows", None) == wl.set_bytes == 64 * 17 * 128_256 * 2
+    assert "filter.cu" in " ".join(bench.KERNEL_SOURCES["filter"])

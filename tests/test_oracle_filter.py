@@ -140,3 +140,22 @@ def test_filtered_verification_is_lossless_against_the_filtered_target(seed, top
     # verifying a filtered draft against the unfiltered target gives a different law
     off = _filtered_first_token_law(lp, lq, top_k, top_p, verify_filter=False)
     assert np.max(np.abs(off - pf)) > 1e-3
+
+
+def test_drafter_top_k_draws_follow_the_top_k_softmax():
+    """The input generator's drafter-side top-k draw (bench workload topkp64):
+    only the top_k largest logits are drawn, each with its softmax
+    probability renormalised over them (frequencies within 4 sigma)."""
+    rng = np.random.default_rng(11)
+    row = workloads.bf16_bits(np.array([0.5, 2.0, -1.0, 1.25, 3.0, 0.0], np.float32))
+    T, top_k, n = 0.8, 3, 60_000
+    draws = np.array([workloads.gumbel_draw_top_k(rng, row, T, top_k) for _ in range(n)])
+    assert set(np.unique(draws)) <= {1, 3, 4}
+    z = np.array([2.0, 1.25, 3.0]) / T
+    p = np.exp(z - z.max())
+    p /= p.sum()
+    freq = np.array([(draws == v).mean() for v in (1, 3, 4)])
+    assert np.all(np.abs(freq - p) <= 4 * np.sqrt(p * (1 - p) / n)), (freq, p)
+    # a tie at the cut takes the lower position
+    tie = workloads.bf16_bits(np.array([1.0, 5.0, 1.0, 1.0], np.float32))
+    assert {workloads.gumbel_draw_top_k(rng, tie, 1.0, 2) for _ in range(200)} <= {0, 1}
