@@ -192,3 +192,43 @@ def test_sample_draw_argument_checks(L):
     assert call(logits=None) == -1 and call(u=None) == -1 and call(tok=None) == -1
     assert call(wsb=need - 1) == -3 and call(w=None) == -3 and call(w=ctypes.c_void_p(0x100010)) == -3
     assert call(B=0) == 0
+
+
+def test_topkp_argument_checks(L):
+    """spec_verify_sample_topkp, spec_sample_topkp and spec_filter_rows reject
+    bad filters and arguments on the host, launching nothing."""
+    P_, I, I64, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    L.spec_verify_sample_topkp.argtypes = [P_, I64, P_, I64, I64, I, I, I, I, F, I, F] + [P_] * 12 + [Z, P_]
+    L.spec_sample_topkp.argtypes = [P_, I64, I, I, I, F, I, F, P_, P_, P_, P_, P_, Z, P_]
+    L.spec_filter_rows.argtypes = [P_, I64, I, I, I, F, I, F, P_, P_, P_, Z, P_]
+    L.spec_workspace_size.restype = ctypes.c_size_t
+    ws = ctypes.c_void_p(0x100000)
+    n0 = L.spec_launch_count()
+
+    def verify(top_k=50, top_p=0.9, dtype=1, B=2, k=4, V=1024, T=1.0):
+        return L.spec_verify_sample_topkp(FAKE, 5 * 1024, FAKE, 4 * 1024, 1024, dtype, B, k, V, T, top_k, top_p,
+                                          FAKE, None, None, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE, ws,
+                                          1 << 30, None)
+    for bad in (dict(top_k=-1), dict(top_p=0.0), dict(top_p=-0.5), dict(top_p=1.5), dict(top_p=float("nan")),
+                dict(T=0.0), dict(k=65), dict(V=0)):
+        assert verify(**bad) == -1, bad
+    assert verify(dtype=7) == -2
+    assert verify(B=0) == 0
+
+    def draw(top_k=50, top_p=0.9, B=8, V=1000, T=1.0, w=ws, wsb=None):
+        wsb = L.spec_workspace_size(4, B, 0, V, 1) if wsb is None else wsb
+        return L.spec_sample_topkp(FAKE, V, 1, B, V, T, top_k, top_p, FAKE, FAKE, None, None, w, wsb, None)
+    assert draw(top_k=-3) == -1 and draw(top_p=2.0) == -1 and draw(T=float("inf")) == -1
+    assert draw(wsb=16) == -3 and draw(w=None) == -3 and draw(w=ctypes.c_void_p(0x100010)) == -3
+    assert draw(B=0) == 0
+
+    def rows(top_k=50, top_p=0.9, R=4, V=1000, T=1.0, theta=FAKE, w=ws, wsb=None, dtype=1):
+        wsb = L.spec_workspace_size(5, R, 0, V, dtype) if wsb is None else wsb
+        return L.spec_filter_rows(FAKE, V, dtype, R, V, T, top_k, top_p, theta, None, w, wsb, None)
+    assert rows(top_k=-1) == -1 and rows(top_p=0.0) == -1 and rows(R=-1) == -1 and rows(V=0) == -1
+    assert rows(theta=None) == -1 and rows(dtype=3) == -2
+    assert rows(wsb=8) == -3 and rows(w=None) == -3
+    assert rows(V=786_433) == -1                       # more than 16 slices of 96 KB of bf16
+    assert rows(V=393_217, dtype=0) == -1              # the same for fp32
+    assert rows(R=0) == 0
+    assert L.spec_launch_count() == n0
