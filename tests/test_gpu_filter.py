@@ -319,7 +319,14 @@ def test_filter_paths(dtype, top_p, reps):
     kinds = ["bin0", "bin1", "dense", "negative", "tiny", "zero"] * reps
     x = np.stack([_path_rows(kd, V, rng) for kd in kinds])
     rows = workloads.bf16_bits(x) if dtype == "bf16" else x
-    g = host(api.spec_filter_rows(to_dev(rows), T, top_k, top_p))
+    api.trace_enable(True)
+    api.trace_collect()
+    try:
+        g = host(api.spec_filter_rows(to_dev(rows), T, top_k, top_p))
+        launched = api.trace_collect()
+    finally:
+        api.trace_enable(False)
+    assert ("chain_filter_rows" if reps > 1 else "chain_filter") in launched, launched
     for r in range(len(kinds)):
         ok, was_near = _cut_ok(rows[r], T, top_k, top_p, float(g["theta"][r]))
         _, theta_o, kept_o = oracle.filter_row(rows[r], T, top_k, top_p)
