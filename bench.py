@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload vocab248k|batch64|topkp64|small|tree60|tree60wor|draw64|ngram|eagle2]
-                    [--chain-path auto|two_pass|fused|grid]
+                    [--chain-path auto|two_pass|fused]
 
 One step is one pass of the path over one batch:
   vocab248k  spec_verify_sample, B=1, k=4, V=248,320 bf16 (the default: the
@@ -287,7 +287,7 @@ class ChainWorkload:
         """Algorithmic bytes of one launch of kernel `name`, averaged over the
         rotating sets (the draw's bytes depend on where each call stopped)."""
         row = self.V * self.es
-        if name.startswith(("chain_stats", "chain_fused", "chain_grid", "chain_filter")):
+        if name.startswith(("chain_stats", "chain_fused", "chain_filter")):
             return self.set_bytes  # every row once (the fused kernel's draw re-reads two from L2)
         if name.startswith("chain_sample_accept"):
             tot = 0.0
@@ -354,7 +354,7 @@ class DrawWorkload:
     def kernel_bytes(self, name, outs):
         """The statistics pass reads every row once; the draw re-reads (at
         most) the row it draws from."""
-        if name.startswith(("chain_stats", "chain_fused", "chain_grid")):
+        if name.startswith(("chain_stats", "chain_fused")):
             return self.set_bytes
         if name.startswith("chain_sample_accept"):
             return self.B * self.V * self.es
@@ -510,7 +510,7 @@ class NgramWorkload:
     def kernel_bytes(self, name, outs):
         if name == "ngram_draft":
             return self.B * self.H * 4
-        if name.startswith(("chain_stats", "chain_fused", "chain_grid")):
+        if name.startswith(("chain_stats", "chain_fused")):
             tot = 0.0
             for d, _ in outs:
                 lens = d["draft_len"].cpu().numpy()
@@ -604,7 +604,7 @@ def run_ours(args):
     __graft_entry__.build()
     from speculative_decoding_verification_02_gb300 import api
     api.set_chain_path({"auto": api.CHAIN_AUTO, "two_pass": api.CHAIN_TWO_PASS,
-                        "fused": api.CHAIN_FUSED, "grid": api.CHAIN_GRID}[args.chain_path])
+                        "fused": api.CHAIN_FUSED}[args.chain_path])
 
     wl = WORKLOADS[args.workload](args.workload)
     # rotating input sets: one cycle reads more than twice the L2
@@ -797,7 +797,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="vocab248k", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--chain-path", choices=["auto", "two_pass", "fused", "grid"], default="auto",
+    ap.add_argument("--chain-path", choices=["auto", "two_pass", "fused"], default="auto",
                     help="chain verification path (same results; for profiling one path)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)

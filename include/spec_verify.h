@@ -31,14 +31,8 @@
  *  - Uniforms are fp32 in [0, 1), drawn by the caller.
  *  - Argmax ties resolve to the lowest index.
  *  - Workspace: `workspace` must hold spec_workspace_size(...) bytes and be
- *    256-byte aligned.  Its first 256 bytes hold the grid path's barrier
- *    counter, which must be zero when a call starts: the library zeroes it
- *    (cudaMemsetAsync on the call's stream) the first time it sees a
- *    workspace address outside stream capture, and every call leaves it
- *    zero.  A caller that writes anything else into those bytes between
- *    calls must zero them again (a call that returned
- *    SPEC_STATUS_SYNC_TIMEOUT may also have left them non-zero).  The rest
- *    needs no initialisation.  A workspace may be reused by any later call
+ *    256-byte aligned.  It needs no initialisation: every call first writes
+ *    whatever it later reads.  A workspace may be reused by any later call
  *    of any shape; calls that may overlap on the GPU (other streams) must
  *    not share one.
  *  - p = softmax(target_logits / T), q = softmax(draft_logits / T), the
@@ -68,7 +62,6 @@ extern "C" {
 #define SPEC_STATUS_TOKEN_RANGE 1 /* a draft/node token is outside [0, V) */
 #define SPEC_STATUS_BAD_TREE 2    /* parents[] is not a tree rooted at 0, or too deep */
 #define SPEC_STATUS_BAD_LENGTH 3  /* draft_len or hist_len outside its range */
-#define SPEC_STATUS_SYNC_TIMEOUT 4 /* a grid-wide wait gave up (the workspace's first 256 bytes were not zero) */
 
 #define SPEC_DTYPE_F32 0
 #define SPEC_DTYPE_BF16 1
@@ -430,13 +423,6 @@ int64_t spec_launch_count(void);
  *                        small problems: latency-bound); when the requests'
  *                        clusters cannot all be resident at once the call
  *                        runs on the two-pass path instead;
- *   SPEC_CHAIN_GRID      one cooperative launch over all SMs: every CTA keeps
- *                        one vocabulary slice of every row in registers and
- *                        two grid-wide barriers order the statistics, the
- *                        decision and the draw (suits calls whose rows fit
- *                        in registers: at most 128 (request, position,
- *                        512-byte chunk) items per CTA); otherwise the call
- *                        runs on the two-pass path;
  *   SPEC_CHAIN_AUTO      the library picks per call (the default).
  * spec_set_chain_path sets the path for calls made after it, process-wide;
  * it returns SPEC_OK, or SPEC_EINVAL for an unknown value.  The workspace
@@ -447,7 +433,6 @@ int64_t spec_launch_count(void);
 #define SPEC_CHAIN_AUTO 0
 #define SPEC_CHAIN_TWO_PASS 1
 #define SPEC_CHAIN_FUSED 2
-#define SPEC_CHAIN_GRID 3
 int spec_set_chain_path(int path);
 
 /*

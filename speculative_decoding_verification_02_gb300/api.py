@@ -19,10 +19,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
 
 SPEC_OK, SPEC_EINVAL, SPEC_EDTYPE, SPEC_EWORKSPACE, SPEC_ECUDA = 0, -1, -2, -3, -4
-STATUS_OK, STATUS_TOKEN_RANGE, STATUS_BAD_TREE, STATUS_BAD_LENGTH, STATUS_SYNC_TIMEOUT = 0, 1, 2, 3, 4
+STATUS_OK, STATUS_TOKEN_RANGE, STATUS_BAD_TREE, STATUS_BAD_LENGTH = 0, 1, 2, 3
 DTYPE_F32, DTYPE_BF16 = 0, 1
 OP_NGRAM, OP_GREEDY, OP_SAMPLE, OP_TREE, OP_DRAW, OP_FILTER = 0, 1, 2, 3, 4, 5
-CHAIN_AUTO, CHAIN_TWO_PASS, CHAIN_FUSED, CHAIN_GRID = 0, 1, 2, 3
+CHAIN_AUTO, CHAIN_TWO_PASS, CHAIN_FUSED = 0, 1, 2
 TREE_SIBLINGS_WITHOUT_REPLACEMENT = 1
 
 _lock = threading.Lock()
@@ -150,7 +150,7 @@ def workspace(nbytes: int, device, stream=None) -> torch.Tensor:
     key = (device.index, s.cuda_stream)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < max(nbytes, 1):
-        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)  # the barrier bytes start at zero
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)  # needs no initialisation
         if ws.data_ptr() % 256:
             raise RuntimeError("workspace allocation is not 256-byte aligned")
         _workspaces[key] = ws
@@ -159,7 +159,7 @@ def workspace(nbytes: int, device, stream=None) -> torch.Tensor:
 
 def set_chain_path(path: int):
     """Chain verification path for later calls, process-wide: CHAIN_AUTO,
-    CHAIN_TWO_PASS, CHAIN_FUSED or CHAIN_GRID (same results, different speed)."""
+    CHAIN_TWO_PASS or CHAIN_FUSED (same results, different speed)."""
     _check(lib().spec_set_chain_path(int(path)), "spec_set_chain_path")
 
 

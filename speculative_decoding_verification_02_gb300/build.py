@@ -21,7 +21,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspecverify.so")
-SOURCES = ["api.cu", "chain.cu", "chain_fused.cu", "chain_grid.cu", "filter.cu", "tree.cu", "rerank.cu", "ngram.cu", "noalloc.cu",
+SOURCES = ["api.cu", "chain.cu", "chain_fused.cu", "filter.cu", "tree.cu", "rerank.cu", "ngram.cu", "noalloc.cu",
            "host_analysis.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++20", "-Xcompiler", "-fPIC", "-I" + INCLUDE,

@@ -45,8 +45,6 @@ constexpr long long kSmCount = 152;
 // V=2,048..248,320).
 std::atomic<int> g_chain_path{SPEC_CHAIN_AUTO};
 constexpr int kFusedAutoMaxV = 0;
-// In AUTO the grid kernel takes every call it fits (chain_grid_plan).
-constexpr bool kGridAuto = false;
 
 int stream_chunk(int dtype, long long rows_total, int V) {
   const long long es = elem_size(dtype);
@@ -70,16 +68,13 @@ int accept_chunk(int B, int V, int dtype) {
 
 int sub_chunk(int dtype) { return 256 * (16 / elem_size(dtype)); }
 
-// Workspace: the grid kernel's barrier counter (the first 256 bytes, which
-// no other path touches), per-(row, chunk) statistics, then for sampling the
-// residual mass per chunk and one arrival counter per request.  The
-// two-pass counters are zeroed by the first kernel of each call; the grid
-// counter must be zero when a call starts and is left zero (see
-// ensure_sync_zero).  The statistics and mass regions are sized for either
-// path.
+// Workspace: per-(row, chunk) statistics, then for sampling the residual
+// mass per sub-chunk, one arrival counter per request (zeroed by the
+// streaming pass of each call, so the workspace needs no initialisation)
+// and each row's top-k / top-p threshold.
 struct ChainLayout {
   int nc, chunk, nc2, chunk2, nsub;
-  size_t sync, part, part2, counter2, theta, total;
+  size_t part, part2, counter2, theta, total;
 };
 
 ChainLayout chain_layout(bool sample, int B, int k, int V, int dtype) {
@@ -90,17 +85,11 @@ ChainLayout chain_layout(bool sample, int B, int k, int V, int dtype) {
   L.nc2 = (V + L.chunk2 - 1) / L.chunk2;
   L.nsub = (V + sub_chunk(dtype) - 1) / sub_chunk(dtype);
   const size_t rows = sample ? 2 * static_cast<size_t>(k) + 1 : static_cast<size_t>(k) + 1;
-  // the grid kernel: a partial per (row, CTA), two slice masses per (request, CTA)
-  const bool grid = static_cast<long long>(B) * (k + 1) <= kGridMaxItems;
-  const size_t grid_parts = grid ? static_cast<size_t>(B) * rows * kGridMaxCtas : 0;
-  const size_t grid_mass = grid && sample ? 2 * static_cast<size_t>(B) * kGridMaxCtas : 0;
   size_t off = 0;
-  L.sync = off;
-  off = 256;
   L.part = off;
-  off = round_up(off + sizeof(Partial) * std::max(B * rows * L.nc, grid_parts), 256);
+  off = round_up(off + sizeof(Partial) * B * rows * L.nc, 256);
   L.part2 = off;
-  off = round_up(off + sizeof(float) * std::max(sample ? B * static_cast<size_t>(L.nsub) : 0, grid_mass), 256);
+  off = round_up(off + sizeof(float) * (sample ? B * static_cast<size_t>(L.nsub) : 0), 256);
   L.counter2 = off;
   off = round_up(off + (sample ? sizeof(int) * B : 0), 256);
   L.theta = off;  // top-k / top-p: each row's threshold
@@ -119,34 +108,6 @@ void tree_geometry(int B, int V, int &cluster, int &slice) {
 }
 
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
-
-// The grid kernel's barrier counter must be zero when a launch starts; each
-// launch leaves it zero.  A workspace address not seen before gets its
-// counter zeroed on the call's stream.  Under stream capture that memset
-// becomes part of the graph (and runs at every replay), so the address is
-// marked as seen only when the memset was enqueued outside capture; an
-// address already seen adds nothing to a captured graph.
-std::mutex g_sync_mu;
-std::vector<std::pair<int, uintptr_t>> g_sync_seen;  // (device, workspace address)
-
-cudaError_t ensure_sync_zero(void *sync, cudaStream_t st) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const std::pair<int, uintptr_t> key{dev, reinterpret_cast<uintptr_t>(sync)};
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  e = cudaStreamIsCapturing(st, &cap);
-  if (e != cudaSuccess) return e;
-  std::lock_guard<std::mutex> g(g_sync_mu);
-  for (const auto &s : g_sync_seen)
-    if (s == key) return cudaSuccess;
-  e = cudaMemsetAsync(sync, 0, 256, st);
-  if (e == cudaSuccess && cap == cudaStreamCaptureStatusNone) {
-    if (g_sync_seen.size() >= 1024) g_sync_seen.erase(g_sync_seen.begin());  // forgotten: zeroed again when seen
-    g_sync_seen.push_back(key);
-  }
-  return e;
-}
 
 // -------------------------------------------------------------- tracing
 
@@ -252,7 +213,6 @@ const char *spec_status_string(int code) {
     case 100 + SPEC_STATUS_TOKEN_RANGE: return "request has a token outside [0, V)";
     case 100 + SPEC_STATUS_BAD_TREE: return "request has a malformed or too deep tree";
     case 100 + SPEC_STATUS_BAD_LENGTH: return "request has a length outside its range";
-    case 100 + SPEC_STATUS_SYNC_TIMEOUT: return "a grid-wide wait gave up (workspace barrier bytes not zero)";
     default: return "unknown code";
   }
 }
@@ -307,7 +267,7 @@ int spec_trace_collect(const char **names, double *total_ms, int64_t *launches, 
 }
 
 int spec_set_chain_path(int path) {
-  if (path != SPEC_CHAIN_AUTO && path != SPEC_CHAIN_TWO_PASS && path != SPEC_CHAIN_FUSED && path != SPEC_CHAIN_GRID)
+  if (path != SPEC_CHAIN_AUTO && path != SPEC_CHAIN_TWO_PASS && path != SPEC_CHAIN_FUSED)
     return SPEC_EINVAL;
   g_chain_path.store(path, std::memory_order_relaxed);
   return SPEC_OK;
@@ -392,11 +352,9 @@ static int chain_common(bool sample, const void *target, int64_t t_req, const vo
   P.counter2 = reinterpret_cast<int *>(ws + L.counter2);
   P.part = reinterpret_cast<Partial *>(ws + L.part);
   P.part2 = reinterpret_cast<float *>(ws + L.part2);
-  P.grid_sync = reinterpret_cast<unsigned *>(ws + L.sync);
   cudaError_t e;
   const bool fvec = vec && V % (16 / es) == 0;  // the fused kernel's 16-byte path also wants V a multiple of a group
   const int path = g_chain_path.load(std::memory_order_relaxed);
-  const bool want_grid = path == SPEC_CHAIN_GRID || (path == SPEC_CHAIN_AUTO && kGridAuto);
   const bool want_fused = path == SPEC_CHAIN_FUSED || (path == SPEC_CHAIN_AUTO && V <= kFusedAutoMaxV);
   if (filtered) {
     // the filter kernel replaces the streaming pass: one partial per row
@@ -413,9 +371,6 @@ static int chain_common(bool sample, const void *target, int64_t t_req, const vo
       if (!chain_accept_plan(P, fvec)) P.cluster = 0;
       e = launch_chain(P, true, vec, fvec, as_stream(stream), false);
     }
-  } else if (want_grid && chain_grid_plan(P, sample, fvec)) {
-    e = ensure_sync_zero(ws + L.sync, as_stream(stream));
-    if (e == cudaSuccess) e = launch_chain_grid(P, sample, fvec, as_stream(stream));
   } else if (want_fused && chain_fused_plan(P, sample, fvec)) {
     e = launch_chain_fused(P, sample, fvec, as_stream(stream));
   } else {

@@ -32,10 +32,6 @@ struct ChainParams {
   int cluster;       // cluster kernels: CTAs per request (sampling accept: 0 = chunked accept kernel)
   int slice;         // logits per CTA of a cluster kernel
   int groups;        // fused kernel: rounds of 16-byte groups per lane (warp ranges of the slice)
-  // grid kernel (chain_grid.cu): CTAs, 16-byte groups per CTA slice, 32-group
-  // chunks per slice row, register slots per warp, and the barrier counter
-  int grid_ctas, grid_gps, grid_cpr, grid_slots;
-  unsigned *grid_sync;
   // top-k / top-p filtering (filter.cu): the filter, and per partial row its
   // threshold (the smallest kept logit) and kept count.  theta == nullptr:
   // unfiltered (the accept kernels keep every logit).
@@ -44,11 +40,6 @@ struct ChainParams {
   float *theta;
   int32_t *kept;
 };
-
-// The grid kernel's limits, which the workspace layout also needs: CTAs
-// (one per SM of a GB300) and (request, position, chunk) items per CTA.
-constexpr int kGridMaxCtas = 152;
-constexpr int kGridMaxItems = 128;
 
 constexpr int kTreeThreads = 512;   // threads per tree-walk CTA
 constexpr int kFusedThreads = 512;  // threads per CTA of the fused chain kernel
@@ -90,12 +81,6 @@ bool chain_fused_plan(ChainParams &P, bool sample, bool vec);
 bool chain_accept_plan(ChainParams &P, bool vec);
 cudaError_t launch_chain_fused(const ChainParams &P, bool sample, bool vec, cudaStream_t st);
 cudaError_t launch_chain_accept_cluster(const ChainParams &P, bool vec, cudaStream_t st);
-// Grid kernel (chain_grid.cu): one cooperative launch, every request's rows
-// held in registers across the CTAs.  The plan fills the grid_* geometry and
-// returns false when the call does not fit (too many requests, positions or
-// partials for one launch) or cooperative launches are unavailable.  The
-// launch needs *grid_sync == 0 and leaves it 0.
-bool chain_grid_plan(ChainParams &P, bool sample, bool vec);
 // Top-k / top-p filter of every partial row (filter.cu): writes the row's
 // statistics over its kept logits as partial P.part[row] (one chunk per row)
 // and its threshold P.theta[row].  The plan picks the cluster geometry
@@ -103,7 +88,6 @@ bool chain_grid_plan(ChainParams &P, bool sample, bool vec);
 // slices of 96 KB).
 bool chain_filter_plan(ChainParams &P);
 cudaError_t launch_chain_filter(const ChainParams &P, bool vec, cudaStream_t st);
-cudaError_t launch_chain_grid(const ChainParams &P, bool sample, bool vec, cudaStream_t st);
 cudaError_t launch_tree(const TreeParams &P, bool vec, cudaStream_t st);
 size_t tree_dynamic_smem(const TreeParams &P);
 cudaError_t launch_ngram(const NgramParams &P, cudaStream_t st);

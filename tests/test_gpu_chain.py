@@ -3,9 +3,8 @@
 Greedy outputs and accept counts are compared bit for bit.  Sampled
 decisions follow the rule in tests/parity.py (near-threshold cases counted),
 per-token probabilities within 1e-5 absolute.  Every test runs once on each
-chain path (two-pass, fused and grid; a fused call whose clusters cannot all
-be resident, or a grid call that does not fit one cooperative launch, runs
-two-pass).
+chain path (two-pass and fused; a fused call whose clusters cannot all be
+resident runs two-pass).
 """
 import numpy as np
 import pytest
@@ -24,9 +23,9 @@ def _built():
     __graft_entry__.build()
 
 
-@pytest.fixture(scope="module", autouse=True, params=["two_pass", "fused", "grid"])
+@pytest.fixture(scope="module", autouse=True, params=["two_pass", "fused"])
 def chain_path(request, _built):
-    api.set_chain_path({"two_pass": api.CHAIN_TWO_PASS, "fused": api.CHAIN_FUSED, "grid": api.CHAIN_GRID}[request.param])
+    api.set_chain_path({"two_pass": api.CHAIN_TWO_PASS, "fused": api.CHAIN_FUSED}[request.param])
     yield request.param
     api.set_chain_path(api.CHAIN_AUTO)
 
