@@ -58,7 +58,7 @@ def _load():
         lib.orc_ngram_draft.argtypes = [P, P, I, I, I, I, P, P, P]
         lib.orc_verify_greedy.argtypes = [P, I, I, I, I, I64, I64, P, P, P, P, P, P, P]
         lib.orc_verify_sample.argtypes = [P, I64, P, I64, I64, I, I, I, I, D, I, D, P, P, P, P,
-                                          P, P, P, P, P, P, P, I, I, P]
+                                          P, P, P, P, P, P, P, I, I, P, P]
         lib.orc_filter_row.argtypes = [P, I, I, D, I, D, P, P, P]
         lib.orc_verify_tree.argtypes = [P, I64, P, I64, I64, I, I, I, I, D, P, P, P, I,
                                         P, P, P, P, P, I, I, P]
@@ -180,13 +180,15 @@ def verify_greedy(target, draft, draft_len=None, max_emit=None):
 
 def verify_sample(target, draft_logits, draft, uniforms, T: float = 1.0, draft_len=None,
                   max_emit=None, variant: int = VARIANT_LOSSLESS, threads: int = 1, top_k: int = 0,
-                  top_p: float = 1.0):
+                  top_p: float = 1.0, top_p_rows=None):
     """Sampling chain verification.
 
     target: [B, k+1, V], draft_logits: [B, k, V] (fp32 or bf16 bits; request
     strides may be 0 to broadcast one problem), draft: [B, k] int32,
     uniforms: [B, k+1] float32.  top_k / top_p filter p and q alike before
-    verification (0 / 1.0: off; see filter_row).
+    verification (0 / 1.0: off; see filter_row).  top_p_rows: optional
+    [B, 2k+1] float64, one top_p per row (target rows 0..k, then draft rows
+    0..k-1) in place of top_p.
     """
     target, code = _logits(target)
     draft_logits, code_d = _logits(draft_logits)
@@ -210,12 +212,16 @@ def verify_sample(target, draft_logits, draft, uniforms, T: float = 1.0, draft_l
                n_emit=np.empty(B, np.int32), p_tok=np.empty((B, k)), q_tok=np.empty((B, k)),
                resid_mass=np.empty(B), status=np.empty(B, np.int32))
     degen = np.zeros(1, dtype=np.int64)
+    if top_p_rows is not None:
+        top_p_rows = np.ascontiguousarray(top_p_rows, dtype=np.float64)
+        if top_p_rows.shape != (B, 2 * k + 1) or not np.all((top_p_rows > 0) & (top_p_rows <= 1)):
+            raise ValueError(f"top_p_rows must be {(B, 2 * k + 1)} values in (0, 1]")
     _check(_load().orc_verify_sample(
         _ptr(target), t_req, _ptr(draft_logits), d_req, row, code, B, k, V, float(T), int(top_k), float(top_p),
         _ptr(draft), _ptr(_i32(draft_len, (B,))), _ptr(_i32(max_emit, (B,))), _ptr(uniforms),
         _ptr(out["accepted"]), _ptr(out["out_tokens"]), _ptr(out["n_emit"]),
         _ptr(out["p_tok"]), _ptr(out["q_tok"]), _ptr(out["resid_mass"]), _ptr(out["status"]),
-        int(variant), int(threads), _ptr(degen)), "verify_sample")
+        int(variant), int(threads), _ptr(degen), _ptr(top_p_rows)), "verify_sample")
     out["degenerate"] = int(degen[0])
     return out
 

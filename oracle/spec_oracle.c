@@ -43,7 +43,7 @@
  *                  Decoding II", section "Context-Aware Dynamic Draft Tree"
  *                  and its worked example)
  *
- * Readings where the pages are silent (all listed in the design doc):
+ * Readings where the pages are silent:
  *   - the uniform u_i tests draft position i; u_k (the last one) drives the
  *     final draw, whether it is a residual draw or the bonus draw;
  *   - "accept with probability min(1, p/q)" is realised as accept iff
@@ -407,7 +407,10 @@ int orc_verify_greedy(const void *target, int dtype, int B, int k, int V,
  * Optional outputs (may be NULL): p_tok/q_tok [B,k] = p_i(x_i), q_i(x_i) for
  * i < draft_len (else -1); resid_mass [B] = sum max(0, p_m - q_m) at the
  * rejected position (0 when every draft token was accepted).
- * degenerate (may be NULL): incremented once per zero-mass residual. */
+ * degenerate (may be NULL): incremented once per zero-mass residual.
+ * top_p_rows (may be NULL): one top_p per row, [B][2k+1] in the order target
+ * rows 0..k then draft rows 0..k-1, in place of top_p (the same filter, each
+ * row with its own mass). */
 int orc_filter_row(const void *row, int dtype, int V, double T, int top_k, double top_p,
                    double *p, double *theta, int32_t *kept)
 {
@@ -427,7 +430,7 @@ int orc_verify_sample(const void *target, int64_t t_req, const void *draft_logit
                       int32_t *accepted, int32_t *out_tokens, int32_t *n_emit,
                       double *p_tok, double *q_tok, double *resid_mass,
                       int32_t *status, int variant, int threads,
-                      int64_t *degenerate)
+                      int64_t *degenerate, const double *top_p_rows)
 {
     if (!target || !draft_logits || B < 0 || k < 0 || V <= 0 || !(T > 0.0) ||
         (dtype != 0 && dtype != 1) || variant < 0 || variant > 2 || !(top_p > 0.0))
@@ -480,11 +483,15 @@ int orc_verify_sample(const void *target, int64_t t_req, const void *draft_logit
         }
         const char *tb = (const char *)target + (int64_t)b * t_req * es;
         const char *db = (const char *)draft_logits + (int64_t)b * d_req * es;
+        /* the top_p of target row i and of draft row i */
+        const double *tpr = top_p_rows ? top_p_rows + (int64_t)b * (2 * k + 1) : NULL;
+#define TP_T(i) (tpr ? tpr[(i)] : top_p)
+#define TP_D(i) (tpr ? tpr[k + 1 + (i)] : top_p)
 
         /* the per-position probabilities of the drafted tokens */
         for (int i = 0; i < L; ++i) {
-            fail |= filter_row(tb + (int64_t)i * row * es, dtype, V, T, top_k, top_p, p, NULL, NULL);
-            fail |= filter_row(db + (int64_t)i * row * es, dtype, V, T, top_k, top_p, q, NULL, NULL);
+            fail |= filter_row(tb + (int64_t)i * row * es, dtype, V, T, top_k, TP_T(i), p, NULL, NULL);
+            fail |= filter_row(db + (int64_t)i * row * es, dtype, V, T, top_k, TP_D(i), q, NULL, NULL);
             if (p_tok)
                 p_tok[(int64_t)b * k + i] = p[x[i]];
             if (q_tok)
@@ -494,12 +501,12 @@ int orc_verify_sample(const void *target, int64_t t_req, const void *draft_logit
         /* left to right: accept, or stop at the first rejection */
         int m = 0, final_tok = -1;
         for (; m < L; ++m) {
-            fail |= filter_row(tb + (int64_t)m * row * es, dtype, V, T, top_k, top_p, p, NULL, NULL);
+            fail |= filter_row(tb + (int64_t)m * row * es, dtype, V, T, top_k, TP_T(m), p, NULL, NULL);
             int acc;
             if (variant == 2) {
                 acc = inverse_cdf(p, V, (double)u[m]) == x[m];
             } else {
-                fail |= filter_row(db + (int64_t)m * row * es, dtype, V, T, top_k, top_p, q, NULL, NULL);
+                fail |= filter_row(db + (int64_t)m * row * es, dtype, V, T, top_k, TP_D(m), q, NULL, NULL);
                 acc = accept_test((double)u[m], p[x[m]], q[x[m]]);
             }
             if (!acc)
@@ -524,9 +531,11 @@ int orc_verify_sample(const void *target, int64_t t_req, const void *draft_logit
             }
         } else {
             /* all L accepted: the bonus token comes from p_L */
-            fail |= filter_row(tb + (int64_t)L * row * es, dtype, V, T, top_k, top_p, p, NULL, NULL);
+            fail |= filter_row(tb + (int64_t)L * row * es, dtype, V, T, top_k, TP_T(L), p, NULL, NULL);
             final_tok = inverse_cdf(p, V, (double)u[k]);
         }
+#undef TP_T
+#undef TP_D
         int cap = max_emit ? max_emit[b] : k + 1;
         int ne = m + 1 < cap ? m + 1 : cap;
         if (ne < 0)

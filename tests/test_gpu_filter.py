@@ -4,13 +4,15 @@ the oracle.
 - spec_filter_rows: the threshold and the kept count are the oracle's,
   exactly for top-k; for top-p the cut may sit one value group off only where
   the oracle's cumulative mass at that cut is within 1e-6 of top_p (counted).
-- spec_verify_sample_topkp: outputs under the chain decision rule of
-  tests/parity.py against the oracle's filtered verification (requests whose
-  GPU filter cut differs from the oracle's in some row -- only allowed where
-  the cut's mass is within 1e-6 of top_p -- are counted and skipped), on the
-  headline shape, bf16 ties at the top-k cut, masked logits, drafts outside
-  the filtered q, lengths, caps and bad tokens; both filters off reproduce
-  spec_verify_sample bit for bit.
+- spec_verify_sample_topkp: every request's outputs under the chain decision
+  rule of tests/parity.py against the oracle's filtered verification.  Where
+  the GPU's filter cut of a row differs from the oracle's (only allowed where
+  the cut's fp64 mass is within 1e-6 of top_p; counted), the oracle filters
+  that row with the top_p that gives the GPU's cut, so no request is left out.
+  On the headline shape, on both accept kernels (cluster, chunked),
+  bf16 ties at the top-k cut, masked logits, drafts outside the filtered q,
+  lengths, caps and bad tokens; both filters off reproduce spec_verify_sample
+  bit for bit.
 - spec_sample_topkp: tokens and q'(x) against the oracle, and 200,000 draws
   from one row follow the filtered distribution.
 """
@@ -120,22 +122,49 @@ def _filtered_chain(seed, B, k, V, dtype, T, top_k, top_p, draft_from_filtered=T
     return prob
 
 
-def _mismatch_requests(prob, top_k, top_p):
-    """Requests with a row whose GPU filter cut differs from the oracle's; each
-    such cut must be a top-p cut within NEAR of top_p in exact arithmetic.
-    (spec_filter_rows runs the same filter kernel, with the same slices and
-    arithmetic, as the filtered verification.)"""
+def _gpu_cut_top_p(row, T, top_k, top_p, theta_g):
+    """A top_p for which the oracle's filter of `row` keeps exactly the GPU's
+    set {x >= theta_g}: top_p itself when the two cuts agree; otherwise (a
+    cut one value group off, allowed only where the fp64 mass at the cut is
+    within NEAR of top_p) the middle of theta_g's value group in the oracle's
+    own fp64 masses, so that the oracle's descending walk reaches it inside
+    that group."""
+    ok, near = _cut_ok(row, T, top_k, top_p, theta_g)
+    assert ok, (theta_g, oracle.filter_row(row, T, top_k, top_p)[1])
+    if not near:
+        return top_p, False
+    x = workloads.logits_as_f64(row).reshape(-1)
+    z = x / T
+    p = np.exp(z - z.max())
+    keep = x >= np.sort(x)[::-1][top_k - 1] if 0 < top_k < x.size else np.ones(x.size, bool)
+    SK = p[keep].sum()
+    before = p[keep & (x > theta_g)].sum() / SK
+    group = p[keep & (x == theta_g)].sum() / SK
+    return before + group / 2, True
+
+
+def _top_p_rows(prob, top_k, top_p):
+    """Each verified row's top_p for the oracle, [B, 2k+1] (target rows 0..k,
+    then draft rows 0..k-1): top_p, except on rows where the GPU's filter cut
+    sits one value group off the oracle's (a top-p cut whose fp64 mass is
+    within NEAR of top_p) -- there the value that gives the oracle the GPU's
+    cut, so that every request is still compared in full.  (spec_filter_rows
+    runs the same filter kernel, with the same slices and arithmetic, as the
+    filtered verification.)"""
     B, R, V = prob["target"].shape
-    rows = np.concatenate([prob["target"].reshape(B * R, V), prob["draft_logits"].reshape(B * (R - 1), V)])
+    k = R - 1
+    rows = np.concatenate([prob["target"].reshape(B * R, V), prob["draft_logits"].reshape(B * k, V)])
     g = host(api.spec_filter_rows(to_dev(rows), prob["T"], top_k, top_p))
-    out = set()
+    tp = np.full((B, 2 * k + 1), float(top_p))
+    near = 0
     for j in range(rows.shape[0]):
         _, theta_o, _ = oracle.filter_row(rows[j], prob["T"], top_k, top_p)
         if float(g["theta"][j]) != theta_o:
-            ok, _ = _cut_ok(rows[j], prob["T"], top_k, top_p, float(g["theta"][j]))
-            assert ok, (j, g["theta"][j], theta_o)
-            out.add(j // R if j < B * R else (j - B * R) // (R - 1))
-    return out
+            b, col = (j // R, j % R) if j < B * R else ((j - B * R) // k, k + 1 + (j - B * R) % k)
+            tp[b, col], was_near = _gpu_cut_top_p(rows[j], prob["T"], top_k, top_p, float(g["theta"][j]))
+            near += was_near
+    assert near <= max(1, rows.shape[0] // 8), near
+    return tp, near
 
 
 def _run(prob, top_k, top_p, draft_len=None, max_emit=None):
@@ -150,23 +179,21 @@ def _run(prob, top_k, top_p, draft_len=None, max_emit=None):
     return host(o)
 
 
-def _check(prob, g, r, top_k, top_p, draft_len=None):
-    skip = _mismatch_requests(prob, top_k, top_p)
-    keep = np.array([b for b in range(prob["target"].shape[0]) if b not in skip], dtype=np.int64)
-    assert len(skip) <= max(1, len(keep) // 8), skip
-    if skip:
-        print("requests with a near top-p cut", sorted(skip))
-    sub = lambda d: {kk: (v[keep] if isinstance(v, np.ndarray) and v.ndim and v.shape[0] == len(keep) + len(skip)
-                          else v) for kk, v in d.items()}
-    # the decision rule's near-threshold replay uses the filtered distributions
-    p2 = dict(prob, target=prob["target"][keep], draft_logits=prob["draft_logits"][keep],
-              draft=prob["draft"][keep], uniforms=prob["uniforms"][keep])
-    return check_chain_sample_filtered(p2, sub(g), sub(r), top_k, top_p,
-                                       None if draft_len is None else draft_len[keep])
+def _check(prob, g, top_k, top_p, draft_len=None, max_emit=None):
+    """Every request of a filtered verification against the oracle's, the
+    oracle run with each row's top_p from _top_p_rows."""
+    tp, near = _top_p_rows(prob, top_k, top_p)
+    if near:
+        print("rows with a near top-p cut", near)
+    r = oracle.verify_sample(prob["target"], prob["draft_logits"], prob["draft"], prob["uniforms"], prob["T"],
+                             draft_len=draft_len, max_emit=max_emit, top_k=top_k, top_p=top_p,
+                             top_p_rows=tp, threads=oracle.max_threads())
+    return check_chain_sample_filtered(prob, g, r, top_k, tp, draft_len)
 
 
-def check_chain_sample_filtered(prob, g, r, top_k, top_p, draft_len=None):
-    """check_chain_sample with the near-threshold replays on filtered p and q."""
+def check_chain_sample_filtered(prob, g, r, top_k, tp, draft_len=None):
+    """check_chain_sample with the near-threshold replays on filtered p and q
+    (tp: each row's top_p, [B, 2k+1])."""
     B, R, V = prob["target"].shape
     k = R - 1
     np.testing.assert_array_equal(g["status"], r["status"])
@@ -190,9 +217,9 @@ def check_chain_sample_filtered(prob, g, r, top_k, top_p, draft_len=None):
         assert abs(g["resid_mass"][b] - r["resid_mass"][b]) <= TOL
         ne = int(r["n_emit"][b])
         if mo < ne and g["out_tokens"][b, mo] != r["out_tokens"][b, mo]:
-            pf = oracle.filter_row(prob["target"][b, mo], prob["T"], top_k, top_p)[0]
+            pf = oracle.filter_row(prob["target"][b, mo], prob["T"], top_k, tp[b, mo])[0]
             if mo < L:
-                qf = oracle.filter_row(prob["draft_logits"][b, mo], prob["T"], top_k, top_p)[0]
+                qf = oracle.filter_row(prob["draft_logits"][b, mo], prob["T"], top_k, tp[b, k + 1 + mo])[0]
                 dist, Rm = oracle.residual(pf, qf)
                 if Rm <= 0:
                     dist = pf
@@ -213,9 +240,7 @@ def test_filtered_verification_parity(seed, B, k, V, dtype, T, top_k, top_p):
     """B=400 takes the chunked accept kernel; the others the cluster accept kernel."""
     prob = _filtered_chain(seed, B, k, V, dtype, T, top_k, top_p)
     g = _run(prob, top_k, top_p)
-    r = oracle.verify_sample(prob["target"], prob["draft_logits"], prob["draft"], prob["uniforms"], T,
-                             top_k=top_k, top_p=top_p, threads=oracle.max_threads())
-    print("near", _check(prob, g, r, top_k, top_p))
+    print("near", _check(prob, g, top_k, top_p))
 
 
 def test_filtered_drafts_outside_the_filter_lengths_caps():
@@ -233,12 +258,9 @@ def test_filtered_drafts_outside_the_filter_lengths_caps():
     draft_len[1] = 2
     max_emit = rng.integers(0, k + 2, B).astype(np.int32)
     g = _run(prob, top_k, top_p, draft_len, max_emit)
-    r = oracle.verify_sample(prob["target"], prob["draft_logits"], prob["draft"], prob["uniforms"], 1.0,
-                             draft_len=draft_len, max_emit=max_emit, top_k=top_k, top_p=top_p,
-                             threads=oracle.max_threads())
-    _check(prob, g, r, top_k, top_p, draft_len)
+    _check(prob, g, top_k, top_p, draft_len, max_emit)
     assert list(g["status"][:2]) == [3, 1]
-    assert (r["q_tok"][r["status"] == 0] == 0).any()      # some drafts lie outside q'
+    assert (g["q_tok"][g["status"] == 0] == 0).any()      # some drafts lie outside q'
 
 
 def test_filters_off_is_the_unfiltered_path():
@@ -348,6 +370,4 @@ def test_filter_paths(dtype, top_p, reps):
             qf = oracle.filter_row(prob["draft_logits"][b, i], T, top_k, top_p)[0]
             prob["draft"][b, i] = rng.choice(V, p=qf / qf.sum())
     gv = _run(prob, top_k, top_p)
-    r = oracle.verify_sample(prob["target"], prob["draft_logits"], prob["draft"], prob["uniforms"], T,
-                             top_k=top_k, top_p=top_p, threads=oracle.max_threads())
-    _check(prob, gv, r, top_k, top_p)
+    _check(prob, gv, top_k, top_p)

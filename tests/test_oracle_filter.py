@@ -159,3 +159,35 @@ def test_drafter_top_k_draws_follow_the_top_k_softmax():
     # a tie at the cut takes the lower position
     tie = workloads.bf16_bits(np.array([1.0, 5.0, 1.0, 1.0], np.float32))
     assert {workloads.gumbel_draw_top_k(rng, tie, 1.0, 2) for _ in range(200)} <= {0, 1}
+
+
+def test_per_row_top_p_filters_each_row_with_its_own_mass():
+    """verify_sample's per-row top_p: filled with top_p it is the scalar form
+    bit for bit; a different value on one row changes that row's filter alone
+    (its p(x) is the filtered row's at that mass, every other row's is
+    unchanged)."""
+    rng = np.random.default_rng(5)
+    B, k, V, T = 3, 3, 40, 0.9
+    t = (rng.standard_normal((B, k + 1, V)) * 2).astype(np.float32)
+    d = (t[:, :k] + rng.standard_normal((B, k, V))).astype(np.float32)
+    x = rng.integers(0, V, (B, k)).astype(np.int32)
+    u = np.full((B, k + 1), 0.999, np.float32)
+    u[:, 0] = 0.0                                     # position 0 accepted whenever p(x) > 0
+    top_k, top_p = 15, 0.8
+    a = oracle.verify_sample(t, d, x, u, T, top_k=top_k, top_p=top_p)
+    b = oracle.verify_sample(t, d, x, u, T, top_k=top_k, top_p=top_p, top_p_rows=np.full((B, 2 * k + 1), top_p))
+    for key in ("accepted", "out_tokens", "n_emit", "p_tok", "q_tok", "resid_mass"):
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    tp = np.full((B, 2 * k + 1), top_p)
+    tp[1, 1] = 0.3                                    # target row 1 of request 1
+    tp[2, k + 1 + 2] = 0.5                            # draft row 2 of request 2
+    c = oracle.verify_sample(t, d, x, u, T, top_k=top_k, top_p=top_p, top_p_rows=tp)
+    assert c["p_tok"][1, 1] == oracle.filter_row(t[1, 1], T, top_k, 0.3)[0][x[1, 1]]
+    assert c["q_tok"][2, 2] == oracle.filter_row(d[2, 2], T, top_k, 0.5)[0][x[2, 2]]
+    same = np.ones((B, k), bool)
+    same[1, 1] = False
+    np.testing.assert_array_equal(c["p_tok"][same], a["p_tok"][same])
+    same = np.ones((B, k), bool)
+    same[2, 2] = False
+    np.testing.assert_array_equal(c["q_tok"][same], a["q_tok"][same])
+    assert oracle.filter_row(t[1, 1], T, top_k, 0.3)[2] < oracle.filter_row(t[1, 1], T, top_k, top_p)[2]
