@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload vocab248k|batch64|topkp64|small|tree60|tree60wor|draw64|ngram|eagle2]
-                    [--chain-path auto|two_pass|fused]
+                    [--chain-path auto|two_pass|fused] [--no-configs]
 
 One step is one pass of the path over one batch:
   vocab248k  spec_verify_sample, B=1, k=4, V=248,320 bf16 (the default: the
@@ -38,12 +38,14 @@ max over ranks.  --impl reference times the fp64 oracle on the host cores.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -159,10 +161,11 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, path=None):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        self.keep = path is not None
+        self.path = path or os.path.join(tempfile.gettempdir(), f"spec_bench_clocks_{os.getpid()}_{gpu_index}.csv")
         self.window = None  # (start, end) of the timed region, wall clock
 
     def count(self) -> int:
@@ -201,9 +204,11 @@ class ClockSampler:
                 self.proc.kill()
             self.f.close()
 
-    def summary(self) -> dict:
-        if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+    def _samples(self):
+        """(timestamp, SM MHz, max MHz, active throttle reasons) per sample,
+        read once; a temporary sample file is removed after reading."""
+        if getattr(self, "_rows", None) is not None:
+            return self._rows
         import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         rows = []
@@ -220,6 +225,18 @@ class ClockSampler:
             except ValueError:
                 ts = None
             rows.append((ts, sm, mx, {n for n, v in zip(names, parts[5:9]) if v.lower() == "active"}))
+        if not self.keep:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
+        self._rows = rows
+        return rows
+
+    def summary(self) -> dict:
+        if self.proc is None or (not os.path.exists(self.path) and getattr(self, "_rows", None) is None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = self._samples()
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         inside = [r for r in rows if self.window and r[0] is not None and
@@ -299,6 +316,10 @@ class ChainWorkload:
             return tot / len(outs)
         return None
 
+    def step_bytes(self, outs):
+        """Algorithmic bytes of one step: every verified row read once."""
+        return self.set_bytes
+
     def oracle_call(self, n, threads):
         """At least n requests through the oracle: a single-request workload is
         broadcast to n requests (no copy), a batch is verified whole, repeatedly."""
@@ -360,6 +381,9 @@ class DrawWorkload:
             return self.B * self.V * self.es
         return None
 
+    def step_bytes(self, outs):
+        return self.set_bytes
+
     def oracle_call(self, n, threads):
         """At least n draws through the oracle (verification with no draft)."""
         import oracle
@@ -420,6 +444,10 @@ class TreeWorkload:
                         tot += row * (2 if int(u) in self.kids[b] else 1)
         return tot / len(outs)
 
+    def step_bytes(self, outs):
+        """The rows on the walked paths (read-everything would be set_bytes)."""
+        return self.kernel_bytes("tree_walk", outs)
+
     def oracle_call(self, n, threads):
         """At least n requests: the batch of trees is verified whole, repeatedly."""
         import oracle
@@ -465,6 +493,9 @@ class EagleWorkload:
         """Inputs (parents, confidences, tokens) and outputs (five int32/fp32
         values per kept node, the m x m mask)."""
         return self.B * (self.N * 12 + self.m * 20 + self.m * self.m)
+
+    def step_bytes(self, outs):
+        return self.kernel_bytes("tree_rerank", outs)
 
     def oracle_call(self, n, threads):
         import oracle
@@ -518,6 +549,10 @@ class NgramWorkload:
             return tot / len(outs)
         return None
 
+    def step_bytes(self, outs):
+        """The histories and the verified rows (draft_len + 1 per request)."""
+        return self.B * self.H * 4 + self.kernel_bytes("chain_stats_greedy", outs)
+
     def oracle_call(self, n, threads):
         import oracle
         p = self.prob
@@ -527,6 +562,10 @@ class NgramWorkload:
             oracle.verify_greedy(p["target"], d, dl)
         return reps * self.rows_per_step
 
+
+# the pages' other configs whose workloads every run also measures (the
+# headline --workload is vocab248k: config 3)
+CONFIG_WORKLOADS = ("batch64", "ngram", "tree60", "topkp64")
 
 WORKLOADS = {"vocab248k": ChainWorkload, "batch64": ChainWorkload, "small": ChainWorkload, "topkp64": ChainWorkload,
              "tree60": TreeWorkload, "tree60wor": TreeWorkload, "draw64": DrawWorkload, "ngram": NgramWorkload, "eagle2": EagleWorkload}
@@ -590,6 +629,203 @@ def run_reference(args):
 
 # -------------------------------------------------------------- our arm
 
+def _external_event():
+    """A timing event that, recorded during stream capture, becomes an
+    event-record node of the graph (None when this torch lacks the option)."""
+    import torch
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None
+
+
+def timed_graphs(wl, sets, outs, stream, steps):
+    """Exactly `steps` calls cycling over the input sets, as CUDA graphs to
+    replay in order: [(graph, replays), ...], and the two timing events.  The
+    first graph's first node and the last graph's last node record the events,
+    so the measured span starts with the first kernel, not with a graph
+    launch; each graph is replayed once here, untimed, so that no replay in
+    the timed region is a graph's first."""
+    import torch
+    nsets = len(sets)
+    ev0, ev1 = _external_event(), _external_event()
+    in_graph = ev0 is not None and ev1 is not None
+
+    def capture(n, head=False, tail=False):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                if head and in_graph:
+                    ev0.record(stream)
+                for i in range(n):
+                    wl.call(sets[i], outs[i], stream)
+                if tail and in_graph:
+                    ev1.record(stream)
+        return g
+
+    full, rem = divmod(steps, nsets)
+    if full == 0:
+        plan = [(capture(rem, True, True), 1)]
+    elif rem:
+        plan = [(capture(nsets, head=True), 1)]
+        if full > 1:
+            plan.append((capture(nsets), full - 1))
+        plan.append((capture(rem, tail=True), 1))
+    elif full == 1:
+        plan = [(capture(nsets, True, True), 1)]
+    else:
+        plan = [(capture(nsets, head=True), 1)]
+        if full > 2:
+            plan.append((capture(nsets), full - 2))
+        plan.append((capture(nsets, tail=True), 1))
+    if not in_graph:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for g, _ in plan:
+            g.replay()
+    return plan, ev0, ev1, in_graph
+
+
+def kernel_times(wl, sets, outs, stream, reps=8):
+    """{kernel: (microseconds per launch, launches per step)}: the calls of one
+    input cycle captured into a graph with every kernel launched `reps` times
+    back to back between a pair of CUDA events on its launching stream
+    (spec_trace_repeat), timed on the graph's last replay; the bracket over
+    reps is the kernel's duration without one launch's set-up."""
+    import torch
+    from speculative_decoding_verification_02_gb300 import api
+    dev = stream.device
+    api.trace_enable(True)
+    api.trace_repeat(reps)
+    api.trace_collect()
+    g = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(len(sets)):
+                    wl.call(sets[i], outs[i], stream)
+    finally:
+        api.trace_enable(False)
+        api.trace_repeat(1)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize(dev)
+    trace = api.trace_collect()
+    del g
+    return {k: (1e3 * t_ms / cnt / reps, cnt / len(sets)) for k, (t_ms, cnt) in trace.items()}
+
+
+def measure(name, args, dev, stream, want_clocks=True):
+    """Times one workload: exactly args.steps calls after args.warmup, inputs
+    rotating over resident sets that put more than twice the L2 between
+    reuses.  Returns (workload, result dict, sets, outs)."""
+    import torch
+    from speculative_decoding_verification_02_gb300 import api
+    wl = WORKLOADS[name](name)
+    nsets = max(2, int(np.ceil(2 * L2_BYTES / wl.set_bytes)))
+    nsets = min(256, int(2 ** np.ceil(np.log2(nsets))))
+    if wl.kind == "tree":
+        nsets = 6   # a walk reads ~1/8 of a set; six sets put ~2.4x L2 between reuses
+    sets = [wl.device_set(dev, i) for i in range(nsets)]
+    with torch.cuda.stream(stream):
+        outs = [wl.call(sets[i], None, stream) for i in range(nsets)]
+    n0 = api.launch_count()
+    with torch.cuda.stream(stream):
+        wl.call(sets[0], outs[0], stream)
+    launches_per_call = api.launch_count() - n0
+    torch.cuda.synchronize(dev)
+    plan, ev0, ev1, in_graph = timed_graphs(wl, sets, outs, stream, args.steps)
+    load_graph = torch.cuda.CUDAGraph()  # untimed load around the timed region (no timing nodes)
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(load_graph, stream=stream):
+            for i in range(nsets):
+                wl.call(sets[i], outs[i], stream)
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(dev.index, args.clock_log) if want_clocks else None
+    with (sampler or contextlib.nullcontext()):
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup // nsets):
+                load_graph.replay()
+            for i in range(args.warmup % nsets):
+                wl.call(sets[i], outs[i], stream)
+        torch.cuda.synchronize(dev)
+
+        def load():
+            with torch.cuda.stream(stream):
+                for _ in range(8):
+                    load_graph.replay()
+            torch.cuda.synchronize(dev)
+
+        if sampler:
+            sampler.keep_busy(load, 2, 3.0)
+        barrier()
+        torch.cuda.synchronize(dev)
+        t_start = time.time()
+        if not in_graph:
+            ev0.record(stream)
+        with torch.cuda.stream(stream):
+            for g, n in plan:
+                for _ in range(n):
+                    g.replay()
+        if not in_graph:
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_end = time.time()
+        barrier()
+        ms = ev0.elapsed_time(ev1)
+        if sampler:
+            sampler.window = (t_start, t_end)
+            sampler.keep_busy(load, 1, 1.5)
+    del plan, load_graph
+    ms_max = reduce_max(ms, dev)
+    ws, _, _ = dist_env()
+    value = reduce_sum(args.steps * wl.rows_per_step, dev) / (ms_max / 1e3)
+    ms_step = ms_max / args.steps
+
+    peak, peak_kind = peak_hbm()
+    kt = kernel_times(wl, sets, outs, stream)
+    kernels = {}
+    busy = sum(us * per for us, per in kt.values())
+    for kname, (us, per) in kt.items():
+        nbytes = wl.kernel_bytes(kname, outs)
+        kernels[kname] = {"avg_us": us, "launches_per_step": per, "share": us * per / busy,
+                          "algorithmic_bytes_per_launch": nbytes,
+                          "achieved_gbs": (nbytes / (us * 1e-6) / 1e9) if nbytes else None}
+    dom = max(kernels, key=lambda n: kernels[n]["avg_us"] * kernels[n]["launches_per_step"])
+    achieved = kernels[dom]["achieved_gbs"]
+    step_bytes = wl.step_bytes(outs)
+    res = {
+        "metric": getattr(wl, "metric", METRIC), "value": value, "unit": getattr(wl, "unit", "rows/s"),
+        "steps": args.steps, "ms_per_step": ms_step,
+        "config": {"workload": wl.desc, "rows_per_step": wl.rows_per_step, "logits": wl.logits,
+                   "parallelism": f"replicas x{ws}",
+                   "l2": (f"inputs rotate over {min(nsets, args.steps)} of {nsets} resident sets "
+                          f"({nsets * wl.set_bytes / 2**20:.0f} MiB), more than twice the L2 between reuses"
+                          if nsets * wl.set_bytes > 2 * L2_BYTES else
+                          f"inputs L2-resident ({nsets} sets, {nsets * wl.set_bytes / 2**20:.1f} MiB): a "
+                          f"latency-bound workload with little data"),
+                   "launch": f"CUDA graphs of {nsets} calls; timing events are graph nodes" if in_graph else
+                             f"CUDA graphs of {nsets} calls", "chain_path": args.chain_path},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
+                     "traffic": profiled_traffic(dom, name, wl.kind),
+                     "avg_launch_us": kernels[dom]["avg_us"],
+                     "algorithmic_bytes_per_launch": kernels[dom]["algorithmic_bytes_per_launch"],
+                     "step_bytes": step_bytes,
+                     "step_frac": step_bytes / (ms_step * 1e-3) / 1e9 / peak if step_bytes else None,
+                     "kernel_timing": "each kernel launched 8 times back to back between CUDA events "
+                                      "in a graph replay; avg_us = bracket / 8",
+                     "kernels": kernels},
+        "gpu_launches": int(launches_per_call * args.steps),
+    }
+    if sampler:
+        res["clocks"] = sampler.summary()
+    return wl, res, sets, outs
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -605,118 +841,21 @@ def run_ours(args):
     from speculative_decoding_verification_02_gb300 import api
     api.set_chain_path({"auto": api.CHAIN_AUTO, "two_pass": api.CHAIN_TWO_PASS,
                         "fused": api.CHAIN_FUSED}[args.chain_path])
-
-    wl = WORKLOADS[args.workload](args.workload)
-    # rotating input sets: one cycle reads more than twice the L2
-    nsets = max(2, int(np.ceil(2 * L2_BYTES / wl.set_bytes)))
-    nsets = min(256, int(2 ** np.ceil(np.log2(nsets))))
-    if wl.kind == "tree":
-        nsets = 6   # a walk reads ~1/8 of a set; six sets put ~2.4x L2 between reuses
-    sets = [wl.device_set(dev, i) for i in range(nsets)]
     stream = torch.cuda.Stream(device=dev)
-    with torch.cuda.stream(stream):
-        outs = [wl.call(sets[i], None, stream) for i in range(nsets)]
-    n0 = api.launch_count()
-    with torch.cuda.stream(stream):
-        wl.call(sets[0], outs[0], stream)
-    launches_per_call = api.launch_count() - n0
-    torch.cuda.synchronize(dev)
-
-    # one graph cycles once through every input set
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(graph, stream=stream):
-            for i in range(nsets):
-                wl.call(sets[i], outs[i], stream)
-    rem = args.steps % nsets
-    graph_rem = None
-    if rem:
-        graph_rem = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(graph_rem, stream=stream):
-                for i in range(rem):
-                    wl.call(sets[i], outs[i], stream)
-    torch.cuda.synchronize(dev)
-
-    sampler = ClockSampler(local)
-    with sampler:
-        with torch.cuda.stream(stream):
-            for _ in range(args.warmup // nsets):
-                graph.replay()
-            for i in range(args.warmup % nsets):
-                wl.call(sets[i], outs[i], stream)
-        torch.cuda.synchronize(dev)
-
-        def load():  # untimed replays of the same graph, so clock samples see the step's load
-            with torch.cuda.stream(stream):
-                for _ in range(8):
-                    graph.replay()
-            torch.cuda.synchronize(dev)
-
-        sampler.keep_busy(load, 2, 3.0)
-        barrier()
-        torch.cuda.synchronize(dev)
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t_start = time.time()
-        ev0.record(stream)
-        with torch.cuda.stream(stream):
-            for _ in range(args.steps // nsets):
-                graph.replay()
-            if graph_rem is not None:
-                graph_rem.replay()
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
-        sampler.window = (t_start, time.time())
-        barrier()
-        ms = ev0.elapsed_time(ev1)
-        sampler.keep_busy(load, 1, 1.5)
-    clocks = sampler.summary()
-    ms_max = reduce_max(ms, dev)
-    total_rows = reduce_sum(args.steps * wl.rows_per_step, dev)
-    value = total_rows / (ms_max / 1e3)
-
-    # kernel timing pass: the same calls captured into a graph with every
-    # kernel bracketed by CUDA events on its launching stream (event-record
-    # nodes; dependent launches serialised), timed on the graph's last replay
-    api.trace_enable(True)
-    api.trace_collect()
-    reps = max(1, min(4, 256 // nsets))
-    tgraph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(tgraph, stream=stream):
-            for r in range(reps):
-                for i in range(nsets):
-                    wl.call(sets[i], outs[i], stream)
-    api.trace_enable(False)
-    torch.cuda.synchronize(dev)
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            tgraph.replay()
-    torch.cuda.synchronize(dev)
-    trace = api.trace_collect()
-    del tgraph
-    peak, peak_kind = peak_hbm()
-    kernels = {}
-    for kname, (t_ms, cnt) in trace.items():
-        avg_s = t_ms / cnt / 1e3
-        nbytes = wl.kernel_bytes(kname, outs)
-        kernels[kname] = {"avg_us": avg_s * 1e6, "launches": cnt, "share": t_ms / sum(v[0] for v in trace.values()),
-                          "algorithmic_bytes_per_launch": nbytes,
-                          "achieved_gbs": (nbytes / avg_s / 1e9) if nbytes else None}
-    dom = max(kernels, key=lambda n: kernels[n]["avg_us"] * kernels[n]["launches"])
-    achieved = kernels[dom]["achieved_gbs"]
+    wl, res, sets, outs = measure(args.workload, args, dev, stream)
 
     # end to end through the C ABI with host buffers: H2D inputs, call, D2H results
     steps_e2e = max(3, min(args.steps, int(2e9 // max(wl.set_bytes, 1)), 2000))
-    n_host = max(1, min(4, nsets, int(1e9 // max(wl.set_bytes, 1))))
+    n_host = max(1, min(4, len(sets), int(1e9 // max(wl.set_bytes, 1))))
     h_sets = [{k2: v.cpu().pin_memory() for k2, v in sets[i].items()} for i in range(n_host)]
     d_in = {k2: torch.empty_like(v) for k2, v in sets[0].items()}
+    del sets, outs
     with torch.cuda.stream(stream):
         d_out = wl.call(d_in, None, stream)
-    res = d_out if isinstance(d_out, tuple) else (d_out,)
+    outs_e = d_out if isinstance(d_out, tuple) else (d_out,)
     keys = wl.result_keys
     h_out = []
-    for o in res:
+    for o in outs_e:
         h_out.append({k2: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k2, v in o.items()
                       if keys is None or k2 in keys})
     h2d = sum(v.numel() * v.element_size() for v in h_sets[0].values())
@@ -748,6 +887,21 @@ def run_ours(args):
     wall = time.perf_counter() - t_wall
     e2e_ms = reduce_max(max(e0.elapsed_time(e1), 1e3 * wall), dev)
     e2e_value = reduce_sum(steps_e2e * wl.rows_per_step, dev) / (e2e_ms / 1e3)
+    del h_sets, d_in, d_out, h_out
+
+    # the other workloads of the pages' configs, measured in the same run
+    configs = {}
+    if not args.no_configs:
+        cargs = argparse.Namespace(**vars(args))
+        cargs.steps = max(1, min(args.steps, args.config_steps))
+        cargs.warmup = max(3, min(args.warmup, 200))
+        for name in CONFIG_WORKLOADS:
+            if name == args.workload:
+                continue
+            _, r, s_, o_ = measure(name, cargs, dev, stream, want_clocks=False)
+            del s_, o_
+            torch.cuda.empty_cache()
+            configs[name] = r
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -758,31 +912,16 @@ def run_ours(args):
                          f"{', OpenMP over requests' if threads > 1 else ', one thread'})"}
 
     if rank == 0:
-        line = {
-            "metric": getattr(wl, "metric", METRIC), "value": value, "unit": getattr(wl, "unit", "rows/s"),
-            "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": wl.desc, "rows_per_step": wl.rows_per_step, "logits": wl.logits,
-                       "parallelism": f"replicas x{ws}",
-                       "l2": (f"inputs rotate over {nsets} resident sets ({nsets * wl.set_bytes / 2**20:.0f} MiB, "
-                              f"more than twice the L2 between reuses)" if nsets * wl.set_bytes > 2 * L2_BYTES else
-                              f"inputs L2-resident ({nsets} sets, {nsets * wl.set_bytes / 2**20:.1f} MiB): a "
-                              f"latency-bound workload with little data"),
-                       "launch": f"CUDA graph of {nsets} calls", "chain_path": args.chain_path},
-            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
-                         "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
-                         "traffic": profiled_traffic(dom, args.workload, wl.kind),
-                         "avg_launch_us": kernels[dom]["avg_us"],
-                         "algorithmic_bytes_per_launch": kernels[dom]["algorithmic_bytes_per_launch"],
-                         "kernels": kernels},
-            "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": getattr(wl, "unit", "rows/s"), "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h,
-                    "steps": steps_e2e},
-            "gpu_launches": int(launches_per_call * args.steps),
-            "clocks": clocks,
-        }
+        line = {"metric": res["metric"], "value": res["value"], "unit": res["unit"], "n_gpus": ws,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic", "config": res["config"], "roofline": res["roofline"],
+                "cpu_baseline": cpu,
+                "e2e": {"value": e2e_value, "unit": res["unit"], "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h, "steps": steps_e2e},
+                "gpu_launches": res["gpu_launches"], "clocks": res["clocks"]}
+        if configs:
+            line["configs"] = configs
         print(json.dumps(line), flush=True)
     if dist.is_initialized():
         dist.destroy_process_group()
@@ -797,6 +936,12 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="vocab248k", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time only --workload (not the other configs' workloads as well)")
+    ap.add_argument("--config-steps", type=int, default=20_000,
+                    help="steps of each other config's workload (at most --steps)")
+    ap.add_argument("--clock-log", default=None,
+                    help="keep the nvidia-smi clock samples in this CSV file (default: a temporary file)")
     ap.add_argument("--chain-path", choices=["auto", "two_pass", "fused"], default="auto",
                     help="chain verification path (same results; for profiling one path)")
     args = ap.parse_args(argv)

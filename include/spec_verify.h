@@ -406,8 +406,15 @@ const char *spec_last_error(void);
  * to be timed (the record keeps one pair per captured launch, whatever the
  * number of replays).  Dependent launches are not chained while tracing is
  * on, so each bracket holds one kernel.
+ * spec_trace_repeat(reps), reps in [1, 1024] (default 1, else SPEC_EINVAL):
+ * while tracing, each kernel is launched reps times back to back inside its
+ * event pair, so the bracket divided by reps approaches the kernel's own
+ * duration (one launch's set-up no longer in it).  Every kernel of the
+ * library gives the same outputs when launched again on its own inputs, so
+ * the results do not change; the launch count grows by the repeats.
  */
 int spec_trace_enable(int on);
+int spec_trace_repeat(int reps);
 int spec_trace_collect(const char **names, double *total_ms, int64_t *launches, int cap);
 
 /* Number of kernels this process has launched through the library. */

@@ -61,6 +61,7 @@ def lib():
         L.spec_last_error.argtypes = []
         L.spec_last_error.restype = ctypes.c_char_p
         L.spec_trace_enable.argtypes = [I]
+        L.spec_trace_repeat.argtypes = [I]
         L.spec_trace_collect.argtypes = [P, P, P, I]
         L.spec_launch_count.argtypes = []
         L.spec_launch_count.restype = ctypes.c_int64
@@ -104,7 +105,16 @@ def _check(rc: int, what: str):
         L = lib()
         msg = L.spec_status_string(rc).decode()
         err = L.spec_last_error().decode()
-        raise SpecError(f"{what}: {msg}" + (f" [{err}]" if err and rc == SPEC_ECUDA else ""))
+        detail = err and rc in (SPEC_ECUDA, SPEC_EWORKSPACE)
+        raise SpecError(f"{what}: {msg}" + (f" [{err}]" if detail else ""))
+
+
+def _call(dev, fn, *args):
+    """fn(*args) with the tensors' device current: the library sizes its
+    launches for the current device, and the no-allocation entry point looks
+    up its scratch array there."""
+    with torch.cuda.device(dev):
+        return fn(*args)
 
 
 def _i32(t, shape, name, device):
@@ -167,6 +177,11 @@ def trace_enable(on: bool = True):
     lib().spec_trace_enable(1 if on else 0)
 
 
+def trace_repeat(reps: int = 1):
+    """While tracing, launch each kernel reps times inside its event pair."""
+    _check(lib().spec_trace_repeat(int(reps)), "spec_trace_repeat")
+
+
 def trace_collect(cap: int = 16) -> dict:
     """{kernel name: (total ms, launches)} since the last collect."""
     names = (ctypes.c_char_p * cap)()
@@ -195,7 +210,7 @@ def spec_ngram_draft(history: torch.Tensor, hist_len: torch.Tensor, window: int,
     o = out or dict(draft=torch.empty((B, k), dtype=torch.int32, device=dev),
                     draft_len=torch.empty(B, dtype=torch.int32, device=dev),
                     status=torch.empty(B, dtype=torch.int32, device=dev))
-    rc = lib().spec_ngram_draft(_p(history), _p(hist_len), B, H, int(window), int(k), _p(o["draft"]),
+    rc = _call(dev, lib().spec_ngram_draft, _p(history), _p(hist_len), B, H, int(window), int(k), _p(o["draft"]),
                                 _p(o["draft_len"]), _p(o["status"]), _stream(stream, dev))
     _check(rc, "spec_ngram_draft")
     return o
@@ -218,7 +233,7 @@ def spec_verify_greedy(target: torch.Tensor, draft: torch.Tensor, draft_len=None
                     out_tokens=torch.empty((B, k + 1), dtype=torch.int32, device=dev),
                     n_emit=torch.empty(B, dtype=torch.int32, device=dev),
                     status=torch.empty(B, dtype=torch.int32, device=dev))
-    rc = lib().spec_verify_greedy(_p(target), target.stride(0), target.stride(1), dt, B, k, V,
+    rc = _call(dev, lib().spec_verify_greedy, _p(target), target.stride(0), target.stride(1), dt, B, k, V,
                                   _p(draft), _p(draft_len), _p(max_emit), _p(o["accepted"]),
                                   _p(o["out_tokens"]), _p(o["n_emit"]), _p(o["status"]), _p(ws),
                                   ws.numel(), _stream(stream, dev))
@@ -265,9 +280,9 @@ def spec_verify_sample(target: torch.Tensor, draft_logits: torch.Tensor, draft: 
             _p(o["n_emit"]), _p(o.get("p_tok")), _p(o.get("q_tok")), _p(o.get("resid_mass")), _p(o["status"]),
             _p(ws), ws.numel(), _stream(stream, dev))
     if top_k or top_p != 1.0:
-        _check(lib().spec_verify_sample_topkp(*head, int(top_k), float(top_p), *tail), "spec_verify_sample_topkp")
+        _check(_call(dev, lib().spec_verify_sample_topkp, *head, int(top_k), float(top_p), *tail), "spec_verify_sample_topkp")
     else:
-        _check(lib().spec_verify_sample(*head, *tail), "spec_verify_sample")
+        _check(_call(dev, lib().spec_verify_sample, *head, *tail), "spec_verify_sample")
     return o
 
 
@@ -304,10 +319,10 @@ def spec_verify_tree(target: torch.Tensor, draft_logits, parents: torch.Tensor, 
     tail = (_p(o["accepted_len"]), _p(o["path_nodes"]), _p(o["out_tokens"]), _p(o["n_emit"]), _p(o["status"]),
             None, 0, _stream(stream, dev))
     if flags:
-        rc = lib().spec_verify_tree_ex(*head, int(flags), *tail)
+        rc = _call(dev, lib().spec_verify_tree_ex, *head, int(flags), *tail)
         _check(rc, "spec_verify_tree_ex")
     else:
-        rc = lib().spec_verify_tree(*head, *tail)
+        rc = _call(dev, lib().spec_verify_tree, *head, *tail)
         _check(rc, "spec_verify_tree")
     return o
 
@@ -336,11 +351,11 @@ def spec_sample(logits: torch.Tensor, uniforms: torch.Tensor, temperature: float
     tail = (_p(uniforms), _p(o["tokens"]), _p(o.get("probs")), _p(o["status"]), _p(ws), ws.numel(),
             _stream(stream, dev))
     if top_k or top_p != 1.0:
-        rc = lib().spec_sample_topkp(_p(logits), logits.stride(0), dt, B, V, float(temperature), int(top_k),
+        rc = _call(dev, lib().spec_sample_topkp, _p(logits), logits.stride(0), dt, B, V, float(temperature), int(top_k),
                                      float(top_p), *tail)
         _check(rc, "spec_sample_topkp")
     else:
-        _check(lib().spec_sample(_p(logits), logits.stride(0), dt, B, V, float(temperature), *tail), "spec_sample")
+        _check(_call(dev, lib().spec_sample, _p(logits), logits.stride(0), dt, B, V, float(temperature), *tail), "spec_sample")
     return o
 
 
@@ -360,7 +375,7 @@ def spec_filter_rows(logits: torch.Tensor, temperature: float = 1.0, top_k: int 
     ws = workspace(spec_workspace_size(OP_FILTER, R, 0, V, dt), dev, stream)
     o = out or dict(theta=torch.empty(R, dtype=torch.float32, device=dev),
                     kept=torch.empty(R, dtype=torch.int32, device=dev))
-    _check(lib().spec_filter_rows(_p(logits), logits.stride(0), dt, R, V, float(temperature), int(top_k),
+    _check(_call(dev, lib().spec_filter_rows, _p(logits), logits.stride(0), dt, R, V, float(temperature), int(top_k),
                                   float(top_p), _p(o["theta"]), _p(o.get("kept")), _p(ws), ws.numel(),
                                   _stream(stream, dev)), "spec_filter_rows")
     return o
@@ -385,7 +400,7 @@ def spec_tree_rerank(parents: torch.Tensor, conf: torch.Tensor, m: int, max_dept
                     sel_tok=torch.empty((B, m), **i32) if node_tok is not None else None,
                     mask=torch.empty((B, m, m), dtype=torch.uint8, device=dev) if mask else None,
                     n_sel=torch.empty(B, **i32), status=torch.empty(B, **i32))
-    rc = lib().spec_tree_rerank(_p(parents), _p(conf), _p(node_tok), B, N, int(m), int(max_depth),
+    rc = _call(dev, lib().spec_tree_rerank, _p(parents), _p(conf), _p(node_tok), B, N, int(m), int(max_depth),
                                 _p(o["sel_nodes"]), _p(o["sel_parents"]), _p(o["sel_depth"]),
                                 _p(o.get("sel_value")), _p(o.get("sel_tok")), _p(o.get("mask")),
                                 _p(o["n_sel"]), _p(o.get("status")), _stream(stream, dev))
@@ -424,7 +439,7 @@ def spec_verify_sample_noalloc(target: torch.Tensor, draft_logits: torch.Tensor,
                     p_tok=torch.empty((B, k), dtype=torch.float32, device=dev),
                     q_tok=torch.empty((B, k), dtype=torch.float32, device=dev),
                     resid_mass=torch.empty(B, dtype=torch.float32, device=dev))
-    rc = fn(_p(target), target.stride(0), _p(draft_logits), draft_logits.stride(0), target.stride(1),
+    rc = _call(dev, fn, _p(target), target.stride(0), _p(draft_logits), draft_logits.stride(0), target.stride(1),
             _dtype_code(target), B, k, V, float(temperature), _p(draft), _p(draft_len), _p(max_emit),
             _p(uniforms), _p(o["accepted"]), _p(o["out_tokens"]), _p(o["n_emit"]), _p(o.get("p_tok")),
             _p(o.get("q_tok")), _p(o.get("resid_mass")), _p(o["status"]), _stream(stream, dev))

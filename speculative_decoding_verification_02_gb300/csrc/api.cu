@@ -33,11 +33,10 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // ------------------------------------------------------------ geometry
 
 // Logits per CTA of the streaming pass, sized from the call's total bytes so
-// that the grid is about four waves of four CTAs on each of the GB300's 152
-// SMs, between 16 KB and 128 KB of one row: small calls spread over every
+// that the grid is about four waves of four CTAs on each SM (152 on a
+// GB300), between 16 KB and 128 KB of one row: small calls spread over every
 // SM, large ones keep each CTA streaming long enough to amortise its
 // start-up and reduction.  The chunked accept kernel uses 16 KB chunks.
-constexpr long long kSmCount = 152;
 
 // Chain path (spec_set_chain_path).  In AUTO the fused kernel takes
 // vocabularies up to kFusedAutoMaxV: 0, since with the cluster accept kernel
@@ -48,7 +47,7 @@ constexpr int kFusedAutoMaxV = 0;
 
 int stream_chunk(int dtype, long long rows_total, int V) {
   const long long es = elem_size(dtype);
-  const long long target_ctas = kSmCount * 4 * 4;
+  const long long target_ctas = static_cast<long long>(device_sm_count()) * 4 * 4;
   const long long per = rows_total * V * es / target_ctas;
   long long bytes = 16384;
   while (bytes < per && bytes < 131072) bytes *= 2;
@@ -59,7 +58,7 @@ int stream_chunk(int dtype, long long rows_total, int V) {
 // SM) over the whole batch, at least 4,096 logits, a multiple of 2,048, at
 // most 64 sub-chunks of 256 x 16 bytes.
 int accept_chunk(int B, int V, int dtype) {
-  const long long per_req = std::max<long long>(1, 2 * kSmCount / std::max(B, 1));
+  const long long per_req = std::max<long long>(1, 2LL * device_sm_count() / std::max(B, 1));
   long long chunk = (V + per_req - 1) / per_req;
   chunk = (chunk + 2047) / 2048 * 2048;
   const long long cap = 64LL * 256 * (16 / elem_size(dtype));
@@ -103,7 +102,7 @@ ChainLayout chain_layout(bool sample, int B, int k, int V, int dtype) {
 // every cluster resident at once (one walk CTA per SM).
 void tree_geometry(int B, int V, int &cluster, int &slice) {
   cluster = V >= 16 * 2048 ? 16 : V >= 8 * 2048 ? 8 : (V >= 4 * 2048 ? 4 : (V >= 2 * 2048 ? 2 : 1));
-  while (cluster > 1 && static_cast<long long>(B) * cluster > kSmCount) cluster /= 2;
+  while (cluster > 1 && static_cast<long long>(B) * cluster > device_sm_count()) cluster /= 2;
   slice = ((V + cluster - 1) / cluster + 7) / 8 * 8;
 }
 
@@ -118,6 +117,7 @@ struct TraceRec {
 
 std::mutex g_trace_mu;
 bool g_trace_on = false;
+int g_trace_reps = 1;
 std::vector<TraceRec> g_trace;
 std::vector<cudaEvent_t> g_event_pool;
 long long g_launches = 0;
@@ -171,9 +171,32 @@ void count_launch() {
 
 void set_last_error(const char *msg) { std::snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
 
+int device_sm_count() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cached[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return 152;  // (a GB300's count; only reached when there is no device to ask)
+  }
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  cached[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
 bool trace_enabled() {
   std::lock_guard<std::mutex> g(g_trace_mu);
   return g_trace_on;
+}
+
+int trace_repeats() {
+  std::lock_guard<std::mutex> g(g_trace_mu);
+  return g_trace_reps;
 }
 
 }  // namespace sv
@@ -222,6 +245,13 @@ const char *spec_last_error(void) { return g_last_error; }
 int spec_trace_enable(int on) {
   std::lock_guard<std::mutex> g(g_trace_mu);
   g_trace_on = on != 0;
+  return SPEC_OK;
+}
+
+int spec_trace_repeat(int reps) {
+  if (reps < 1 || reps > 1024) return SPEC_EINVAL;
+  std::lock_guard<std::mutex> g(g_trace_mu);
+  g_trace_reps = reps;
   return SPEC_OK;
 }
 
@@ -356,6 +386,7 @@ static int chain_common(bool sample, const void *target, int64_t t_req, const vo
   const bool fvec = vec && V % (16 / es) == 0;  // the fused kernel's 16-byte path also wants V a multiple of a group
   const int path = g_chain_path.load(std::memory_order_relaxed);
   const bool want_fused = path == SPEC_CHAIN_FUSED || (path == SPEC_CHAIN_AUTO && V <= kFusedAutoMaxV);
+
   if (filtered) {
     // the filter kernel replaces the streaming pass: one partial per row
     // (statistics over the kept logits) and each row's threshold, then the

@@ -56,7 +56,7 @@ constexpr int kFilterThreads = 512;
 constexpr int kFilterWarps = kFilterThreads / 32;
 constexpr int kFilterListCap = 1024;             // candidate logits per CTA on the list path
 constexpr int kFilterRowListCap = 4096;          // the same in row mode (one CTA per row)
-constexpr int kFilterRowMinRows = 2 * 152;       // row mode from this many rows (two per SM of the 152)
+constexpr int kFilterRowMinRowsPerSm = 2;       // row mode from this many rows per SM
 constexpr int kFilterLoadBatch = 6;              // 16-byte loads each thread keeps in flight
 constexpr double kMassScale = 17592186044416.0;  // 2^44: fixed-point unit of the histogram masses
 
@@ -604,7 +604,7 @@ cudaError_t launch_chain_filter(const ChainParams &P, bool vec, cudaStream_t st)
   const int rows = P.B * (2 * P.k + 1);
   // row mode when top-k is on (its window needs it) and the rows alone fill
   // the GPU; otherwise a cluster per row splits each row over several SMs
-  const bool row_mode = P.top_k > 0 && P.top_k < P.V && rows >= kFilterRowMinRows;
+  const bool row_mode = P.top_k > 0 && P.top_k < P.V && rows >= kFilterRowMinRowsPerSm * device_sm_count();
   const int cs = row_mode ? 1 : P.cluster;
   const size_t smem = row_mode ? 0 : static_cast<size_t>(P.slice) * es;
   auto go = [&](auto kern) -> cudaError_t {

@@ -12,6 +12,7 @@ namespace sv {
 
 struct Partial;
 
+
 struct ChainParams {
   const char *target;
   const char *draftl;
@@ -73,6 +74,8 @@ struct NgramParams {
 // stats = false (sampling only): the accept kernel alone, on partials the
 // filter kernel wrote.
 cudaError_t launch_chain(const ChainParams &P, bool sample, bool vec, bool cvec, cudaStream_t st, bool stats = true);
+// Streaming multiprocessors of the current device (queried once per device).
+int device_sm_count();
 // Cluster kernels (chain_fused.cu).  The plans pick the cluster geometry
 // (cluster, slice, groups) and return false when the requests' clusters
 // cannot all be resident at once.  chain_fused_plan: the fused one-launch
@@ -116,24 +119,34 @@ void set_last_error(const char *msg);
 // dependent kernels without programmatic dependent launch, so that each
 // kernel's event pair brackets only its own execution.
 bool trace_enabled();
+// Launches of each kernel inside its event pair while tracing (1 otherwise).
+int trace_repeats();
 
 template <class F>
 cudaError_t trace_launch(const char *name, cudaStream_t st, F &&launch) {
   const int slot = trace_begin(name, st);
-  launch();
-  const cudaError_t e = cudaGetLastError();
+  const int reps = slot >= 0 ? trace_repeats() : 1;
+  cudaError_t e = cudaSuccess;
+  for (int r = 0; r < reps && e == cudaSuccess; ++r) {
+    launch();
+    e = cudaGetLastError();
+    count_launch();
+  }
   trace_end(slot, st);
-  count_launch();
   return e;
 }
 
 template <class F>
 cudaError_t trace_launch_ex(const char *name, cudaStream_t st, F &&launch) {
   const int slot = trace_begin(name, st);
-  cudaError_t e = launch();
-  if (e == cudaSuccess) e = cudaGetLastError();
+  const int reps = slot >= 0 ? trace_repeats() : 1;
+  cudaError_t e = cudaSuccess;
+  for (int r = 0; r < reps && e == cudaSuccess; ++r) {
+    e = launch();
+    if (e == cudaSuccess) e = cudaGetLastError();
+    count_launch();
+  }
   trace_end(slot, st);
-  count_launch();
   return e;
 }
 

@@ -90,3 +90,24 @@ def test_noalloc_refuses_problems_beyond_its_scratch(L):
                                       1.0, fake, None, None, fake, fake, fake, fake, None, None, None, None, None)
     assert rc == api.SPEC_EWORKSPACE
     assert b"needs" in L.spec_last_error() and b"scratch" in L.spec_last_error()
+
+
+def test_noalloc_python_binding_matches_workspace_binding(L):
+    """The Python wrapper api.spec_verify_sample_noalloc (argument checks,
+    strides, draft_len / max_emit, current device) against api.spec_verify_sample,
+    and its refusal of an oversized problem with the library's message."""
+    prob = workloads.chain_problem(303, 12, 5, 20000, "bf16", 0.9, target_std=2.0, noise_std=0.7)
+    rng = np.random.default_rng(303)
+    dl = to_dev(rng.integers(0, 6, 12).astype(np.int32))
+    me = to_dev(rng.integers(1, 7, 12).astype(np.int32))
+    args = (to_dev(prob["target"]), to_dev(prob["draft_logits"]), to_dev(prob["draft"]), to_dev(prob["uniforms"]),
+            prob["T"], dl, me)
+    for _ in range(2):
+        got = host(api.spec_verify_sample_noalloc(*args))
+        torch.cuda.synchronize()
+        _same(got, host(api.spec_verify_sample(*args)))
+    # B=4096, k=64: 4096 x 129 row partials of 16 bytes, more than the 4 MiB array
+    big = torch.zeros((4096, 65, 64), dtype=torch.float32, device="cuda")
+    with pytest.raises(api.SpecError, match="needs .* bytes of scratch"):
+        api.spec_verify_sample_noalloc(big, big[:, :64], torch.zeros((4096, 64), dtype=torch.int32, device="cuda"),
+                                       torch.zeros((4096, 65), dtype=torch.float32, device="cuda"), 1.0)
