@@ -45,6 +45,18 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 
 // ---------------------------------------------------------------- loads
 
+// 16-byte asynchronous copy global -> shared (L2 only), and its group
+// commit / wait (hardware waits: the thread's own copies of all but the N
+// most recent groups have landed).
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // 16-byte streaming load that does not allocate in L1 (rows are read once).
 __device__ __forceinline__ uint4 ld_stream16(const void *p) {
   uint4 r;

@@ -57,7 +57,8 @@ constexpr int kFilterWarps = kFilterThreads / 32;
 constexpr int kFilterListCap = 1024;             // candidate logits per CTA on the list path
 constexpr int kFilterRowListCap = 4096;          // the same in row mode (one CTA per row)
 constexpr int kFilterRowMinRowsPerSm = 2;       // row mode from this many rows per SM
-constexpr int kFilterLoadBatch = 6;              // 16-byte loads each thread keeps in flight
+constexpr int kFilterLoadBatch = 4;              // 16-byte loads each thread keeps in flight
+
 constexpr double kMassScale = 17592186044416.0;  // 2^44: fixed-point unit of the histogram masses
 
 // Order-preserving unsigned key of an fp32 value (its bits); -0 maps to +0.
@@ -156,41 +157,103 @@ __device__ __forceinline__ void filter_row(const ChainParams &P, const int j) {
   // ---- the slice into shared memory, and the slice max
   float mloc = -INFINITY;
   const int ng = VEC ? n / EPG : 0;  // n is a multiple of EPG on the 16-byte path
+  __shared__ uint32_t s_list[kCap];
+  __shared__ int s_nlist;
   if (!STAGE) {
-    // row mode: the max only, batches of 16-byte loads in flight per thread,
-    // marked evict-last in L2 so that the row is still there for the passes
-    // that read it again
+    // row mode: one pass over the row (batches of 16-byte loads in flight per
+    // thread) for its max and, with top-k on, the candidate list: each warp
+    // keeps its running max and appends every logit at or above the floor of
+    // that max's top-byte bin.  The threshold only rises and the row's own
+    // bin floor is at least every warp's, so the list holds every logit of
+    // the window the list path needs (plus smaller ones, which change
+    // neither the top_k-th largest nor the kept set); the rows whose list
+    // overflows, or whose window holds fewer than top_k logits, are read
+    // again below.
     if (VEC) {
       const uint4 *g16 = reinterpret_cast<const uint4 *>(row);
-      unsigned long long keep;
-      asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
-      __nv_bfloat162 mx2 = __float2bfloat162_rn(-INFINITY);
-      for (int g0 = tid; g0 < ng; g0 += kFilterThreads * kFilterLoadBatch) {
-        uint4 w[kFilterLoadBatch];
+      const bool spec = P.top_k > 0 && P.top_k < V;
+      if (tid == 0) s_nlist = 0;
+      __syncthreads();
+      constexpr uint32_t kNegInf = DT == SPEC_DTYPE_F32 ? 0xff800000u : 0xff80ff80u;  // -inf words
+      constexpr int kLoadBatch = kFilterLoadBatch;
+      for (int gw = tid - lane; gw < ng; gw += kFilterThreads * kLoadBatch) {  // (warp-uniform)
+        const int g0 = gw + lane;  // the lane's groups: g0 + kFilterThreads u
+        uint4 w[kLoadBatch];
 #pragma unroll
-        for (int u = 0; u < kFilterLoadBatch; ++u)
-          if (g0 + u * kFilterThreads < ng) {
-            const uint4 *a = g16 + g0 + u * kFilterThreads;
-            asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-                : "=r"(w[u].x), "=r"(w[u].y), "=r"(w[u].z), "=r"(w[u].w)
-                : "l"(a), "l"(keep));
+        for (int u = 0; u < kLoadBatch; ++u)
+          w[u] = g0 + u * kFilterThreads < ng ? ld_stream16(g16 + g0 + u * kFilterThreads)
+                                              : make_uint4(kNegInf, kNegInf, kNegInf, kNegInf);
+        float bmax = -INFINITY;  // this thread's max over the batch
+        if (DT == SPEC_DTYPE_BF16) {
+          __nv_bfloat162 mx2 = *reinterpret_cast<const __nv_bfloat162 *>(&w[0].x);
+#pragma unroll
+          for (int u = 0; u < kLoadBatch; ++u) {
+            mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162 *>(&w[u].x));
+            mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162 *>(&w[u].y));
+            mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162 *>(&w[u].z));
+            mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162 *>(&w[u].w));
           }
+          bmax = fmaxf(__low2float(mx2), __high2float(mx2));
+        } else {
 #pragma unroll
-        for (int u = 0; u < kFilterLoadBatch; ++u) {
-          if (g0 + u * kFilterThreads < ng) {
-            if (DT == SPEC_DTYPE_BF16) {
-              mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162 *>(&w[u].x));
-              mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162 *>(&w[u].y));
-              mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162 *>(&w[u].z));
-              mx2 = __hmax2(mx2, *reinterpret_cast<const __nv_bfloat162 *>(&w[u].w));
-            } else {
-              mloc = fmaxf(mloc, fmaxf(fmaxf(__uint_as_float(w[u].x), __uint_as_float(w[u].y)),
-                                       fmaxf(__uint_as_float(w[u].z), __uint_as_float(w[u].w))));
+          for (int u = 0; u < kLoadBatch; ++u)
+            bmax = fmaxf(bmax, fmaxf(fmaxf(__uint_as_float(w[u].x), __uint_as_float(w[u].y)),
+                                     fmaxf(__uint_as_float(w[u].z), __uint_as_float(w[u].w))));
+        }
+        mloc = fmaxf(mloc, bmax);
+        if (spec) {
+          const uint32_t dw = order_key(__float_as_uint(warp_allmax(mloc))) >> 24;
+          const float tw = (dw >= 2u && (dw | 1u) != 0x81u) ? bin_floor<DT>(dw) : -INFINITY;
+          // (a thread whose batch max is below tw has nothing to append; most
+          // batches of most rows have no such logit in the whole warp)
+          const bool has = bmax >= tw;
+          if (!__any_sync(0xffffffffu, has)) continue;
+          // this lane's logits >= tw, counted; one reservation of list slots
+          // per warp (a shuffle scan of the counts, one atomic); then each
+          // lane writes its own -- no warp-wide step inside the divergent part
+          int mine = 0;
+          const uint32_t t2 = (__float_as_uint(tw) >> 16) * 0x10001u;
+#pragma unroll
+          for (int u = 0; u < kLoadBatch; ++u) {
+            if (!has || g0 + u * kFilterThreads >= ng) continue;  // (past the row's end)
+            const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              if (DT == SPEC_DTYPE_BF16) mine += __popc(ge_pair(ws[h], t2));
+              else mine += __uint_as_float(ws[h]) >= tw;
             }
           }
+          int incl = mine;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+          }
+          const int wtot = __shfl_sync(0xffffffffu, incl, 31);
+          int base = 0;
+          if (lane == 31 && wtot > 0) base = atomicAdd(&s_nlist, wtot);
+          base = __shfl_sync(0xffffffffu, base, 31);
+          int pos = base + incl - mine;
+          if (mine > 0 && pos < kCap) {
+#pragma unroll
+            for (int u = 0; u < kLoadBatch; ++u) {
+              if (g0 + u * kFilterThreads >= ng) continue;
+              const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+              for (int h = 0; h < 4 * (DT == SPEC_DTYPE_BF16 ? 2 : 1); ++h) {
+                const uint32_t bits = DT == SPEC_DTYPE_F32 ? ws[h]
+                                      : ((h & 1) ? (ws[h >> 1] & 0xffff0000u) : (ws[h >> 1] << 16));
+                if (__uint_as_float(bits) >= tw) {
+                  if (pos < kCap) s_list[pos] = bits;
+                  ++pos;
+                }
+              }
+            }
+          }
+          __syncwarp();
         }
       }
-      if (DT == SPEC_DTYPE_BF16) mloc = fmaxf(__low2float(mx2), __high2float(mx2));
+
     } else {
       for (int e = tid; e < n; e += kFilterThreads) mloc = fmaxf(mloc, load_one<DT>(row, e));
     }
@@ -243,17 +306,45 @@ __device__ __forceinline__ void filter_row(const ChainParams &P, const int j) {
   // ---- the list path (top-k on): the window of the max's top-byte bin, or
   // of that bin and the one below, when the window holds top_k logits and
   // each CTA's share fits the list
-  __shared__ uint32_t s_list[kCap];
-  __shared__ int s_nlist;
   __shared__ uint32_t s_xc[2][kMaxCS];  // per rank: logits >= tau0, logits >= tau1
   __shared__ uint32_t s_w0[kFilterWarps], s_w1[kFilterWarps];
   bool use_list = false;  // the walk runs over s_union[0, nlist) in rank 0 alone
+  bool top_bin = false;   // and every logit the walks need shares the max's top byte
   int nlist = 0;
   uint32_t *s_union = s_list;
   const uint32_t BM = order_key(__float_as_uint(M)) >> 24;
   // (not for a max in the two bins at +0, whose floors +0 and the smallest
   // normal would let a flushed subnormal compare on the wrong side)
-  if (P.top_k > 0 && P.top_k < V && BM >= 2u && (BM | 1u) != 0x81u) {
+  const bool window_ok = P.top_k > 0 && P.top_k < V && BM >= 2u && (BM | 1u) != 0x81u;
+  if (!STAGE && VEC && window_ok) {
+    // row mode: the list the first pass built serves when it did not
+    // overflow and holds top_k logits of the max's bin.  Thread 0 reads the
+    // list's length and publishes one decision, so every thread of the CTA
+    // takes the same branch (and meets the same barriers).
+    __shared__ int s_listn;
+    if (tid == 0) {
+      const int len = *reinterpret_cast<volatile int *>(&s_nlist);
+      s_listn = len <= kCap ? len : -1;
+    }
+    __syncthreads();
+    const int nl = s_listn;
+    if (nl >= 0) {
+      const float tau0 = bin_floor<DT>(BM);
+      uint32_t c0 = 0u;
+      for (int e = tid; e < nl; e += kFilterThreads) c0 += __uint_as_float(s_list[e]) >= tau0;
+      c0 = __reduce_add_sync(0xffffffffu, c0);
+      if (lane == 0) s_w0[warp] = c0;
+      __syncthreads();
+      c0 = __reduce_add_sync(0xffffffffu, lane < kFilterWarps ? s_w0[lane] : 0u);
+      if (c0 >= static_cast<uint32_t>(P.top_k)) {
+        use_list = true;
+        top_bin = true;
+        nlist = nl;
+      }
+      __syncthreads();  // (s_w0 is written again below)
+    }
+  }
+  if (!use_list && window_ok) {
     const float tau0 = bin_floor<DT>(BM), tau1 = bin_floor<DT>(BM - 1u);
     // appends every logit >= tau to the list (up to its capacity); with
     // COUNT, also counts the logits >= tau0 and >= tau1 (tau = tau0)
@@ -328,6 +419,7 @@ __device__ __forceinline__ void filter_row(const ChainParams &P, const int j) {
     int win = -1;  // the window taken: 0 (>= tau0), 1 (>= tau1), -1 none
     if (T0 >= K && A0 <= static_cast<uint32_t>(kCap)) {
       win = 0;  // the lists hold every logit >= tau0
+      top_bin = true;
     } else if (T1 >= K && A1 <= static_cast<uint32_t>(kCap)) {
       if (tid == 0) s_nlist = 0;
       __syncthreads();
@@ -342,7 +434,7 @@ __device__ __forceinline__ void filter_row(const ChainParams &P, const int j) {
       // goes on alone
       use_list = true;
       __syncthreads();
-      const int mine = min(s_nlist, kCap);
+      const int mine = min(*reinterpret_cast<volatile int *>(&s_nlist), kCap);
       if (STAGE && CS > 1) {
         uint32_t off = 0u, total = 0u;
         for (int q = 0; q < CS; ++q) {
@@ -472,12 +564,16 @@ __device__ __forceinline__ void filter_row(const ChainParams &P, const int j) {
     return s_sel_digit;
   };
 
-  // ---- top-k: the top_k-th largest key
+  // ---- top-k: the top_k-th largest key.  When the list holds the max's
+  // top-byte bin and that bin holds top_k logits, the answer and every kept
+  // logit have the max's top byte BM: the walks start at the second byte.
+  const int lv0 = top_bin ? 1 : 0;
+  const uint32_t prefix0 = top_bin ? BM : 0u;
   float theta = -INFINITY;
   if (P.top_k > 0 && P.top_k < V) {
-    uint32_t prefix = 0u;
+    uint32_t prefix = prefix0;
     unsigned long long need = static_cast<unsigned long long>(P.top_k), rest = 0ull;
-    for (int lv = 0; lv < kLevels; ++lv) {
+    for (int lv = lv0; lv < kLevels; ++lv) {
       const int shift = 24 - 8 * lv;
       const uint32_t d = level(shift, prefix, lv == 0, -INFINITY, false, need, rest);
       prefix = (prefix << 8) | d;
@@ -487,11 +583,11 @@ __device__ __forceinline__ void filter_row(const ChainParams &P, const int j) {
   }
   // ---- top-p over the logits top-k kept
   if (P.top_p < 1.0f) {
-    uint32_t prefix = 0u;
+    uint32_t prefix = prefix0;
     unsigned long long need = 0ull, rest = 0ull;
-    for (int lv = 0; lv < kLevels; ++lv) {
+    for (int lv = lv0; lv < kLevels; ++lv) {
       // the first level's walk needs top_p of the kept mass it histograms
-      const uint32_t d = level(24 - 8 * lv, prefix, lv == 0, theta, true, need, rest, lv == 0 ? P.top_p : 0.0f);
+      const uint32_t d = level(24 - 8 * lv, prefix, lv == 0, theta, true, need, rest, lv == lv0 ? P.top_p : 0.0f);
       prefix = (prefix << 8) | d;
       need = rest;
     }
@@ -579,7 +675,7 @@ __device__ __forceinline__ void filter_row(const ChainParams &P, const int j) {
 // loop alone raised the kernel to 60 registers, two CTAs per SM instead of
 // three.)
 template <int DT, bool VEC, bool STAGE>
-__global__ void __launch_bounds__(kFilterThreads) chain_filter_kernel(const ChainParams P) {
+__global__ void __launch_bounds__(kFilterThreads, STAGE ? 2 : 4) chain_filter_kernel(const ChainParams P) {
   pdl_wait();  // the draft lengths and tokens may come from the previous kernel
   pdl_launch_dependents();
   filter_row<DT, VEC, STAGE>(P, STAGE ? static_cast<int>(blockIdx.x) / P.cluster : static_cast<int>(blockIdx.x));
