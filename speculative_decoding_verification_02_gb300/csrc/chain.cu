@@ -239,11 +239,12 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
         const int gv = v0 + ((i0 + q) * kThreads + tid) * EPG;
         float ws = 0.0f;
         if (full[q]) {
-          float a[EPG], bb[EPG];
+          float a[EPG], bb[EPG], w[EPG];
           unpack16<DT>(A[q], a);
           if (W.b != nullptr) unpack16<DT>(Bv[q], bb);
+          weights_group<EPG, FILT>(W, a, bb, w);
 #pragma unroll
-          for (int e = 0; e < EPG; ++e) ws += weight_at<DT, FILT>(W, a[e], bb[e]);
+          for (int e = 0; e < EPG; ++e) ws += w[e];
         } else {
           for (int e = 0; e < EPG; ++e) {
             const int v = gv + e;

@@ -74,12 +74,13 @@ __device__ __forceinline__ float lane_weight_sum(const Weights &W, int lo, int h
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       if (j0 + u < G) {
-        float x[EPG], y[EPG];
+        float x[EPG], y[EPG], w[EPG];
         unpack16<DT>(xa[u], x);
         if (W.b) unpack16<DT>(xb[u], y);
+        weights_group<EPG, FILT>(W, x, y, w);
         float gs = 0.0f;
 #pragma unroll
-        for (int e = 0; e < EPG; ++e) gs += weight_at<DT, FILT>(W, x[e], W.b ? y[e] : 0.0f);
+        for (int e = 0; e < EPG; ++e) gs += w[e];
         gsum[g0 + 32 * u] = gs;
         acc += gs;
       }
@@ -304,8 +305,7 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
     float x[EPG], y[EPG];
     unpack16<DT>(load_group<DT, VEC>(W.a, lo + g * EPG, hi), x);
     if (W.b) unpack16<DT>(load_group<DT, VEC>(W.b, lo + g * EPG, hi), y);
-#pragma unroll
-    for (int e = 0; e < EPG; ++e) w[e] = weight_at<DT, FILT>(W, x[e], W.b ? y[e] : 0.0f);
+    weights_group<EPG, FILT>(W, x, y, w);
   });
   if (tid == 0) {
     if (m < ne) P.out_tokens[static_cast<int64_t>(b) * (k + 1) + m] = tok;

@@ -174,13 +174,49 @@ struct Weights {
   float ta, tb;
 };
 
-// FILT = false compiles the thresholds out: the unfiltered rows' loops keep
-// their instruction count (the masks cost a compare and a select per logit).
+// The weights of two elements (a, b: their logits in the two rows), in
+// packed f32x2 arithmetic: one instruction subtracts, scales or combines
+// both, so a residual weight costs about nine instructions instead of
+// twelve (the scans of these weights are bound by instruction issue, not by
+// the exponentials).  FILT = false compiles the thresholds out (the masks
+// cost a compare and a select per logit).  Every sum and scan of the
+// weights, single elements included (weight_at), goes through this
+// function, so they agree bit for bit.
+template <bool FILT>
+__device__ __forceinline__ float2 weight_pair(const Weights &W, float2 a, float2 b) {
+  const float2 cc = make_float2(W.c, W.c);
+  const float2 za = __fmul2_rn(__fadd2_rn(a, make_float2(-W.Ma, -W.Ma)), cc);
+  float2 w = __fmul2_rn(make_float2(ex2(za.x), ex2(za.y)), make_float2(W.alpha, W.alpha));
+  if (FILT) {
+    if (!(a.x >= W.ta)) w.x = 0.0f;
+    if (!(a.y >= W.ta)) w.y = 0.0f;
+  }
+  if (W.b != nullptr) {
+    const float2 zb = __fmul2_rn(__fadd2_rn(b, make_float2(-W.Mb, -W.Mb)), cc);
+    float2 q = make_float2(ex2(zb.x), ex2(zb.y));
+    if (FILT) {
+      if (!(b.x >= W.tb)) q.x = 0.0f;
+      if (!(b.y >= W.tb)) q.y = 0.0f;
+    }
+    w = __ffma2_rn(make_float2(-W.beta, -W.beta), q, w);
+  }
+  return make_float2(fmaxf(w.x, 0.0f), fmaxf(w.y, 0.0f));
+}
+
 template <int DT, bool FILT = true>
 __device__ __forceinline__ float weight_at(const Weights &W, float a, float b) {
-  float w = (!FILT || a >= W.ta) ? W.alpha * ex2((a - W.Ma) * W.c) : 0.0f;
-  if (W.b != nullptr && (!FILT || b >= W.tb)) w -= W.beta * ex2((b - W.Mb) * W.c);
-  return fmaxf(w, 0.0f);
+  return weight_pair<FILT>(W, make_float2(a, a), make_float2(b, b)).x;
+}
+
+// The weights of EPG consecutive elements (a, b: their logits; EPG even).
+template <int EPG, bool FILT = true>
+__device__ __forceinline__ void weights_group(const Weights &W, const float *a, const float *b, float *w) {
+#pragma unroll
+  for (int e = 0; e < EPG; e += 2) {
+    const float2 r = weight_pair<FILT>(W, make_float2(a[e], a[e + 1]), make_float2(b[e], b[e + 1]));
+    w[e] = r.x;
+    w[e + 1] = r.y;
+  }
 }
 
 // True when either row of W has a top-k / top-p threshold.
@@ -216,8 +252,10 @@ __device__ __forceinline__ void weights8(const Weights &W, int v0, int hi, float
       b[e] = (in && W.b != nullptr) ? load_one<DT>(W.b, v0 + e) : -INFINITY;
     }
   }
+  weights_group<8>(W, a, b, w);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) w[e] = (v0 + e < hi) ? weight_at<DT>(W, a[e], b[e]) : 0.0f;
+  for (int e = 0; e < 8; ++e)
+    if (v0 + e >= hi) w[e] = 0.0f;
 }
 
 // Block-wide inverse-CDF selection inside [lo, hi): the smallest v with
