@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload vocab248k|batch64|topkp64|small|tree60|tree60wor|draw64|ngram|eagle2]
-                    [--chain-path auto|two_pass|fused] [--no-configs]
+                    [--chain-path auto|two_pass|fused|chunked] [--no-configs]
 
 One step is one pass of the path over one batch:
   vocab248k  spec_verify_sample, B=1, k=4, V=248,320 bf16 (the default: the
@@ -839,8 +839,8 @@ def run_ours(args):
     import __graft_entry__
     __graft_entry__.build()
     from speculative_decoding_verification_02_gb300 import api
-    api.set_chain_path({"auto": api.CHAIN_AUTO, "two_pass": api.CHAIN_TWO_PASS,
-                        "fused": api.CHAIN_FUSED}[args.chain_path])
+    api.set_chain_path({"auto": api.CHAIN_AUTO, "two_pass": api.CHAIN_TWO_PASS, "fused": api.CHAIN_FUSED,
+                        "chunked": api.CHAIN_CHUNKED}[args.chain_path])
     stream = torch.cuda.Stream(device=dev)
     wl, res, sets, outs = measure(args.workload, args, dev, stream)
 
@@ -942,7 +942,7 @@ def main(argv=None):
                     help="steps of each other config's workload (at most --steps)")
     ap.add_argument("--clock-log", default=None,
                     help="keep the nvidia-smi clock samples in this CSV file (default: a temporary file)")
-    ap.add_argument("--chain-path", choices=["auto", "two_pass", "fused"], default="auto",
+    ap.add_argument("--chain-path", choices=["auto", "two_pass", "fused", "chunked"], default="auto",
                     help="chain verification path (same results; for profiling one path)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)

@@ -423,8 +423,13 @@ int64_t spec_launch_count(void);
 /*
  * Chain verification paths.  spec_verify_greedy and spec_verify_sample give
  * the same results on either path; the paths differ in speed:
- *   SPEC_CHAIN_TWO_PASS  a streaming pass over every row on all SMs, then an
- *                        accept kernel (suits large batches: bandwidth-bound);
+ *   SPEC_CHAIN_TWO_PASS  a streaming pass over every row on all SMs, then the
+ *                        cluster accept kernel: one thread-block cluster
+ *                        per request forms the final draw (the chunked one
+ *                        below when the clusters cannot all be resident);
+ *   SPEC_CHAIN_CHUNKED   the streaming pass, then the chunked accept kernel:
+ *                        CTAs over chunks of every request's draw row, the
+ *                        last of a request's CTAs to finish draws;
  *   SPEC_CHAIN_FUSED     one thread-block cluster per request does the whole
  *                        call in one launch and uses no workspace (suits
  *                        small problems: latency-bound); when the requests'
@@ -435,11 +440,12 @@ int64_t spec_launch_count(void);
  * it returns SPEC_OK, or SPEC_EINVAL for an unknown value.  The workspace
  * requirements of the entry points do not change with the path.  This
  * switch has no counterpart in the method; it exists for tuning and so that
- * both paths can be tested on any shape.
+ * every path can be tested on any shape.
  */
 #define SPEC_CHAIN_AUTO 0
 #define SPEC_CHAIN_TWO_PASS 1
 #define SPEC_CHAIN_FUSED 2
+#define SPEC_CHAIN_CHUNKED 3
 int spec_set_chain_path(int path);
 
 /*

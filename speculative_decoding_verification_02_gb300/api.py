@@ -22,7 +22,7 @@ SPEC_OK, SPEC_EINVAL, SPEC_EDTYPE, SPEC_EWORKSPACE, SPEC_ECUDA = 0, -1, -2, -3, 
 STATUS_OK, STATUS_TOKEN_RANGE, STATUS_BAD_TREE, STATUS_BAD_LENGTH = 0, 1, 2, 3
 DTYPE_F32, DTYPE_BF16 = 0, 1
 OP_NGRAM, OP_GREEDY, OP_SAMPLE, OP_TREE, OP_DRAW, OP_FILTER = 0, 1, 2, 3, 4, 5
-CHAIN_AUTO, CHAIN_TWO_PASS, CHAIN_FUSED = 0, 1, 2
+CHAIN_AUTO, CHAIN_TWO_PASS, CHAIN_FUSED, CHAIN_CHUNKED = 0, 1, 2, 3
 TREE_SIBLINGS_WITHOUT_REPLACEMENT = 1
 
 _lock = threading.Lock()
@@ -169,7 +169,8 @@ def workspace(nbytes: int, device, stream=None) -> torch.Tensor:
 
 def set_chain_path(path: int):
     """Chain verification path for later calls, process-wide: CHAIN_AUTO,
-    CHAIN_TWO_PASS or CHAIN_FUSED (same results, different speed)."""
+    CHAIN_TWO_PASS, CHAIN_FUSED or CHAIN_CHUNKED (same results, different
+    speed)."""
     _check(lib().spec_set_chain_path(int(path)), "spec_set_chain_path")
 
 

@@ -36,7 +36,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // that the grid is about four waves of four CTAs on each SM (152 on a
 // GB300), between 16 KB and 128 KB of one row: small calls spread over every
 // SM, large ones keep each CTA streaming long enough to amortise its
-// start-up and reduction.  The chunked accept kernel uses 16 KB chunks.
+// start-up and reduction.
 
 // Chain path (spec_set_chain_path).  In AUTO the fused kernel takes
 // vocabularies up to kFusedAutoMaxV: 0, since with the cluster accept kernel
@@ -55,24 +55,24 @@ int stream_chunk(int dtype, long long rows_total, int V) {
 }
 
 // Chunks of the chunked accept kernel: about one wave of its CTAs (two per
-// SM) over the whole batch, at least 4,096 logits, a multiple of 2,048, at
-// most 64 sub-chunks of 256 x 16 bytes.
+// SM) over the whole batch, and at most kThreads chunks per request (the
+// last CTA to arrive reads one chunk per thread).  A chunk is G rounds of
+// one 16-byte group per thread, G >= 1.
 int accept_chunk(int B, int V, int dtype) {
+  const long long unit = static_cast<long long>(kThreads) * (16 / elem_size(dtype));
   const long long per_req = std::max<long long>(1, 2LL * device_sm_count() / std::max(B, 1));
-  long long chunk = (V + per_req - 1) / per_req;
-  chunk = (chunk + 2047) / 2048 * 2048;
-  const long long cap = 64LL * 256 * (16 / elem_size(dtype));
-  return static_cast<int>(std::min(std::max<long long>(chunk, 4096), cap));
+  long long g = (V + per_req * unit - 1) / (per_req * unit);
+  g = std::max(g, (V + kThreads * unit - 1) / (kThreads * unit));
+  return static_cast<int>(std::max<long long>(g, 1) * unit);
 }
 
-int sub_chunk(int dtype) { return 256 * (16 / elem_size(dtype)); }
-
-// Workspace: per-(row, chunk) statistics, then for sampling the residual
-// mass per sub-chunk, one arrival counter per request (zeroed by the
+// Workspace: per-(row, chunk) statistics, then for sampling the draw's
+// weight mass per warp range of the chunked accept kernel, one arrival
+// counter per request (zeroed by the
 // streaming pass of each call, so the workspace needs no initialisation)
 // and each row's top-k / top-p threshold.
 struct ChainLayout {
-  int nc, chunk, nc2, chunk2, nsub;
+  int nc, chunk, nc2, chunk2;
   size_t part, part2, counter2, theta, total;
 };
 
@@ -82,13 +82,12 @@ ChainLayout chain_layout(bool sample, int B, int k, int V, int dtype) {
   L.nc = (V + L.chunk - 1) / L.chunk;
   L.chunk2 = accept_chunk(B, V, dtype);
   L.nc2 = (V + L.chunk2 - 1) / L.chunk2;
-  L.nsub = (V + sub_chunk(dtype) - 1) / sub_chunk(dtype);
   const size_t rows = sample ? 2 * static_cast<size_t>(k) + 1 : static_cast<size_t>(k) + 1;
   size_t off = 0;
   L.part = off;
   off = round_up(off + sizeof(Partial) * B * rows * L.nc, 256);
   L.part2 = off;
-  off = round_up(off + sizeof(float) * (sample ? B * static_cast<size_t>(L.nsub) : 0), 256);
+  off = round_up(off + sizeof(float) * (sample ? B * static_cast<size_t>(L.nc2) * kWarps : 0), 256);
   L.counter2 = off;
   off = round_up(off + (sample ? sizeof(int) * B : 0), 256);
   L.theta = off;  // top-k / top-p: each row's threshold
@@ -297,7 +296,8 @@ int spec_trace_collect(const char **names, double *total_ms, int64_t *launches, 
 }
 
 int spec_set_chain_path(int path) {
-  if (path != SPEC_CHAIN_AUTO && path != SPEC_CHAIN_TWO_PASS && path != SPEC_CHAIN_FUSED)
+  if (path != SPEC_CHAIN_AUTO && path != SPEC_CHAIN_TWO_PASS && path != SPEC_CHAIN_FUSED &&
+      path != SPEC_CHAIN_CHUNKED)
     return SPEC_EINVAL;
   g_chain_path.store(path, std::memory_order_relaxed);
   return SPEC_OK;
@@ -365,7 +365,6 @@ static int chain_common(bool sample, const void *target, int64_t t_req, const vo
   P.chunk = L.chunk;
   P.nc2 = L.nc2;
   P.chunk2 = L.chunk2;
-  P.nsub = L.nsub;
   P.c = sample ? static_cast<float>(1.4426950408889634 / static_cast<double>(T)) : 1.0f;
   P.draft = draft;
   P.draft_len = draft_len;
@@ -386,6 +385,7 @@ static int chain_common(bool sample, const void *target, int64_t t_req, const vo
   const bool fvec = vec && V % (16 / es) == 0;  // the fused kernel's 16-byte path also wants V a multiple of a group
   const int path = g_chain_path.load(std::memory_order_relaxed);
   const bool want_fused = path == SPEC_CHAIN_FUSED || (path == SPEC_CHAIN_AUTO && V <= kFusedAutoMaxV);
+  const bool chunked = path == SPEC_CHAIN_CHUNKED;
 
   if (filtered) {
     // the filter kernel replaces the streaming pass: one partial per row
@@ -399,14 +399,14 @@ static int chain_common(bool sample, const void *target, int64_t t_req, const vo
     if (!chain_filter_plan(P)) return SPEC_EINVAL;  // a row longer than 16 slices of 96 KB
     e = launch_chain_filter(P, fvec, as_stream(stream));
     if (e == cudaSuccess) {
-      if (!chain_accept_plan(P, fvec)) P.cluster = 0;
+      if (chunked || !chain_accept_plan(P, fvec)) P.cluster = 0;
       e = launch_chain(P, true, vec, fvec, as_stream(stream), false);
     }
   } else if (want_fused && chain_fused_plan(P, sample, fvec)) {
     e = launch_chain_fused(P, sample, fvec, as_stream(stream));
   } else {
     // two-pass: the cluster accept kernel when every request's cluster is resident
-    if (!(sample && chain_accept_plan(P, fvec))) P.cluster = 0;
+    if (chunked || !(sample && chain_accept_plan(P, fvec))) P.cluster = 0;
     e = launch_chain(P, sample, vec, fvec, as_stream(stream));
   }
   return e == cudaSuccess ? SPEC_OK : fail_cuda(e, sample ? "spec_verify_sample" : "spec_verify_greedy");

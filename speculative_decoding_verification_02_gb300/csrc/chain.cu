@@ -44,8 +44,6 @@ namespace sv {
 
 constexpr int kMaxRows = 2 * SPEC_MAX_K + 1;
 constexpr int kPickCache = 512;  // chunk weights kept in shared memory by warp_pick
-constexpr int kMaxSubs = 64;     // sub-chunks per CTA of the chunked accept kernel
-constexpr int kSubBatch = 8;     // sub-chunk groups whose loads are in flight together
 
 // Arrival counter with release (this thread's earlier writes become visible
 // first) and acquire (the caller sees what earlier arrivals published).
@@ -135,21 +133,20 @@ __global__ void __launch_bounds__(kThreads) chain_greedy_accept_kernel(const Cha
   write_common<false>(P, b, 0, pr.L, m, max(0, min(m + 1, pr.cap)), sTok, nullptr, nullptr, true, sA[m]);
 }
 
-template <int DT, bool VEC>
+template <int DT, bool VEC, bool CVEC>
 __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const ChainParams P) {
+  static_assert(kWarps == 8, "a chunk's warp masses are two 16-byte words");
   __shared__ float sM[kMaxRows], sS[kMaxRows], sX[kMaxRows], sTh[kMaxRows];
   __shared__ int sTok[SPEC_MAX_K];
   __shared__ float sU[SPEC_MAX_K + 1], sP[SPEC_MAX_K], sQ[SPEC_MAX_K];
-  __shared__ float s_sub[kWarps][kMaxSubs];
-  __shared__ float s_wcache[kPickCache];
-  __shared__ int s_last, s_j, s_m;
-  __shared__ float s_thr, s_tot, s_drawn;
-  __shared__ bool s_fallback;
-  const int nc = P.nc;
-  const int b = blockIdx.x / P.nc2, j = blockIdx.x - b * P.nc2;
+  __shared__ float s_wcache[kPickCache], s_wm[kWarps];
+  __shared__ int s_last, s_j, s_jlast, s_w;
+  __shared__ float s_thr;
+  const int nc = P.nc, nch = P.nc2;
+  const int b = blockIdx.x / nch, j = blockIdx.x - b * nch;
   const int k = P.k, rows = 2 * k + 1;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const Prologue pr = read_request(P, b, sTok, sU, true);
+  const Prologue pr = read_request(P, b, sTok, sU, true);  // (the inputs, before the wait)
   pdl_wait();
   if (pr.bad) {
     if (j == 0) write_common<true>(P, b, pr.bad, pr.L, 0, 0, sTok, sP, sQ, true, -1);
@@ -185,136 +182,171 @@ __global__ void __launch_bounds__(kThreads) chain_sample_accept_kernel(const Cha
     }
   }
   __syncthreads();
-  if (tid == 0) {
-    int m = 0;
-    for (int i = 0; i < L; ++i) {
+  // Every warp tests the positions itself (lane i: positions i, i + 32, ...);
+  // warp 0 keeps p and q for the outputs, and chunk 0's warp 0 writes them.
+  int m = L;  // the first rejected position
+  for (int i0 = 0; i0 < L; i0 += 32) {
+    const int i = i0 + lane;
+    bool ok = true;
+    if (i < L) {
       // (a drafted token below its row's threshold has probability 0)
       const float p = sX[i] >= sTh[i] ? ex2((sX[i] - sM[i]) * P.c) / sS[i] : 0.0f;
       const float q = sX[L + 1 + i] >= sTh[L + 1 + i] ? ex2((sX[L + 1 + i] - sM[L + 1 + i]) * P.c) / sS[L + 1 + i]
                                                       : 0.0f;
-      sP[i] = p;
-      sQ[i] = q;
-      if (m == i && sU[i] * q < p) m = i + 1;
+      if (warp == 0) {
+        sP[i] = p;
+        sQ[i] = q;
+      }
+      ok = sU[i] * q < p;
     }
-    s_m = m;
+    const unsigned rej = __ballot_sync(0xffffffffu, !ok);
+    if (rej && m == L) m = i0 + __ffs(rej) - 1;
   }
-  __syncthreads();
-  const int m = s_m;
   const int ne = max(0, min(m + 1, pr.cap));
-  if (j == 0) write_common<true>(P, b, 0, L, m, ne, sTok, sP, sQ, false, -1);
+  if (j == 0 && warp == 0) {
+    __syncwarp();
+    write_common<true>(P, b, 0, L, m, ne, sTok, sP, sQ, false, -1, lane, 32);
+  }
   const float u_final = sU[k];
 
   // the final draw: the residual max(0, p_m - q_m) after a rejection, p_L
-  // after a full accept; the mass of this CTA's chunk, then the last CTA to
-  // arrive picks the chunk where u * total falls and scans it
+  // after a full accept.  Each warp adds up the weights of its range of the
+  // chunk (G rounds of 32 16-byte groups, the lane_group split); thread 0
+  // publishes the chunk's warp masses and arrives; the last CTA to arrive
+  // finds the chunk, then the warp range, where u * total falls, and one
+  // warp walks that range.
   Weights W = m < L
                   ? Weights{row_ptr<DT>(P.target, P.t_req, P.row, b, m), row_ptr<DT>(P.draftl, P.d_req, P.row, b, m),
                             sM[m], sM[L + 1 + m], 1.0f / sS[m], 1.0f / sS[L + 1 + m], P.c, sTh[m], sTh[L + 1 + m]}
                   : Weights{row_ptr<DT>(P.target, P.t_req, P.row, b, L), nullptr, sM[L], 0.0f, 1.0f / sS[L], 0.0f,
                             P.c, sTh[L], -INFINITY};
-  // Per sub-chunk of kThreads 16-byte groups (each thread adds up its one
-  // group of it), so the last CTA only has to scan one sub-chunk.
   constexpr int EPG = Elems<DT>::kPerGroup;
-  constexpr int ES = Elems<DT>::kSize;
-  const int sub = kThreads * EPG;
+  const int G = P.chunk2 / (kThreads * EPG);
   const int v0 = j * P.chunk2, v1 = min(P.V, v0 + P.chunk2);
-  const int nsub = (v1 - v0 + sub - 1) / sub;  // <= kMaxSubs by the choice of chunk2
-  // (FILT = false when neither row has a threshold: no mask in the loop)
-  auto weight_pass = [&]<bool FILT>() {
-    for (int i0 = 0; i0 < nsub; i0 += kSubBatch) {
-      uint4 A[kSubBatch], Bv[kSubBatch];
-      bool full[kSubBatch];
-#pragma unroll
-      for (int q = 0; q < kSubBatch; ++q) {
-        const int gv = v0 + ((i0 + q) * kThreads + tid) * EPG;  // first logit of this thread's group
-        full[q] = VEC && i0 + q < nsub && gv + EPG <= v1;
-        if (full[q]) {
-          A[q] = __ldcg(reinterpret_cast<const uint4 *>(W.a + static_cast<int64_t>(gv) * ES));
-          if (W.b != nullptr) Bv[q] = __ldcg(reinterpret_cast<const uint4 *>(W.b + static_cast<int64_t>(gv) * ES));
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < kSubBatch; ++q) {
-        if (i0 + q >= nsub) break;
-        const int gv = v0 + ((i0 + q) * kThreads + tid) * EPG;
-        float ws = 0.0f;
-        if (full[q]) {
-          float a[EPG], bb[EPG], w[EPG];
-          unpack16<DT>(A[q], a);
-          if (W.b != nullptr) unpack16<DT>(Bv[q], bb);
-          weights_group<EPG, FILT>(W, a, bb, w);
-#pragma unroll
-          for (int e = 0; e < EPG; ++e) ws += w[e];
-        } else {
-          for (int e = 0; e < EPG; ++e) {
-            const int v = gv + e;
-            if (v < v1)
-              ws += weight_at<DT, FILT>(W, load_one<DT>(W.a, v), W.b != nullptr ? load_one<DT>(W.b, v) : -INFINITY);
-          }
-        }
-        ws = warp_sum(ws);
-        if (lane == 0) s_sub[warp][i0 + q] = ws;
-      }
-    }
-  };
-  if (weights_filtered(W)) weight_pass.template operator()<true>();
-  else weight_pass.template operator()<false>();
+  const bool filt = weights_filtered(W);  // (no mask in the loops without a threshold)
+  const float wm = warp_sum(filt ? lane_weight_sum<DT, CVEC, true>(W, v0, v1, G, nullptr)
+                                 : lane_weight_sum<DT, CVEC, false>(W, v0, v1, G, nullptr));
+  if (lane == 0) s_wm[warp] = wm;
   __syncthreads();
-  const int nsub_all = P.nsub;
-  float *part2 = P.part2 + static_cast<int64_t>(b) * nsub_all;
-  if (tid < nsub) {
-    float t = 0.0f;
-    for (int w = 0; w < kWarps; ++w) t += s_sub[w][tid];
-    part2[v0 / sub + tid] = t;
+  float *wmg = P.part2 + static_cast<int64_t>(b) * nch * kWarps;  // [chunk][warp]
+  if (tid == 0) {
+    // thread 0 alone publishes, then arrives (release); the last of every
+    // nch arrivals draws, so a launch repeated on the same partials draws again
+    float4 *dst = reinterpret_cast<float4 *>(wmg + static_cast<int64_t>(j) * kWarps);
+    dst[0] = make_float4(s_wm[0], s_wm[1], s_wm[2], s_wm[3]);
+    dst[1] = make_float4(s_wm[4], s_wm[5], s_wm[6], s_wm[7]);
+    s_last = (atomic_add_acq_rel(P.counter2 + b, 1) + 1) % nch == 0;
+    s_j = kNoIndex;
+    s_jlast = -1;
   }
-  __syncthreads();
-  // publishes part2 (cumulative); the last of every nc2 arrivals draws, so a
-  // launch repeated on the same partials (the tracing repeats) draws again
-  if (tid == 0) s_last = (atomic_add_acq_rel(P.counter2 + b, 1) + 1) % P.nc2 == 0;
   __syncthreads();
   if (!s_last) return;
-  if (warp == 0) {
-    int js;
-    float th, tot;
-    warp_pick([&](int jj) { return __ldcg(part2 + jj); }, nsub_all, u_final, s_wcache, kPickCache, js, th, tot);
-    const bool fallback = !(tot > 0.0f) && m < L;
-    if (fallback) {
-      // zero residual mass (only through rounding): draw from p_m instead,
-      // its chunks picked from the streaming pass's statistics
-      const Partial *p1 = P.part + (static_cast<int64_t>(b) * rows + m) * nc;
-      const float M = sM[m], c = P.c;
-      float tp;
-      warp_pick([&](int jj) { const Partial q = ld_partial(p1 + jj); return q.s * ex2((q.m - M) * c); }, nc,
-                u_final, s_wcache, kPickCache, js, th, tp);
-      tot = tp;
+
+  // ---- the last CTA: thread t holds chunk t's warp masses (nch <= kThreads)
+  float wv[kWarps];
+  float cm = 0.0f;
+  if (tid < nch) {
+    const float4 lo4 = __ldcg(reinterpret_cast<const float4 *>(wmg + static_cast<int64_t>(tid) * kWarps));
+    const float4 hi4 = __ldcg(reinterpret_cast<const float4 *>(wmg + static_cast<int64_t>(tid) * kWarps + 4));
+    wv[0] = lo4.x; wv[1] = lo4.y; wv[2] = lo4.z; wv[3] = lo4.w;
+    wv[4] = hi4.x; wv[5] = hi4.y; wv[6] = hi4.z; wv[7] = hi4.w;
+  } else {
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) wv[w] = 0.0f;
+  }
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) cm += wv[w];
+  // block-wide scan of the chunk masses in chunk order
+  const float incl_w = warp_inclusive_scan(cm, lane);
+  float excl_w = __shfl_up_sync(0xffffffffu, incl_w, 1);
+  if (lane == 0) excl_w = 0.0f;
+  if (lane == 31) s_wm[warp] = incl_w;
+  __syncthreads();
+  float before = 0.0f, total = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const float t = s_wm[w];
+    if (w < warp) before += t;
+    total += t;
+  }
+  const bool fallback = !(total > 0.0f) && m < L;
+  if (!fallback) {
+    const float thr = u_final * total;
+    if (cm > 0.0f) {
+      if (before + incl_w > thr) atomicMin(&s_j, tid);
+      atomicMax(&s_jlast, tid);
     }
+    __syncthreads();
+    const int jsel = s_j != kNoIndex ? s_j : max(s_jlast, 0);  // (rounding: the last chunk with mass)
+    if (tid == jsel) {
+      // the warp range of chunk jsel where the threshold falls
+      const float thr_c = s_j != kNoIndex ? thr - (before + excl_w) : INFINITY;
+      float run = 0.0f, t_w = INFINITY;
+      int wsel = -1, wlast = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        if (wv[w] > 0.0f) {
+          wlast = w;
+          if (wsel < 0 && run + wv[w] > thr_c) {
+            wsel = w;
+            t_w = thr_c - run;
+          }
+        }
+        run += wv[w];
+      }
+      s_w = wsel >= 0 ? wsel : wlast;
+      s_thr = wsel >= 0 ? t_w : INFINITY;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    const int lo = jsel * P.chunk2, hi = min(P.V, lo + P.chunk2);
+    auto walk = [&]<bool FILT>() {
+      return warp_walk_range<EPG>(s_w, G, s_thr, [&](int g, float *w) {
+        float x[EPG], y[EPG];
+        unpack16<DT>(load_group<DT, CVEC>(W.a, lo + g * EPG, hi), x);
+        if (W.b) unpack16<DT>(load_group<DT, CVEC>(W.b, lo + g * EPG, hi), y);
+        weights_group<EPG, FILT>(W, x, y, w);
+      });
+    };
+    const int pick = filt ? walk.template operator()<true>() : walk.template operator()<false>();
+    const int tok = pick >= 0 ? lo + pick : lo;  // (a range without mass: its first logit)
     if (lane == 0) {
-      s_j = js;
-      s_thr = th;
-      s_tot = fallback ? 0.0f : tot;  // the residual mass (0 after the fallback)
-      s_fallback = fallback;
-      s_drawn = tot;                   // the mass of the distribution the token is drawn from
+      if (m < ne) P.out_tokens[static_cast<int64_t>(b) * (k + 1) + m] = tok;
+      if (P.resid_mass) P.resid_mass[b] = m < L ? total : 0.0f;
+      if (P.final_prob)
+        P.final_prob[b] = weight_at<DT>(W, load_one<DT>(W.a, tok), W.b ? load_one<DT>(W.b, tok) : 0.0f) / total;
+    }
+    return;
+  }
+  // zero residual mass (only through rounding): draw from p_m instead, its
+  // chunks picked from the streaming pass's statistics
+  __shared__ int s_fj;
+  __shared__ float s_fthr, s_ftot;
+  if (warp == 0) {
+    const Partial *p1 = P.part + (static_cast<int64_t>(b) * rows + m) * nc;
+    const float M = sM[m], c = P.c;
+    int js;
+    float th, tp;
+    warp_pick([&](int jj) { const Partial q = ld_partial(p1 + jj); return q.s * ex2((q.m - M) * c); }, nc, u_final,
+              s_wcache, kPickCache, js, th, tp);
+    if (lane == 0) {
+      s_fj = js;
+      s_fthr = th;
+      s_ftot = tp;
     }
   }
   __syncthreads();
-  int lo, hi;
-  if (s_fallback) {
-    W.b = nullptr;
-    W.alpha = 1.0f;
-    W.beta = 0.0f;
-    lo = s_j * P.chunk;
-    hi = min(P.V, lo + P.chunk);
-  } else {
-    lo = s_j * sub;
-    hi = min(P.V, lo + sub);
-  }
-  int tok = block_select<DT, VEC>(W, lo, hi, s_thr);
+  W.b = nullptr;
+  W.alpha = 1.0f;
+  W.beta = 0.0f;
+  const int lo = s_fj * P.chunk, hi = min(P.V, lo + P.chunk);
+  int tok = block_select<DT, VEC>(W, lo, hi, s_fthr);
   if (tok < 0) tok = lo;  // no positive weight in the range (a row without mass): its first logit
   if (tid == 0) {
     if (m < ne) P.out_tokens[static_cast<int64_t>(b) * (k + 1) + m] = tok;
-    if (P.resid_mass) P.resid_mass[b] = (m < L && !s_fallback) ? s_tot : 0.0f;
+    if (P.resid_mass) P.resid_mass[b] = 0.0f;
     if (P.final_prob)
-      P.final_prob[b] = weight_at<DT>(W, load_one<DT>(W.a, tok), W.b ? load_one<DT>(W.b, tok) : 0.0f) / s_drawn;
+      P.final_prob[b] = weight_at<DT>(W, load_one<DT>(W.a, tok), 0.0f) / s_ftot;
   }
 }
 
@@ -354,7 +386,7 @@ static cudaError_t launch_chain_t(const ChainParams &P, bool sample, bool stats,
     if (P.cluster > 0) return launch_chain_accept_cluster(P, CVEC, st);
     const unsigned grid2 = static_cast<unsigned>(static_cast<long long>(P.B) * P.nc2);
     return trace_launch_ex("chain_sample_accept", st, [&] {
-      return launch_dependent(chain_sample_accept_kernel<DT, VEC>, grid2, st, P);
+      return launch_dependent(chain_sample_accept_kernel<DT, VEC, CVEC>, grid2, st, P);
     });
   }
   cudaError_t e = trace_launch_ex("chain_stats_greedy", st, [&] {

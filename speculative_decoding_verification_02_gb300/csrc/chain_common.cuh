@@ -47,15 +47,17 @@ __device__ __forceinline__ Prologue read_request(const ChainParams &P, int b, in
   return check_request(P, s_L, s_cap, sTok);
 }
 
-// The outputs that do not depend on the final draw (written once per request).
+// The outputs that do not depend on the final draw (written once per
+// request), by threads t = 0 .. nt - 1 (the whole block by default).
 template <bool SAMPLE>
 __device__ __forceinline__ void write_common(const ChainParams &P, int b, int bad, int L, int m, int ne,
                                              const int *sTok, const float *sP, const float *sQ,
-                                             bool final_known, int final_tok) {
+                                             bool final_known, int final_tok, int t = threadIdx.x,
+                                             int nt = blockDim.x) {
   const int k = P.k;
   int32_t *out = P.out_tokens + static_cast<int64_t>(b) * (k + 1);
-  const int tid = threadIdx.x;
-  for (int j = tid; j <= k; j += blockDim.x) {
+  const int tid = t;
+  for (int j = tid; j <= k; j += nt) {
     if (bad) {
       out[j] = -1;
     } else {
@@ -64,7 +66,7 @@ __device__ __forceinline__ void write_common(const ChainParams &P, int b, int ba
     }
   }
   if (SAMPLE) {
-    for (int j = tid; j < k; j += blockDim.x) {
+    for (int j = tid; j < k; j += nt) {
       const bool ok = !bad && j < L;
       if (P.p_tok) P.p_tok[static_cast<int64_t>(b) * k + j] = ok ? sP[j] : -1.0f;
       if (P.q_tok) P.q_tok[static_cast<int64_t>(b) * k + j] = ok ? sQ[j] : -1.0f;

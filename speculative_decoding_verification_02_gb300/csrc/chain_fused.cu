@@ -53,42 +53,6 @@ struct __align__(16) RowPart {
   float pad;
 };
 
-// This lane's sum of the draw weights W over its groups (lane_group split of
-// [lo, hi), G rounds; logits >= hi weigh 0).  Each group's own sum goes to
-// gsum[g].
-template <int DT, bool VEC, bool FILT>
-__device__ __forceinline__ float lane_weight_sum(const Weights &W, int lo, int hi, int G, float *gsum) {
-  constexpr int EPG = Elems<DT>::kPerGroup;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float acc = 0.0f;
-  for (int j0 = 0; j0 < G; j0 += kBatch) {
-    const int g0 = lane_group(warp, j0, G, lane);  // round j0 + u: group g0 + 32 u
-    uint4 xa[kBatch], xb[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      if (j0 + u < G) {
-        xa[u] = load_group<DT, VEC>(W.a, lo + (g0 + 32 * u) * EPG, hi);
-        if (W.b) xb[u] = load_group<DT, VEC>(W.b, lo + (g0 + 32 * u) * EPG, hi);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      if (j0 + u < G) {
-        float x[EPG], y[EPG], w[EPG];
-        unpack16<DT>(xa[u], x);
-        if (W.b) unpack16<DT>(xb[u], y);
-        weights_group<EPG, FILT>(W, x, y, w);
-        float gs = 0.0f;
-#pragma unroll
-        for (int e = 0; e < EPG; ++e) gs += w[e];
-        gsum[g0 + 32 * u] = gs;
-        acc += gs;
-      }
-    }
-  }
-  return acc;
-}
-
 // The streaming pass's statistics of one (request, row, chunk).
 __device__ __forceinline__ float4 ld_part(const Partial *p) { return __ldcg(reinterpret_cast<const float4 *>(p)); }
 
@@ -116,7 +80,7 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
   RowPart *s_cpart = s_wpart + kFusedWarps * rows_max;    // [rank][row] slice statistics (streamed here)
   float *s_gsum = reinterpret_cast<float *>(ACCEPT ? dyn_parts : s_cpart + kFusedMaxCluster * rows_max);
   // s_gsum: [threads * groups] weight sum of each 16-byte group of the slice (sampling)
-  __shared__ int sTok[SPEC_MAX_K], sOk[SPEC_MAX_K], sA[kFusedMaxRows];
+  __shared__ int sTok[SPEC_MAX_K], sA[kFusedMaxRows];
   __shared__ float sU[SPEC_MAX_K + 1], sP[SPEC_MAX_K], sQ[SPEC_MAX_K];
   __shared__ float sM[kFusedMaxRows], sS[kFusedMaxRows], sX[kFusedMaxRows], sTh[kFusedMaxRows];
   __shared__ float s_red[kFusedWarps], s_z[2][kFusedMaxCluster];
@@ -131,12 +95,17 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
     // ignored); the drafted token's logit is the largest x over the chunks
     // (the one chunk holding the token has it, the others -inf)
     pdl_launch_dependents();
-    pdl_wait();  // the streaming pass's partials
+    // The request's own inputs do not come from the streaming pass: they are
+    // read and checked while it still runs.  (This kernel starts only after
+    // the streaming pass has waited for whatever kernel wrote them.)
     __shared__ int s_L, s_cap;
     if (tid == 0) s_L = P.draft_len ? P.draft_len[b] : k;
     if (tid == 32) s_cap = P.max_emit ? P.max_emit[b] : k + 1;
     if (tid < k) sTok[tid] = P.draft[static_cast<int64_t>(b) * k + tid];
     if (tid >= 64 && tid <= 64 + k) sU[tid - 64] = P.uniforms[static_cast<int64_t>(b) * (k + 1) + tid - 64];
+    __syncthreads();
+    pr = check_request(P, s_L, s_cap, sTok);
+    pdl_wait();  // the streaming pass's partials
     const int nc = P.nc;
     const Partial *base = P.part + static_cast<int64_t>(b) * (2 * k + 1) * nc;
     for (int r = warp; r < 2 * k + 1; r += kFusedWarps) {
@@ -158,7 +127,6 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
       }
     }
     __syncthreads();
-    pr = check_request(P, s_L, s_cap, sTok);
   } else {
     pdl_wait();  // the inputs may be the previous kernel's outputs
     pdl_launch_dependents();
@@ -232,31 +200,36 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
   // the statistics of draft row i: after the target rows 0..L here, after
   // rows 0..k in the streaming pass's layout
   auto drow = [&](int i) { return (ACCEPT ? k : L) + 1 + i; };
-  if (tid < L) {
-    if (SAMPLE) {
-      // (a drafted token below its row's threshold has probability 0)
-      const float p = !FILT || sX[tid] >= sTh[tid] ? ex2((sX[tid] - sM[tid]) * c) / sS[tid] : 0.0f;
-      const float q = !FILT || sX[drow(tid)] >= sTh[drow(tid)]
-                          ? ex2((sX[drow(tid)] - sM[drow(tid)]) * c) / sS[drow(tid)]
-                          : 0.0f;
-      sP[tid] = p;
-      sQ[tid] = q;
-      sOk[tid] = sU[tid] * q < p;
-    } else {
-      sOk[tid] = sA[tid] == sTok[tid];
-    }
-  }
-  __syncthreads();
+  // Every warp tests the positions itself (lane i: positions i, i + 32),
+  // so no barrier separates the test from the draw; warp 0 keeps p and q
+  // for the outputs and writes the request's outputs.
   int m = L;  // the first rejected position
   for (int i0 = 0; i0 < L; i0 += 32) {
-    const unsigned rej = __ballot_sync(0xffffffffu, i0 + lane < L && !sOk[i0 + lane]);
-    if (rej) {
-      m = i0 + __ffs(rej) - 1;
-      break;
+    const int i = i0 + lane;
+    bool ok = true;
+    if (i < L) {
+      if (SAMPLE) {
+        // (a drafted token below its row's threshold has probability 0)
+        const float p = !FILT || sX[i] >= sTh[i] ? ex2((sX[i] - sM[i]) * c) / sS[i] : 0.0f;
+        const float q =
+            !FILT || sX[drow(i)] >= sTh[drow(i)] ? ex2((sX[drow(i)] - sM[drow(i)]) * c) / sS[drow(i)] : 0.0f;
+        if (warp == 0) {
+          sP[i] = p;
+          sQ[i] = q;
+        }
+        ok = sU[i] * q < p;
+      } else {
+        ok = sA[i] == sTok[i];
+      }
     }
+    const unsigned rej = __ballot_sync(0xffffffffu, !ok);
+    if (rej && m == L) m = i0 + __ffs(rej) - 1;
   }
   const int ne = max(0, min(m + 1, pr.cap));
-  if (rank == 0) write_common<SAMPLE>(P, b, 0, L, m, ne, sTok, sP, sQ, !SAMPLE, sA[m]);
+  if (rank == 0 && warp == 0) {
+    __syncwarp();
+    write_common<SAMPLE>(P, b, 0, L, m, ne, sTok, sP, sQ, !SAMPLE, sA[m], lane, 32);
+  }
   if (!SAMPLE) return;
 
   // ---- 3. the final draw: residual after a rejection, p_L after a full accept
@@ -276,7 +249,7 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
     }
     cluster.sync();
     rmass = lane < CS ? s_z[attempt][lane] : 0.0f;  // lane r: rank r's mass
-    total = warp_sum(rmass);
+    total = __shfl_sync(0xffffffffu, warp_inclusive_scan(rmass, lane), 31);
     if (!(total > 0.0f) && m < L && attempt == 0) {
       // zero residual mass (only through rounding): draw from p_m instead
       W.b = nullptr;
@@ -287,7 +260,7 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
   }
   // the rank whose slice holds u * total
   const float incl_r = warp_inclusive_scan(rmass, lane);
-  const float thr = sU[k] * __shfl_sync(0xffffffffu, incl_r, 31);
+  const float thr = sU[k] * total;
   const unsigned hit_r = __ballot_sync(0xffffffffu, lane < CS && rmass > 0.0f && incl_r > thr);
   const unsigned pos_r = __ballot_sync(0xffffffffu, lane < CS && rmass > 0.0f);
   int draw_rank;
@@ -301,13 +274,15 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
   }
   if (rank != draw_rank) return;  // no CTA touches another's shared memory from here on
   // (the fallback `lo` is unreachable: the drawing rank has mass, so one of its warps has)
-  const int tok = range_draw<kFusedThreads, EPG>(wmass, tl, lo, G, lo, s_gsum, [&](int g, float *w) {
+  // (the warp masses of the last attempt are in s_red; the drawing warp
+  // writes the token)
+  const int tok = range_draw<kFusedThreads, EPG, false>(wmass, tl, lo, G, lo, s_gsum, [&](int g, float *w) {
     float x[EPG], y[EPG];
     unpack16<DT>(load_group<DT, VEC>(W.a, lo + g * EPG, hi), x);
     if (W.b) unpack16<DT>(load_group<DT, VEC>(W.b, lo + g * EPG, hi), y);
     weights_group<EPG, FILT>(W, x, y, w);
-  });
-  if (tid == 0) {
+  }, s_red);
+  if (tok >= 0 && lane == 0) {
     if (m < ne) P.out_tokens[static_cast<int64_t>(b) * (k + 1) + m] = tok;
     if (P.resid_mass) P.resid_mass[b] = (m < L && W.b != nullptr) ? total : 0.0f;
     if (P.final_prob)

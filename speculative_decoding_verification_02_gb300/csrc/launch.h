@@ -19,8 +19,7 @@ struct ChainParams {
   int64_t t_req, d_req, row;  // element strides
   int dtype, B, k, V;
   int nc, chunk;    // streaming pass: chunks per row, logits per chunk
-  int nc2, chunk2;  // chunked accept kernel: chunks per row, logits per chunk
-  int nsub;         // sub-chunks (256 groups of 16 bytes) per row in part2
+  int nc2, chunk2;  // chunked accept kernel: chunks per row (<= 256), logits per chunk
   float c;          // log2(e) / T
   const int32_t *draft, *draft_len, *max_emit;
   const float *uniforms;
@@ -28,7 +27,7 @@ struct ChainParams {
   float *p_tok, *q_tok, *resid_mass;
   float *final_prob;  // or null: the final token's probability under the distribution it was drawn from
   Partial *part;     // [B][rows][nc] streaming-pass statistics
-  float *part2;      // [B][nsub] mass of the final draw's weights per sub-chunk
+  float *part2;      // [B][nc2][8] chunked accept kernel: the final draw's weight mass per warp range
   int *counter2;     // [B] arrival counter of the residual pass
   int cluster;       // cluster kernels: CTAs per request (sampling accept: 0 = chunked accept kernel)
   int slice;         // logits per CTA of a cluster kernel

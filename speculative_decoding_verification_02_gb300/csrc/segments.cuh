@@ -255,6 +255,93 @@ __device__ __forceinline__ void lane_rows_stats(const char *const *rows, int lo,
   }
 }
 
+// One warp walks the range of warp `wsel` of a slice (the lane_group split,
+// G rounds of 32 groups), 32 groups at a time, for the first weight whose
+// running sum over the range passes thr.  Returns its offset from the
+// slice start, the same in every lane; when rounding leaves no crossing,
+// the range's last positive weight; -1 when the range has none.
+// group_weights(g, w) writes the EPG weights of group g.
+template <int EPG, class GroupWeights>
+__device__ __forceinline__ int warp_walk_range(int wsel, int G, float thr, GroupWeights &&group_weights) {
+  const int lane = threadIdx.x & 31;
+  int pick = -1, lastp = -1;
+  float run = 0.0f;
+  for (int j = 0; j < G; ++j) {
+    const int g = lane_group(wsel, j, G, lane);
+    float w[EPG];
+    group_weights(g, w);
+    float lm = 0.0f;
+    int le = -1;  // this lane's last positive weight
+#pragma unroll
+    for (int e = 0; e < EPG; ++e) {
+      lm += w[e];
+      if (w[e] > 0.0f) le = e;
+    }
+    const float incl = warp_inclusive_scan(lm, lane);
+    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = 0.0f;
+    const unsigned hit = __ballot_sync(0xffffffffu, lm > 0.0f && run + incl > thr);
+    const unsigned pos = __ballot_sync(0xffffffffu, lm > 0.0f);
+    if (pos) {
+      const int hl = 31 - __clz(pos);
+      lastp = (g - lane + hl) * EPG + __shfl_sync(0xffffffffu, le, hl);
+    }
+    if (hit) {
+      const int lh = __ffs(hit) - 1;
+      int pe = le;  // rounding inside the lane: its last positive weight
+      float r = run + excl;
+#pragma unroll
+      for (int e = 0; e < EPG; ++e) {
+        r += w[e];
+        if (w[e] > 0.0f && r > thr) {
+          pe = e;
+          break;
+        }
+      }
+      pick = (g - lane + lh) * EPG + __shfl_sync(0xffffffffu, pe, lh);
+      break;
+    }
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return pick >= 0 ? pick : lastp;
+}
+
+// This lane's sum of the draw weights W over its groups (lane_group split
+// of [lo, hi), G rounds; logits >= hi weigh 0).  With gsum, each group's
+// own sum goes to gsum[g].
+template <int DT, bool VEC, bool FILT>
+__device__ __forceinline__ float lane_weight_sum(const Weights &W, int lo, int hi, int G, float *gsum) {
+  constexpr int EPG = Elems<DT>::kPerGroup;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float acc = 0.0f;
+  for (int j0 = 0; j0 < G; j0 += kBatch) {
+    const int g0 = lane_group(warp, j0, G, lane);  // round j0 + u: group g0 + 32 u
+    uint4 xa[kBatch], xb[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (j0 + u < G) {
+        xa[u] = load_group<DT, VEC>(W.a, lo + (g0 + 32 * u) * EPG, hi);
+        if (W.b) xb[u] = load_group<DT, VEC>(W.b, lo + (g0 + 32 * u) * EPG, hi);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (j0 + u < G) {
+        float x[EPG], y[EPG], w[EPG];
+        unpack16<DT>(xa[u], x);
+        if (W.b) unpack16<DT>(xb[u], y);
+        weights_group<EPG, FILT>(W, x, y, w);
+        float gs = 0.0f;
+#pragma unroll
+        for (int e = 0; e < EPG; ++e) gs += w[e];
+        if (gsum != nullptr) gsum[g0 + 32 * u] = gs;
+        acc += gs;
+      }
+    }
+  }
+  return acc;
+}
+
 // Inverse-CDF draw inside one CTA's slice [lo, hi) from per-warp masses
 // (the lane_group split).  `wmass` is the calling warp's sum of weights
 // (the same in all its lanes); the drawn logit is the first whose running
@@ -267,18 +354,25 @@ __device__ __forceinline__ void lane_rows_stats(const char *const *rows, int lo,
 // time.  group_weights(g, w) writes the EPG weights of group g (0 for
 // logits >= hi).  Rounding between the scans falls back to the last
 // positive weight of the last warp with mass; `fallback` is returned when
-// no warp has any.  Called by all NT threads; returns the token in every
-// thread.
-template <int NT, int EPG, class GroupWeights>
+// no warp has any.  Called by all NT threads.  BCAST: returns the token in
+// every thread.  Otherwise (no barrier after the warp scan) it returns the
+// token in every lane of one warp -- the drawing warp, or warp 0 when no
+// warp has mass -- and -1 in all other threads.  wsums (or null): the NW
+// warp masses already in shared memory and visible to every thread, which
+// saves publishing them again.
+template <int NT, int EPG, bool BCAST = true, class GroupWeights>
 __device__ int range_draw(float wmass, float tl, int lo, int G, int fallback, const float *gsum,
-                          GroupWeights &&group_weights) {
+                          GroupWeights &&group_weights, const float *wsums = nullptr) {
   constexpr int NW = NT / 32;
   __shared__ float s_wsum[NW];
   __shared__ int s_tok;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) s_wsum[warp] = wmass;
-  __syncthreads();
-  const float wv = lane < NW ? s_wsum[lane] : 0.0f;
+  if (wsums == nullptr) {
+    if (lane == 0) s_wsum[warp] = wmass;
+    __syncthreads();
+    wsums = s_wsum;
+  }
+  const float wv = lane < NW ? wsums[lane] : 0.0f;
   const float winc = warp_inclusive_scan(wv, lane);
   const unsigned hit_w = __ballot_sync(0xffffffffu, wv > 0.0f && winc > tl);
   const unsigned pos_w = __ballot_sync(0xffffffffu, wv > 0.0f);
@@ -292,7 +386,7 @@ __device__ int range_draw(float wmass, float tl, int lo, int G, int fallback, co
     wsel = 31 - __clz(pos_w);
   }
   if (warp == wsel) {
-    int pick = -1, lastp = -1;
+    int pick = -1;
     // the crossing within group g, given the running sum `run` before it
     auto scan_group = [&](int g, float run, bool cross) {
       float w[EPG];
@@ -343,50 +437,14 @@ __device__ int range_draw(float wmass, float tl, int lo, int G, int fallback, co
       }
       if (lh >= 0) pick = __shfl_sync(0xffffffffu, pick, lh);
     } else {
-      float run = 0.0f;
-      for (int j = 0; j < G; ++j) {
-        const int g = lane_group(wsel, j, G, lane);
-        float w[EPG];
-        group_weights(g, w);
-        float lm = 0.0f;
-        int le = -1;  // this lane's last positive weight
-#pragma unroll
-        for (int e = 0; e < EPG; ++e) {
-          lm += w[e];
-          if (w[e] > 0.0f) le = e;
-        }
-        const float incl = warp_inclusive_scan(lm, lane);
-        float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-        if (lane == 0) excl = 0.0f;
-        const unsigned hit = __ballot_sync(0xffffffffu, lm > 0.0f && run + incl > thr_local);
-        const unsigned pos = __ballot_sync(0xffffffffu, lm > 0.0f);
-        if (pos) {
-          const int hl = 31 - __clz(pos);
-          lastp = (g - lane + hl) * EPG + __shfl_sync(0xffffffffu, le, hl);
-        }
-        if (hit) {
-          const int lh = __ffs(hit) - 1;
-          int pe = le;  // rounding inside the lane: its last positive weight
-          float r = run + excl;
-#pragma unroll
-          for (int e = 0; e < EPG; ++e) {
-            r += w[e];
-            if (w[e] > 0.0f && r > thr_local) {
-              pe = e;
-              break;
-            }
-          }
-          pick = (g - lane + lh) * EPG + __shfl_sync(0xffffffffu, pe, lh);
-          break;
-        }
-        run += __shfl_sync(0xffffffffu, incl, 31);
-      }
-      if (pick < 0) pick = lastp;
+      pick = warp_walk_range<EPG>(wsel, G, thr_local, group_weights);
     }
+    if (!BCAST) return pick >= 0 ? lo + pick : fallback;  // (pick is the same in every lane)
     if (lane == 0) s_tok = pick >= 0 ? lo + pick : fallback;
   } else if (wsel < 0 && threadIdx.x == 0) {
     s_tok = fallback;  // no positive weight in the slice (underflow only)
   }
+  if (!BCAST) return wsel < 0 && warp == 0 ? fallback : -1;
   __syncthreads();
   const int r = s_tok;
   __syncthreads();  // the shared words are free again

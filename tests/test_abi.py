@@ -46,15 +46,16 @@ def test_header_constants_match_binding():
     assert int(consts["SPEC_DTYPE_BF16"]) == api.DTYPE_BF16
     assert int(consts["SPEC_STATUS_BAD_TREE"]) == api.STATUS_BAD_TREE
     assert int(consts["SPEC_TREE_SIBLINGS_WITHOUT_REPLACEMENT"]) == api.TREE_SIBLINGS_WITHOUT_REPLACEMENT
-    assert (int(consts["SPEC_CHAIN_AUTO"]), int(consts["SPEC_CHAIN_TWO_PASS"]), int(consts["SPEC_CHAIN_FUSED"])) == \
-        (api.CHAIN_AUTO, api.CHAIN_TWO_PASS, api.CHAIN_FUSED)
+    assert (int(consts["SPEC_CHAIN_AUTO"]), int(consts["SPEC_CHAIN_TWO_PASS"]), int(consts["SPEC_CHAIN_FUSED"]),
+            int(consts["SPEC_CHAIN_CHUNKED"])) == (api.CHAIN_AUTO, api.CHAIN_TWO_PASS, api.CHAIN_FUSED,
+                                                   api.CHAIN_CHUNKED)
 
 
 def test_chain_path_switch(L):
     L.spec_set_chain_path.argtypes = [ctypes.c_int]
-    for bad in (-1, 3, 4, 1 << 20):
+    for bad in (-1, 4, 5, 1 << 20):
         assert L.spec_set_chain_path(bad) == -1          # SPEC_EINVAL
-    for good in (2, 1, 0):
+    for good in (3, 2, 1, 0):
         assert L.spec_set_chain_path(good) == 0
 
 

@@ -9,7 +9,8 @@ the oracle.
   the GPU's filter cut of a row differs from the oracle's (only allowed where
   the cut's fp64 mass is within 1e-6 of top_p; counted), the oracle filters
   that row with the top_p that gives the GPU's cut, so no request is left out.
-  On the headline shape, on both accept kernels (cluster, chunked),
+  On the headline shape, on both accept kernels (cluster, chunked, each
+  forced in turn),
   bf16 ties at the top-k cut, masked logits, drafts outside the filtered q,
   lengths, caps and bad tokens; both filters off reproduce spec_verify_sample
   bit for bit.
@@ -231,19 +232,28 @@ def check_chain_sample_filtered(prob, g, r, top_k, tp, draft_len=None):
     return near
 
 
+@pytest.fixture(params=["cluster", "chunked"])
+def accept_kernel(request):
+    """The accept kernel after the filter: the cluster one where the plan
+    fits (AUTO), or the chunked one on every call."""
+    api.set_chain_path(api.CHAIN_AUTO if request.param == "cluster" else api.CHAIN_CHUNKED)
+    yield request.param
+    api.set_chain_path(api.CHAIN_AUTO)
+
+
 @pytest.mark.parametrize("seed,B,k,V,dtype,T,top_k,top_p", [
     (1, 1, 4, 248_320, "bf16", 1.0, 50, 1.0), (2, 2, 4, 248_320, "bf16", 1.0, 0, 0.6),
     (3, 16, 4, 3000, "fp32", 1.0, 20, 0.9), (4, 64, 3, 2048, "bf16", 0.8, 0, 0.95),
     (5, 400, 2, 4000, "bf16", 1.0, 40, 0.9), (6, 8, 6, 40_003, "bf16", 1.2, 100, 1.0),
     (7, 4, 0, 50_000, "fp32", 1.0, 10, 0.8)])
-def test_filtered_verification_parity(seed, B, k, V, dtype, T, top_k, top_p):
-    """B=400 takes the chunked accept kernel; the others the cluster accept kernel."""
+def test_filtered_verification_parity(seed, B, k, V, dtype, T, top_k, top_p, accept_kernel):
+    """B=400 takes the chunked accept kernel on either setting."""
     prob = _filtered_chain(seed, B, k, V, dtype, T, top_k, top_p)
     g = _run(prob, top_k, top_p)
     print("near", _check(prob, g, top_k, top_p))
 
 
-def test_filtered_drafts_outside_the_filter_lengths_caps():
+def test_filtered_drafts_outside_the_filter_lengths_caps(accept_kernel):
     """Drafts drawn from the unfiltered q (some fall outside q'), variable
     lengths, caps and a bad token, masked logits."""
     B, k, V, top_k, top_p = 24, 5, 6000, 30, 0.9

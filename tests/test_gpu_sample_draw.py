@@ -22,9 +22,10 @@ def _built():
     __graft_entry__.build()
 
 
-@pytest.fixture(scope="module", autouse=True, params=["two_pass", "fused"])
+@pytest.fixture(scope="module", autouse=True, params=["two_pass", "fused", "chunked"])
 def chain_path(request, _built):
-    api.set_chain_path({"two_pass": api.CHAIN_TWO_PASS, "fused": api.CHAIN_FUSED}[request.param])
+    api.set_chain_path({"two_pass": api.CHAIN_TWO_PASS, "fused": api.CHAIN_FUSED,
+                         "chunked": api.CHAIN_CHUNKED}[request.param])
     yield request.param
     api.set_chain_path(api.CHAIN_AUTO)
 
