@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
   __shared__ int sTok[SPEC_MAX_K], sA[kFusedMaxRows];
   __shared__ float sU[SPEC_MAX_K + 1], sP[SPEC_MAX_K], sQ[SPEC_MAX_K];
   __shared__ float sM[kFusedMaxRows], sS[kFusedMaxRows], sX[kFusedMaxRows], sTh[kFusedMaxRows];
+  __shared__ float sIS[kFusedMaxRows];  // 1 / sS
   __shared__ float s_red[kFusedWarps], s_z[2][kFusedMaxCluster];
   const RowPart kEmpty{-INFINITY, 0.0f, kNoIndex, 0.0f};
 
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
       if (lane == 0) {
         sM[r] = m;
         sS[r] = s;
+        sIS[r] = 1.0f / s;
         sX[r] = x;
         if (FILT) sTh[r] = row_theta(P.theta, static_cast<int64_t>(b) * (2 * k + 1) + r);
       }
@@ -192,6 +194,7 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
       if (lane == 0) {
         sM[rr] = x.m;
         sS[rr] = x.s;
+        sIS[rr] = 1.0f / x.s;
         sA[rr] = x.i == kNoIndex ? 0 : x.i;
       }
     }
@@ -210,9 +213,9 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
     if (i < L) {
       if (SAMPLE) {
         // (a drafted token below its row's threshold has probability 0)
-        const float p = !FILT || sX[i] >= sTh[i] ? ex2((sX[i] - sM[i]) * c) / sS[i] : 0.0f;
+        const float p = !FILT || sX[i] >= sTh[i] ? ex2((sX[i] - sM[i]) * c) * sIS[i] : 0.0f;
         const float q =
-            !FILT || sX[drow(i)] >= sTh[drow(i)] ? ex2((sX[drow(i)] - sM[drow(i)]) * c) / sS[drow(i)] : 0.0f;
+            !FILT || sX[drow(i)] >= sTh[drow(i)] ? ex2((sX[drow(i)] - sM[drow(i)]) * c) * sIS[drow(i)] : 0.0f;
         if (warp == 0) {
           sP[i] = p;
           sQ[i] = q;
@@ -233,9 +236,9 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
   if (!SAMPLE) return;
 
   // ---- 3. the final draw: residual after a rejection, p_L after a full accept
-  Weights W = m < L ? Weights{row_of(m), row_of(L + 1 + m), sM[m], sM[drow(m)], 1.0f / sS[m],
-                              1.0f / sS[drow(m)], c, FILT ? sTh[m] : -INFINITY, FILT ? sTh[drow(m)] : -INFINITY}
-                    : Weights{row_of(L), nullptr, sM[L], 0.0f, 1.0f / sS[L], 0.0f, c, FILT ? sTh[L] : -INFINITY,
+  Weights W = m < L ? Weights{row_of(m), row_of(L + 1 + m), sM[m], sM[drow(m)], sIS[m],
+                              sIS[drow(m)], c, FILT ? sTh[m] : -INFINITY, FILT ? sTh[drow(m)] : -INFINITY}
+                    : Weights{row_of(L), nullptr, sM[L], 0.0f, sIS[L], 0.0f, c, FILT ? sTh[L] : -INFINITY,
                               -INFINITY};
   float wmass = 0.0f, rmass = 0.0f, total = 0.0f;
   for (int attempt = 0; attempt < 2; ++attempt) {
