@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
   float *s_q = s_p + static_cast<size_t>(G) * EPG * kTreeThreads;  // staged q
   __shared__ Slot s_all[2][kMaxCluster];  // [exchange parity][source rank]
   __shared__ Slot s_part[kTreeWarps];
-  __shared__ float s_red[kTreeWarps];
+  __shared__ float s_wz[2][kMaxCluster][kTreeWarps];  // [exchange parity][source rank][warp]
   __shared__ int s_path[SPEC_MAX_DEPTH + 1], s_out[SPEC_MAX_DEPTH + 1];
   __shared__ int s_bad, s_cnt[kTreeWarps];
   const Slot kEmpty{-INFINITY, 0.0f, -INFINITY, 0.0f, kNoIndex, 0.0f, 0, 0};
@@ -196,15 +196,20 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(const TreeParam
     return ph;
   };
   // Sum of x over the cluster, in every thread; lane r of every warp also
-  // gets rank r's part, and ws the calling warp's.
+  // gets rank r's part, and ws the calling warp's.  Every warp pushes its
+  // sum into every rank (no block barrier, no second reduction in the CTA);
+  // lane r adds up rank r's warp sums in warp order.
   auto cluster_sum = [&](float x, float &part_of_lane, float &ws) {
     ws = warp_sum(x);
-    if (lane == 0) s_red[warp] = ws;
-    __syncthreads();
-    Slot z = kEmpty;
-    if (warp == 0) z.z = warp_sum(lane < kTreeWarps ? s_red[lane] : 0.0f);
-    const int ph = push_and_sync(z);
-    part_of_lane = lane < ncl ? s_all[ph][lane].z : 0.0f;
+    const int ph = phase & 1;
+    if (lane < ncl) *cluster.map_shared_rank(&s_wz[ph][rank][warp], lane) = ws;
+    cluster.sync();
+    ++phase;
+    float part = 0.0f;
+    if (lane < ncl)
+#pragma unroll
+      for (int w = 0; w < kTreeWarps; ++w) part += s_wz[ph][lane][w];
+    part_of_lane = part;
     return warp_sum(part_of_lane);
   };
   // Children of `node` in increasing id order into s_kids; their number.
