@@ -17,17 +17,15 @@
 //     a request merges the request's partials in the same order, so all of
 //     them reach the same decision: p_i(x_i), q_i(x_i), accept while
 //     u_i q_i(x_i) < p_i(x_i), i.e. u_i < min(1, p/q)
-//     ("投机解码:为什么一个字都不改", 改进方案).  Then
-//       all accepted  the bonus token is drawn from p_L: one warp finds the
-//                     chunk holding u * sum from the chunk totals, and only
-//                     the CTA of that chunk scans it;
-//       rejected at m every CTA adds up max(0, p_m - q_m) over its chunk;
-//                     the last to finish (an arrival counter that the stats
-//                     kernel zeroed, so the workspace needs no
-//                     initialisation) picks the chunk where u * R falls and
-//                     scans it: a draw from norm(max(0, p - q)).
-//     When every request's thread-block cluster fits on the GPU at once,
-//     the cluster accept kernel (chain_fused.cu) replaces it.
+//     ("投机解码:为什么一个字都不改", 改进方案).  Every warp then adds up the
+//     final draw's weights over its range of the chunk -- max(0, p_m - q_m)
+//     after a rejection at m, p_L after a full accept -- and the CTA
+//     publishes its warp masses and arrives on the request's counter (which
+//     the stats kernel zeroed, so the workspace needs no initialisation).
+//     The last CTA to arrive finds the chunk and the warp range where
+//     u * total falls and walks that range: a draw from norm(max(0, p - q))
+//     or from p_L.  When every request's thread-block cluster fits on the GPU
+//     at once, the cluster accept kernel (chain_fused.cu) replaces it.
 // The accept kernels read their inputs before waiting on the stats grid.
 // No kernel waits on another CTA.
 #include <cooperative_groups.h>

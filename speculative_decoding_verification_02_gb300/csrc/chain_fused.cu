@@ -90,11 +90,11 @@ __global__ void __launch_bounds__(kFusedThreads, ACCEPT ? 2 : 1) chain_fused_ker
   const float c = P.c;
   Prologue pr;
   if (ACCEPT) {
-    // the request's inputs and every row's partials, loaded in one round trip:
-    // warp w merges rows w, w + 16, ... of the streaming pass's layout (target
-    // rows 0..k, draft rows k + 1..2k; rows the pass skipped are merged too and
-    // ignored); the drafted token's logit is the largest x over the chunks
-    // (the one chunk holding the token has it, the others -inf)
+    // after the wait, warp w merges rows w, w + 16, ... of the streaming
+    // pass's layout (target rows 0..k, draft rows k + 1..2k; rows the pass
+    // skipped are merged too and ignored); the drafted token's logit is the
+    // largest x over the chunks (the one chunk holding the token has it, the
+    // others -inf)
     pdl_launch_dependents();
     // The request's own inputs do not come from the streaming pass: they are
     // read and checked while it still runs.  (This kernel starts only after

@@ -1,7 +1,6 @@
 // Merging the streaming pass's per-(row, chunk) statistics into row
-// statistics, and the one-warp inverse-CDF pick over a list of masses.
-// Shared by the accept kernels of chain.cu and the slice kernels of
-// chain_slice.cu.
+// statistics, and the one-warp inverse-CDF pick over a list of masses, for
+// the accept kernels of chain.cu.
 #pragma once
 
 #include "common.cuh"
